@@ -1,0 +1,423 @@
+"""Benchmark of the batched block-preconditioner step (DASH-style Shampoo) on GB300.
+
+Workload (default): a 24-layer Llama-style stack with d = 2048 -- per layer four
+2048 x 2048 attention weights and three 2048 x 5632 MLP weights -- cut into
+1024 x 1024 gradient blocks (Ng = 1248, the 512-wide MLP remainders
+zero-padded), so that the L and R factors of all blocks form one
+(2496, 1024, 1024) fp32 stack.  One step is the whole hot path with
+preconditioner refresh every step (f = 1):
+    accumulate (beta = 0.95, bf16 gradients) -> multi-vector power-iteration
+    scale (32 vectors, 10 products, ridge 1e-6) -> Coupled Newton inverse 4th
+    root in FP16 (10 iterations) -> preconditioned update L^-1/4 G R^-1/4 (TF32).
+value  = factor blocks (inverse 4th roots) per second over the whole step;
+ms_per_step = optimizer-step milliseconds.  Inputs (10.5 GB of factors) exceed
+L2 (129 MB) many times over, so no flush is needed between steps.
+
+--impl reference times the float64 CPU oracle instead (the only reference this
+method has here), on a bounded sample of the same workload.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+LAYERS = 24
+BS = 1024
+BETA = 0.95
+RIDGE = 1e-6
+POWER_ITERS = 10
+NVEC = 32
+CN_ITERS = 10
+NDB_ITERS = 10
+SEED = 1004
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Nominal dense ratios to bf16 (GB300): tf32 1.1 / 2.25 PFLOP/s.
+TF32_RATIO = 1.1 / 2.25
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        d["_source"] = "measured"
+        return d
+    d = dict(FALLBACK_PEAKS)
+    d["_source"] = "fallback"
+    return d
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms in the background."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------- GPU arm
+
+
+class Workload:
+    def __init__(self, torch, dr, synth, device, root_prec, ndb=False):
+        self.torch = torch
+        self.dr = dr
+        dev = device
+        G, vr, vc = synth.llama_layer_blocks(LAYERS, seed=SEED, var=1e-2, bs=BS, device=dev)
+        self.G, self.vr, self.vc = G, vr, vc
+        self.ng = G.shape[0]
+        self.nf = 2 * self.ng
+        self.F = torch.zeros((self.nf, BS, BS), dtype=torch.float32, device=dev)
+        self.Froot = torch.empty_like(self.F)
+        self.U = torch.empty((self.ng, BS, BS), dtype=torch.float32, device=dev)
+        self.V0 = synth.start_vectors(self.nf, BS, NVEC, seed=SEED + 1, device=dev)
+        self.lam = torch.empty(self.nf, dtype=torch.float32, device=dev)
+        self.root_prec = root_prec
+        self.apply_prec = dr.TF32 if root_prec in (dr.FP16, dr.BF16, dr.TF32) else dr.FP32_3XTF32
+        self.ndb = ndb
+        cap = 48 << 30
+        self.ws_scale = dr.workspace(dr.OP_SPECTRAL_SCALE, self.nf, BS, 0, NVEC, device=dev)
+        op = dr.OP_INV_ROOT_NDB if ndb else dr.OP_INV_ROOT_CN
+        self.ws_root = dr.workspace(op, self.nf, BS, root_prec, NDB_ITERS if ndb else CN_ITERS,
+                                    device=dev, max_bytes=cap)
+        self.ws_apply = dr.workspace(dr.OP_PRECONDITION_APPLY, self.ng, BS, self.apply_prec,
+                                     device=dev, max_bytes=16 << 30)
+
+    def step(self):
+        dr = self.dr
+        dr.shampoo_accumulate(self.G, self.F, BETA, self.vr, self.vc)
+        dr.spectral_scale(self.F, dr.SCALE_POWER, self.V0, POWER_ITERS, ridge=RIDGE, out=self.lam,
+                          ws=self.ws_scale)
+        if self.ndb:
+            dr.inv_root_ndb(self.F, self.lam, NDB_ITERS, self.root_prec, ridge=RIDGE, X=self.Froot,
+                            ws=self.ws_root)
+        else:
+            dr.inv_root_cn(self.F, self.lam, CN_ITERS, self.root_prec, ridge=RIDGE, X=self.Froot,
+                           ws=self.ws_root)
+        dr.precondition_apply(self.G, self.Froot, self.apply_prec, U=self.U, ws=self.ws_apply)
+
+    def free(self):
+        for k in ("G", "F", "Froot", "U", "V0", "ws_scale", "ws_root", "ws_apply"):
+            setattr(self, k, None)
+
+
+def timed_steps(torch, fn, steps, dist=None):
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        fn()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    return t0.elapsed_time(t1) / steps
+
+
+def roofline_from_trace(records, peaks):
+    by = {}
+    for kind, fl, b, ms in records:
+        e = by.setdefault(kind, [0, 0.0, 0.0, 0.0])
+        e[0] += 1
+        e[1] += fl
+        e[2] += b
+        e[3] += ms
+    total_ms = sum(v[3] for v in by.values())
+    dom = max(by, key=lambda k: by[k][3])
+    n, fl, b, ms = by[dom]
+    shares = {k: {"launches": v[0], "ms": round(v[3], 3),
+                  "share": round(v[3] / total_ms, 4) if total_ms else 0.0} for k, v in by.items()}
+    if dom.startswith("gemm"):
+        base = peaks["bf16_tflops_sustained"]
+        if dom == "gemm_tf32":
+            peak = base * TF32_RATIO
+        elif dom == "gemm_3xtf32":
+            peak = base * TF32_RATIO / 3.0
+        else:
+            peak = base
+        achieved = fl / (ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "kernel": "gemm_tc_kernel (%s)" % dom,
+                "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4),
+                "peak_note": "%s bf16 sustained%s" % (
+                    peaks["_source"], "" if dom in ("gemm_f16", "gemm_bf16")
+                    else " x nominal tf32/bf16 ratio" + (" / 3" if dom == "gemm_3xtf32" else "")),
+                "launches": n, "avg_launch_ms": round(ms / n, 4),
+                "flops_per_launch": fl / n, "traffic": None}
+    else:
+        peak = peaks["hbm_gbs"]
+        achieved = b / (ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(achieved / peak, 4), "launches": n,
+                "avg_launch_ms": round(ms / n, 4), "traffic": None}
+    return roof, shares, sum(v[0] for v in by.values())
+
+
+def cpu_sample(ng_sample, rng_seed=SEED):
+    """One oracle step on ng_sample gradient blocks (2*ng_sample factor blocks)."""
+    import oracle
+
+    rng = np.random.default_rng(rng_seed)
+    G = rng.standard_normal((ng_sample, BS, BS)) * 0.1
+    G = G.astype(np.float32).astype(np.float64)
+    F = np.zeros((2 * ng_sample, BS, BS))
+    V0 = rng.standard_normal((2 * ng_sample, BS, NVEC))
+    t0 = time.perf_counter()
+    F = oracle.accumulate(F, G, BETA)
+    lam = oracle.power_lambda(F, V0, POWER_ITERS, ridge=RIDGE)
+    X, _, _ = oracle.cn_inv_root(F, lam, CN_ITERS, ridge=RIDGE)
+    oracle.apply_preconditioner(G, X)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(ng_sample=4):
+    secs = cpu_sample(ng_sample)
+    blocks = 2 * ng_sample
+    return {"value": round(blocks / secs, 4), "unit": "blocks/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": "float64 oracle step (accumulate, 32-vector power x10, CN x10, apply) on "
+                      "%d gradient blocks = %d factor blocks of 1024^2, %.1f s; numpy BLAS on "
+                      "all host cores" % (ng_sample, blocks, secs)}
+
+
+def run_gpu(args):
+    import torch
+
+    import matrix_inverse_roots_gb300 as dr
+    import synth
+
+    rank, world, local = dist_env()
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+
+        torch.cuda.set_device(local)
+        tdist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        dist = tdist
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    dr.load_library()
+    peaks = load_peaks()
+
+    wl = Workload(torch, dr, synth, dev, dr.FP16)
+    for _ in range(args.warmup):
+        wl.step()
+    torch.cuda.synchronize()
+    # Timed region: library kernel trace on, clocks sampled.
+    launches_per_step = 250
+    dr.trace_start(launches_per_step * args.steps + 64)
+    clk = ClockSampler(dev.index)
+    clk.start()
+    ms = timed_steps(torch, wl.step, args.steps, dist)
+    clocks = clk.stop()
+    records = dr.trace_records()
+    dr.trace_stop()
+    assert dr.device_status() == 0, "device-side wait timed out"
+    roof, shares, launches = roofline_from_trace(records, peaks)
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = wl.nf * world / (ms * 1e-3)
+
+    # Root-only throughput of the same kernel chain (CN FP16 on the whole stack).
+    root_ms = timed_steps(torch, lambda: dr.inv_root_cn(wl.F, wl.lam, CN_ITERS, dr.FP16, ridge=RIDGE,
+                                                         X=wl.Froot, ws=wl.ws_root), 2)
+
+    # End to end: gradients from pinned host memory in, update back to pinned host memory.
+    G_host = torch.empty(wl.G.shape, dtype=wl.G.dtype, pin_memory=True)
+    G_host.copy_(wl.G)
+    U_host = torch.empty(wl.U.shape, dtype=wl.U.dtype, pin_memory=True)
+
+    def e2e_step():
+        wl.G.copy_(G_host, non_blocking=True)
+        wl.step()
+        U_host.copy_(wl.U, non_blocking=True)
+
+    e2e_step()
+    e2e_ms = timed_steps(torch, e2e_step, max(2, args.steps // 2), dist)
+    h2d = G_host.numel() * G_host.element_size()
+    d2h = U_host.numel() * U_host.element_size()
+    del G_host, U_host
+    wl.free()
+    torch.cuda.empty_cache()
+
+    # Same step with NDB in fp32 (3xTF32), a shorter run.
+    ndb_ms = None
+    if not args.no_ndb:
+        wn = Workload(torch, dr, synth, dev, dr.FP32_3XTF32, ndb=True)
+        wn.step()
+        ndb_ms = timed_steps(torch, wn.step, 2, dist)
+        wn.free()
+        torch.cuda.empty_cache()
+
+    line = {
+        "metric": "B=1024 inverse-4th-root blocks/sec and optimizer-step ms; % tensor-core peak",
+        "value": round(value, 2),
+        "unit": "blocks/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16",
+        "data": "synthetic",
+        "config": {
+            "workload": "llama-d2048 x24 layers: 1248 bf16 gradient blocks, (2496,1024,1024) fp32 "
+                        "factor stack; step = accumulate(beta 0.95) + power scale(32 vec x10) + "
+                        "CN fp16 x10 + apply tf32, f=1",
+            "blocks": wl.nf, "block": BS, "root": "cn-fp16", "iters": CN_ITERS,
+            "l2": "inputs 10.5 GB >> 129 MB L2, no flush",
+        },
+        "roofline": roof,
+        "kernel_shares": shares,
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "e2e": {"value": round(wl.nf * world / (e2e_ms * 1e-3), 2), "unit": "blocks/s",
+                "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "root_only_blocks_per_s": round(wl.nf / (root_ms * 1e-3), 1),
+        "ndb_fp32_step_ms": None if ndb_ms is None else round(ndb_ms, 2),
+        "peaks_source": peaks["_source"],
+    }
+    if rank == 0 and world == 1 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ reference arm
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    ng = 2
+    for _ in range(args.warmup):
+        cpu_sample(ng)
+    times = [cpu_sample(ng) for _ in range(args.steps)]
+    secs = sum(times) / len(times)
+    blocks = 2 * ng
+    value = blocks / secs
+    nf = 2 * sum(1 for _ in range(1)) * 0 + 2496
+    line = {
+        "impl": "reference",
+        "metric": "B=1024 inverse-4th-root blocks/sec and optimizer-step ms; % tensor-core peak",
+        "value": round(value, 4),
+        "unit": "blocks/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(secs * 1e3 * nf / blocks, 1),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "llama-d2048 x24 layers step (as the GPU arm), timed on a sample "
+                               "of %d gradient blocks per step; ms_per_step extrapolated to "
+                               "2496 factor blocks" % ng,
+                   "blocks": nf, "block": BS},
+        "cpu_baseline": {"value": round(value, 4), "unit": "blocks/s", "cores": os.cpu_count(),
+                         "kind": "oracle",
+                         "sample": "%d gradient blocks (%d factor blocks) per step" % (ng, blocks)},
+        "e2e": {"value": round(value, 4), "unit": "blocks/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="dash", choices=["dash", "reference"])
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--no-ndb", action="store_true", help="skip the NDB fp32 step")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

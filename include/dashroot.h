@@ -1,0 +1,255 @@
+/*
+ * dashroot: the batched block-preconditioner step of DASH-style Shampoo on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Method source: "DASH: Faster Shampoo via Batched Block Preconditioning and
+ * Efficient Inverse-Root Solvers" (arXiv 2602.02016), as summarised by
+ *   [pt]  gist.science/pt technical summary ("Definicao do Problema",
+ *         "Metodologia" 1-2, "Principais Contribuicoes", "Resultados")
+ *   [tg]  tgviewer.app, Telegram channel quant_prune_distill, post 646
+ *   [abs] arxivdaily.com, the authors' abstract
+ * The pages name the operations below and their properties but print no
+ * formulas; each entry point states the reading it implements.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Stacks.  A stack of N square blocks of order B is one contiguous row-major
+ *   (N, B, B) array; block k starts B*B elements after block k-1 ([pt]
+ *   Metodologia 1, "Empilhamento de Tensores 3D": blocks stacked into an
+ *   (N, B, B) tensor and processed together).  B must be a multiple of 128 with
+ *   128 <= B <= 2048.  N >= 0; N == 0 is a no-op returning DASH_OK.
+ * Memory.  Every pointer is caller-owned DEVICE memory unless stated
+ *   otherwise, 16-byte aligned (else DASH_ERR_INVALID_ARG).  Inputs are const
+ *   and are never written.  Outputs must not overlap inputs or the workspace,
+ *   except where an argument says "in place".
+ * Execution.  Work is enqueued on the caller's CUDA stream (a cudaStream_t
+ *   passed as void*, NULL = legacy default stream) and runs asynchronously.
+ *   No entry point allocates device memory or synchronises the stream.
+ * Workspace.  Entry points that take (ws, ws_bytes) use that caller-owned
+ *   device scratch; dash_workspace_size gives the size that lets a call
+ *   process all N blocks in one pass.  A smaller workspace is accepted as long
+ *   as it holds the per-call arrays plus one block's iterates: the call then
+ *   walks the stack in chunks of as many blocks as fit.  Too small for one
+ *   block: DASH_ERR_WORKSPACE_TOO_SMALL.  The workspace needs 256-byte
+ *   alignment.
+ * Precision.  dash_prec selects the tensor-core arithmetic of the dense
+ *   B x B x B products: DASH_FP32_3XTF32 (each fp32 operand split into two
+ *   TF32 parts, three TF32 products per tile, fp32-level accuracy),
+ *   DASH_TF32, DASH_FP16 and DASH_BF16 (operands and stored iterates in that
+ *   format).  All accumulation is fp32; every epilogue computes in fp32.
+ * Errors.  Argument errors are detected on the host before anything is
+ *   enqueued.  CUDA launch errors return DASH_ERR_CUDA.  A device-side wait
+ *   that exceeds its time limit never traps: the kernel records
+ *   DASH_ERR_TIMEOUT in a device flag and returns; dash_device_status reads
+ *   and clears that flag.  Non-finite numbers are not errors: they propagate
+ *   into the outputs and residuals.
+ */
+#ifndef DASHROOT_H
+#define DASHROOT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DASH_OK = 0,
+  DASH_ERR_INVALID_ARG = 1,
+  DASH_ERR_UNSUPPORTED = 2,
+  DASH_ERR_CUDA = 3,
+  DASH_ERR_WORKSPACE_TOO_SMALL = 4,
+  DASH_ERR_TIMEOUT = 5
+} dash_status;
+
+typedef enum {
+  DASH_FP32_3XTF32 = 0,
+  DASH_TF32 = 1,
+  DASH_FP16 = 2,
+  DASH_BF16 = 3
+} dash_prec;
+
+typedef enum { DASH_DT_F32 = 0, DASH_DT_BF16 = 1, DASH_DT_F16 = 2 } dash_dtype;
+
+typedef enum { DASH_SCALE_POWER = 0, DASH_SCALE_FROBENIUS = 1 } dash_scale_mode;
+
+typedef enum {
+  DASH_OP_ACCUMULATE = 0,
+  DASH_OP_SPECTRAL_SCALE = 1,
+  DASH_OP_INV_ROOT_CN = 2,
+  DASH_OP_INV_ROOT_NDB = 3,
+  DASH_OP_INV_ROOT_CHEB = 4,
+  DASH_OP_PRECONDITION_APPLY = 5
+} dash_op;
+
+/*
+ * shampoo_accumulate -- EMA update of the stacked Shampoo factors.
+ * Source: [tg] second paragraph (Shampoo keeps L and R built from gradient
+ * products and raises them to the -1/4 power), [tg] block-diagonal paragraph
+ * (L and R of all blocks stacked in one tensor), [pt] Metodologia 1.
+ * Reading: for every gradient block j < Ng
+ *     F[j]      <- beta F[j]      + (1 - beta) G_j G_j^T      (L_j)
+ *     F[Ng + j] <- beta F[Ng + j] + (1 - beta) G_j^T G_j      (R_j)
+ * then rows and columns >= valid_rows[j] of L_j (>= valid_cols[j] of R_j) are
+ * reset to the identity's (0 off the diagonal, 1 on it) -- the treatment of a
+ * zero-padded gradient block.
+ *   G           (Ng, B, B) gradient blocks, dtype gdt (DASH_DT_BF16 runs
+ *               bf16 tensor-core products, exact products with fp32
+ *               accumulation; DASH_DT_F32 runs 3xTF32).
+ *   F           (2*Ng, B, B) fp32 factors, updated IN PLACE.
+ *   valid_rows, valid_cols  (Ng,) int32 device arrays, or NULL (= B).
+ *   ws/ws_bytes workspace; only DASH_DT_F32 needs one (see dash_workspace_size).
+ */
+dash_status shampoo_accumulate(const void* G, int gdt, int64_t Ng, int B, float beta,
+                               float* F, const int32_t* valid_rows,
+                               const int32_t* valid_cols, void* ws, size_t ws_bytes,
+                               void* stream);
+
+/*
+ * spectral_scale -- per-block scale s_k for the iterative root solvers.
+ * Source: [pt] Metodologia 2, "Multi-Power-Iteration para Escalonamento"
+ * (lambda_max from up to 32 start vectors run in parallel), [tg] paragraph on
+ * scaling (Rayleigh-quotient estimate instead of the Frobenius norm), [pt]
+ * Definicao do Problema item 3 (Frobenius scaling).
+ *   mode DASH_SCALE_POWER: with V = V0[k] (B x n_vec, row-major, fp32), take
+ *     power_iters products W = (A_k + ridge I) V; after every product but the
+ *     last, normalise each column of W to unit 2-norm and continue with it;
+ *     after the last, lambda_out[k] = max_j (v_j . w_j) / (v_j . v_j).
+ *     1 <= n_vec <= 32, power_iters >= 1, V0 (N, B, n_vec) fp32.
+ *   mode DASH_SCALE_FROBENIUS: lambda_out[k] = ||A_k + ridge I||_F
+ *     (n_vec, power_iters, V0 ignored; may be 0 / NULL).
+ *   A (N, B, B) fp32 symmetric blocks; lambda_out (N,) fp32.
+ * Arithmetic: fp32 FMA with fp32 column sums (power); fp32 partial sums (Frobenius).
+ */
+dash_status spectral_scale(const float* A, float ridge, int64_t N, int B, int mode,
+                           int n_vec, int power_iters, const float* V0,
+                           float* lambda_out, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * inv_root_cn -- Coupled Newton inverse 4th root of every block.
+ * Source: [pt] Definicao do Problema item 2 and [tg] list item 1 (Coupled
+ * Newton, a matmul-only iteration for matrix roots).  Reading (coupled inverse
+ * p-th root iteration, p = 4): A_s = (A_k + ridge I) / scale[k];
+ *   X_0 = I, M_0 = A_s;  T_i = (5I - M_i)/4;  X_{i+1} = X_i T_i;
+ *   M_{i+1} = (T_i^2)^2 M_i;   X[k] = scale[k]^{-1/4} X_iters.
+ * 4*iters - 4 products per block for iters >= 2, none for iters = 1 (iteration 0
+ * needs no X product, the last no
+ * M update).
+ *   A (N, B, B) fp32; scale (N,) fp32 > 0 (e.g. from spectral_scale);
+ *   iters >= 1; prec any dash_prec; X (N, B, B) fp32 output;
+ *   resid_out (N, iters) fp32 or NULL: resid_out[k*iters + i] =
+ *   ||M_i - I||_F / sqrt(B), the residual ||X_i^4 A_s - I|| of iterate i.
+ */
+dash_status inv_root_cn(const float* A, float ridge, const float* scale, int64_t N, int B,
+                        int iters, int prec, float* X, float* resid_out, void* ws,
+                        size_t ws_bytes, void* stream);
+
+/*
+ * inv_root_ndb -- Newton-Denman-Beavers inverse 4th root of every block.
+ * Source: [pt] Metodologia 2, NDB bullet (yields square root and inverse
+ * square root together; first iteration trimmed; three products per step,
+ * fewer in practice), [tg] list item 2.  Reading (matmul-only Newton-Schulz
+ * form of Denman-Beavers): one stage on C runs Y_0 = C, Z_0 = I,
+ *   T_i = (3I - Z_i Y_i)/2, Y_{i+1} = Y_i T_i, Z_{i+1} = T_i Z_i;
+ * stage 1 on C = A_s keeps Y (~A_s^{1/2}); stage 2 on C = that Y keeps Z
+ * (~A_s^{-1/4}); X[k] = scale[k]^{-1/4} Z.  iters counts iterations PER STAGE;
+ * 6*iters - 6 products per block for iters >= 2 (one for iters = 1).
+ *   resid_out (N, 2, iters) fp32 or NULL: ||Z_i Y_i - I||_F / sqrt(B) per stage.
+ *   Other arguments as inv_root_cn.  Half precision runs but the pages report
+ *   it unstable ([pt] Resultados, Precisao).
+ */
+dash_status inv_root_ndb(const float* A, float ridge, const float* scale, int64_t N, int B,
+                         int iters, int prec, float* X, float* resid_out, void* ws,
+                         size_t ws_bytes, void* stream);
+
+/*
+ * inv_root_cheb -- Chebyshev/Clenshaw inverse 4th root of every block.
+ * Source: [pt] Metodologia 2, Chebyshev bullet (Clenshaw's algorithm to
+ * approximate matrix powers).  Reading: p = degree-d interpolant of x^{-1/4}
+ * at the d+1 first-kind Chebyshev points of [lo, hi] (coefficients computed on
+ * the host in double); S = (2 A_s - (lo+hi) I)/(hi - lo);
+ *   b_{d+1} = b_{d+2} = 0, b_j = c_j I + 2 S b_{j+1} - b_{j+2},
+ *   P = c_0 I + S b_1 - b_2,  X[k] = scale[k]^{-1/4} P.
+ * d - 1 products per block.  1 <= degree <= 64, 0 < lo < hi.
+ */
+dash_status inv_root_cheb(const float* A, float ridge, const float* scale, int64_t N, int B,
+                          int degree, double lo, double hi, int prec, float* X, void* ws,
+                          size_t ws_bytes, void* stream);
+
+/*
+ * precondition_apply -- the preconditioned update U_j = L_j^{-1/4} G_j R_j^{-1/4}.
+ * Source: [tg] second paragraph (the -1/4 powers of L and R precondition the
+ * gradient).  Froot (2*Ng, B, B) fp32 holds the roots in the factor order of
+ * shampoo_accumulate (L roots, then R roots).  G (Ng, B, B) of dtype gdt;
+ * U (Ng, B, B) fp32 output.  Two products per block in precision prec.
+ */
+dash_status precondition_apply(const void* G, int gdt, const float* Froot, int64_t Ng,
+                               int B, int prec, float* U, void* ws, size_t ws_bytes,
+                               void* stream);
+
+/*
+ * dash_gemm -- the batched tensor-core product the solvers are built from,
+ * exposed for tests and roofline measurement (no counterpart on the pages).
+ * C[k] = op(A[k]) op(B[k]) for k < N, op = transpose when trans_* != 0.
+ * Operands are already in the format of prec: fp32 containers for TF32 (the
+ * tensor core reads their TF32 part), fp32 hi and lo arrays for
+ * DASH_FP32_3XTF32 (A_lo / B_lo; C = hi*hi + hi*lo + lo*hi), 16-bit arrays
+ * for DASH_FP16 / DASH_BF16 (A_lo, B_lo ignored).  C (N, B, B) fp32.
+ */
+dash_status dash_gemm(const void* A, const void* A_lo, int trans_a, const void* Bm,
+                      const void* B_lo, int trans_b, int64_t N, int B, int prec, float* C,
+                      void* stream);
+
+/* Workspace bytes for op on N blocks of order B (param: iters for CN/NDB,
+ * degree for Chebyshev, n_vec for spectral_scale; gdt for accumulate/apply is
+ * taken from prec: pass DASH_FP32_3XTF32 for fp32 gradients). */
+dash_status dash_workspace_size(int op, int64_t N, int B, int prec, int param,
+                                size_t* bytes);
+
+/* Dense B x B x B products one call of op issues per block (the matmul
+ * counts stated above). */
+int64_t dash_op_matmuls(int op, int param);
+
+/*
+ * Kernel trace, for benchmarks (no counterpart on the pages).  While a trace
+ * is active, every kernel the library launches is bracketed by a pair of CUDA
+ * events recorded on the stream it is launched on, with the kernel's class and
+ * its algorithmic work.  dash_trace_start(capacity) begins a trace of up to
+ * capacity launches (events are created once and reused; further launches are
+ * not recorded); dash_trace_count() gives the number recorded so far;
+ * dash_trace_read(i, ...) waits for record i's end event and returns its class
+ * (dash_trace_kind), algorithmic flops (2 B^3 per block for a product, any
+ * precision), algorithmic bytes and device milliseconds; dash_trace_stop() ends
+ * the trace.  Host-side state, one trace per process; not thread-safe against
+ * concurrent library calls on other threads.
+ */
+typedef enum {
+  DASH_TRACE_GEMM_F16 = 0,
+  DASH_TRACE_GEMM_BF16 = 1,
+  DASH_TRACE_GEMM_TF32 = 2,
+  DASH_TRACE_GEMM_3XTF32 = 3,
+  DASH_TRACE_ELEMENTWISE = 4,
+  DASH_TRACE_POWER = 5,
+  DASH_TRACE_REDUCE = 6
+} dash_trace_kind;
+
+dash_status dash_trace_start(int capacity);
+int dash_trace_count(void);
+dash_status dash_trace_read(int i, int* kind, double* flops, double* bytes, float* ms);
+dash_status dash_trace_stop(void);
+
+/* Reads and clears the device-side error flag of the current device
+ * (DASH_OK or DASH_ERR_TIMEOUT).  Synchronises the device. */
+dash_status dash_device_status(void);
+
+const char* dash_status_string(int status);
+
+/* Library version, e.g. "dashroot 0.1 sm_103a". */
+const char* dash_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DASHROOT_H */

@@ -1,0 +1,325 @@
+"""Python binding of dashroot, the GB300 library for the batched block-preconditioner
+step of DASH-style Shampoo (factor accumulation, spectral scaling, inverse 4th
+roots by Coupled Newton / Newton-Denman-Beavers / Chebyshev-Clenshaw, and the
+preconditioned update).
+
+This module only marshals arguments: it checks tensor shapes and dtypes, passes
+raw device pointers and the current CUDA stream to the C ABI declared in
+``include/dashroot.h``, and allocates workspaces with PyTorch.  Every step of the
+computation runs in the library's CUDA kernels.  There is no fallback: if
+``libdashroot.so`` is missing the first call raises.
+"""
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdashroot.so")
+
+# dash_prec
+FP32_3XTF32 = 0
+TF32 = 1
+FP16 = 2
+BF16 = 3
+PRECISIONS = {"3xtf32": FP32_3XTF32, "fp32": FP32_3XTF32, "tf32": TF32, "fp16": FP16,
+              "bf16": BF16}
+
+# dash_dtype
+DT_F32 = 0
+DT_BF16 = 1
+DT_F16 = 2
+
+# dash_scale_mode
+SCALE_POWER = 0
+SCALE_FROBENIUS = 1
+
+# dash_op
+OP_ACCUMULATE = 0
+OP_SPECTRAL_SCALE = 1
+OP_INV_ROOT_CN = 2
+OP_INV_ROOT_NDB = 3
+OP_INV_ROOT_CHEB = 4
+OP_PRECONDITION_APPLY = 5
+
+# Exported C symbols (kept in step with include/dashroot.h).
+SYMBOLS = (
+    "shampoo_accumulate", "spectral_scale", "inv_root_cn", "inv_root_ndb", "inv_root_cheb",
+    "precondition_apply", "dash_gemm", "dash_workspace_size", "dash_op_matmuls",
+    "dash_device_status", "dash_status_string", "dash_version", "dash_trace_start",
+    "dash_trace_count", "dash_trace_read", "dash_trace_stop",
+)
+
+_lib = None
+
+
+class DashError(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        super().__init__("%s: %s" % (what, status_string(status)))
+
+
+def load_library(path=None):
+    """Load libdashroot.so (raises OSError if it was not built)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise OSError("libdashroot.so not found at %s: build it with "
+                      "`python -m matrix_inverse_roots_gb300.build`" % p)
+    lib = ctypes.CDLL(p)
+    vp, i64, i32, f32, f64, sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+                                  ctypes.c_float, ctypes.c_double, ctypes.c_size_t)
+    lib.shampoo_accumulate.argtypes = [vp, i32, i64, i32, f32, vp, vp, vp, vp, sz, vp]
+    lib.spectral_scale.argtypes = [vp, f32, i64, i32, i32, i32, i32, vp, vp, vp, sz, vp]
+    lib.inv_root_cn.argtypes = [vp, f32, vp, i64, i32, i32, i32, vp, vp, vp, sz, vp]
+    lib.inv_root_ndb.argtypes = [vp, f32, vp, i64, i32, i32, i32, vp, vp, vp, sz, vp]
+    lib.inv_root_cheb.argtypes = [vp, f32, vp, i64, i32, i32, f64, f64, i32, vp, vp, sz, vp]
+    lib.precondition_apply.argtypes = [vp, i32, vp, i64, i32, i32, vp, vp, sz, vp]
+    lib.dash_gemm.argtypes = [vp, vp, i32, vp, vp, i32, i64, i32, i32, vp, vp]
+    lib.dash_workspace_size.argtypes = [i32, i64, i32, i32, i32, ctypes.POINTER(sz)]
+    lib.dash_op_matmuls.argtypes = [i32, i32]
+    lib.dash_op_matmuls.restype = i64
+    lib.dash_device_status.argtypes = []
+    lib.dash_status_string.argtypes = [i32]
+    lib.dash_status_string.restype = ctypes.c_char_p
+    lib.dash_version.restype = ctypes.c_char_p
+    lib.dash_trace_start.argtypes = [i32]
+    lib.dash_trace_count.argtypes = []
+    lib.dash_trace_count.restype = i32
+    lib.dash_trace_read.argtypes = [i32, ctypes.POINTER(i32), ctypes.POINTER(f64),
+                                    ctypes.POINTER(f64), ctypes.POINTER(f32)]
+    lib.dash_trace_stop.argtypes = []
+    for name in ("shampoo_accumulate", "spectral_scale", "inv_root_cn", "inv_root_ndb",
+                 "inv_root_cheb", "precondition_apply", "dash_gemm", "dash_workspace_size",
+                 "dash_device_status", "dash_trace_start", "dash_trace_read", "dash_trace_stop"):
+        getattr(lib, name).restype = ctypes.c_int
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_string(status):
+    try:
+        return load_library().dash_status_string(int(status)).decode()
+    except OSError:
+        return "status %d" % status
+
+
+def _check(status, what):
+    if status != 0:
+        raise DashError(status, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _stack(t, name, dtype=torch.float32):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t
+
+
+def _gdt(t):
+    if t.dtype == torch.float32:
+        return DT_F32
+    if t.dtype == torch.bfloat16:
+        return DT_BF16
+    if t.dtype == torch.float16:
+        return DT_F16
+    raise TypeError("gradient dtype must be float32, bfloat16 or float16")
+
+
+def _prec(p):
+    if isinstance(p, str):
+        return PRECISIONS[p.lower()]
+    return int(p)
+
+
+def version():
+    return load_library().dash_version().decode()
+
+
+def workspace_size(op, n, b, prec=FP32_3XTF32, param=0):
+    out = ctypes.c_size_t(0)
+    _check(load_library().dash_workspace_size(int(op), int(n), int(b), _prec(prec), int(param),
+                                              ctypes.byref(out)), "dash_workspace_size")
+    return out.value
+
+
+def workspace(op, n, b, prec=FP32_3XTF32, param=0, device=None, max_bytes=None):
+    """Allocate a workspace with PyTorch (optionally capped at max_bytes)."""
+    nbytes = workspace_size(op, n, b, prec, param)
+    if max_bytes is not None:
+        nbytes = min(nbytes, int(max_bytes))
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device or "cuda")
+
+
+# dash_trace_kind
+TRACE_KINDS = ("gemm_f16", "gemm_bf16", "gemm_tf32", "gemm_3xtf32", "elementwise", "power",
+               "reduce")
+
+
+def trace_start(capacity=4096):
+    """Record CUDA events around every library kernel launch from now on."""
+    _check(load_library().dash_trace_start(int(capacity)), "dash_trace_start")
+
+
+def trace_stop():
+    _check(load_library().dash_trace_stop(), "dash_trace_stop")
+
+
+def trace_records():
+    """[(kind name, algorithmic flops, algorithmic bytes, device ms)] of the trace."""
+    lib = load_library()
+    out = []
+    k = ctypes.c_int(0)
+    fl = ctypes.c_double(0)
+    by = ctypes.c_double(0)
+    ms = ctypes.c_float(0)
+    for i in range(lib.dash_trace_count()):
+        _check(lib.dash_trace_read(i, ctypes.byref(k), ctypes.byref(fl), ctypes.byref(by),
+                                   ctypes.byref(ms)), "dash_trace_read")
+        out.append((TRACE_KINDS[k.value], fl.value, by.value, ms.value))
+    return out
+
+
+def op_matmuls(op, param):
+    return int(load_library().dash_op_matmuls(int(op), int(param)))
+
+
+def device_status():
+    return int(load_library().dash_device_status())
+
+
+def shampoo_accumulate(G, F, beta, valid_rows=None, valid_cols=None, ws=None):
+    """In place: F[j] <- beta F[j] + (1-beta) G_j G_j^T, F[Ng+j] likewise with G_j^T G_j."""
+    lib = load_library()
+    ng, b, _ = G.shape
+    _stack(G, "G", G.dtype)
+    _stack(F, "F")
+    if F.shape != (2 * ng, b, b):
+        raise ValueError("F must have shape (2*Ng, B, B)")
+    gdt = _gdt(G)
+    if ws is None and gdt == DT_F32:
+        ws = workspace(OP_ACCUMULATE, ng, b, FP32_3XTF32, device=G.device)
+    vr = None if valid_rows is None else _stack(valid_rows, "valid_rows", torch.int32)
+    vc = None if valid_cols is None else _stack(valid_cols, "valid_cols", torch.int32)
+    _check(lib.shampoo_accumulate(_ptr(G), gdt, ng, b, float(beta), _ptr(F), _ptr(vr), _ptr(vc),
+                                  _ptr(ws), 0 if ws is None else ws.numel(), _stream()),
+           "shampoo_accumulate")
+    return F
+
+
+def spectral_scale(A, mode=SCALE_POWER, V0=None, power_iters=10, ridge=0.0, out=None, ws=None):
+    """Per-block scale: multi-vector power-iteration lambda_max or Frobenius norm."""
+    lib = load_library()
+    _stack(A, "A")
+    n, b, _ = A.shape
+    nv = 0
+    if mode == SCALE_POWER:
+        _stack(V0, "V0")
+        if V0.shape[0] != n or V0.shape[1] != b:
+            raise ValueError("V0 must have shape (N, B, n_vec)")
+        nv = V0.shape[2]
+    if out is None:
+        out = torch.empty(n, dtype=torch.float32, device=A.device)
+    if ws is None:
+        ws = workspace(OP_SPECTRAL_SCALE, n, b, FP32_3XTF32, nv, device=A.device)
+    _check(lib.spectral_scale(_ptr(A), float(ridge), n, b, int(mode), nv, int(power_iters),
+                              _ptr(V0), _ptr(out), _ptr(ws), ws.numel(), _stream()),
+           "spectral_scale")
+    return out
+
+
+def _root_common(A, scale, X):
+    _stack(A, "A")
+    n, b, _ = A.shape
+    _stack(scale, "scale")
+    if scale.shape != (n,):
+        raise ValueError("scale must have shape (N,)")
+    if X is None:
+        X = torch.empty_like(A)
+    _stack(X, "X")
+    return n, b, X
+
+
+def inv_root_cn(A, scale, iters=10, prec=FP32_3XTF32, ridge=0.0, X=None, resid=False, ws=None):
+    """Coupled Newton A^{-1/4}; returns X or (X, resid (N, iters))."""
+    lib = load_library()
+    n, b, X = _root_common(A, scale, X)
+    p = _prec(prec)
+    r = torch.empty((n, iters), dtype=torch.float32, device=A.device) if resid else None
+    if ws is None:
+        ws = workspace(OP_INV_ROOT_CN, n, b, p, iters, device=A.device)
+    _check(lib.inv_root_cn(_ptr(A), float(ridge), _ptr(scale), n, b, int(iters), p, _ptr(X),
+                           _ptr(r), _ptr(ws), ws.numel(), _stream()), "inv_root_cn")
+    return (X, r) if resid else X
+
+
+def inv_root_ndb(A, scale, iters=10, prec=FP32_3XTF32, ridge=0.0, X=None, resid=False, ws=None):
+    """Newton-Denman-Beavers A^{-1/4}; returns X or (X, resid (N, 2, iters))."""
+    lib = load_library()
+    n, b, X = _root_common(A, scale, X)
+    p = _prec(prec)
+    r = torch.empty((n, 2, iters), dtype=torch.float32, device=A.device) if resid else None
+    if ws is None:
+        ws = workspace(OP_INV_ROOT_NDB, n, b, p, iters, device=A.device)
+    _check(lib.inv_root_ndb(_ptr(A), float(ridge), _ptr(scale), n, b, int(iters), p, _ptr(X),
+                            _ptr(r), _ptr(ws), ws.numel(), _stream()), "inv_root_ndb")
+    return (X, r) if resid else X
+
+
+def inv_root_cheb(A, scale, degree=16, lo=1e-2, hi=1.05, prec=FP32_3XTF32, ridge=0.0, X=None,
+                  ws=None):
+    """Chebyshev-Clenshaw A^{-1/4} of degree `degree` on [lo, hi]."""
+    lib = load_library()
+    n, b, X = _root_common(A, scale, X)
+    p = _prec(prec)
+    if ws is None:
+        ws = workspace(OP_INV_ROOT_CHEB, n, b, p, degree, device=A.device)
+    _check(lib.inv_root_cheb(_ptr(A), float(ridge), _ptr(scale), n, b, int(degree), float(lo),
+                             float(hi), p, _ptr(X), _ptr(ws), ws.numel(), _stream()),
+           "inv_root_cheb")
+    return X
+
+
+def precondition_apply(G, Froot, prec=FP32_3XTF32, U=None, ws=None):
+    """U_j = Froot[j] G_j Froot[Ng + j]."""
+    lib = load_library()
+    _stack(G, "G", G.dtype)
+    ng, b, _ = G.shape
+    _stack(Froot, "Froot")
+    if Froot.shape != (2 * ng, b, b):
+        raise ValueError("Froot must have shape (2*Ng, B, B)")
+    p = _prec(prec)
+    if U is None:
+        U = torch.empty((ng, b, b), dtype=torch.float32, device=G.device)
+    if ws is None:
+        ws = workspace(OP_PRECONDITION_APPLY, ng, b, p, device=G.device)
+    _check(lib.precondition_apply(_ptr(G), _gdt(G), _ptr(Froot), ng, b, p, _ptr(U), _ptr(ws),
+                                  ws.numel(), _stream()), "precondition_apply")
+    return U
+
+
+def gemm(A, B, prec=TF32, trans_a=False, trans_b=False, A_lo=None, B_lo=None, C=None):
+    """C[k] = op(A[k]) op(B[k]) on the tensor cores; operands already in prec's format."""
+    lib = load_library()
+    p = _prec(prec)
+    n, b, _ = A.shape
+    if C is None:
+        C = torch.empty((n, b, b), dtype=torch.float32, device=A.device)
+    _check(lib.dash_gemm(_ptr(A), _ptr(A_lo), int(bool(trans_a)), _ptr(B), _ptr(B_lo),
+                         int(bool(trans_b)), n, b, p, _ptr(C), _stream()), "dash_gemm")
+    return C

@@ -1,0 +1,818 @@
+// C-ABI entry points of dashroot: argument checks, workspace carving, chunking
+// over the block stack, and the launch sequences of the four hot-path steps.
+// The arithmetic lives in gemm_tc.cu (dense products, fused epilogues) and
+// elementwise.cu (prologues, reductions, power iteration).
+#include <cmath>
+#include <cstring>
+#include <vector>
+
+#include "dash_common.cuh"
+#include "dash_internal.h"
+#include "dashroot.h"
+
+using namespace dash;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool valid_dim(int B) { return B >= 128 && B <= 2048 && (B % 128) == 0; }
+
+bool valid_prec(int prec) { return prec >= DASH_FP32_3XTF32 && prec <= DASH_BF16; }
+
+int prec_fmt(int prec) {
+  switch (prec) {
+    case DASH_FP32_3XTF32: return FMT_SPLIT;
+    case DASH_TF32: return FMT_TF32;
+    case DASH_FP16: return FMT_F16;
+    default: return FMT_BF16;
+  }
+}
+
+int prec_kind(int prec) {
+  switch (prec) {
+    case DASH_FP32_3XTF32: return KIND_TF32X3;
+    case DASH_TF32: return KIND_TF32;
+    case DASH_FP16: return KIND_F16;
+    default: return KIND_BF16;
+  }
+}
+
+// Bytes one B x B operand-format matrix takes (both halves for the split format).
+size_t operand_bytes(int prec, int B) {
+  const size_t e = (prec == DASH_FP32_3XTF32) ? 8 : (prec == DASH_TF32 ? 4 : 2);
+  return e * static_cast<size_t>(B) * B;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// A stack of nblocks operand-format matrices inside the workspace.
+struct Buf {
+  void* hi = nullptr;
+  void* lo = nullptr;
+};
+
+struct Carver {
+  char* p;
+  size_t left;
+  bool ok = true;
+  Carver(void* ws, size_t bytes) : p(static_cast<char*>(ws)), left(bytes) {}
+  void* take(size_t bytes) {
+    bytes = round256(bytes);
+    if (bytes > left || p == nullptr) {
+      ok = false;
+      return nullptr;
+    }
+    void* r = p;
+    p += bytes;
+    left -= bytes;
+    return r;
+  }
+  Buf take_buf(int prec, int B, long long nblk) {
+    Buf b;
+    const size_t elems = static_cast<size_t>(B) * B * nblk;
+    if (prec == DASH_FP32_3XTF32) {
+      b.hi = take(elems * 4);
+      b.lo = take(elems * 4);
+    } else {
+      b.hi = take(elems * (prec == DASH_TF32 ? 4 : 2));
+    }
+    return b;
+  }
+};
+
+// Per-block bytes of the operand buffers, rounded the way the carver rounds
+// them when a chunk holds nblk blocks (used to size chunks).
+size_t bufs_bytes(int prec, int B, long long nblk, int nbufs) {
+  const size_t elems = static_cast<size_t>(B) * B * nblk;
+  size_t one = (prec == DASH_FP32_3XTF32) ? 2 * round256(elems * 4)
+                                          : round256(elems * (prec == DASH_TF32 ? 4 : 2));
+  return one * nbufs;
+}
+
+// Largest chunk (<= N blocks) whose operand buffers fit in `avail` bytes.
+long long fit_chunk(int prec, int B, long long N, int nbufs, size_t avail) {
+  if (nbufs == 0) return N;
+  const size_t per = operand_bytes(prec, B) * nbufs;
+  long long c = static_cast<long long>(avail / per);
+  if (c > N) c = N;
+  while (c > 0 && bufs_bytes(prec, B, c, nbufs) > avail) --c;
+  return c;
+}
+
+template <typename T>
+T* offset_blocks(T* p, long long blocks, int B, size_t esize) {
+  return reinterpret_cast<T*>(reinterpret_cast<char*>(p) +
+                              static_cast<size_t>(blocks) * B * B * esize);
+}
+
+template <typename T>
+const T* offset_blocks(const T* p, long long blocks, int B, size_t esize) {
+  return reinterpret_cast<const T*>(reinterpret_cast<const char*>(p) +
+                                    static_cast<size_t>(blocks) * B * B * esize);
+}
+
+#define DASH_TRY(expr)                \
+  do {                                \
+    dash_status _s = (expr);          \
+    if (_s != DASH_OK) return _s;     \
+  } while (0)
+
+EpiParams epi_none() {
+  EpiParams e;
+  std::memset(&e, 0, sizeof(e));
+  return e;
+}
+
+EpiOut eout(const Buf& b, int fmt, float alpha, float gamma, float eps = 0.0f,
+            const float* mult = nullptr) {
+  EpiOut o;
+  o.hi = b.hi;
+  o.lo = b.lo;
+  o.mult = mult;
+  o.alpha = alpha;
+  o.gamma = gamma;
+  o.eps = eps;
+  o.fmt = fmt;
+  return o;
+}
+
+EpiOut eout_f32(float* p, float alpha, float gamma, float eps, const float* mult) {
+  Buf b;
+  b.hi = p;
+  return eout(b, FMT_F32, alpha, gamma, eps, mult);
+}
+
+AffOut aout(const Buf& b, int fmt, float alpha, float gamma, const float* mult = nullptr) {
+  AffOut o;
+  o.hi = b.hi;
+  o.lo = b.lo;
+  o.mult = mult;
+  o.alpha = alpha;
+  o.gamma = gamma;
+  o.fmt = fmt;
+  return o;
+}
+
+AffParams aff_from(const void* src_hi, const void* src_lo, int src_fmt, int B, long long n) {
+  AffParams a;
+  std::memset(&a, 0, sizeof(a));
+  a.src_hi = src_hi;
+  a.src_lo = src_lo;
+  a.src_fmt = src_fmt;
+  a.dim = B;
+  a.nblocks = n;
+  return a;
+}
+
+// One GEMM launch C = X * Y over nc blocks in precision prec.
+dash_status gemm(int prec, int B, long long nc, const Buf& X, int tX, const Buf& Y, int tY,
+                 const EpiParams& e, cudaStream_t st) {
+  GemmLaunch g;
+  g.kind = prec_kind(prec);
+  g.dim = B;
+  g.nblocks = nc;
+  g.A = X.hi;
+  g.A_lo = X.lo;
+  g.transA = tX;
+  g.B = Y.hi;
+  g.B_lo = Y.lo;
+  g.transB = tY;
+  g.epi = e;
+  return launch_gemm(g, st);
+}
+
+// Small per-call arrays shared by the root solvers.
+struct RootSmall {
+  float* inv_s;
+  float* s_m14;
+  float* racc;
+};
+
+size_t root_small_bytes(long long N, long long nres) {
+  return round256(N * 4) * 2 + round256(static_cast<size_t>(nres > 0 ? nres : 1) * 4);
+}
+
+dash_status common_root_checks(const float* A, const float* scale, long long N, int B, int iters,
+                               int prec, const float* X, const void* ws) {
+  if (N < 0 || !valid_dim(B) || !valid_prec(prec) || iters < 1) return DASH_ERR_INVALID_ARG;
+  if (N == 0) return DASH_OK;
+  if (!A || !scale || !X || !aligned16(A) || !aligned16(X) || !aligned16(scale))
+    return DASH_ERR_INVALID_ARG;
+  if (ws && (reinterpret_cast<uintptr_t>(ws) & 255u)) return DASH_ERR_INVALID_ARG;
+  return DASH_OK;
+}
+
+constexpr int CN_BUFS = 7;
+constexpr int NDB_BUFS = 6;
+constexpr int CHEB_BUFS = 4;
+constexpr int APPLY_BUFS = 4;
+
+}  // namespace
+
+// ============================================================================ API
+
+extern "C" {
+
+const char* dash_status_string(int s) {
+  switch (s) {
+    case DASH_OK: return "DASH_OK";
+    case DASH_ERR_INVALID_ARG: return "DASH_ERR_INVALID_ARG: invalid argument";
+    case DASH_ERR_UNSUPPORTED: return "DASH_ERR_UNSUPPORTED: unsupported configuration";
+    case DASH_ERR_CUDA: return "DASH_ERR_CUDA: CUDA runtime or launch error";
+    case DASH_ERR_WORKSPACE_TOO_SMALL: return "DASH_ERR_WORKSPACE_TOO_SMALL: workspace too small";
+    case DASH_ERR_TIMEOUT: return "DASH_ERR_TIMEOUT: a device-side wait timed out";
+    default: return "unknown dash_status";
+  }
+}
+
+const char* dash_version(void) { return "dashroot 0.1 sm_103a"; }
+
+dash_status dash_device_status(void) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return DASH_ERR_CUDA;
+  const int a = gemm_read_clear_error();
+  const int b = elementwise_read_clear_error();
+  if (a < 0 || b < 0) return DASH_ERR_CUDA;
+  if (a == DASH_ERR_TIMEOUT || b == DASH_ERR_TIMEOUT) return DASH_ERR_TIMEOUT;
+  return DASH_OK;
+}
+
+int64_t dash_op_matmuls(int op, int param) {
+  switch (op) {
+    case DASH_OP_ACCUMULATE: return 2;  // one per factor, L and R
+    case DASH_OP_INV_ROOT_CN: return param <= 1 ? 0 : 4LL * param - 4;
+    case DASH_OP_INV_ROOT_NDB: return param <= 1 ? 1 : 6LL * param - 6;
+    case DASH_OP_INV_ROOT_CHEB: return param <= 1 ? 0 : param - 1;
+    case DASH_OP_PRECONDITION_APPLY: return 2;
+    default: return 0;
+  }
+}
+
+dash_status dash_workspace_size(int op, int64_t N, int B, int prec, int param, size_t* bytes) {
+  if (!bytes || N < 0 || !valid_dim(B) || !valid_prec(prec)) return DASH_ERR_INVALID_ARG;
+  size_t s = 0;
+  switch (op) {
+    case DASH_OP_ACCUMULATE:
+      // fp32 gradients are split into TF32 hi/lo (prec DASH_FP32_3XTF32); others need none.
+      s = (prec == DASH_FP32_3XTF32) ? bufs_bytes(DASH_FP32_3XTF32, B, N, 1) : 0;
+      break;
+    case DASH_OP_SPECTRAL_SCALE:
+      s = 2 * round256(static_cast<size_t>(N) * B * 32 * 4) + 3 * round256(N * 32 * 4) + 256;
+      break;
+    case DASH_OP_INV_ROOT_CN:
+      s = root_small_bytes(N, N * (param > 0 ? param : 1)) + bufs_bytes(prec, B, N, CN_BUFS);
+      break;
+    case DASH_OP_INV_ROOT_NDB:
+      s = root_small_bytes(N, 2 * N * (param > 0 ? param : 1)) + bufs_bytes(prec, B, N, NDB_BUFS);
+      break;
+    case DASH_OP_INV_ROOT_CHEB:
+      s = root_small_bytes(N, 0) + bufs_bytes(prec, B, N, CHEB_BUFS);
+      break;
+    case DASH_OP_PRECONDITION_APPLY:
+      s = bufs_bytes(prec, B, N, APPLY_BUFS);
+      break;
+    default:
+      return DASH_ERR_INVALID_ARG;
+  }
+  *bytes = s;
+  return DASH_OK;
+}
+
+dash_status dash_gemm(const void* A, const void* A_lo, int trans_a, const void* Bm,
+                      const void* B_lo, int trans_b, int64_t N, int B, int prec, float* C,
+                      void* stream) {
+  if (N < 0 || !valid_dim(B) || !valid_prec(prec)) return DASH_ERR_INVALID_ARG;
+  if (N == 0) return DASH_OK;
+  if (!A || !Bm || !C || !aligned16(A) || !aligned16(Bm) || !aligned16(C))
+    return DASH_ERR_INVALID_ARG;
+  if (prec == DASH_FP32_3XTF32 && (!A_lo || !B_lo || !aligned16(A_lo) || !aligned16(B_lo)))
+    return DASH_ERR_INVALID_ARG;
+  Buf X, Y;
+  X.hi = const_cast<void*>(A);
+  X.lo = const_cast<void*>(A_lo);
+  Y.hi = const_cast<void*>(Bm);
+  Y.lo = const_cast<void*>(B_lo);
+  EpiParams e = epi_none();
+  e.nout = 1;
+  e.out[0] = eout_f32(C, 1.0f, 0.0f, 0.0f, nullptr);
+  return gemm(prec, B, N, X, trans_a, Y, trans_b, e, static_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------- accumulate
+
+dash_status shampoo_accumulate(const void* G, int gdt, int64_t Ng, int B, float beta, float* F,
+                               const int32_t* valid_rows, const int32_t* valid_cols, void* ws,
+                               size_t ws_bytes, void* stream) {
+  if (Ng < 0 || !valid_dim(B) || !(gdt == DASH_DT_F32 || gdt == DASH_DT_BF16 || gdt == DASH_DT_F16))
+    return DASH_ERR_INVALID_ARG;
+  if (!(beta >= 0.0f && beta <= 1.0f)) return DASH_ERR_INVALID_ARG;
+  if (Ng == 0) return DASH_OK;
+  if (!G || !F || !aligned16(G) || !aligned16(F)) return DASH_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int gprec = (gdt == DASH_DT_F32) ? DASH_FP32_3XTF32 : (gdt == DASH_DT_BF16 ? DASH_BF16 : DASH_FP16);
+  long long chunk = Ng;
+  Buf split;
+  if (gdt == DASH_DT_F32) {
+    if (ws && (reinterpret_cast<uintptr_t>(ws) & 255u)) return DASH_ERR_INVALID_ARG;
+    chunk = fit_chunk(gprec, B, Ng, 1, ws ? ws_bytes : 0);
+    if (chunk < 1) return DASH_ERR_WORKSPACE_TOO_SMALL;
+    Carver cv(ws, ws_bytes);
+    split = cv.take_buf(gprec, B, chunk);
+    if (!cv.ok) return DASH_ERR_WORKSPACE_TOO_SMALL;
+  }
+  const size_t gsz = (gdt == DASH_DT_F32) ? 4 : 2;
+  for (long long c0 = 0; c0 < Ng; c0 += chunk) {
+    const long long nc = (Ng - c0 < chunk) ? Ng - c0 : chunk;
+    Buf g;
+    const void* gsrc = offset_blocks(static_cast<const char*>(G), c0, B, gsz);
+    if (gdt == DASH_DT_F32) {
+      AffParams a = aff_from(gsrc, nullptr, FMT_F32, B, nc);
+      a.nout = 1;
+      a.out[0] = aout(split, FMT_SPLIT, 1.0f, 0.0f);
+      DASH_TRY(launch_affine(a, st));
+      g = split;
+    } else {
+      g.hi = const_cast<void*>(gsrc);
+    }
+    float* FL = offset_blocks(F, c0, B, 4);
+    float* FR = offset_blocks(F, Ng + c0, B, 4);
+    EpiParams e = epi_none();
+    e.nout = 1;
+    e.E_fmt = FMT_F32;
+    // L_j = beta L_j + (1 - beta) G G^T
+    e.out[0] = eout_f32(FL, 1.0f - beta, 0.0f, beta, nullptr);
+    e.E_hi = FL;
+    e.pad_valid = valid_rows ? valid_rows + c0 : nullptr;
+    DASH_TRY(gemm(gprec, B, nc, g, 0, g, 1, e, st));
+    // R_j = beta R_j + (1 - beta) G^T G
+    e.out[0] = eout_f32(FR, 1.0f - beta, 0.0f, beta, nullptr);
+    e.E_hi = FR;
+    e.pad_valid = valid_cols ? valid_cols + c0 : nullptr;
+    DASH_TRY(gemm(gprec, B, nc, g, 1, g, 0, e, st));
+  }
+  return DASH_OK;
+}
+
+// ---------------------------------------------------------------- scaling
+
+dash_status spectral_scale(const float* A, float ridge, int64_t N, int B, int mode, int n_vec,
+                           int power_iters, const float* V0, float* lambda_out, void* ws,
+                           size_t ws_bytes, void* stream) {
+  if (N < 0 || !valid_dim(B)) return DASH_ERR_INVALID_ARG;
+  if (mode != DASH_SCALE_POWER && mode != DASH_SCALE_FROBENIUS) return DASH_ERR_INVALID_ARG;
+  if (mode == DASH_SCALE_POWER && (n_vec < 1 || n_vec > 32 || power_iters < 1 || !V0))
+    return DASH_ERR_INVALID_ARG;
+  if (N == 0) return DASH_OK;
+  if (!A || !lambda_out || !aligned16(A)) return DASH_ERR_INVALID_ARG;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return DASH_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (mode == DASH_SCALE_FROBENIUS) {
+    Carver cv(ws, ws_bytes);
+    float* acc = static_cast<float*>(cv.take(static_cast<size_t>(N) * 4));
+    if (!cv.ok) return DASH_ERR_WORKSPACE_TOO_SMALL;
+    if (cudaMemsetAsync(acc, 0, static_cast<size_t>(N) * 4, st) != cudaSuccess) return DASH_ERR_CUDA;
+    DASH_TRY(launch_frob_acc(A, ridge, B, N, acc, st));
+    return launch_sqrt_scale(acc, lambda_out, N, 1.0f, st);
+  }
+  // Power iteration, chunked so each chunk's vectors fit in the workspace.
+  const size_t per_blk = 2 * static_cast<size_t>(B) * 32 * 4 + 3 * 32 * 4;
+  long long chunk = static_cast<long long>(ws_bytes / (per_blk + 64));
+  if (chunk > N) chunk = N;
+  if (chunk > 65535) chunk = 65535;
+  while (chunk > 0) {
+    const size_t need = 2 * round256(static_cast<size_t>(chunk) * B * 32 * 4) +
+                        3 * round256(static_cast<size_t>(chunk) * 32 * 4);
+    if (need <= ws_bytes) break;
+    --chunk;
+  }
+  if (chunk < 1) return DASH_ERR_WORKSPACE_TOO_SMALL;
+  Carver cv(ws, ws_bytes);
+  float* V[2];
+  V[0] = static_cast<float*>(cv.take(static_cast<size_t>(chunk) * B * 32 * 4));
+  V[1] = static_cast<float*>(cv.take(static_cast<size_t>(chunk) * B * 32 * 4));
+  float* nrm[2];
+  nrm[0] = static_cast<float*>(cv.take(static_cast<size_t>(chunk) * 32 * 4));
+  nrm[1] = static_cast<float*>(cv.take(static_cast<size_t>(chunk) * 32 * 4));
+  float* den = static_cast<float*>(cv.take(static_cast<size_t>(chunk) * 32 * 4));
+  if (!cv.ok) return DASH_ERR_WORKSPACE_TOO_SMALL;
+  const size_t acc_bytes = static_cast<size_t>(chunk) * 32 * 4;
+  for (long long c0 = 0; c0 < N; c0 += chunk) {
+    const long long nc = (N - c0 < chunk) ? N - c0 : chunk;
+    const float* Ac = offset_blocks(A, c0, B, 4);
+    const float* vin = V0 + static_cast<size_t>(c0) * B * n_vec;
+    int vstride = n_vec;
+    const float* in_n = nullptr;
+    int cur = 0;
+    for (int it = 0; it < power_iters; ++it) {
+      const int last = (it == power_iters - 1);
+      if (cudaMemsetAsync(nrm[cur], 0, acc_bytes, st) != cudaSuccess) return DASH_ERR_CUDA;
+      if (last && cudaMemsetAsync(den, 0, acc_bytes, st) != cudaSuccess) return DASH_ERR_CUDA;
+      DASH_TRY(launch_power_step(Ac, ridge, B, nc, vin, vstride, n_vec, in_n, V[cur], nrm[cur],
+                                 den, last, st));
+      vin = V[cur];
+      vstride = 32;
+      in_n = nrm[cur];
+      cur ^= 1;
+    }
+    // After the loop the last step's numerators sit in nrm[cur ^ 1].
+    DASH_TRY(launch_power_finish(nrm[cur ^ 1], den, n_vec, nc, lambda_out + c0, st));
+  }
+  return DASH_OK;
+}
+
+// ---------------------------------------------------------------- Coupled Newton
+
+dash_status inv_root_cn(const float* A, float ridge, const float* scale, int64_t N, int B,
+                        int iters, int prec, float* X, float* resid_out, void* ws,
+                        size_t ws_bytes, void* stream) {
+  DASH_TRY(common_root_checks(A, scale, N, B, iters, prec, X, ws));
+  if (N == 0) return DASH_OK;
+  if (resid_out && !aligned16(resid_out)) return DASH_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int K = iters;
+  const int fmt = prec_fmt(prec);
+  Carver cv(ws, ws_bytes);
+  RootSmall sm;
+  sm.inv_s = static_cast<float*>(cv.take(N * 4));
+  sm.s_m14 = static_cast<float*>(cv.take(N * 4));
+  sm.racc = static_cast<float*>(cv.take(static_cast<size_t>(N) * K * 4));
+  if (!cv.ok) return DASH_ERR_WORKSPACE_TOO_SMALL;
+  const int nbufs = (K >= 2) ? CN_BUFS : 0;
+  const long long chunk = fit_chunk(prec, B, N, nbufs, cv.left);
+  if (chunk < 1) return DASH_ERR_WORKSPACE_TOO_SMALL;
+  Buf bx[2], bm[2], bT, bT2, bT4;
+  if (K >= 2) {
+    bx[0] = cv.take_buf(prec, B, chunk);
+    bx[1] = cv.take_buf(prec, B, chunk);
+    bm[0] = cv.take_buf(prec, B, chunk);
+    bm[1] = cv.take_buf(prec, B, chunk);
+    bT = cv.take_buf(prec, B, chunk);
+    bT2 = cv.take_buf(prec, B, chunk);
+    bT4 = cv.take_buf(prec, B, chunk);
+    if (!cv.ok) return DASH_ERR_WORKSPACE_TOO_SMALL;
+  }
+  DASH_TRY(launch_scale_factors(scale, sm.inv_s, sm.s_m14, N, st));
+  if (resid_out &&
+      cudaMemsetAsync(sm.racc, 0, static_cast<size_t>(N) * K * 4, st) != cudaSuccess)
+    return DASH_ERR_CUDA;
+
+  for (long long c0 = 0; c0 < N; c0 += chunk) {
+    const long long nc = (N - c0 < chunk) ? N - c0 : chunk;
+    const float* Ac = offset_blocks(A, c0, B, 4);
+    float* Xc = offset_blocks(X, c0, B, 4);
+    const float* inv_s = sm.inv_s + c0;
+    const float* m14 = sm.s_m14 + c0;
+    float* racc = resid_out ? sm.racc + c0 * K : nullptr;
+    // Prologue: M_0 = A_s, T_0 = (5I - A_s)/4, X_1 = T_0; residual of M_0.
+    AffParams a = aff_from(Ac, nullptr, FMT_F32, B, nc);
+    a.ridge = ridge;
+    a.inv_s = inv_s;
+    a.resid_acc = racc;
+    a.resid_stride = K;
+    if (K == 1) {
+      a.nout = 1;
+      Buf xb;
+      xb.hi = Xc;
+      a.out[0] = aout(xb, FMT_F32, -0.25f, 1.25f, m14);
+      DASH_TRY(launch_affine(a, st));
+      continue;
+    }
+    a.nout = 3;
+    a.out[0] = aout(bm[0], fmt, 1.0f, 0.0f);
+    a.out[1] = aout(bT, fmt, -0.25f, 1.25f);
+    a.out[2] = aout(bx[0], fmt, -0.25f, 1.25f);
+    DASH_TRY(launch_affine(a, st));
+    int mc = 0, xc = 0;
+    for (int k = 0; k < K; ++k) {
+      if (k == K - 1) {
+        // X_K = X_{K-1} T_{K-1}, scaled by s^{-1/4}, into the caller's fp32 output.
+        EpiParams e = epi_none();
+        e.nout = 1;
+        e.out[0] = eout_f32(Xc, 1.0f, 0.0f, 0.0f, m14);
+        DASH_TRY(gemm(prec, B, nc, bx[xc], 0, bT, 0, e, st));
+        break;
+      }
+      if (k >= 1) {
+        EpiParams e = epi_none();
+        e.nout = 1;
+        e.out[0] = eout(bx[xc ^ 1], fmt, 1.0f, 0.0f);
+        DASH_TRY(gemm(prec, B, nc, bx[xc], 0, bT, 0, e, st));
+        xc ^= 1;
+      }
+      EpiParams e2 = epi_none();
+      e2.nout = 1;
+      e2.out[0] = eout(bT2, fmt, 1.0f, 0.0f);
+      DASH_TRY(gemm(prec, B, nc, bT, 0, bT, 0, e2, st));
+      e2.out[0] = eout(bT4, fmt, 1.0f, 0.0f);
+      DASH_TRY(gemm(prec, B, nc, bT2, 0, bT2, 0, e2, st));
+      // M_{k+1} = T^4 M_k; the same epilogue forms T_{k+1} and the residual of M_{k+1}.
+      EpiParams em = epi_none();
+      em.nout = 2;
+      em.out[0] = eout(bm[mc ^ 1], fmt, 1.0f, 0.0f);
+      em.out[1] = eout(bT, fmt, -0.25f, 1.25f);
+      em.resid_acc = racc ? racc + (k + 1) : nullptr;
+      em.resid_stride = K;
+      DASH_TRY(gemm(prec, B, nc, bT4, 0, bm[mc], 0, em, st));
+      mc ^= 1;
+    }
+  }
+  if (resid_out)
+    DASH_TRY(launch_sqrt_scale(sm.racc, resid_out, N * K, 1.0f / std::sqrt(static_cast<float>(B)), st));
+  return DASH_OK;
+}
+
+// ---------------------------------------------------------------- Newton-Denman-Beavers
+
+dash_status inv_root_ndb(const float* A, float ridge, const float* scale, int64_t N, int B,
+                         int iters, int prec, float* X, float* resid_out, void* ws,
+                         size_t ws_bytes, void* stream) {
+  DASH_TRY(common_root_checks(A, scale, N, B, iters, prec, X, ws));
+  if (N == 0) return DASH_OK;
+  if (resid_out && !aligned16(resid_out)) return DASH_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int K = iters;
+  const int fmt = prec_fmt(prec);
+  Carver cv(ws, ws_bytes);
+  RootSmall sm;
+  sm.inv_s = static_cast<float*>(cv.take(N * 4));
+  sm.s_m14 = static_cast<float*>(cv.take(N * 4));
+  sm.racc = static_cast<float*>(cv.take(static_cast<size_t>(N) * 2 * K * 4));
+  if (!cv.ok) return DASH_ERR_WORKSPACE_TOO_SMALL;
+  const long long chunk = fit_chunk(prec, B, N, NDB_BUFS, cv.left);
+  if (chunk < 1) return DASH_ERR_WORKSPACE_TOO_SMALL;
+  Buf pool[NDB_BUFS];
+  for (int i = 0; i < NDB_BUFS; ++i) pool[i] = cv.take_buf(prec, B, chunk);
+  if (!cv.ok) return DASH_ERR_WORKSPACE_TOO_SMALL;
+  DASH_TRY(launch_scale_factors(scale, sm.inv_s, sm.s_m14, N, st));
+  if (resid_out &&
+      cudaMemsetAsync(sm.racc, 0, static_cast<size_t>(N) * 2 * K * 4, st) != cudaSuccess)
+    return DASH_ERR_CUDA;
+
+  for (long long c0 = 0; c0 < N; c0 += chunk) {
+    const long long nc = (N - c0 < chunk) ? N - c0 : chunk;
+    const float* Ac = offset_blocks(A, c0, B, 4);
+    float* Xc = offset_blocks(X, c0, B, 4);
+    Buf Xout;
+    Xout.hi = Xc;
+    const float* inv_s = sm.inv_s + c0;
+    const float* m14 = sm.s_m14 + c0;
+    float* racc = resid_out ? sm.racc + c0 * 2 * K : nullptr;
+    const long long rstride = 2LL * K;
+    // Buffer roles are indices into pool; `used` marks buffers holding live data.
+    int iC = 0, iT = 1, iZ = 2;
+    // Stage-1 prologue: C = A_s, T_0 = (3I - A_s)/2, Z_1 = T_0, residual of C.
+    AffParams a = aff_from(Ac, nullptr, FMT_F32, B, nc);
+    a.ridge = ridge;
+    a.inv_s = inv_s;
+    a.resid_acc = racc;
+    a.resid_stride = rstride;
+    a.nout = 3;
+    a.out[0] = aout(pool[iC], fmt, 1.0f, 0.0f);
+    a.out[1] = aout(pool[iT], fmt, -0.5f, 1.5f);
+    a.out[2] = aout(pool[iZ], fmt, -0.5f, 1.5f);
+    DASH_TRY(launch_affine(a, st));
+
+    for (int stage = 0; stage < 2; ++stage) {
+      // Live: C (= Y_0) in iC, T_0 in iT, Z_1 = T_0 in iZ.
+      int iY = iC;
+      auto free_buf = [&](int a0, int a1, int a2) {
+        for (int i = 0; i < NDB_BUFS; ++i)
+          if (i != a0 && i != a1 && i != a2) return i;
+        return -1;
+      };
+      float* racc_s = racc ? racc + stage * K : nullptr;
+      const bool keepY = (stage == 0);
+      for (int k = 0; k < K; ++k) {
+        const bool lastk = (k == K - 1);
+        if (k >= 1) {
+          // P = Z_k Y_k -> T_k = (3I - P)/2 and the residual of P.
+          EpiParams ep = epi_none();
+          ep.nout = 1;
+          ep.out[0] = eout(pool[iT], fmt, -0.5f, 1.5f);
+          ep.resid_acc = racc_s ? racc_s + k : nullptr;
+          ep.resid_stride = rstride;
+          DASH_TRY(gemm(prec, B, nc, pool[iZ], 0, pool[iY], 0, ep, st));
+        }
+        if (!lastk) {
+          const int iYn = free_buf(iY, iZ, iT);
+          EpiParams ey = epi_none();
+          ey.nout = 1;
+          ey.out[0] = eout(pool[iYn], fmt, 1.0f, 0.0f);
+          DASH_TRY(gemm(prec, B, nc, pool[iY], 0, pool[iT], 0, ey, st));
+          iY = iYn;
+          if (k >= 1) {
+            const int iZn = free_buf(iY, iZ, iT);
+            EpiParams ez = epi_none();
+            ez.nout = 1;
+            ez.out[0] = eout(pool[iZn], fmt, 1.0f, 0.0f);
+            DASH_TRY(gemm(prec, B, nc, pool[iT], 0, pool[iZ], 0, ez, st));
+            iZ = iZn;
+          }
+          continue;
+        }
+        // Last iteration of the stage.
+        if (keepY) {
+          // Y_K = Y_{K-1} T_{K-1}; its epilogue starts stage 2 on C' = Y_K:
+          // C' (kept), T'_0 = (3I - C')/2, Z'_1 = T'_0, residual of C'.
+          // With one iteration per stage, stage 2's answer is Z'_1 itself.
+          const int iCn = free_buf(iY, iT, -1);
+          const int iTn = free_buf(iY, iT, iCn);
+          int iZn = -1;
+          for (int i = 0; i < NDB_BUFS; ++i)
+            if (i != iY && i != iT && i != iCn && i != iTn) {
+              iZn = i;
+              break;
+            }
+          EpiParams ey = epi_none();
+          ey.resid_acc = racc ? racc + K : nullptr;
+          ey.resid_stride = rstride;
+          if (K == 1) {
+            ey.nout = 1;
+            ey.out[0] = eout(Xout, FMT_F32, -0.5f, 1.5f, 0.0f, m14);
+            // residual of C' = product itself
+            DASH_TRY(gemm(prec, B, nc, pool[iY], 0, pool[iT], 0, ey, st));
+          } else {
+            ey.nout = 3;
+            ey.out[0] = eout(pool[iCn], fmt, 1.0f, 0.0f);
+            ey.out[1] = eout(pool[iTn], fmt, -0.5f, 1.5f);
+            ey.out[2] = eout(pool[iZn], fmt, -0.5f, 1.5f);
+            DASH_TRY(gemm(prec, B, nc, pool[iY], 0, pool[iT], 0, ey, st));
+          }
+          iC = iCn;
+          iT = iTn;
+          iZ = iZn;
+        } else {
+          // Z_K = T_{K-1} Z_{K-1}, scaled by s^{-1/4}, into the caller's output.
+          EpiParams ez = epi_none();
+          ez.nout = 1;
+          ez.out[0] = eout(Xout, FMT_F32, 1.0f, 0.0f, 0.0f, m14);
+          DASH_TRY(gemm(prec, B, nc, pool[iT], 0, pool[iZ], 0, ez, st));
+        }
+      }
+      if (stage == 0 && K == 1) break;  // stage 2 finished inside stage 1's epilogue
+    }
+  }
+  if (resid_out)
+    DASH_TRY(launch_sqrt_scale(sm.racc, resid_out, N * 2 * K,
+                               1.0f / std::sqrt(static_cast<float>(B)), st));
+  return DASH_OK;
+}
+
+// ---------------------------------------------------------------- Chebyshev / Clenshaw
+
+dash_status inv_root_cheb(const float* A, float ridge, const float* scale, int64_t N, int B,
+                          int degree, double lo, double hi, int prec, float* X, void* ws,
+                          size_t ws_bytes, void* stream) {
+  DASH_TRY(common_root_checks(A, scale, N, B, 1, prec, X, ws));
+  if (degree < 1 || degree > 64 || !(lo > 0.0) || !(hi > lo) || !std::isfinite(hi))
+    return DASH_ERR_INVALID_ARG;
+  if (N == 0) return DASH_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int d = degree;
+  const int fmt = prec_fmt(prec);
+  // Coefficients of the degree-d interpolant of x^{-1/4} at the first-kind
+  // Chebyshev points of [lo, hi], in the Chebyshev basis of t in [-1, 1].
+  std::vector<double> c(d + 1);
+  const double pi = 3.14159265358979323846;
+  for (int j = 0; j <= d; ++j) {
+    double acc = 0.0;
+    for (int i = 0; i <= d; ++i) {
+      const double th = pi * (i + 0.5) / (d + 1);
+      const double x = 0.5 * (hi - lo) * std::cos(th) + 0.5 * (hi + lo);
+      acc += std::pow(x, -0.25) * std::cos(j * th);
+    }
+    c[j] = 2.0 * acc / (d + 1);
+  }
+  c[0] *= 0.5;
+  const double aS = 2.0 / (hi - lo), gS = -(hi + lo) / (hi - lo);
+
+  Carver cv(ws, ws_bytes);
+  float* inv_s = static_cast<float*>(cv.take(N * 4));
+  float* s_m14 = static_cast<float*>(cv.take(N * 4));
+  cv.take(4);
+  if (!cv.ok) return DASH_ERR_WORKSPACE_TOO_SMALL;
+  const int nbufs = (d >= 2) ? CHEB_BUFS : 0;
+  const long long chunk = fit_chunk(prec, B, N, nbufs, cv.left);
+  if (chunk < 1) return DASH_ERR_WORKSPACE_TOO_SMALL;
+  Buf bS, bb[3];
+  if (d >= 2) {
+    bS = cv.take_buf(prec, B, chunk);
+    for (int i = 0; i < 3; ++i) bb[i] = cv.take_buf(prec, B, chunk);
+    if (!cv.ok) return DASH_ERR_WORKSPACE_TOO_SMALL;
+  }
+  DASH_TRY(launch_scale_factors(scale, inv_s, s_m14, N, st));
+  for (long long c0 = 0; c0 < N; c0 += chunk) {
+    const long long nc = (N - c0 < chunk) ? N - c0 : chunk;
+    const float* Ac = offset_blocks(A, c0, B, 4);
+    float* Xc = offset_blocks(X, c0, B, 4);
+    const float* m14 = s_m14 + c0;
+    AffParams a = aff_from(Ac, nullptr, FMT_F32, B, nc);
+    a.ridge = ridge;
+    a.inv_s = inv_s + c0;
+    if (d == 1) {
+      // P = c_0 I + c_1 S.
+      Buf xb;
+      xb.hi = Xc;
+      a.nout = 1;
+      a.out[0] = aout(xb, FMT_F32, static_cast<float>(c[1] * aS),
+                      static_cast<float>(c[0] + c[1] * gS), m14);
+      DASH_TRY(launch_affine(a, st));
+      continue;
+    }
+    // S and b_{d-1} = c_{d-1} I + 2 c_d S.
+    a.nout = 2;
+    a.out[0] = aout(bS, fmt, static_cast<float>(aS), static_cast<float>(gS));
+    a.out[1] = aout(bb[0], fmt, static_cast<float>(2.0 * c[d] * aS),
+                    static_cast<float>(c[d - 1] + 2.0 * c[d] * gS));
+    DASH_TRY(launch_affine(a, st));
+    Buf xb;
+    xb.hi = Xc;
+    if (d == 2) {
+      EpiParams e = epi_none();
+      e.nout = 1;
+      e.out[0] = eout(xb, FMT_F32, 1.0f, static_cast<float>(c[0] - c[2]), 0.0f, m14);
+      DASH_TRY(gemm(prec, B, nc, bS, 0, bb[0], 0, e, st));
+      continue;
+    }
+    // b_{d-2} = 2 S b_{d-1} + (c_{d-2} - c_d) I
+    int i1 = 0, i2 = -1, i0 = 1;  // b_{j+1}, b_{j+2}, b_j
+    {
+      EpiParams e = epi_none();
+      e.nout = 1;
+      e.out[0] = eout(bb[i0], fmt, 2.0f, static_cast<float>(c[d - 2] - c[d]));
+      DASH_TRY(gemm(prec, B, nc, bS, 0, bb[i1], 0, e, st));
+      i2 = i1;
+      i1 = i0;
+    }
+    for (int j = d - 3; j >= 1; --j) {
+      i0 = 3 - i1 - i2;
+      EpiParams e = epi_none();
+      e.nout = 1;
+      e.out[0] = eout(bb[i0], fmt, 2.0f, static_cast<float>(c[j]), -1.0f);
+      e.E_hi = bb[i2].hi;
+      e.E_lo = bb[i2].lo;
+      e.E_fmt = fmt;
+      DASH_TRY(gemm(prec, B, nc, bS, 0, bb[i1], 0, e, st));
+      i2 = i1;
+      i1 = i0;
+    }
+    // P = S b_1 + c_0 I - b_2
+    EpiParams e = epi_none();
+    e.nout = 1;
+    e.out[0] = eout(xb, FMT_F32, 1.0f, static_cast<float>(c[0]), -1.0f, m14);
+    e.E_hi = bb[i2].hi;
+    e.E_lo = bb[i2].lo;
+    e.E_fmt = fmt;
+    DASH_TRY(gemm(prec, B, nc, bS, 0, bb[i1], 0, e, st));
+  }
+  return DASH_OK;
+}
+
+// ---------------------------------------------------------------- apply
+
+dash_status precondition_apply(const void* G, int gdt, const float* Froot, int64_t Ng, int B,
+                               int prec, float* U, void* ws, size_t ws_bytes, void* stream) {
+  if (Ng < 0 || !valid_dim(B) || !valid_prec(prec) ||
+      !(gdt == DASH_DT_F32 || gdt == DASH_DT_BF16 || gdt == DASH_DT_F16))
+    return DASH_ERR_INVALID_ARG;
+  if (Ng == 0) return DASH_OK;
+  if (!G || !Froot || !U || !aligned16(G) || !aligned16(Froot) || !aligned16(U))
+    return DASH_ERR_INVALID_ARG;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return DASH_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int fmt = prec_fmt(prec);
+  const long long chunk = fit_chunk(prec, B, Ng, APPLY_BUFS, ws_bytes);
+  if (chunk < 1) return DASH_ERR_WORKSPACE_TOO_SMALL;
+  Carver cv(ws, ws_bytes);
+  Buf bG = cv.take_buf(prec, B, chunk);
+  Buf bL = cv.take_buf(prec, B, chunk);
+  Buf bR = cv.take_buf(prec, B, chunk);
+  Buf bT = cv.take_buf(prec, B, chunk);
+  if (!cv.ok) return DASH_ERR_WORKSPACE_TOO_SMALL;
+  const int gfmt = (gdt == DASH_DT_F32) ? FMT_F32 : (gdt == DASH_DT_BF16 ? FMT_BF16 : FMT_F16);
+  const size_t gsz = (gdt == DASH_DT_F32) ? 4 : 2;
+  for (long long c0 = 0; c0 < Ng; c0 += chunk) {
+    const long long nc = (Ng - c0 < chunk) ? Ng - c0 : chunk;
+    AffParams a = aff_from(offset_blocks(static_cast<const char*>(G), c0, B, gsz), nullptr, gfmt, B, nc);
+    a.nout = 1;
+    a.out[0] = aout(bG, fmt, 1.0f, 0.0f);
+    DASH_TRY(launch_affine(a, st));
+    a = aff_from(offset_blocks(Froot, c0, B, 4), nullptr, FMT_F32, B, nc);
+    a.nout = 1;
+    a.out[0] = aout(bL, fmt, 1.0f, 0.0f);
+    DASH_TRY(launch_affine(a, st));
+    a = aff_from(offset_blocks(Froot, Ng + c0, B, 4), nullptr, FMT_F32, B, nc);
+    a.nout = 1;
+    a.out[0] = aout(bR, fmt, 1.0f, 0.0f);
+    DASH_TRY(launch_affine(a, st));
+    EpiParams e = epi_none();
+    e.nout = 1;
+    e.out[0] = eout(bT, fmt, 1.0f, 0.0f);
+    DASH_TRY(gemm(prec, B, nc, bL, 0, bG, 0, e, st));
+    e.out[0] = eout_f32(offset_blocks(U, c0, B, 4), 1.0f, 0.0f, 0.0f, nullptr);
+    DASH_TRY(gemm(prec, B, nc, bT, 0, bR, 0, e, st));
+  }
+  return DASH_OK;
+}
+
+}  // extern "C"

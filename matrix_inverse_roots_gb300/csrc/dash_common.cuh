@@ -1,0 +1,291 @@
+// Shared device helpers for the dashroot kernels: operand formats, bounded
+// mbarrier waits, TMA and tcgen05 (5th-generation tensor core) wrappers.
+// Everything here is written for sm_103a.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dash {
+
+// Storage format of a stacked matrix inside the library.
+enum Fmt : int {
+  FMT_F32 = 0,    // plain fp32
+  FMT_TF32 = 1,   // fp32 container holding a value rounded to TF32 (RNA)
+  FMT_SPLIT = 2,  // two fp32 arrays: hi = rna_tf32(x), lo = rna_tf32(x - hi)
+  FMT_F16 = 3,
+  FMT_BF16 = 4,
+};
+
+// Tensor-core operand kinds.
+enum Kind : int { KIND_F16 = 0, KIND_BF16 = 1, KIND_TF32 = 2, KIND_TF32X3 = 3 };
+
+// Device error codes recorded in g_dash_error (mirrors dash_status values).
+constexpr int DEV_ERR_TIMEOUT = 5;
+
+// Time limit of any single device-side wait, in nanoseconds of %globaltimer.
+constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;
+
+// One flag per translation unit; each unit exports a host reader for it.
+static __device__ int g_dash_error = 0;
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- mbarrier
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits until the phase with the given parity of barrier `bar` has completed.
+// Gives up when *abort becomes non-zero (another role gave up) or after
+// WAIT_LIMIT_NS; on a time-out it raises *abort and the device error flag.
+// Returns false when it gave up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  unsigned long long t0 = globaltimer_ns();
+  uint32_t n = 0;
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((++n & 255u) == 0) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+        *abort = 1;
+        atomicExch(&g_dash_error, DEV_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- TMA
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+
+// 3-D tiled bulk tensor load global -> shared, completion on mbarrier `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, uint32_t bar,
+                                            int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+// ---------------------------------------------------------------- tcgen05
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Warp-wide TMEM allocation; the base address is written to shared memory.
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// Shared-memory matrix layouts understood by tcgen05 descriptors.
+constexpr uint32_t LAYOUT_SW128 = 2;         // 128-byte swizzle of 16-byte chunks
+constexpr uint32_t LAYOUT_SW128_BASE32 = 1;  // 128-byte swizzle of 32-byte chunks (MN-major TF32)
+
+// Shared-memory matrix descriptor, descriptor version 1.  lbo / sbo in bytes
+// (multiples of 16); layout one of LAYOUT_*.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t layout) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;  // version
+  d |= static_cast<uint64_t>(layout & 7u) << 61;
+  return d;
+}
+
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return smem_desc(saddr, lbo, sbo, LAYOUT_SW128);
+}
+
+// Instruction descriptor for kind::f16 / kind::tf32 with fp32 accumulation.
+// fmt: 0 = F16, 1 = BF16, 2 = TF32.  major: 0 = K-major, 1 = MN-major.
+__host__ __device__ constexpr uint32_t make_idesc(uint32_t fmt, uint32_t a_mn, uint32_t b_mn,
+                                                  uint32_t M, uint32_t N) {
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | (a_mn << 15) | (b_mn << 16) |
+         ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every tcgen05 operation this thread issued so far is done.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// 32 lanes x 32 bits, 16 consecutive columns: thread i gets lane (base + i).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- formats
+
+// Round an fp32 value to the nearest TF32 value (ties away from zero).
+__device__ __forceinline__ float rna_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
+}
+
+// Bytes per element of a storage format (both halves for the split format).
+__host__ __device__ constexpr int fmt_bytes(int fmt) {
+  return fmt == FMT_SPLIT ? 8 : ((fmt == FMT_F16 || fmt == FMT_BF16) ? 2 : 4);
+}
+
+// Element offset helpers use 64-bit arithmetic throughout.
+__device__ __forceinline__ float load_elem(int fmt, const void* hi, const void* lo, int64_t i) {
+  switch (fmt) {
+    case FMT_F16:
+      return __half2float(static_cast<const __half*>(hi)[i]);
+    case FMT_BF16:
+      return __bfloat162float(static_cast<const __nv_bfloat16*>(hi)[i]);
+    case FMT_SPLIT:
+      return static_cast<const float*>(hi)[i] + static_cast<const float*>(lo)[i];
+    default:
+      return static_cast<const float*>(hi)[i];
+  }
+}
+
+// Loads 4 consecutive elements starting at i (i a multiple of 4).
+__device__ __forceinline__ void load4(int fmt, const void* hi, const void* lo, int64_t i,
+                                      float (&v)[4]) {
+  if (fmt == FMT_F16) {
+    const uint2 u = *reinterpret_cast<const uint2*>(static_cast<const __half*>(hi) + i);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+    v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+  } else if (fmt == FMT_BF16) {
+    const uint2 u = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(hi) + i);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+  } else {
+    const float4 a = *reinterpret_cast<const float4*>(static_cast<const float*>(hi) + i);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    if (fmt == FMT_SPLIT) {
+      const float4 b = *reinterpret_cast<const float4*>(static_cast<const float*>(lo) + i);
+      v[0] += b.x; v[1] += b.y; v[2] += b.z; v[3] += b.w;
+    }
+  }
+}
+
+// Stores 4 consecutive elements starting at i (i a multiple of 4).
+__device__ __forceinline__ void store4(int fmt, void* hi, void* lo, int64_t i, const float (&v)[4]) {
+  if (fmt == FMT_F16) {
+    __half2 a = __floats2half2_rn(v[0], v[1]);
+    __half2 b = __floats2half2_rn(v[2], v[3]);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(static_cast<__half*>(hi) + i) = u;
+  } else if (fmt == FMT_BF16) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]);
+    __nv_bfloat162 b = __floats2bfloat162_rn(v[2], v[3]);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(hi) + i) = u;
+  } else if (fmt == FMT_TF32) {
+    float4 a = make_float4(rna_tf32(v[0]), rna_tf32(v[1]), rna_tf32(v[2]), rna_tf32(v[3]));
+    *reinterpret_cast<float4*>(static_cast<float*>(hi) + i) = a;
+  } else if (fmt == FMT_SPLIT) {
+    float h[4], l[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      h[j] = rna_tf32(v[j]);
+      l[j] = rna_tf32(v[j] - h[j]);
+    }
+    *reinterpret_cast<float4*>(static_cast<float*>(hi) + i) = make_float4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<float4*>(static_cast<float*>(lo) + i) = make_float4(l[0], l[1], l[2], l[3]);
+  } else {
+    *reinterpret_cast<float4*>(static_cast<float*>(hi) + i) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+}
+
+}  // namespace dash

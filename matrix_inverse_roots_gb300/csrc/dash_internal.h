@@ -1,0 +1,110 @@
+// Host-side interfaces between the C-ABI layer (dash_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dashroot.h"
+
+namespace dash {
+
+// One output of a fused epilogue:
+//   D = mult[blk] * (alpha * C + gamma * I + eps * E)   stored in format fmt.
+// (mult may be null = 1; E is the launch's optional extra matrix.)
+struct EpiOut {
+  void* hi;
+  void* lo;
+  const float* mult;
+  float alpha, gamma, eps;
+  int fmt;
+};
+
+struct EpiParams {
+  EpiOut out[3];
+  int nout;
+  const void* E_hi;  // optional matrix read by the epilogue (same stacking as C)
+  const void* E_lo;
+  int E_fmt;
+  float* resid_acc;        // if set: resid_acc[blk * resid_stride] += sum (C - I)^2
+  long long resid_stride;
+  const int* pad_valid;    // if set: rows / cols >= pad_valid[blk] become the identity's
+};
+
+// C[k] = op(A[k]) op(B[k]) for k < nblocks, fused with the epilogue.
+struct GemmLaunch {
+  int kind;  // KIND_*
+  int dim;
+  long long nblocks;
+  const void* A;
+  const void* A_lo;
+  int transA;
+  const void* B;
+  const void* B_lo;
+  int transB;
+  EpiParams epi;
+};
+
+dash_status launch_gemm(const GemmLaunch& g, cudaStream_t st);
+
+// Element-wise affine map of a stack:  x = (src + ridge I) * inv_s[blk]  (inv_s
+// may be null = 1), then each output D = mult[blk] * (alpha x + gamma I) and,
+// if resid_acc is set, resid_acc[blk * resid_stride] += sum (x - I)^2.
+struct AffOut {
+  void* hi;
+  void* lo;
+  const float* mult;
+  float alpha, gamma;
+  int fmt;
+};
+
+struct AffParams {
+  const void* src_hi;
+  const void* src_lo;
+  int src_fmt;
+  float ridge;
+  const float* inv_s;
+  AffOut out[3];
+  int nout;
+  float* resid_acc;
+  long long resid_stride;
+  int dim;
+  long long nblocks;
+};
+
+dash_status launch_affine(const AffParams& p, cudaStream_t st);
+
+// inv_s[k] = 1 / s[k], s_m14[k] = s[k]^{-1/4}.
+dash_status launch_scale_factors(const float* s, float* inv_s, float* s_m14, long long n,
+                                 cudaStream_t st);
+
+// out[i] = sqrt(acc[i]) * mul.
+dash_status launch_sqrt_scale(const float* acc, float* out, long long n, float mul,
+                              cudaStream_t st);
+
+// acc[k] += sum over block k of (A + ridge I)^2 (acc zeroed by the caller).
+dash_status launch_frob_acc(const float* A, float ridge, int dim, long long nblocks, float* acc,
+                            cudaStream_t st);
+
+// One power-iteration product W = (A + ridge I) V for every block; V is read as
+// Vin[blk][row][c] * rsqrt(in_nrm2[blk][c]) (in_nrm2 null = unscaled).
+// Not last: writes W (stride 32) and acc0[blk][c] += sum_r W^2.
+// Last: acc0[blk][c] += sum_r v w, acc1[blk][c] += sum_r v v (W not written).
+dash_status launch_power_step(const float* A, float ridge, int dim, long long nblocks,
+                              const float* Vin, int vin_stride, int nv, const float* in_nrm2,
+                              float* Wout, float* acc0, float* acc1, int last,
+                              cudaStream_t st);
+
+// lambda[k] = max_{c < nv} num[k][c] / den[k][c].
+dash_status launch_power_finish(const float* num, const float* den, int nv, long long nblocks,
+                                float* lambda, cudaStream_t st);
+
+// Kernel trace hooks (no-ops unless dash_trace_start was called).
+int trace_begin(cudaStream_t st);
+void trace_end(int rec, cudaStream_t st, int kind, double flops, double bytes);
+
+int gemm_read_clear_error();
+int elementwise_read_clear_error();
+
+int device_sm_count();
+
+}  // namespace dash

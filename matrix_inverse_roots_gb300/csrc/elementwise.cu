@@ -1,0 +1,341 @@
+// Memory-bound kernels of the preconditioner step: the element-wise prologue
+// that scales a block and writes the first iterates in operand format, the
+// Frobenius reduction, per-block scale factors, and the multi-vector power
+// iteration.  All are HBM-bound: 16-byte vector accesses along rows, warp-shuffle
+// reductions, one atomic per CTA and block for the per-block sums.
+#include <cmath>
+
+#include "dash_common.cuh"
+#include "dash_internal.h"
+
+namespace dash {
+
+int elementwise_read_clear_error() {
+  int v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_dash_error, sizeof(int)) != cudaSuccess) return -1;
+  if (cudaMemcpyToSymbol(g_dash_error, &z, sizeof(int)) != cudaSuccess) return -1;
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+// Block-wide sum of v over 256 threads; result valid in thread 0.
+__device__ __forceinline__ float block_sum256(float v, float* red) {
+  v = warp_sum(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  float s = 0.0f;
+  if (threadIdx.x < 32) {
+    s = (l < 8) ? red[l] : 0.0f;
+    s = warp_sum(s);
+  }
+  __syncthreads();
+  return s;
+}
+
+constexpr int EW_THREADS = 256;
+constexpr int EW_VEC_PER_THREAD = 8;
+
+// grid.x: chunks of one block, grid.y: blocks (strided over nblocks).
+__global__ void __launch_bounds__(EW_THREADS) affine_kernel(const __grid_constant__ AffParams p) {
+  __shared__ float red[8];
+  const long long dd = static_cast<long long>(p.dim) * p.dim;
+  const long long n4 = dd / 4;
+  for (long long blk = blockIdx.y; blk < p.nblocks; blk += gridDim.y) {
+    const float inv_s = (p.inv_s != nullptr) ? p.inv_s[blk] : 1.0f;
+    float mult[3];
+#pragma unroll
+    for (int o = 0; o < 3; ++o)
+      mult[o] = (o < p.nout && p.out[o].mult != nullptr) ? p.out[o].mult[blk] : 1.0f;
+    float rsum = 0.0f;
+    for (long long v = static_cast<long long>(blockIdx.x) * EW_THREADS + threadIdx.x; v < n4;
+         v += static_cast<long long>(gridDim.x) * EW_THREADS) {
+      const long long e = blk * dd + 4 * v;
+      const int row = static_cast<int>((4 * v) / p.dim);
+      const int col0 = static_cast<int>((4 * v) % p.dim);
+      float x[4];
+      load4(p.src_fmt, p.src_hi, p.src_lo, e, x);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const bool diag = (row == col0 + j);
+        x[j] = (x[j] + (diag ? p.ridge : 0.0f)) * inv_s;
+        if (p.resid_acc != nullptr) {
+          const float d = x[j] - (diag ? 1.0f : 0.0f);
+          rsum = fmaf(d, d, rsum);
+        }
+      }
+#pragma unroll
+      for (int o = 0; o < 3; ++o) {
+        if (o < p.nout) {
+          float d[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float t = p.out[o].alpha * x[j];
+            if (row == col0 + j) t += p.out[o].gamma;
+            d[j] = t * mult[o];
+          }
+          store4(p.out[o].fmt, p.out[o].hi, p.out[o].lo, e, d);
+        }
+      }
+    }
+    if (p.resid_acc != nullptr) {
+      const float s = block_sum256(rsum, red);
+      if (threadIdx.x == 0) atomicAdd(p.resid_acc + blk * p.resid_stride, s);
+    }
+  }
+}
+
+static dim3 ew_grid(int dim, long long nblocks) {
+  const long long n4 = static_cast<long long>(dim) * dim / 4;
+  long long gx = (n4 + EW_THREADS * EW_VEC_PER_THREAD - 1) / (EW_THREADS * EW_VEC_PER_THREAD);
+  if (gx < 1) gx = 1;
+  const long long gy = nblocks < 65535 ? nblocks : 65535;
+  return dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy), 1);
+}
+
+dash_status launch_affine(const AffParams& p, cudaStream_t st) {
+  if (p.nblocks <= 0) return DASH_OK;
+  const int rec = trace_begin(st);
+  affine_kernel<<<ew_grid(p.dim, p.nblocks), EW_THREADS, 0, st>>>(p);
+  const cudaError_t err = cudaGetLastError();
+  if (rec >= 0) {
+    const double bb = static_cast<double>(p.dim) * p.dim * p.nblocks;
+    double bytes = bb * fmt_bytes(p.src_fmt);
+    for (int o = 0; o < p.nout; ++o) bytes += bb * fmt_bytes(p.out[o].fmt);
+    trace_end(rec, st, DASH_TRACE_ELEMENTWISE, 0.0, bytes);
+  }
+  return err == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
+}
+
+__global__ void scale_factors_kernel(const float* s, float* inv_s, float* s_m14, long long n) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const double v = static_cast<double>(s[i]);
+  inv_s[i] = static_cast<float>(1.0 / v);
+  s_m14[i] = static_cast<float>(pow(v, -0.25));
+}
+
+dash_status launch_scale_factors(const float* s, float* inv_s, float* s_m14, long long n,
+                                 cudaStream_t st) {
+  if (n <= 0) return DASH_OK;
+  scale_factors_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(s, inv_s, s_m14, n);
+  return cudaGetLastError() == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
+}
+
+__global__ void sqrt_scale_kernel(const float* acc, float* out, long long n, float mul) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < n) out[i] = sqrtf(acc[i]) * mul;
+}
+
+dash_status launch_sqrt_scale(const float* acc, float* out, long long n, float mul,
+                              cudaStream_t st) {
+  if (n <= 0) return DASH_OK;
+  sqrt_scale_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(acc, out, n, mul);
+  return cudaGetLastError() == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
+}
+
+__global__ void __launch_bounds__(EW_THREADS)
+    frob_kernel(const float* A, float ridge, int dim, long long nblocks, float* acc) {
+  __shared__ float red[8];
+  const long long dd = static_cast<long long>(dim) * dim;
+  const long long n4 = dd / 4;
+  for (long long blk = blockIdx.y; blk < nblocks; blk += gridDim.y) {
+    float s = 0.0f;
+    for (long long v = static_cast<long long>(blockIdx.x) * EW_THREADS + threadIdx.x; v < n4;
+         v += static_cast<long long>(gridDim.x) * EW_THREADS) {
+      const float4 a = *reinterpret_cast<const float4*>(A + blk * dd + 4 * v);
+      const int row = static_cast<int>((4 * v) / dim);
+      const int col0 = static_cast<int>((4 * v) % dim);
+      float x[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float t = x[j] + ((row == col0 + j) ? ridge : 0.0f);
+        s = fmaf(t, t, s);
+      }
+    }
+    s = block_sum256(s, red);
+    if (threadIdx.x == 0) atomicAdd(acc + blk, s);
+  }
+}
+
+dash_status launch_frob_acc(const float* A, float ridge, int dim, long long nblocks, float* acc,
+                            cudaStream_t st) {
+  if (nblocks <= 0) return DASH_OK;
+  const int rec = trace_begin(st);
+  frob_kernel<<<ew_grid(dim, nblocks), EW_THREADS, 0, st>>>(A, ridge, dim, nblocks, acc);
+  const cudaError_t err = cudaGetLastError();
+  const double bb = static_cast<double>(dim) * dim * nblocks;
+  trace_end(rec, st, DASH_TRACE_REDUCE, 2.0 * bb, 4.0 * bb);
+  return err == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- power iteration
+// One CTA computes 64 rows x 32 vectors of W = (A + ridge I) V for one block.
+// A is streamed once in 64 x 64 chunks (coalesced float4 rows, transposed into
+// shared memory); the matching 64 x 32 slab of V (normalised on the fly) sits
+// beside it; each thread owns a 2 x 4 register tile of W.
+constexpr int PW_ROWS = 64;
+constexpr int PW_KC = 64;
+constexpr int PW_NV = 32;
+
+__global__ void __launch_bounds__(256)
+    power_step_kernel(const float* A, float ridge, int dim, long long nblocks, const float* Vin,
+                      int vin_stride, int nv, const float* in_nrm2, float* Wout, float* acc0,
+                      float* acc1, int last) {
+  __shared__ float As[PW_KC][PW_ROWS + 1];
+  __shared__ __align__(16) float Vs[PW_KC][PW_NV];
+  __shared__ float vscale[PW_NV];
+  __shared__ float red0[8][PW_NV];
+  __shared__ float red1[8][PW_NV];
+
+  const long long blk = blockIdx.y;
+  const int r0 = blockIdx.x * PW_ROWS;
+  const int tid = threadIdx.x;
+  const int tx = tid & 7;   // vector group: columns 4tx..4tx+3
+  const int ty = tid >> 3;  // row pair: rows 2ty, 2ty+1
+  const long long dd = static_cast<long long>(dim) * dim;
+  const float* Ab = A + blk * dd;
+  const float* Vb = Vin + blk * static_cast<long long>(dim) * vin_stride;
+
+  if (tid < PW_NV) {
+    float sc = 0.0f;
+    if (tid < nv) sc = (in_nrm2 != nullptr) ? 1.0f / sqrtf(in_nrm2[blk * PW_NV + tid]) : 1.0f;
+    vscale[tid] = sc;
+  }
+  __syncthreads();
+
+  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  for (int kc = 0; kc < dim; kc += PW_KC) {
+    // A chunk: rows r0..r0+63, columns kc..kc+63 -> As[col][row].
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int f = tid + 256 * u;
+      const int i = f >> 4;
+      const int j4 = f & 15;
+      const float4 a =
+          *reinterpret_cast<const float4*>(Ab + static_cast<long long>(r0 + i) * dim + kc + 4 * j4);
+      As[4 * j4 + 0][i] = a.x;
+      As[4 * j4 + 1][i] = a.y;
+      As[4 * j4 + 2][i] = a.z;
+      As[4 * j4 + 3][i] = a.w;
+    }
+    // V slab: rows kc..kc+63, all 32 vector slots (zero beyond nv).
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int f = tid + 256 * u;
+      const int j = f >> 5;
+      const int c = f & 31;
+      float v = 0.0f;
+      if (c < nv) v = Vb[static_cast<long long>(kc + j) * vin_stride + c] * vscale[c];
+      Vs[j][c] = v;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int k = 0; k < PW_KC; ++k) {
+      const float a0 = As[k][2 * ty];
+      const float a1 = As[k][2 * ty + 1];
+      const float4 v = *reinterpret_cast<const float4*>(&Vs[k][4 * tx]);
+      acc[0][0] = fmaf(a0, v.x, acc[0][0]);
+      acc[0][1] = fmaf(a0, v.y, acc[0][1]);
+      acc[0][2] = fmaf(a0, v.z, acc[0][2]);
+      acc[0][3] = fmaf(a0, v.w, acc[0][3]);
+      acc[1][0] = fmaf(a1, v.x, acc[1][0]);
+      acc[1][1] = fmaf(a1, v.y, acc[1][1]);
+      acc[1][2] = fmaf(a1, v.z, acc[1][2]);
+      acc[1][3] = fmaf(a1, v.w, acc[1][3]);
+    }
+    __syncthreads();
+  }
+
+  // Ridge term and the per-column statistics.
+  float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    const int row = r0 + 2 * ty + rr;
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      const int c = 4 * tx + cc;
+      const float v = (c < nv) ? Vb[static_cast<long long>(row) * vin_stride + c] * vscale[c] : 0.0f;
+      const float w = fmaf(ridge, v, acc[rr][cc]);
+      acc[rr][cc] = w;
+      if (last) {
+        s0[cc] = fmaf(v, w, s0[cc]);
+        s1[cc] = fmaf(v, v, s1[cc]);
+      } else {
+        s0[cc] = fmaf(w, w, s0[cc]);
+      }
+    }
+    if (!last) {
+      float4 o = make_float4(acc[rr][0], acc[rr][1], acc[rr][2], acc[rr][3]);
+      *reinterpret_cast<float4*>(Wout + blk * static_cast<long long>(dim) * PW_NV +
+                                 static_cast<long long>(row) * PW_NV + 4 * tx) = o;
+    }
+  }
+  // Reduce over the 32 row pairs: lanes tx, tx+8, tx+16, tx+24 share columns.
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {
+    s0[cc] += __shfl_xor_sync(0xffffffffu, s0[cc], 8);
+    s0[cc] += __shfl_xor_sync(0xffffffffu, s0[cc], 16);
+    s1[cc] += __shfl_xor_sync(0xffffffffu, s1[cc], 8);
+    s1[cc] += __shfl_xor_sync(0xffffffffu, s1[cc], 16);
+  }
+  const int w = tid >> 5, l = tid & 31;
+  if (l < 8) {
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      red0[w][4 * l + cc] = s0[cc];
+      red1[w][4 * l + cc] = s1[cc];
+    }
+  }
+  __syncthreads();
+  if (tid < PW_NV && tid < nv) {
+    float a = 0.f, b = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      a += red0[i][tid];
+      b += red1[i][tid];
+    }
+    atomicAdd(acc0 + blk * PW_NV + tid, a);
+    if (last) atomicAdd(acc1 + blk * PW_NV + tid, b);
+  }
+}
+
+dash_status launch_power_step(const float* A, float ridge, int dim, long long nblocks,
+                              const float* Vin, int vin_stride, int nv, const float* in_nrm2,
+                              float* Wout, float* acc0, float* acc1, int last, cudaStream_t st) {
+  if (nblocks <= 0) return DASH_OK;
+  if (nblocks > 65535) return DASH_ERR_INVALID_ARG;
+  dim3 grid(dim / PW_ROWS, static_cast<unsigned>(nblocks), 1);
+  const int rec = trace_begin(st);
+  power_step_kernel<<<grid, 256, 0, st>>>(A, ridge, dim, nblocks, Vin, vin_stride, nv, in_nrm2,
+                                          Wout, acc0, acc1, last);
+  const cudaError_t err = cudaGetLastError();
+  const double bb = static_cast<double>(dim) * dim * nblocks;
+  const double vb = static_cast<double>(dim) * nblocks * 4.0;
+  trace_end(rec, st, DASH_TRACE_POWER, 2.0 * bb * nv, 4.0 * bb + vb * (vin_stride + (last ? 0 : 32)));
+  return err == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
+}
+
+__global__ void power_finish_kernel(const float* num, const float* den, int nv, long long nblocks,
+                                    float* lambda) {
+  const long long k = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (k >= nblocks) return;
+  float best = -INFINITY;
+  for (int c = 0; c < nv; ++c) best = fmaxf(best, num[k * PW_NV + c] / den[k * PW_NV + c]);
+  lambda[k] = best;
+}
+
+dash_status launch_power_finish(const float* num, const float* den, int nv, long long nblocks,
+                                float* lambda, cudaStream_t st) {
+  if (nblocks <= 0) return DASH_OK;
+  power_finish_kernel<<<static_cast<unsigned>((nblocks + 127) / 128), 128, 0, st>>>(num, den, nv,
+                                                                                    nblocks, lambda);
+  return cudaGetLastError() == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
+}
+
+}  // namespace dash

@@ -1,0 +1,497 @@
+// Batched square GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA)
+// with a fused epilogue.  Every dense B x B x B product of the preconditioner
+// step (factor accumulation, the Coupled Newton / Newton-Denman-Beavers /
+// Clenshaw iterations, the preconditioned update) runs through this kernel.
+//
+// Design (one CTA per SM, persistent):
+//   warp 0      TMA producer: streams 128-byte-wide, 128B-swizzled operand tiles
+//               into a ring of shared-memory stages (mbarrier full/empty pairs).
+//   warp 1      allocates TMEM and issues tcgen05.mma from one thread into one of
+//               two TMEM accumulators (128 x BN fp32 each), so the epilogue of
+//               tile i overlaps the MMAs of tile i+1.
+//   warps 2..5  epilogue: tcgen05.ld the accumulator (one TMEM lane = one row per
+//               thread), apply D = mult*(alpha C + gamma I + eps E), optional
+//               residual sum (C - I)^2 and identity padding, and store in the
+//               requested format (fp32, TF32-rounded, hi/lo split, fp16, bf16).
+// Tiles are ordered block-major so that concurrently running CTAs share the
+// operands of a few blocks in L2.
+// Precisions: kind::f16 (fp16 / bf16 operands), kind::tf32, and 3xTF32, which
+// issues hi*lo, lo*hi and hi*hi products into the same accumulator.
+// Every wait is bounded (see mbar_wait); a time-out sets the device error flag
+// and the CTA drains its in-flight copies and MMAs, frees TMEM and returns.
+#include <cstdio>
+#include <mutex>
+
+#include "dash_common.cuh"
+#include "dash_internal.h"
+
+namespace dash {
+
+int gemm_read_clear_error() {
+  int v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_dash_error, sizeof(int)) != cudaSuccess) return -1;
+  if (cudaMemcpyToSymbol(g_dash_error, &z, sizeof(int)) != cudaSuccess) return -1;
+  return v;
+}
+
+// KT: 0 = 16-bit operands (kind::f16), 1 = TF32, 2 = 3xTF32.
+template <int BN, int KT>
+struct Cfg {
+  static constexpr int BM = 128;
+  static constexpr int EB = (KT == 0) ? 2 : 4;  // operand element bytes
+  static constexpr int BK = 128 / EB;           // elements per 128-byte row
+  static constexpr int UK = (KT == 0) ? 16 : 8; // K of one MMA
+  static constexpr int NSUB = BK / UK;          // MMAs per k-block
+  static constexpr int A_BYTES = BM * 128;
+  static constexpr int B_BYTES = BN * 128;
+  static constexpr int NPART = (KT == 2) ? 2 : 1;
+  static constexpr int STAGE_BYTES = (A_BYTES + B_BYTES) * NPART;
+  static constexpr int STAGES_RAW = (192 * 1024) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int MN_ATOM = 128 / EB;      // elements in one 128-byte MN row
+  static constexpr int A_BOXES_MN = BM / MN_ATOM;
+  static constexpr int B_BOXES_MN = BN / MN_ATOM;
+  static constexpr int MN_BOX_BYTES = BK * 128;  // one MN-major box: BK rows of 128 B
+  // MN-major 32-bit operands are read with 32-byte swizzle atoms; that layout
+  // groups K in slabs of 4 rows (512 B), the 16-byte-atom layout in slabs of 8.
+  static constexpr uint32_t MN_LAYOUT = (KT == 0) ? LAYOUT_SW128 : LAYOUT_SW128_BASE32;
+  static constexpr uint32_t MN_SBO = (KT == 0) ? 1024 : 512;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + BAR_BYTES;
+  static_assert(STAGES >= 2, "need at least two pipeline stages");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+struct KParams {
+  int dim;
+  int tiles_m, tiles_n;
+  long long total_tiles;
+  int nkb;
+  uint32_t idesc;
+  int a_mn, b_mn;
+  EpiParams epi;
+};
+
+__device__ __forceinline__ void decode_tile(long long t, const KParams& p, long long& blk, int& m0,
+                                            int& n0, int bn) {
+  const long long per = static_cast<long long>(p.tiles_m) * p.tiles_n;
+  blk = t / per;
+  const int r = static_cast<int>(t - blk * per);
+  m0 = (r / p.tiles_n) * 128;
+  n0 = (r % p.tiles_n) * bn;
+}
+
+// Bounded wait used only while draining after an abort: ignores the abort flag.
+__device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
+  const unsigned long long t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+      atomicExch(&g_dash_error, DEV_ERR_TIMEOUT);
+      return;
+    }
+  }
+}
+
+// Epilogue for 16 consecutive columns of one row.
+__device__ __forceinline__ void epilogue16(const EpiParams& e, long long blk, int rg, int cg0,
+                                           long long idx, const uint32_t (&r)[16], float& rsum) {
+  float c[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) c[j] = __uint_as_float(r[j]);
+  if (e.resid_acc != nullptr) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float d = c[j] - ((rg == cg0 + j) ? 1.0f : 0.0f);
+      rsum = fmaf(d, d, rsum);
+    }
+  }
+  float ev[16];
+  if (e.E_hi != nullptr) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      float t[4];
+      load4(e.E_fmt, e.E_hi, e.E_lo, idx + 4 * g, t);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) ev[4 * g + j] = t[j];
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) ev[j] = 0.0f;
+  }
+  const int pv = (e.pad_valid != nullptr) ? e.pad_valid[blk] : 0x7fffffff;
+#pragma unroll
+  for (int o = 0; o < 3; ++o) {
+    if (o < e.nout) {
+      const EpiOut& O = e.out[o];
+      const float m = (O.mult != nullptr) ? O.mult[blk] : 1.0f;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        float d[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int col = cg0 + 4 * g + j;
+          float v = fmaf(O.alpha, c[4 * g + j], O.eps * ev[4 * g + j]);
+          if (rg == col) v += O.gamma;
+          v *= m;
+          if (rg >= pv || col >= pv) v = (rg == col) ? 1.0f : 0.0f;
+          d[j] = v;
+        }
+        store4(O.fmt, O.hi, O.lo, idx + 4 * g, d);
+      }
+    }
+  }
+}
+
+template <int BN, int KT>
+__global__ void __launch_bounds__(192, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tB,
+                   const __grid_constant__ CUtensorMap tAl,
+                   const __grid_constant__ CUtensorMap tBl, const __grid_constant__ KParams p) {
+  using C = Cfg<BN, KT>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw_base & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sbase = raw_base + pad;
+
+  uint8_t* bar_area = smem + C::STAGES * C::STAGE_BYTES;
+  const uint32_t bar0 = sbase + C::STAGES * C::STAGE_BYTES;
+  // barrier addresses
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + 2 + a); };
+  const uint32_t fin_bar = bar0 + 8u * (2 * C::STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * (2 * C::STAGES + 5));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * (2 * C::STAGES + 5) + 8);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 4);
+    }
+    mbar_init(fin_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tA);
+    tma_prefetch_desc(&tB);
+    if (KT == 2) {
+      tma_prefetch_desc(&tAl);
+      tma_prefetch_desc(&tBl);
+    }
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_par = 0;
+      bool ok = true;
+      for (long long t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+        long long blk;
+        int m0, n0;
+        decode_tile(t, p, blk, m0, n0, BN);
+        const int z = static_cast<int>(blk);
+        for (int kb = 0; kb < p.nkb; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full_bar(stage);
+          mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+          armed |= 1u << stage;
+          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          const int k0 = kb * C::BK;
+          for (int part = 0; part < C::NPART; ++part) {
+            const uint32_t sA = sbase + stage * C::STAGE_BYTES + part * (C::A_BYTES + C::B_BYTES);
+            const uint32_t sB = sA + C::A_BYTES;
+            const CUtensorMap* ma = part ? &tAl : &tA;
+            const CUtensorMap* mb = part ? &tBl : &tB;
+            if (!p.a_mn) {
+              tma_load_3d(sA, ma, fb, k0, m0, z);
+            } else {
+#pragma unroll
+              for (int i = 0; i < C::A_BOXES_MN; ++i)
+                tma_load_3d(sA + i * C::MN_BOX_BYTES, ma, fb, m0 + i * C::MN_ATOM, k0, z);
+            }
+            if (!p.b_mn) {
+              tma_load_3d(sB, mb, fb, k0, n0, z);
+            } else {
+#pragma unroll
+              for (int i = 0; i < C::B_BOXES_MN; ++i)
+                tma_load_3d(sB + i * C::MN_BOX_BYTES, mb, fb, n0 + i * C::MN_ATOM, k0, z);
+            }
+          }
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // Wait for the copies this thread started so none lands after exit.
+        for (int s = 0; s < C::STAGES; ++s)
+          if (armed & (1u << s)) mbar_wait_drain(full_bar(s), (armed_par >> s) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (long long t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < p.nkb; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sA = sbase + stage * C::STAGE_BYTES;
+          const uint32_t sB = sA + C::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < C::NSUB; ++kk) {
+            const uint64_t da =
+                p.a_mn ? smem_desc(sA + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO, C::MN_LAYOUT)
+                       : smem_desc_sw128(sA + kk * 32, 16, 1024);
+            const uint64_t db =
+                p.b_mn ? smem_desc(sB + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO, C::MN_LAYOUT)
+                       : smem_desc_sw128(sB + kk * 32, 16, 1024);
+            const uint32_t accum = (kb | kk) ? 1u : 0u;
+            if (KT == 0) {
+              mma_f16(d_tmem, da, db, p.idesc, accum);
+            } else if (KT == 1) {
+              mma_tf32(d_tmem, da, db, p.idesc, accum);
+            } else {
+              const uint32_t lo_off = C::A_BYTES + C::B_BYTES;
+              const uint64_t dal =
+                  p.a_mn ? smem_desc(sA + lo_off + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO,
+                                     C::MN_LAYOUT)
+                         : smem_desc_sw128(sA + lo_off + kk * 32, 16, 1024);
+              const uint64_t dbl =
+                  p.b_mn ? smem_desc(sB + lo_off + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO,
+                                     C::MN_LAYOUT)
+                         : smem_desc_sw128(sB + lo_off + kk * 32, 16, 1024);
+              mma_tf32(d_tmem, dal, db, p.idesc, accum);
+              mma_tf32(d_tmem, da, dbl, p.idesc, 1u);
+              mma_tf32(d_tmem, da, db, p.idesc, 1u);
+            }
+          }
+          mma_commit(empty_bar(stage));
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(tfull_bar(acc));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // Every MMA issued above must be complete before TMEM is released.
+      mma_commit(fin_bar);
+      mbar_wait_drain(fin_bar, 0);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;
+    const long long dd = static_cast<long long>(p.dim) * p.dim;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+      if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag)) break;
+      tc_fence_after();
+      long long blk;
+      int m0, n0;
+      decode_tile(t, p, blk, m0, n0, BN);
+      const int rg = m0 + row;
+      const long long rbase = blk * dd + static_cast<long long>(rg) * p.dim;
+      float rsum = 0.0f;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 16; ++c) {
+        uint32_t r[16];
+        tmem_ld16(taddr + c * 16, r);
+        tmem_wait_ld();
+        const int cg0 = n0 + c * 16;
+        epilogue16(p.epi, blk, rg, cg0, rbase + cg0, r, rsum);
+      }
+      if (p.epi.resid_acc != nullptr) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) rsum += __shfl_xor_sync(0xffffffffu, rsum, off);
+        if (lane == 0) atomicAdd(p.epi.resid_acc + blk * p.epi.resid_stride, rsum);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, []() {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// Tensor map over a stack of nblocks row-major dim x dim matrices, box
+// (box_inner elements along the contiguous axis) x box_outer rows, 128B swizzle.
+static bool make_tmap(CUtensorMap* m, const void* base, int esize, int dim, long long nblocks,
+                      uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) return false;
+  const CUtensorMapDataType dt =
+      esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  cuuint64_t gdim[3] = {static_cast<cuuint64_t>(dim), static_cast<cuuint64_t>(dim),
+                        static_cast<cuuint64_t>(nblocks)};
+  cuuint64_t gstride[2] = {static_cast<cuuint64_t>(dim) * esize,
+                           static_cast<cuuint64_t>(dim) * dim * esize};
+  cuuint32_t box[3] = {box_inner, box_outer, 1};
+  cuuint32_t estride[3] = {1, 1, 1};
+  CUresult r = enc(m, dt, 3, const_cast<void*>(base), gdim, gstride, box, estride,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int device_sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev < 0 || dev >= 64) return 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+template <int BN, int KT>
+static dash_status run_gemm(const GemmLaunch& g, cudaStream_t st) {
+  using C = Cfg<BN, KT>;
+  CUtensorMap tA, tB, tAl, tBl;
+  const int a_mn = g.transA ? 1 : 0;
+  const int b_mn = g.transB ? 0 : 1;
+  const uint32_t a_in = a_mn ? C::MN_ATOM : C::BK, a_out = a_mn ? C::BK : 128;
+  const uint32_t b_in = b_mn ? C::MN_ATOM : C::BK, b_out = b_mn ? C::BK : BN;
+  // The TMA swizzle must produce the layout the MMA descriptor names.
+  const CUtensorMapSwizzle mn_swz =
+      (KT == 0) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B;
+  const CUtensorMapSwizzle a_swz = a_mn ? mn_swz : CU_TENSOR_MAP_SWIZZLE_128B;
+  const CUtensorMapSwizzle b_swz = b_mn ? mn_swz : CU_TENSOR_MAP_SWIZZLE_128B;
+  if (!make_tmap(&tA, g.A, C::EB, g.dim, g.nblocks, a_in, a_out, a_swz)) return DASH_ERR_CUDA;
+  if (!make_tmap(&tB, g.B, C::EB, g.dim, g.nblocks, b_in, b_out, b_swz)) return DASH_ERR_CUDA;
+  if (KT == 2) {
+    if (!make_tmap(&tAl, g.A_lo, C::EB, g.dim, g.nblocks, a_in, a_out, a_swz))
+      return DASH_ERR_CUDA;
+    if (!make_tmap(&tBl, g.B_lo, C::EB, g.dim, g.nblocks, b_in, b_out, b_swz))
+      return DASH_ERR_CUDA;
+  } else {
+    tAl = tA;
+    tBl = tB;
+  }
+  KParams p;
+  p.dim = g.dim;
+  p.tiles_m = g.dim / 128;
+  p.tiles_n = g.dim / BN;
+  p.total_tiles = g.nblocks * p.tiles_m * p.tiles_n;
+  p.nkb = g.dim / C::BK;
+  const uint32_t fmt = (g.kind == KIND_BF16) ? 1u : (g.kind == KIND_F16 ? 0u : 2u);
+  p.idesc = make_idesc(fmt, a_mn, b_mn, 128, BN);
+  p.a_mn = a_mn;
+  p.b_mn = b_mn;
+  p.epi = g.epi;
+  if (cudaFuncSetAttribute(gemm_tc_kernel<BN, KT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::SMEM_BYTES) != cudaSuccess)
+    return DASH_ERR_CUDA;
+  const int sms = device_sm_count();
+  if (sms <= 0) return DASH_ERR_CUDA;
+  const long long grid = p.total_tiles < sms ? p.total_tiles : sms;
+  const int rec = trace_begin(st);
+  gemm_tc_kernel<BN, KT><<<static_cast<unsigned>(grid), 192, C::SMEM_BYTES, st>>>(tA, tB, tAl,
+                                                                                  tBl, p);
+  const cudaError_t err = cudaGetLastError();
+  if (rec >= 0) {
+    const double bb = static_cast<double>(g.dim) * g.dim * g.nblocks;
+    double bytes = 2.0 * bb * (KT == 2 ? 8 : C::EB);
+    for (int o = 0; o < g.epi.nout; ++o) bytes += bb * fmt_bytes(g.epi.out[o].fmt);
+    if (g.epi.E_hi != nullptr) bytes += bb * fmt_bytes(g.epi.E_fmt);
+    const int kind = KT == 2 ? DASH_TRACE_GEMM_3XTF32
+                             : (KT == 1 ? DASH_TRACE_GEMM_TF32
+                                        : (g.kind == KIND_BF16 ? DASH_TRACE_GEMM_BF16
+                                                               : DASH_TRACE_GEMM_F16));
+    trace_end(rec, st, kind, 2.0 * bb * g.dim, bytes);
+  }
+  return err == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
+}
+
+dash_status launch_gemm(const GemmLaunch& g, cudaStream_t st) {
+  if (g.nblocks <= 0) return DASH_OK;
+  if (g.dim % 128 != 0 || g.dim < 128 || g.dim > 2048) return DASH_ERR_INVALID_ARG;
+  const bool wide = (g.dim % 256) == 0;
+  switch (g.kind) {
+    case KIND_F16:
+    case KIND_BF16:
+      return wide ? run_gemm<256, 0>(g, st) : run_gemm<128, 0>(g, st);
+    case KIND_TF32:
+      return wide ? run_gemm<256, 1>(g, st) : run_gemm<128, 1>(g, st);
+    case KIND_TF32X3:
+      return wide ? run_gemm<256, 2>(g, st) : run_gemm<128, 2>(g, st);
+    default:
+      return DASH_ERR_INVALID_ARG;
+  }
+}
+
+}  // namespace dash

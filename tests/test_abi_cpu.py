@@ -1,0 +1,104 @@
+"""Host-side checks of the C ABI: the library builds, loads and exports every
+declared entry point, and rejects bad arguments before touching a GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+from tests.helpers import library
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "dashroot.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol():
+    dr = library()
+    lib = dr.load_library()
+    names = declared_functions()
+    assert len(names) >= 12, names
+    for n in names:
+        assert hasattr(lib, n), "missing export %s" % n
+    assert set(names) == set(dr.SYMBOLS)
+    assert "sm_103a" in dr.version()
+
+
+def test_status_strings():
+    dr = library()
+    for s in range(6):
+        assert dr.status_string(s).startswith("DASH_")
+
+
+def test_matmul_counts_match_oracle():
+    dr = library()
+    import numpy as np
+
+    A = np.eye(4)[None] * 0.5
+    s = np.array([1.0])
+    for k in (1, 2, 3, 10):
+        assert dr.op_matmuls(dr.OP_INV_ROOT_CN, k) == oracle.cn_inv_root(A, s, k)[2]
+        assert dr.op_matmuls(dr.OP_INV_ROOT_NDB, k) == oracle.ndb_inv_root(A, s, k)[2]
+    for d in (1, 2, 3, 8, 16, 32):
+        assert dr.op_matmuls(dr.OP_INV_ROOT_CHEB, d) == oracle.cheb_inv_root(A, s, d, 0.01, 1.05)[1]
+    assert dr.op_matmuls(dr.OP_INV_ROOT_CN, 10) == 36
+    assert dr.op_matmuls(dr.OP_INV_ROOT_NDB, 10) == 54
+
+
+def test_workspace_sizes():
+    dr = library()
+    b = 1024
+    mat = b * b
+    assert dr.workspace_size(dr.OP_INV_ROOT_CN, 10, b, dr.FP16, 10) >= 7 * 10 * mat * 2
+    assert dr.workspace_size(dr.OP_INV_ROOT_CN, 10, b, dr.FP32_3XTF32, 10) >= 7 * 10 * mat * 8
+    assert dr.workspace_size(dr.OP_INV_ROOT_NDB, 10, b, dr.TF32, 10) >= 6 * 10 * mat * 4
+    assert dr.workspace_size(dr.OP_INV_ROOT_CHEB, 10, b, dr.BF16, 16) >= 4 * 10 * mat * 2
+    assert dr.workspace_size(dr.OP_ACCUMULATE, 10, b, dr.BF16, 0) == 0
+    assert dr.workspace_size(dr.OP_SPECTRAL_SCALE, 10, b, 0, 32) >= 2 * 10 * b * 32 * 4
+
+
+def test_bad_arguments_rejected_on_host():
+    dr = library()
+    lib = dr.load_library()
+    null = ctypes.c_void_p(0)
+    bad = ctypes.c_void_p(8)  # misaligned, never dereferenced
+    sz = ctypes.c_size_t(0)
+    # B not a multiple of 128 / out of range / bad precision.
+    assert lib.dash_workspace_size(2, 4, 100, 0, 10, ctypes.byref(sz)) == 1
+    assert lib.dash_workspace_size(2, 4, 4096, 0, 10, ctypes.byref(sz)) == 1
+    assert lib.dash_workspace_size(2, 4, 256, 9, 10, ctypes.byref(sz)) == 1
+    assert lib.inv_root_cn(null, 0.0, null, 4, 100, 10, 0, null, null, null, 0, null) == 1
+    assert lib.inv_root_cn(null, 0.0, null, 4, 128, 0, 0, null, null, null, 0, null) == 1
+    assert lib.inv_root_ndb(null, 0.0, null, 4, 128, 10, 7, null, null, null, 0, null) == 1
+    assert lib.inv_root_cheb(null, 0.0, null, 4, 128, 0, 0.01, 1.0, 0, null, null, 0, null) == 1
+    assert lib.inv_root_cheb(null, 0.0, null, 4, 128, 8, 1.0, 0.5, 0, null, null, 0, null) == 1
+    # Misaligned pointers.
+    assert lib.inv_root_cn(bad, 0.0, bad, 4, 128, 10, 0, bad, null, null, 0, null) == 1
+    assert lib.dash_gemm(bad, null, 0, bad, null, 0, 2, 128, 1, bad, null) == 1
+    # Null workspace where one is required.
+    assert lib.spectral_scale(ctypes.c_void_p(256), 0.0, 2, 128, 0, 32, 10,
+                              ctypes.c_void_p(512), ctypes.c_void_p(1024), null, 0, null) == 1
+    # beta outside [0, 1].
+    assert lib.shampoo_accumulate(ctypes.c_void_p(256), 1, 2, 128, ctypes.c_float(1.5),
+                                  ctypes.c_void_p(512), null, null, null, 0, null) == 1
+    # N == 0 is a no-op.
+    assert lib.inv_root_cn(null, 0.0, null, 0, 128, 10, 0, null, null, null, 0, null) == 0
+    assert lib.dash_gemm(null, null, 0, null, null, 0, 0, 128, 1, null, null) == 0
+
+
+def test_workspace_too_small_reported():
+    dr = library()
+    lib = dr.load_library()
+    p = ctypes.c_void_p(1 << 20)  # 256-aligned, never dereferenced: fails before any launch
+    # Room for the per-call arrays but not for one block's iterates.
+    assert lib.inv_root_cn(p, 0.0, p, 4, 1024, 10, 0, p, None, p, 4096, None) == 4
+    assert lib.inv_root_ndb(p, 0.0, p, 4, 1024, 10, 2, p, None, p, 4096, None) == 4
+    assert lib.precondition_apply(p, 1, p, 4, 1024, 0, p, p, 4096, None) == 4

@@ -1,0 +1,206 @@
+"""GPU path against the float64 oracle on the same seeded inputs.
+
+Each test hands the oracle the exact fp32 bits the GPU consumed (and, for the
+root solvers, the GPU's own fp32 scale), so every step is checked on its own.
+Gates (relative Frobenius error of the result, per block):
+  3xTF32 1e-4, TF32 2e-3, FP16/BF16 Coupled Newton and Chebyshev 1e-2;
+  NDB in half precision is reported, not gated (the pages call it unstable).
+Power-iteration lambda: relative error 1e-5.  Accumulate / apply: 1e-5 / 1e-4.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests.helpers import library, rel_fro_blocks, require_gpu, to64
+
+pytestmark = pytest.mark.gpu
+
+GATE = {"3xtf32": 1e-4, "tf32": 2e-3, "fp16": 1e-2, "bf16": 1e-2}
+PRECS = ["3xtf32", "tf32", "fp16", "bf16"]
+
+
+def wishart_case(n, b, seed):
+    A = synth.wishart(n, b, seed=seed, device="cuda")
+    V0 = synth.start_vectors(n, b, 32, seed=seed + 1, device="cuda")
+    return A, V0
+
+
+@pytest.mark.parametrize("b", [128, 384])
+def test_power_lambda(b):
+    require_gpu()
+    dr = library()
+    A, V0 = wishart_case(8, b, 1000 + b)
+    for iters, nv in ((10, 32), (1, 5), (3, 17)):
+        lam = dr.spectral_scale(A, dr.SCALE_POWER, V0[:, :, :nv].contiguous(), iters, ridge=1e-3)
+        torch.cuda.synchronize()
+        ref = oracle.power_lambda(to64(A), to64(V0[:, :, :nv]), iters, ridge=1e-3)
+        assert np.max(np.abs(to64(lam) - ref) / ref) < 1e-5, (iters, nv)
+    assert dr.device_status() == 0
+
+
+def test_frobenius_scale():
+    require_gpu()
+    dr = library()
+    A, _ = wishart_case(5, 256, 7)
+    s = dr.spectral_scale(A, dr.SCALE_FROBENIUS, ridge=0.5)
+    ref = oracle.frobenius_norm(to64(A), ridge=0.5)
+    assert np.max(np.abs(to64(s) - ref) / ref) < 1e-5
+
+
+@pytest.mark.parametrize("prec", PRECS)
+@pytest.mark.parametrize("iters", [1, 2, 10])
+def test_cn_parity(prec, iters):
+    require_gpu()
+    dr = library()
+    A, V0 = wishart_case(8, 128, 1001)
+    lam = dr.spectral_scale(A, dr.SCALE_POWER, V0, 10)
+    X, r = dr.inv_root_cn(A, lam, iters=iters, prec=prec, resid=True)
+    torch.cuda.synchronize()
+    assert dr.device_status() == 0
+    Xr, rr, _ = oracle.cn_inv_root(to64(A), to64(lam), iters)
+    err = rel_fro_blocks(to64(X), Xr)
+    assert err.max() < GATE[prec], err
+    tol = 1e-4 if prec == "3xtf32" else 5e-2
+    assert np.max(np.abs(to64(r) - rr)) < tol * max(1.0, rr.max())
+
+
+@pytest.mark.parametrize("prec", PRECS)
+@pytest.mark.parametrize("iters", [1, 2, 10])
+def test_ndb_parity(prec, iters):
+    require_gpu()
+    dr = library()
+    A, V0 = wishart_case(8, 128, 1002)
+    lam = dr.spectral_scale(A, dr.SCALE_POWER, V0, 10)
+    X, r = dr.inv_root_ndb(A, lam, iters=iters, prec=prec, resid=True)
+    torch.cuda.synchronize()
+    assert dr.device_status() == 0
+    Xr, rr, _ = oracle.ndb_inv_root(to64(A), to64(lam), iters)
+    err = rel_fro_blocks(to64(X), Xr)
+    print("NDB %s iters=%d max rel err %.3e" % (prec, iters, err.max()))
+    if prec in ("3xtf32", "tf32"):
+        assert err.max() < GATE[prec], err
+        tol = 1e-4 if prec == "3xtf32" else 5e-2
+        assert np.max(np.abs(to64(r) - rr)) < tol * max(1.0, rr.max())
+    else:
+        pass  # half-precision NDB: reported above, not gated
+
+
+@pytest.mark.parametrize("prec", PRECS)
+@pytest.mark.parametrize("degree", [1, 2, 3, 16])
+def test_cheb_parity(prec, degree):
+    require_gpu()
+    dr = library()
+    A, V0 = wishart_case(8, 128, 1003)
+    lam = dr.spectral_scale(A, dr.SCALE_POWER, V0, 10)
+    X = dr.inv_root_cheb(A, lam, degree=degree, lo=1e-2, hi=1.05, prec=prec)
+    torch.cuda.synchronize()
+    assert dr.device_status() == 0
+    Xr, _ = oracle.cheb_inv_root(to64(A), to64(lam), degree, 1e-2, 1.05)
+    err = rel_fro_blocks(to64(X), Xr)
+    assert err.max() < GATE[prec], err
+
+
+@pytest.mark.parametrize("b", [256, 384])
+def test_roots_other_sizes(b):
+    require_gpu()
+    dr = library()
+    A, V0 = wishart_case(3, b, 1004 + b)
+    lam = dr.spectral_scale(A, dr.SCALE_POWER, V0, 10)
+    lam64 = to64(lam)
+    X = dr.inv_root_cn(A, lam, iters=8, prec="3xtf32", ridge=1e-4)
+    Xr, _, _ = oracle.cn_inv_root(to64(A), lam64, 8, ridge=1e-4)
+    assert rel_fro_blocks(to64(X), Xr).max() < 1e-4
+    X = dr.inv_root_ndb(A, lam, iters=6, prec="tf32", ridge=1e-4)
+    Xr, _, _ = oracle.ndb_inv_root(to64(A), lam64, 6, ridge=1e-4)
+    assert rel_fro_blocks(to64(X), Xr).max() < 2e-3
+    X = dr.inv_root_cheb(A, lam, degree=8, prec="3xtf32", ridge=1e-4)
+    Xr, _ = oracle.cheb_inv_root(to64(A), lam64, 8, 1e-2, 1.05, ridge=1e-4)
+    assert rel_fro_blocks(to64(X), Xr).max() < 1e-4
+    assert dr.device_status() == 0
+
+
+def test_chunked_workspace_is_bitwise_identical():
+    require_gpu()
+    dr = library()
+    A, V0 = wishart_case(8, 128, 1005)
+    lam = dr.spectral_scale(A, dr.SCALE_POWER, V0, 10)
+    for op, fn, kw in ((dr.OP_INV_ROOT_CN, dr.inv_root_cn, {"iters": 5}),
+                       (dr.OP_INV_ROOT_NDB, dr.inv_root_ndb, {"iters": 4}),
+                       (dr.OP_INV_ROOT_CHEB, dr.inv_root_cheb, {"degree": 6})):
+        full = fn(A, lam, prec="tf32", **kw)
+        param = kw.get("iters", kw.get("degree"))
+        whole = dr.workspace_size(op, 8, 128, dr.TF32, param)
+        small = dr.workspace(op, 8, 128, dr.TF32, param, max_bytes=whole // 3)
+        part = fn(A, lam, prec="tf32", ws=small, **kw)
+        torch.cuda.synchronize()
+        assert torch.equal(full, part), op
+    assert dr.device_status() == 0
+
+
+def test_accumulate_bf16_with_padding():
+    require_gpu()
+    dr = library()
+    ng, b = 4, 256
+    g = torch.Generator(device="cuda")
+    g.manual_seed(77)
+    G = (0.1 * torch.randn((ng, b, b), generator=g, device="cuda")).to(torch.bfloat16)
+    vr = torch.tensor([256, 200, 256, 128], dtype=torch.int32, device="cuda")
+    vc = torch.tensor([256, 256, 72, 128], dtype=torch.int32, device="cuda")
+    for j in range(ng):
+        G[j, int(vr[j]):, :] = 0
+        G[j, :, int(vc[j]):] = 0
+    F0 = torch.randn((2 * ng, b, b), generator=g, device="cuda")
+    F0 = 0.5 * (F0 + F0.transpose(1, 2))
+    F = F0.clone()
+    dr.shampoo_accumulate(G, F, 0.95, vr, vc)
+    torch.cuda.synchronize()
+    ref = oracle.accumulate(to64(F0), to64(G), 0.95, vr.tolist(), vc.tolist())
+    assert rel_fro_blocks(to64(F), ref).max() < 1e-5
+    # Padded part is exactly the identity's.
+    Fh = F.cpu()
+    assert torch.equal(Fh[1, 200:, 200:], torch.eye(56))
+    assert torch.equal(Fh[ng + 2, 72:, :72], torch.zeros(184, 72))
+    assert dr.device_status() == 0
+
+
+def test_accumulate_fp32_gradients():
+    require_gpu()
+    dr = library()
+    ng, b = 3, 128
+    G = torch.randn((ng, b, b), device="cuda")
+    F = torch.zeros((2 * ng, b, b), device="cuda")
+    dr.shampoo_accumulate(G, F, 0.9)
+    dr.shampoo_accumulate(G, F, 0.9)
+    torch.cuda.synchronize()
+    ref = oracle.accumulate(np.zeros((2 * ng, b, b)), to64(G), 0.9)
+    ref = oracle.accumulate(ref, to64(G), 0.9)
+    assert rel_fro_blocks(to64(F), ref).max() < 1e-5
+
+
+@pytest.mark.parametrize("prec", PRECS)
+def test_apply_parity(prec):
+    require_gpu()
+    dr = library()
+    ng, b = 3, 256
+    g = torch.Generator(device="cuda")
+    g.manual_seed(5)
+    G = torch.randn((ng, b, b), generator=g, device="cuda").to(torch.bfloat16)
+    Fr = synth.wishart(2 * ng, b, seed=9, device="cuda") / 2.0
+    U = dr.precondition_apply(G, Fr, prec=prec)
+    torch.cuda.synchronize()
+    ref = oracle.apply_preconditioner(to64(G), to64(Fr))
+    err = rel_fro_blocks(to64(U), ref)
+    gate = {"3xtf32": 1e-5, "tf32": 2e-3, "fp16": 5e-3, "bf16": 2e-2}[prec]
+    assert err.max() < gate, err
+
+
+def test_empty_stack_is_noop():
+    require_gpu()
+    dr = library()
+    A = torch.empty((0, 128, 128), device="cuda")
+    s = torch.empty((0,), device="cuda")
+    X = dr.inv_root_cn(A, s, iters=3, ws=torch.empty(256, dtype=torch.uint8, device="cuda"))
+    assert X.shape == (0, 128, 128)
