@@ -376,7 +376,7 @@ dash_status spectral_scale(const float* A, float ridge, int64_t N, int B, int mo
   }
   // Power iteration, chunked so each chunk's vectors fit in the workspace.
   const size_t per_blk = 2 * static_cast<size_t>(B) * 32 * 4 + 3 * 32 * 4;
-  long long chunk = static_cast<long long>(ws_bytes / (per_blk + 64));
+  long long chunk = static_cast<long long>(ws_bytes / per_blk);
   if (chunk > N) chunk = N;
   if (chunk > 65535) chunk = 65535;
   while (chunk > 0) {

@@ -123,8 +123,11 @@ __global__ void scale_factors_kernel(const float* s, float* inv_s, float* s_m14,
 dash_status launch_scale_factors(const float* s, float* inv_s, float* s_m14, long long n,
                                  cudaStream_t st) {
   if (n <= 0) return DASH_OK;
+  const int rec = trace_begin(st);
   scale_factors_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(s, inv_s, s_m14, n);
-  return cudaGetLastError() == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
+  const cudaError_t err = cudaGetLastError();
+  trace_end(rec, st, DASH_TRACE_REDUCE, 0.0, 12.0 * n);
+  return err == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
 }
 
 __global__ void sqrt_scale_kernel(const float* acc, float* out, long long n, float mul) {
@@ -135,8 +138,11 @@ __global__ void sqrt_scale_kernel(const float* acc, float* out, long long n, flo
 dash_status launch_sqrt_scale(const float* acc, float* out, long long n, float mul,
                               cudaStream_t st) {
   if (n <= 0) return DASH_OK;
+  const int rec = trace_begin(st);
   sqrt_scale_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(acc, out, n, mul);
-  return cudaGetLastError() == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
+  const cudaError_t err = cudaGetLastError();
+  trace_end(rec, st, DASH_TRACE_REDUCE, 0.0, 8.0 * n);
+  return err == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
 }
 
 __global__ void __launch_bounds__(EW_THREADS)
@@ -333,9 +339,12 @@ __global__ void power_finish_kernel(const float* num, const float* den, int nv, 
 dash_status launch_power_finish(const float* num, const float* den, int nv, long long nblocks,
                                 float* lambda, cudaStream_t st) {
   if (nblocks <= 0) return DASH_OK;
+  const int rec = trace_begin(st);
   power_finish_kernel<<<static_cast<unsigned>((nblocks + 127) / 128), 128, 0, st>>>(num, den, nv,
                                                                                     nblocks, lambda);
-  return cudaGetLastError() == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
+  const cudaError_t err = cudaGetLastError();
+  trace_end(rec, st, DASH_TRACE_REDUCE, 0.0, 8.0 * 32 * nblocks);
+  return err == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
 }
 
 }  // namespace dash
