@@ -201,6 +201,32 @@ dash_status dash_gemm(const void* A, const void* A_lo, int trans_a, const void* 
                       const void* B_lo, int trans_b, int64_t N, int B, int prec, float* C,
                       void* stream);
 
+/*
+ * spectral_scale_noalloc -- spectral_scale for callers that cannot allocate
+ * device memory when they run (work being captured into a CUDA graph, hooks
+ * inside another framework's memory manager, fixed-budget or real-time loops).
+ * The pages have no counterpart: it is spectral_scale with its scratch taken
+ * from a static device array of DASH_NOALLOC_SCRATCH_BYTES (32 MiB) built into
+ * the library, which every GPU that loads the library keeps until the process
+ * exits.  Arguments and results are those of spectral_scale without ws/ws_bytes.
+ *   Limit: one pass over all N blocks must fit the array, i.e.
+ *   dash_workspace_size(DASH_OP_SPECTRAL_SCALE, N, B, ...) <= 32 MiB in power
+ *   mode (N <= 127 blocks at B = 1024, N <= 1012 at B = 128) and 4*N bytes in
+ *   Frobenius mode; larger requests return DASH_ERR_WORKSPACE_TOO_SMALL before
+ *   anything is enqueued.
+ *   No cudaMalloc, cudaFree or other allocating call is made.  The first call on
+ *   each device looks up the array's device address (cudaGetSymbolAddress), so
+ *   make that first call before any stream capture.
+ *   All calls share the one array and it keeps the previous call's contents
+ *   (the call clears what it accumulates before use); calls that may overlap
+ *   on the GPU -- different streams, or different host threads -- race on it
+ *   and must be serialised by the caller.
+ */
+#define DASH_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+dash_status spectral_scale_noalloc(const float* A, float ridge, int64_t N, int B, int mode,
+                                   int n_vec, int power_iters, const float* V0,
+                                   float* lambda_out, void* stream);
+
 /* Workspace bytes for op on N blocks of order B (param: iters for CN/NDB,
  * degree for Chebyshev, n_vec for spectral_scale; gdt for accumulate/apply is
  * taken from prec: pass DASH_FP32_3XTF32 for fp32 gradients). */

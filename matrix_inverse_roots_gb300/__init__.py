@@ -48,7 +48,7 @@ SYMBOLS = (
     "shampoo_accumulate", "spectral_scale", "inv_root_cn", "inv_root_ndb", "inv_root_cheb",
     "precondition_apply", "dash_gemm", "dash_workspace_size", "dash_op_matmuls",
     "dash_device_status", "dash_status_string", "dash_version", "dash_trace_start",
-    "dash_trace_count", "dash_trace_read", "dash_trace_stop",
+    "dash_trace_count", "dash_trace_read", "dash_trace_stop", "spectral_scale_noalloc",
 )
 
 _lib = None
@@ -86,6 +86,8 @@ def load_library(path=None):
     lib.dash_status_string.argtypes = [i32]
     lib.dash_status_string.restype = ctypes.c_char_p
     lib.dash_version.restype = ctypes.c_char_p
+    lib.spectral_scale_noalloc.argtypes = [vp, f32, i64, i32, i32, i32, i32, vp, vp, vp]
+    lib.spectral_scale_noalloc.restype = ctypes.c_int
     lib.dash_trace_start.argtypes = [i32]
     lib.dash_trace_count.argtypes = []
     lib.dash_trace_count.restype = i32
@@ -240,6 +242,33 @@ def spectral_scale(A, mode=SCALE_POWER, V0=None, power_iters=10, ridge=0.0, out=
     _check(lib.spectral_scale(_ptr(A), float(ridge), n, b, int(mode), nv, int(power_iters),
                               _ptr(V0), _ptr(out), _ptr(ws), ws.numel(), _stream()),
            "spectral_scale")
+    return out
+
+
+# Bytes of the library's built-in scratch used by spectral_scale_noalloc.
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+
+
+def spectral_scale_noalloc(A, mode=SCALE_POWER, V0=None, power_iters=10, ridge=0.0, out=None):
+    """spectral_scale without a workspace: for callers that may not allocate device
+    memory when they run.  Scratch comes from a fixed 32 MiB array inside the
+    library, so one call handles at most that much (127 blocks of 1024^2 with
+    32 vectors); calls overlapping on the GPU share that array and must not run
+    concurrently.  `out` lets the caller avoid this wrapper's own allocation."""
+    lib = load_library()
+    _stack(A, "A")
+    n, b, _ = A.shape
+    nv = 0
+    if mode == SCALE_POWER:
+        _stack(V0, "V0")
+        if V0.shape[0] != n or V0.shape[1] != b:
+            raise ValueError("V0 must have shape (N, B, n_vec)")
+        nv = V0.shape[2]
+    if out is None:
+        out = torch.empty(n, dtype=torch.float32, device=A.device)
+    _check(lib.spectral_scale_noalloc(_ptr(A), float(ridge), n, b, int(mode), nv,
+                                      int(power_iters), _ptr(V0), _ptr(out), _stream()),
+           "spectral_scale_noalloc")
     return out
 
 
