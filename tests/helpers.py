@@ -49,3 +49,37 @@ def library():
     b.build()
     dr.load_library()
     return dr
+
+
+def cn_f32(a, s, iters, ridge=0.0):
+    """Coupled Newton in plain float32 torch on the CPU (the same iteration as
+    the library's), used only to show the error floor of 32-bit arithmetic."""
+    a = a.float()
+    b = a.shape[0]
+    eye = torch.eye(b, dtype=torch.float32)
+    M = (a + ridge * eye) / s
+    X = eye
+    for i in range(iters):
+        T = (5 * eye - M) / 4
+        X = T if i == 0 else X @ T
+        if i < iters - 1:
+            T2 = T @ T
+            M = (T2 @ T2) @ M
+    return (X * s ** -0.25).double().numpy()
+
+
+def ndb_f32(a, s, iters, ridge=0.0):
+    """Two-stage Newton-Denman-Beavers in plain float32 torch on the CPU."""
+    a = a.float()
+    b = a.shape[0]
+    eye = torch.eye(b, dtype=torch.float32)
+
+    def stage(C, keep_y):
+        Y, Z = C, eye
+        for i in range(iters):
+            P = C if i == 0 else Z @ Y
+            T = (3 * eye - P) / 2
+            Y, Z = Y @ T, (T if i == 0 else T @ Z)
+        return Y if keep_y else Z
+
+    return (stage(stage((a + ridge * eye) / s, True), False) * s ** -0.25).double().numpy()
