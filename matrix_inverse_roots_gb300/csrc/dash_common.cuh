@@ -111,6 +111,29 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
+// 3-D tiled load multicast to every CTA of the cluster named in cta_mask; dst and
+// bar are CTA-relative shared addresses, valid in each destination CTA.
+__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* m, uint32_t bar,
+                                               int x, int y, int z, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "r"(z), "h"(cta_mask)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Full barrier across the thread block cluster (every thread of every CTA).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -186,6 +209,15 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// As mma_commit, arriving on the barrier at the same offset in every CTA of cta_mask.
+__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
       : "memory");
 }
 
@@ -286,6 +318,108 @@ __device__ __forceinline__ void store4(int fmt, void* hi, void* lo, int64_t i, c
   } else {
     *reinterpret_cast<float4*>(static_cast<float*>(hi) + i) = make_float4(v[0], v[1], v[2], v[3]);
   }
+}
+
+// ---------------------------------------------------------------- 256-bit access
+// 32 consecutive bytes per thread: a whole L2 sector per access.
+
+__device__ __forceinline__ void st_v8(void* p, const uint32_t (&r)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
+__device__ __forceinline__ void ld_v8(const void* p, uint32_t (&r)[8]) {
+  asm volatile("ld.global.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "l"(p));
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
+  __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t pack_bf162(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Stores 16 consecutive elements starting at i (i a multiple of 16) with 256-bit
+// stores; the base pointers must be 32-byte aligned.
+__device__ __forceinline__ void store16_v8(int fmt, void* hi, void* lo, int64_t i,
+                                           const float (&v)[16]) {
+  if (fmt == FMT_F16 || fmt == FMT_BF16) {
+    uint32_t r[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      r[j] = (fmt == FMT_F16) ? pack_half2(v[2 * j], v[2 * j + 1])
+                              : pack_bf162(v[2 * j], v[2 * j + 1]);
+    st_v8(static_cast<uint16_t*>(hi) + i, r);
+    return;
+  }
+  uint32_t h[16], l[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    float x = v[j];
+    if (fmt == FMT_TF32 || fmt == FMT_SPLIT) x = rna_tf32(v[j]);
+    h[j] = __float_as_uint(x);
+    if (fmt == FMT_SPLIT) l[j] = __float_as_uint(rna_tf32(v[j] - x));
+  }
+  float* ph = static_cast<float*>(hi) + i;
+  st_v8(ph, *reinterpret_cast<const uint32_t(*)[8]>(&h[0]));
+  st_v8(ph + 8, *reinterpret_cast<const uint32_t(*)[8]>(&h[8]));
+  if (fmt == FMT_SPLIT) {
+    float* pl = static_cast<float*>(lo) + i;
+    st_v8(pl, *reinterpret_cast<const uint32_t(*)[8]>(&l[0]));
+    st_v8(pl + 8, *reinterpret_cast<const uint32_t(*)[8]>(&l[8]));
+  }
+}
+
+// Loads 16 consecutive elements starting at i (i a multiple of 16) with 256-bit
+// loads; the base pointers must be 32-byte aligned.
+__device__ __forceinline__ void load16_v8(int fmt, const void* hi, const void* lo, int64_t i,
+                                          float (&v)[16]) {
+  if (fmt == FMT_F16 || fmt == FMT_BF16) {
+    uint32_t r[8];
+    ld_v8(static_cast<const uint16_t*>(hi) + i, r);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (fmt == FMT_F16) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&r[j]));
+        v[2 * j] = f.x;
+        v[2 * j + 1] = f.y;
+      } else {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r[j]));
+        v[2 * j] = f.x;
+        v[2 * j + 1] = f.y;
+      }
+    }
+    return;
+  }
+  uint32_t a[8], b[8];
+  const float* ph = static_cast<const float*>(hi) + i;
+  ld_v8(ph, a);
+  ld_v8(ph + 8, b);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    v[j] = __uint_as_float(a[j]);
+    v[8 + j] = __uint_as_float(b[j]);
+  }
+  if (fmt == FMT_SPLIT) {
+    const float* pl = static_cast<const float*>(lo) + i;
+    ld_v8(pl, a);
+    ld_v8(pl + 8, b);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      v[j] += __uint_as_float(a[j]);
+      v[8 + j] += __uint_as_float(b[j]);
+    }
+  }
+}
+
+__device__ __forceinline__ bool aligned32(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 31u) == 0;
 }
 
 }  // namespace dash

@@ -67,18 +67,22 @@ struct KParams {
   int dim;
   int tiles_m, tiles_n;
   long long total_tiles;
+  long long total_units;  // tiles / cluster size: one unit per cluster step
   int nkb;
   uint32_t idesc;
   int a_mn, b_mn;
   EpiParams epi;
 };
 
-__device__ __forceinline__ void decode_tile(long long t, const KParams& p, long long& blk, int& m0,
-                                            int& n0, int bn) {
-  const long long per = static_cast<long long>(p.tiles_m) * p.tiles_n;
-  blk = t / per;
-  const int r = static_cast<int>(t - blk * per);
-  m0 = (r / p.tiles_n) * 128;
+// A unit is the group of CL tiles one cluster computes together: the CTAs of a
+// cluster take adjacent 128-row M tiles that share one BN-wide N tile.
+template <int CL>
+__device__ __forceinline__ void decode_unit(long long u, const KParams& p, uint32_t crank,
+                                            long long& blk, int& m0, int& n0, int bn) {
+  const long long per = static_cast<long long>(p.tiles_m / CL) * p.tiles_n;
+  blk = u / per;
+  const int r = static_cast<int>(u - blk * per);
+  m0 = ((r / p.tiles_n) * CL + static_cast<int>(crank)) * 128;
   n0 = (r % p.tiles_n) * bn;
 }
 
@@ -93,7 +97,9 @@ __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
   }
 }
 
-// Epilogue for 16 consecutive columns of one row.
+// Epilogue for 16 consecutive columns of one row.  Stores and the optional
+// E read are 256-bit (one whole L2 sector per thread) when the base pointers
+// allow it, 128-bit otherwise.
 __device__ __forceinline__ void epilogue16(const EpiParams& e, long long blk, int rg, int cg0,
                                            long long idx, const uint32_t (&r)[16], float& rsum) {
   float c[16];
@@ -108,12 +114,16 @@ __device__ __forceinline__ void epilogue16(const EpiParams& e, long long blk, in
   }
   float ev[16];
   if (e.E_hi != nullptr) {
+    if (aligned32(e.E_hi) && (e.E_fmt != FMT_SPLIT || aligned32(e.E_lo))) {
+      load16_v8(e.E_fmt, e.E_hi, e.E_lo, idx, ev);
+    } else {
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      float t[4];
-      load4(e.E_fmt, e.E_hi, e.E_lo, idx + 4 * g, t);
+      for (int g = 0; g < 4; ++g) {
+        float t[4];
+        load4(e.E_fmt, e.E_hi, e.E_lo, idx + 4 * g, t);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) ev[4 * g + j] = t[j];
+        for (int j = 0; j < 4; ++j) ev[4 * g + j] = t[j];
+      }
     }
   } else {
 #pragma unroll
@@ -125,25 +135,30 @@ __device__ __forceinline__ void epilogue16(const EpiParams& e, long long blk, in
     if (o < e.nout) {
       const EpiOut& O = e.out[o];
       const float m = (O.mult != nullptr) ? O.mult[blk] : 1.0f;
+      float d[16];
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        float d[4];
+      for (int j = 0; j < 16; ++j) {
+        const int col = cg0 + j;
+        float v = fmaf(O.alpha, c[j], O.eps * ev[j]);
+        if (rg == col) v += O.gamma;
+        v *= m;
+        if (rg >= pv || col >= pv) v = (rg == col) ? 1.0f : 0.0f;
+        d[j] = v;
+      }
+      if (aligned32(O.hi) && (O.fmt != FMT_SPLIT || aligned32(O.lo))) {
+        store16_v8(O.fmt, O.hi, O.lo, idx, d);
+      } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int col = cg0 + 4 * g + j;
-          float v = fmaf(O.alpha, c[4 * g + j], O.eps * ev[4 * g + j]);
-          if (rg == col) v += O.gamma;
-          v *= m;
-          if (rg >= pv || col >= pv) v = (rg == col) ? 1.0f : 0.0f;
-          d[j] = v;
+        for (int g = 0; g < 4; ++g) {
+          const float q[4] = {d[4 * g], d[4 * g + 1], d[4 * g + 2], d[4 * g + 3]};
+          store4(O.fmt, O.hi, O.lo, idx + 4 * g, q);
         }
-        store4(O.fmt, O.hi, O.lo, idx + 4 * g, d);
       }
     }
   }
 }
 
-template <int BN, int KT>
+template <int BN, int KT, int CL>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tB,
                    const __grid_constant__ CUtensorMap tAl,
@@ -168,11 +183,16 @@ __global__ void __launch_bounds__(192, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // Cluster of CL CTAs: rank within the cluster, cluster index and count.
+  const uint32_t crank = (CL > 1) ? cluster_ctarank() : 0u;
+  const long long cid = blockIdx.x / CL;
+  const long long ncl = gridDim.x / CL;
+  constexpr uint16_t kMask = (1u << CL) - 1u;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), CL);  // released by the MMA warp of every CTA
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
@@ -192,7 +212,11 @@ __global__ void __launch_bounds__(192, 1)
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
   tc_fence_before();
-  __syncthreads();
+  // Barriers must be initialised in every CTA before any peer multicasts into it.
+  if (CL > 1)
+    cluster_sync();
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -203,10 +227,10 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t phase = 0;
       uint32_t armed = 0, armed_par = 0;
       bool ok = true;
-      for (long long t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+      for (long long u = cid; u < p.total_units && ok; u += ncl) {
         long long blk;
         int m0, n0;
-        decode_tile(t, p, blk, m0, n0, BN);
+        decode_unit<CL>(u, p, crank, blk, m0, n0, BN);
         const int z = static_cast<int>(blk);
         for (int kb = 0; kb < p.nkb; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
@@ -230,12 +254,28 @@ __global__ void __launch_bounds__(192, 1)
               for (int i = 0; i < C::A_BOXES_MN; ++i)
                 tma_load_3d(sA + i * C::MN_BOX_BYTES, ma, fb, m0 + i * C::MN_ATOM, k0, z);
             }
-            if (!p.b_mn) {
-              tma_load_3d(sB, mb, fb, k0, n0, z);
-            } else {
+            if (CL == 1) {
+              if (!p.b_mn) {
+                tma_load_3d(sB, mb, fb, k0, n0, z);
+              } else {
 #pragma unroll
-              for (int i = 0; i < C::B_BOXES_MN; ++i)
-                tma_load_3d(sB + i * C::MN_BOX_BYTES, mb, fb, n0 + i * C::MN_ATOM, k0, z);
+                for (int i = 0; i < C::B_BOXES_MN; ++i)
+                  tma_load_3d(sB + i * C::MN_BOX_BYTES, mb, fb, n0 + i * C::MN_ATOM, k0, z);
+              }
+            } else {
+              // The shared N tile: each CTA fetches its share and multicasts it to all.
+              if (!p.b_mn) {
+                const int rows = BN / CL;
+                tma_load_3d_mc(sB + crank * rows * 128, mb, fb, k0, n0 + crank * rows, z, kMask);
+              } else {
+                constexpr int per = C::B_BOXES_MN / CL;
+#pragma unroll
+                for (int j = 0; j < per; ++j) {
+                  const int i = static_cast<int>(crank) * per + j;
+                  tma_load_3d_mc(sB + i * C::MN_BOX_BYTES, mb, fb, n0 + i * C::MN_ATOM, k0, z,
+                                 kMask);
+                }
+              }
             }
           }
           if (++stage == C::STAGES) {
@@ -258,7 +298,7 @@ __global__ void __launch_bounds__(192, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (long long t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+      for (long long u = cid; u < p.total_units && ok; u += ncl) {
         if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag)) {
           ok = false;
           break;
@@ -301,7 +341,11 @@ __global__ void __launch_bounds__(192, 1)
               mma_tf32(d_tmem, da, db, p.idesc, 1u);
             }
           }
-          mma_commit(empty_bar(stage));
+          // The stage is free once every CTA that received the multicast is done.
+          if (CL > 1)
+            mma_commit_mc(empty_bar(stage), kMask);
+          else
+            mma_commit(empty_bar(stage));
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -323,12 +367,12 @@ __global__ void __launch_bounds__(192, 1)
     const long long dd = static_cast<long long>(p.dim) * p.dim;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+    for (long long u = cid; u < p.total_units; u += ncl) {
       if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag)) break;
       tc_fence_after();
       long long blk;
       int m0, n0;
-      decode_tile(t, p, blk, m0, n0, BN);
+      decode_unit<CL>(u, p, crank, blk, m0, n0, BN);
       const int rg = m0 + row;
       const long long rbase = blk * dd + static_cast<long long>(rg) * p.dim;
       float rsum = 0.0f;
@@ -357,6 +401,8 @@ __global__ void __launch_bounds__(192, 1)
 
   tc_fence_before();
   __syncthreads();
+  // No CTA may leave while a peer can still multicast into it or arrive on it.
+  if (CL > 1) cluster_sync();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -418,14 +464,41 @@ int device_sm_count() {
   return cache[dev];
 }
 
-template <int BN, int KT>
+// Largest number of CL-CTA clusters of this kernel that can be resident at once.
+template <int BN, int KT, int CL>
+static int max_active_clusters() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cache[dev] == 0) {
+    using C = Cfg<BN, KT>;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(CL * 256, 1, 1);
+    cfg.blockDim = dim3(192, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, KT, CL>, &cfg) != cudaSuccess)
+      n = 0;
+    cache[dev] = n > 0 ? n : -1;
+  }
+  return cache[dev];
+}
+
+template <int BN, int KT, int CL>
 static dash_status run_gemm(const GemmLaunch& g, cudaStream_t st) {
   using C = Cfg<BN, KT>;
   CUtensorMap tA, tB, tAl, tBl;
   const int a_mn = g.transA ? 1 : 0;
   const int b_mn = g.transB ? 0 : 1;
   const uint32_t a_in = a_mn ? C::MN_ATOM : C::BK, a_out = a_mn ? C::BK : 128;
-  const uint32_t b_in = b_mn ? C::MN_ATOM : C::BK, b_out = b_mn ? C::BK : BN;
+  const uint32_t b_in = b_mn ? C::MN_ATOM : C::BK, b_out = b_mn ? C::BK : BN / CL;
   // The TMA swizzle must produce the layout the MMA descriptor names.
   const CUtensorMapSwizzle mn_swz =
       (KT == 0) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B;
@@ -447,22 +520,42 @@ static dash_status run_gemm(const GemmLaunch& g, cudaStream_t st) {
   p.tiles_m = g.dim / 128;
   p.tiles_n = g.dim / BN;
   p.total_tiles = g.nblocks * p.tiles_m * p.tiles_n;
+  p.total_units = p.total_tiles / CL;
   p.nkb = g.dim / C::BK;
   const uint32_t fmt = (g.kind == KIND_BF16) ? 1u : (g.kind == KIND_F16 ? 0u : 2u);
   p.idesc = make_idesc(fmt, a_mn, b_mn, 128, BN);
   p.a_mn = a_mn;
   p.b_mn = b_mn;
   p.epi = g.epi;
-  if (cudaFuncSetAttribute(gemm_tc_kernel<BN, KT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(gemm_tc_kernel<BN, KT, CL>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::SMEM_BYTES) != cudaSuccess)
     return DASH_ERR_CUDA;
   const int sms = device_sm_count();
   if (sms <= 0) return DASH_ERR_CUDA;
-  const long long grid = p.total_tiles < sms ? p.total_tiles : sms;
+  // Persistent grid: one CTA per SM, or as many clusters as can be co-resident.
+  long long slots = sms / CL;
+  if (CL > 1) {
+    const int mac = max_active_clusters<BN, KT, CL>();
+    if (mac <= 0) return DASH_ERR_CUDA;
+    if (mac < slots) slots = mac;
+  }
+  const long long nclusters = p.total_units < slots ? p.total_units : slots;
   const int rec = trace_begin(st);
-  gemm_tc_kernel<BN, KT><<<static_cast<unsigned>(grid), 192, C::SMEM_BYTES, st>>>(tA, tB, tAl,
-                                                                                  tBl, p);
-  const cudaError_t err = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(nclusters * CL), 1, 1);
+  cfg.blockDim = dim3(192, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t err = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, KT, CL>, tA, tB, tAl, tBl, p);
+  if (err == cudaSuccess) err = cudaGetLastError();
   if (rec >= 0) {
     const double bb = static_cast<double>(g.dim) * g.dim * g.nblocks;
     double bytes = 2.0 * bb * (KT == 2 ? 8 : C::EB);
@@ -482,13 +575,14 @@ dash_status launch_gemm(const GemmLaunch& g, cudaStream_t st) {
   if (g.dim % 128 != 0 || g.dim < 128 || g.dim > 2048) return DASH_ERR_INVALID_ARG;
   const bool wide = (g.dim % 256) == 0;
   switch (g.kind) {
+    // B a multiple of 256: 128x256 tiles, clusters of two CTAs sharing the N tile.
     case KIND_F16:
     case KIND_BF16:
-      return wide ? run_gemm<256, 0>(g, st) : run_gemm<128, 0>(g, st);
+      return wide ? run_gemm<256, 0, 2>(g, st) : run_gemm<128, 0, 1>(g, st);
     case KIND_TF32:
-      return wide ? run_gemm<256, 1>(g, st) : run_gemm<128, 1>(g, st);
+      return wide ? run_gemm<256, 1, 2>(g, st) : run_gemm<128, 1, 1>(g, st);
     case KIND_TF32X3:
-      return wide ? run_gemm<256, 2>(g, st) : run_gemm<128, 2>(g, st);
+      return wide ? run_gemm<256, 2, 2>(g, st) : run_gemm<128, 2, 1>(g, st);
     default:
       return DASH_ERR_INVALID_ARG;
   }
