@@ -399,8 +399,10 @@ dash_status spectral_scale(const float* A, float ridge, int64_t N, int B, int mo
   for (long long c0 = 0; c0 < N; c0 += chunk) {
     const long long nc = (N - c0 < chunk) ? N - c0 : chunk;
     const float* Ac = offset_blocks(A, c0, B, 4);
-    const float* vin = V0 + static_cast<size_t>(c0) * B * n_vec;
-    int vstride = n_vec;
+    // Start vectors into the 32-column layout the product kernel streams.
+    DASH_TRY(launch_pad_vectors(V0 + static_cast<size_t>(c0) * B * n_vec, n_vec, B, nc, V[1], st));
+    const float* vin = V[1];
+    int vstride = 32;
     const float* in_n = nullptr;
     int cur = 0;
     for (int it = 0; it < power_iters; ++it) {

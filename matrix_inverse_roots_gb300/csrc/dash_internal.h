@@ -86,13 +86,18 @@ dash_status launch_frob_acc(const float* A, float ridge, int dim, long long nblo
                             cudaStream_t st);
 
 // One power-iteration product W = (A + ridge I) V for every block; V is read as
-// Vin[blk][row][c] * rsqrt(in_nrm2[blk][c]) (in_nrm2 null = unscaled).
+// Vin[blk][row][c] / sqrt(in_nrm2[blk][c]) (in_nrm2 null = unscaled); Vin has
+// row stride 32 (vin_stride is ignored).
 // Not last: writes W (stride 32) and acc0[blk][c] += sum_r W^2.
 // Last: acc0[blk][c] += sum_r v w, acc1[blk][c] += sum_r v v (W not written).
 dash_status launch_power_step(const float* A, float ridge, int dim, long long nblocks,
                               const float* Vin, int vin_stride, int nv, const float* in_nrm2,
                               float* Wout, float* acc0, float* acc1, int last,
                               cudaStream_t st);
+
+// V (nblocks, dim, 32) = V0 (nblocks, dim, nv) with columns nv..31 zero.
+dash_status launch_pad_vectors(const float* V0, int nv, int dim, long long nblocks, float* V,
+                               cudaStream_t st);
 
 // lambda[k] = max_{c < nv} num[k][c] / den[k][c].
 dash_status launch_power_finish(const float* num, const float* den, int nv, long long nblocks,

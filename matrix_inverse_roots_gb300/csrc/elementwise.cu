@@ -181,32 +181,56 @@ dash_status launch_frob_acc(const float* A, float ridge, int dim, long long nblo
 }
 
 // ---------------------------------------------------------------- power iteration
-// One CTA computes 64 rows x 32 vectors of W = (A + ridge I) V for one block.
-// A is streamed once in 64 x 64 chunks (coalesced float4 rows, transposed into
-// shared memory); the matching 64 x 32 slab of V (normalised on the fly) sits
-// beside it; each thread owns a 2 x 4 register tile of W.
-constexpr int PW_ROWS = 64;
-constexpr int PW_KC = 64;
+// W = (A + ridge I) V for every block, V being B x 32 (n_v <= 32 used columns,
+// stored with a row stride of 32; the previous step's column norms are applied
+// as W = (A V_raw) D + ridge V_raw D, D = diag(1/||column||)).
+// One CTA owns R = min(B, 512) rows of one block (rows a multiple of R/8 apart
+// share a thread), R/2 threads, each with an 8 rows x 8 vectors register tile.
+// A and V stream through shared memory in 16-column chunks with cp.async,
+// double-buffered.  Per column of A a thread does 8 scalar shared loads
+// (conflict-free: its warp's 8 rows are consecutive and the staged row stride is
+// 20 words) and two float4 loads of V for 64 FMAs.
 constexpr int PW_NV = 32;
+constexpr int PW_KC = 16;
+constexpr int PW_STRIDE = 20;  // words per staged row of A (16 used, 16-byte aligned)
+constexpr int PW_MAXR = 512;
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all_but_one() {
+  asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
 
 __global__ void __launch_bounds__(256)
     power_step_kernel(const float* A, float ridge, int dim, long long nblocks, const float* Vin,
                       int vin_stride, int nv, const float* in_nrm2, float* Wout, float* acc0,
-                      float* acc1, int last) {
-  __shared__ float As[PW_KC][PW_ROWS + 1];
-  __shared__ __align__(16) float Vs[PW_KC][PW_NV];
+                      float* acc1, int last, int rows) {
+  extern __shared__ __align__(16) float pw_smem[];
+  float* As = pw_smem;                                    // [2][rows][PW_STRIDE]
+  float* Vs = pw_smem + 2 * rows * PW_STRIDE;             // [2][PW_KC][PW_NV]
   __shared__ float vscale[PW_NV];
   __shared__ float red0[8][PW_NV];
   __shared__ float red1[8][PW_NV];
 
   const long long blk = blockIdx.y;
-  const int r0 = blockIdx.x * PW_ROWS;
+  const int r0 = blockIdx.x * rows;
   const int tid = threadIdx.x;
-  const int tx = tid & 7;   // vector group: columns 4tx..4tx+3
-  const int ty = tid >> 3;  // row pair: rows 2ty, 2ty+1
+  const int nthreads = blockDim.x;  // rows / 2
+  const int groups = rows / 8;      // row groups; group g owns rows g + groups * i
+  const int cg = tid & 3;           // vector columns 8cg .. 8cg+7
+  const int g = tid >> 2;
   const long long dd = static_cast<long long>(dim) * dim;
-  const float* Ab = A + blk * dd;
-  const float* Vb = Vin + blk * static_cast<long long>(dim) * vin_stride;
+  const float* Ab = A + blk * dd + static_cast<long long>(r0) * dim;
+  const float* Vb = Vin + blk * static_cast<long long>(dim) * PW_NV;
+  (void)vin_stride;
 
   if (tid < PW_NV) {
     float sc = 0.0f;
@@ -215,94 +239,114 @@ __global__ void __launch_bounds__(256)
   }
   __syncthreads();
 
-  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-  for (int kc = 0; kc < dim; kc += PW_KC) {
-    // A chunk: rows r0..r0+63, columns kc..kc+63 -> As[col][row].
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int f = tid + 256 * u;
-      const int i = f >> 4;
-      const int j4 = f & 15;
-      const float4 a =
-          *reinterpret_cast<const float4*>(Ab + static_cast<long long>(r0 + i) * dim + kc + 4 * j4);
-      As[4 * j4 + 0][i] = a.x;
-      As[4 * j4 + 1][i] = a.y;
-      As[4 * j4 + 2][i] = a.z;
-      As[4 * j4 + 3][i] = a.w;
+  // Stage chunk kc into buffer b: A rows r0..r0+rows-1 and V rows kc..kc+15,
+  // columns kc..kc+15 of A; all with 16-byte cp.async.
+  auto stage = [&](int b, int kc) {
+    float* Ad = As + b * rows * PW_STRIDE;
+    const int nvec = rows * (PW_KC / 4);
+    for (int f = tid; f < nvec; f += nthreads) {
+      const int r = f >> 2, q = f & 3;
+      cp_async16(Ad + r * PW_STRIDE + 4 * q, Ab + static_cast<long long>(r) * dim + kc + 4 * q);
     }
-    // V slab: rows kc..kc+63, all 32 vector slots (zero beyond nv).
+    float* Vd = Vs + b * PW_KC * PW_NV;
+    for (int f = tid; f < PW_KC * PW_NV / 4; f += nthreads)
+      cp_async16(Vd + 4 * f, Vb + static_cast<long long>(kc) * PW_NV + 4 * f);
+    cp_async_commit();
+  };
+
+  float acc[8][8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int f = tid + 256 * u;
-      const int j = f >> 5;
-      const int c = f & 31;
-      float v = 0.0f;
-      if (c < nv) v = Vb[static_cast<long long>(kc + j) * vin_stride + c] * vscale[c];
-      Vs[j][c] = v;
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+
+  const int nchunks = dim / PW_KC;
+  stage(0, 0);
+  for (int ch = 0; ch < nchunks; ++ch) {
+    const int b = ch & 1;
+    if (ch + 1 < nchunks) {
+      stage(b ^ 1, (ch + 1) * PW_KC);
+      cp_async_wait_all_but_one();
+    } else {
+      cp_async_wait_all();
     }
     __syncthreads();
-#pragma unroll 8
+    const float* Ac = As + b * rows * PW_STRIDE;
+    const float* Vc = Vs + b * PW_KC * PW_NV;
+#pragma unroll
     for (int k = 0; k < PW_KC; ++k) {
-      const float a0 = As[k][2 * ty];
-      const float a1 = As[k][2 * ty + 1];
-      const float4 v = *reinterpret_cast<const float4*>(&Vs[k][4 * tx]);
-      acc[0][0] = fmaf(a0, v.x, acc[0][0]);
-      acc[0][1] = fmaf(a0, v.y, acc[0][1]);
-      acc[0][2] = fmaf(a0, v.z, acc[0][2]);
-      acc[0][3] = fmaf(a0, v.w, acc[0][3]);
-      acc[1][0] = fmaf(a1, v.x, acc[1][0]);
-      acc[1][1] = fmaf(a1, v.y, acc[1][1]);
-      acc[1][2] = fmaf(a1, v.z, acc[1][2]);
-      acc[1][3] = fmaf(a1, v.w, acc[1][3]);
+      float a[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) a[i] = Ac[(g + groups * i) * PW_STRIDE + k];
+      const float4 v0 = *reinterpret_cast<const float4*>(Vc + k * PW_NV + 8 * cg);
+      const float4 v1 = *reinterpret_cast<const float4*>(Vc + k * PW_NV + 8 * cg + 4);
+      const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], v[j], acc[i][j]);
     }
     __syncthreads();
   }
 
-  // Ridge term and the per-column statistics.
-  float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+  // Ridge term, output and per-column statistics.
+  float s0[8], s1[8];
 #pragma unroll
-  for (int rr = 0; rr < 2; ++rr) {
-    const int row = r0 + 2 * ty + rr;
+  for (int j = 0; j < 8; ++j) {
+    s0[j] = 0.0f;
+    s1[j] = 0.0f;
+  }
+  float sc[8];
 #pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
-      const int c = 4 * tx + cc;
-      const float v = (c < nv) ? Vb[static_cast<long long>(row) * vin_stride + c] * vscale[c] : 0.0f;
-      const float w = fmaf(ridge, v, acc[rr][cc]);
-      acc[rr][cc] = w;
+  for (int j = 0; j < 8; ++j) sc[j] = vscale[8 * cg + j];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int row = r0 + g + groups * i;
+    const float* vr = Vb + static_cast<long long>(row) * PW_NV + 8 * cg;
+    const float4 va = *reinterpret_cast<const float4*>(vr);
+    const float4 vb = *reinterpret_cast<const float4*>(vr + 4);
+    const float vraw[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+    float w[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float v = vraw[j] * sc[j];
+      w[j] = fmaf(ridge, v, acc[i][j] * sc[j]);
       if (last) {
-        s0[cc] = fmaf(v, w, s0[cc]);
-        s1[cc] = fmaf(v, v, s1[cc]);
+        s0[j] = fmaf(v, w[j], s0[j]);
+        s1[j] = fmaf(v, v, s1[j]);
       } else {
-        s0[cc] = fmaf(w, w, s0[cc]);
+        s0[j] = fmaf(w[j], w[j], s0[j]);
       }
     }
     if (!last) {
-      float4 o = make_float4(acc[rr][0], acc[rr][1], acc[rr][2], acc[rr][3]);
-      *reinterpret_cast<float4*>(Wout + blk * static_cast<long long>(dim) * PW_NV +
-                                 static_cast<long long>(row) * PW_NV + 4 * tx) = o;
+      float* o = Wout + blk * static_cast<long long>(dim) * PW_NV +
+                 static_cast<long long>(row) * PW_NV + 8 * cg;
+      *reinterpret_cast<float4*>(o) = make_float4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<float4*>(o + 4) = make_float4(w[4], w[5], w[6], w[7]);
     }
   }
-  // Reduce over the 32 row pairs: lanes tx, tx+8, tx+16, tx+24 share columns.
+  // Lanes cg, cg+4, ..., cg+28 hold the same columns.
 #pragma unroll
-  for (int cc = 0; cc < 4; ++cc) {
-    s0[cc] += __shfl_xor_sync(0xffffffffu, s0[cc], 8);
-    s0[cc] += __shfl_xor_sync(0xffffffffu, s0[cc], 16);
-    s1[cc] += __shfl_xor_sync(0xffffffffu, s1[cc], 8);
-    s1[cc] += __shfl_xor_sync(0xffffffffu, s1[cc], 16);
+  for (int j = 0; j < 8; ++j) {
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      s0[j] += __shfl_xor_sync(0xffffffffu, s0[j], off);
+      s1[j] += __shfl_xor_sync(0xffffffffu, s1[j], off);
+    }
   }
   const int w = tid >> 5, l = tid & 31;
-  if (l < 8) {
+  const int nwarps = nthreads >> 5;
+  if (l < 4) {
 #pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
-      red0[w][4 * l + cc] = s0[cc];
-      red1[w][4 * l + cc] = s1[cc];
+    for (int j = 0; j < 8; ++j) {
+      red0[w][8 * l + j] = s0[j];
+      red1[w][8 * l + j] = s1[j];
     }
   }
   __syncthreads();
   if (tid < PW_NV && tid < nv) {
     float a = 0.f, b = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < nwarps; ++i) {
       a += red0[i][tid];
       b += red1[i][tid];
     }
@@ -311,19 +355,51 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// V[blk][r][c] = V0[blk][r][c] for c < nv, 0 for nv <= c < 32.
+__global__ void pad_vectors_kernel(const float* V0, int nv, long long rows_total, float* V) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= rows_total * PW_NV) return;
+  const long long r = i >> 5;
+  const int c = static_cast<int>(i & 31);
+  V[i] = (c < nv) ? V0[r * nv + c] : 0.0f;
+}
+
+dash_status launch_pad_vectors(const float* V0, int nv, int dim, long long nblocks, float* V,
+                               cudaStream_t st) {
+  if (nblocks <= 0) return DASH_OK;
+  const long long n = static_cast<long long>(dim) * nblocks * PW_NV;
+  const int rec = trace_begin(st);
+  pad_vectors_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
+      V0, nv, static_cast<long long>(dim) * nblocks, V);
+  const cudaError_t err = cudaGetLastError();
+  trace_end(rec, st, DASH_TRACE_ELEMENTWISE, 0.0, 4.0 * static_cast<double>(dim) * nblocks * (nv + 32));
+  return err == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
+}
+
+static int power_rows(int dim) {
+  if (dim % 512 == 0) return 512;
+  if (dim % 256 == 0) return 256;
+  return 128;
+}
+
 dash_status launch_power_step(const float* A, float ridge, int dim, long long nblocks,
                               const float* Vin, int vin_stride, int nv, const float* in_nrm2,
                               float* Wout, float* acc0, float* acc1, int last, cudaStream_t st) {
   if (nblocks <= 0) return DASH_OK;
   if (nblocks > 65535) return DASH_ERR_INVALID_ARG;
-  dim3 grid(dim / PW_ROWS, static_cast<unsigned>(nblocks), 1);
+  const int rows = power_rows(dim);
+  const size_t smem = (2 * static_cast<size_t>(rows) * PW_STRIDE + 2 * PW_KC * PW_NV) * 4;
+  if (cudaFuncSetAttribute(power_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return DASH_ERR_CUDA;
+  dim3 grid(dim / rows, static_cast<unsigned>(nblocks), 1);
   const int rec = trace_begin(st);
-  power_step_kernel<<<grid, 256, 0, st>>>(A, ridge, dim, nblocks, Vin, vin_stride, nv, in_nrm2,
-                                          Wout, acc0, acc1, last);
+  power_step_kernel<<<grid, rows / 2, smem, st>>>(A, ridge, dim, nblocks, Vin, vin_stride, nv,
+                                                  in_nrm2, Wout, acc0, acc1, last, rows);
   const cudaError_t err = cudaGetLastError();
   const double bb = static_cast<double>(dim) * dim * nblocks;
   const double vb = static_cast<double>(dim) * nblocks * 4.0;
-  trace_end(rec, st, DASH_TRACE_POWER, 2.0 * bb * nv, 4.0 * bb + vb * (vin_stride + (last ? 0 : 32)));
+  trace_end(rec, st, DASH_TRACE_POWER, 2.0 * bb * nv, 4.0 * bb + vb * (32 + (last ? 0 : 32)));
   return err == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
 }
 
