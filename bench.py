@@ -256,6 +256,7 @@ def run_gpu(args):
 
     import matrix_inverse_roots_gb300 as dr
     import synth
+    from matrix_inverse_roots_gb300.shard import job_throughput, max_over_ranks
 
     rank, world, local = dist_env()
     dist = None
@@ -286,11 +287,9 @@ def run_gpu(args):
     dr.trace_stop()
     assert dr.device_status() == 0, "device-side wait timed out"
     roof, shares, launches = roofline_from_trace(records, peaks)
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = wl.nf * world / (ms * 1e-3)
+    # Weak scaling: every rank refreshes its own stack of wl.nf blocks; the job
+    # time is the slowest rank's and throughput counts the blocks of all ranks.
+    value, ms = job_throughput(wl.nf, ms, device=dev)
 
     # Root-only throughput of the same kernel chain (CN FP16 on the whole stack).
     root_ms = timed_steps(torch, lambda: dr.inv_root_cn(wl.F, wl.lam, CN_ITERS, dr.FP16, ridge=RIDGE,
@@ -307,7 +306,7 @@ def run_gpu(args):
         U_host.copy_(wl.U, non_blocking=True)
 
     e2e_step()
-    e2e_ms = timed_steps(torch, e2e_step, max(2, args.steps // 2), dist)
+    e2e_ms = max_over_ranks(timed_steps(torch, e2e_step, max(2, args.steps // 2), dist), dev)
     h2d = G_host.numel() * G_host.element_size()
     d2h = U_host.numel() * U_host.element_size()
     del G_host, U_host
