@@ -361,6 +361,64 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------------------ solver sweep
+
+
+SWEEP_SIZES = ((256, 61035), (512, 15259), (1024, 3815), (2048, 954))
+SWEEP_RUNS = (("cn", "fp16"), ("cn", "bf16"), ("cn", "tf32"), ("cn", "3xtf32"),
+              ("ndb", "tf32"), ("ndb", "3xtf32"), ("cheb8", "3xtf32"), ("cheb16", "3xtf32"),
+              ("cheb32", "3xtf32"))
+
+
+def run_sweep(args):
+    """Inverse-root throughput over ~16 GB Wishart stacks per block size (one JSON
+    line per block size, solver and precision; not the headline line)."""
+    import torch
+
+    import matrix_inverse_roots_gb300 as dr
+    import synth
+
+    torch.cuda.set_device(0)
+    dr.load_library()
+    peaks = load_peaks()
+    sizes = SWEEP_SIZES if not args.sweep_b else [x for x in SWEEP_SIZES if x[0] in args.sweep_b]
+    for b, n in sizes:
+        A = synth.wishart(n, b, seed=1005 + b, device="cuda", chunk=256)
+        s = dr.spectral_scale(A, dr.SCALE_FROBENIUS)
+        X = torch.empty_like(A)
+        for solver, prec in SWEEP_RUNS:
+            p = dr.PRECISIONS[prec]
+            if solver == "cn":
+                op, param = dr.OP_INV_ROOT_CN, CN_ITERS
+            elif solver == "ndb":
+                op, param = dr.OP_INV_ROOT_NDB, NDB_ITERS
+            else:
+                op, param = dr.OP_INV_ROOT_CHEB, int(solver[4:])
+            ws = dr.workspace(op, n, b, p, param, max_bytes=48 << 30)
+            if solver == "cn":
+                fn = lambda: dr.inv_root_cn(A, s, CN_ITERS, p, X=X, ws=ws)
+            elif solver == "ndb":
+                fn = lambda: dr.inv_root_ndb(A, s, NDB_ITERS, p, X=X, ws=ws)
+            else:
+                fn = lambda: dr.inv_root_cheb(A, s, param, 1e-2, 1.05, p, X=X, ws=ws)
+            fn()
+            ms = timed_steps(torch, fn, 2)
+            mm = dr.op_matmuls(op, param)
+            tflops = mm * 2.0 * b ** 3 * n / (ms * 1e-3) / 1e12
+            base = peaks["bf16_tflops_sustained"]
+            peak = base if prec in ("fp16", "bf16") else (
+                base * TF32_RATIO if prec == "tf32" else base * TF32_RATIO / 3.0)
+            print(json.dumps({"sweep": True, "B": b, "N": n, "solver": solver, "prec": prec,
+                              "ms": round(ms, 2), "blocks_per_s": round(n / (ms * 1e-3), 1),
+                              "matmuls_per_block": mm, "tflops": round(tflops, 1),
+                              "peak_tflops": round(peak, 1), "frac": round(tflops / peak, 4)}),
+                  flush=True)
+            del ws
+            torch.cuda.empty_cache()
+        del A, X, s
+        torch.cuda.empty_cache()
+
+
 # ------------------------------------------------------------------ reference arm
 
 
@@ -411,8 +469,13 @@ def main():
     ap.add_argument("--impl", default="dash", choices=["dash", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--no-ndb", action="store_true", help="skip the NDB fp32 step")
+    ap.add_argument("--sweep", action="store_true",
+                    help="inverse-root throughput sweep over block sizes and precisions")
+    ap.add_argument("--sweep-b", type=int, nargs="*", default=None)
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.sweep:
+        run_sweep(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)

@@ -378,13 +378,18 @@ __global__ void __launch_bounds__(192, 1)
       float rsum = 0.0f;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * BN);
+      // Two register sets: the TMEM load of chunk c+1 is in flight while chunk c
+      // is processed.
+      uint32_t ra[16], rb[16];
+      tmem_ld16(taddr, ra);
 #pragma unroll 1
-      for (int c = 0; c < BN / 16; ++c) {
-        uint32_t r[16];
-        tmem_ld16(taddr + c * 16, r);
-        tmem_wait_ld();
-        const int cg0 = n0 + c * 16;
-        epilogue16(p.epi, blk, rg, cg0, rbase + cg0, r, rsum);
+      for (int c = 0; c < BN / 16; c += 2) {
+        tmem_wait_ld(ra);
+        tmem_ld16(taddr + (c + 1) * 16, rb);
+        epilogue16(p.epi, blk, rg, n0 + c * 16, rbase + n0 + c * 16, ra, rsum);
+        tmem_wait_ld(rb);
+        if (c + 2 < BN / 16) tmem_ld16(taddr + (c + 2) * 16, ra);
+        epilogue16(p.epi, blk, rg, n0 + (c + 1) * 16, rbase + n0 + (c + 1) * 16, rb, rsum);
       }
       if (p.epi.resid_acc != nullptr) {
 #pragma unroll
