@@ -419,6 +419,35 @@ def run_sweep(args):
         torch.cuda.empty_cache()
 
 
+# ------------------------------------------------------------------ profiling case
+
+
+def run_case(args):
+    """A small untimed case for ncu captures: Wishart blocks, a scale, one root call."""
+    import torch
+
+    import matrix_inverse_roots_gb300 as dr
+    import synth
+
+    torch.cuda.set_device(0)
+    dr.load_library()
+    n, b = args.case_n, args.case_b
+    A = synth.wishart(n, b, seed=5, device="cuda")
+    if args.case_scale == "power":
+        s = dr.spectral_scale(A, dr.SCALE_POWER, synth.start_vectors(n, b, 32, seed=6, device="cuda"),
+                              POWER_ITERS)
+    else:
+        s = dr.spectral_scale(A, dr.SCALE_FROBENIUS)
+    if args.case == "cn":
+        dr.inv_root_cn(A, s, args.case_iters, args.case_prec)
+    elif args.case == "ndb":
+        dr.inv_root_ndb(A, s, args.case_iters, args.case_prec)
+    else:
+        dr.inv_root_cheb(A, s, args.case_iters, 1e-2, 1.05, args.case_prec)
+    torch.cuda.synchronize()
+    print("case ok, device status", dr.device_status())
+
+
 # ------------------------------------------------------------------ reference arm
 
 
@@ -472,8 +501,17 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="inverse-root throughput sweep over block sizes and precisions")
     ap.add_argument("--sweep-b", type=int, nargs="*", default=None)
+    ap.add_argument("--case", choices=["cn", "ndb", "cheb"], default=None,
+                    help="run one small untimed case (for profiler captures)")
+    ap.add_argument("--case-n", type=int, default=64)
+    ap.add_argument("--case-b", type=int, default=1024)
+    ap.add_argument("--case-prec", default="fp16")
+    ap.add_argument("--case-iters", type=int, default=3)
+    ap.add_argument("--case-scale", choices=["power", "frobenius"], default="power")
     args = ap.parse_args()
-    if args.sweep:
+    if args.case:
+        run_case(args)
+    elif args.sweep:
         run_sweep(args)
     elif args.impl == "reference":
         run_reference(args)
