@@ -193,7 +193,6 @@ dash_status launch_frob_acc(const float* A, float ridge, int dim, long long nblo
 constexpr int PW_NV = 32;
 constexpr int PW_KC = 16;
 constexpr int PW_STRIDE = 20;  // words per staged row of A (16 used, 16-byte aligned)
-constexpr int PW_MAXR = 512;
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem)

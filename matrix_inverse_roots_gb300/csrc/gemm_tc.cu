@@ -3,7 +3,10 @@
 // step (factor accumulation, the Coupled Newton / Newton-Denman-Beavers /
 // Clenshaw iterations, the preconditioned update) runs through this kernel.
 //
-// Design (one CTA per SM, persistent):
+// Design (one CTA per SM, persistent; for B a multiple of 256 the CTAs run in
+// pairs, cta_group::2, that share one 256 x 256 tile: each stages its own 128
+// rows of A and half of B, the even CTA issues the MMAs, each CTA holds 128
+// accumulator rows):
 //   warp 0      TMA producer: streams 128-byte-wide, 128B-swizzled operand tiles
 //               into a ring of shared-memory stages (mbarrier full/empty pairs).
 //   warp 1      allocates TMEM and issues tcgen05.mma from one thread into one of
@@ -35,23 +38,34 @@ int gemm_read_clear_error() {
 }
 
 // KT: 0 = 16-bit operands (kind::f16), 1 = TF32, 2 = 3xTF32.
-template <int BN, int KT>
+// MODE: 0 = one CTA per 128 x BN tile;
+//       1 = clusters of two CTAs on adjacent 128-row tiles that share the N tile,
+//           each fetching half of B and multicasting it to both;
+//       2 = CTA pairs running one 256 x BN MMA (cta_group::2): each CTA stages
+//           its own 128 rows of A and half of B, the even CTA issues the MMA and
+//           both CTAs hold 128 rows of the accumulator.
+template <int BN, int KT, int MODE>
 struct Cfg {
-  static constexpr int BM = 128;
+  static constexpr int CL = MODE ? 2 : 1;       // CTAs per cluster
+  static constexpr int BM = 128;                // accumulator rows per CTA
   static constexpr int EB = (KT == 0) ? 2 : 4;  // operand element bytes
   static constexpr int BK = 128 / EB;           // elements per 128-byte row
   static constexpr int UK = (KT == 0) ? 16 : 8; // K of one MMA
   static constexpr int NSUB = BK / UK;          // MMAs per k-block
   static constexpr int A_BYTES = BM * 128;
-  static constexpr int B_BYTES = BN * 128;
+  static constexpr int B_ROWS = (MODE == 2) ? BN / 2 : BN;  // B rows staged per CTA
+  static constexpr int B_BYTES = B_ROWS * 128;
   static constexpr int NPART = (KT == 2) ? 2 : 1;
   static constexpr int STAGE_BYTES = (A_BYTES + B_BYTES) * NPART;
-  static constexpr int STAGES_RAW = (192 * 1024) / STAGE_BYTES;
+  // Bytes the barrier owner waits for per stage (both CTAs' loads for a pair).
+  static constexpr int EXPECT_BYTES = (MODE == 2 ? 2 : 1) * STAGE_BYTES;
+  static constexpr int STAGES_RAW = (224 * 1024) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
   static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int MMA_M = (MODE == 2) ? 256 : 128;
   static constexpr int MN_ATOM = 128 / EB;      // elements in one 128-byte MN row
   static constexpr int A_BOXES_MN = BM / MN_ATOM;
-  static constexpr int B_BOXES_MN = BN / MN_ATOM;
+  static constexpr int B_BOXES_MN = B_ROWS / MN_ATOM;  // MN-major boxes of B per CTA tile
   static constexpr int MN_BOX_BYTES = BK * 128;  // one MN-major box: BK rows of 128 B
   // MN-major 32-bit operands are read with 32-byte swizzle atoms; that layout
   // groups K in slabs of 4 rows (512 B), the 16-byte-atom layout in slabs of 8.
@@ -158,12 +172,13 @@ __device__ __forceinline__ void epilogue16(const EpiParams& e, long long blk, in
   }
 }
 
-template <int BN, int KT, int CL>
+template <int BN, int KT, int MODE>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tB,
                    const __grid_constant__ CUtensorMap tAl,
                    const __grid_constant__ CUtensorMap tBl, const __grid_constant__ KParams p) {
-  using C = Cfg<BN, KT>;
+  using C = Cfg<BN, KT, MODE>;
+  constexpr int CL = C::CL;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw_base & 1023u)) & 1023u;
@@ -185,6 +200,7 @@ __global__ void __launch_bounds__(192, 1)
   const int lane = threadIdx.x & 31;
   // Cluster of CL CTAs: rank within the cluster, cluster index and count.
   const uint32_t crank = (CL > 1) ? cluster_ctarank() : 0u;
+  const bool leader = (crank == 0);  // in MODE 2 the leader issues the pair's MMAs
   const long long cid = blockIdx.x / CL;
   const long long ncl = gridDim.x / CL;
   constexpr uint16_t kMask = (1u << CL) - 1u;
@@ -192,11 +208,13 @@ __global__ void __launch_bounds__(192, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), CL);  // released by the MMA warp of every CTA
+      // MODE 1: released by the MMA warp of both CTAs; MODE 2: by the leader's.
+      mbar_init(empty_bar(s), MODE == 1 ? 2 : 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 4);
+      // MODE 2: the leader's accumulator is freed by the epilogues of both CTAs.
+      mbar_init(tempty_bar(a), MODE == 2 ? 8 : 4);
     }
     mbar_init(fin_bar, 1);
     *abort_flag = 0;
@@ -210,9 +228,14 @@ __global__ void __launch_bounds__(192, 1)
       tma_prefetch_desc(&tBl);
     }
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+  if (warp == 1) {
+    if (MODE == 2)
+      tmem_alloc_pair(smem_u32(tmem_slot), C::TMEM_COLS);
+    else
+      tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+  }
   tc_fence_before();
-  // Barriers must be initialised in every CTA before any peer multicasts into it.
+  // Barriers must be initialised in every CTA before any peer signals into it.
   if (CL > 1)
     cluster_sync();
   else
@@ -237,16 +260,38 @@ __global__ void __launch_bounds__(192, 1)
             ok = false;
             break;
           }
-          const uint32_t fb = full_bar(stage);
-          mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-          armed |= 1u << stage;
-          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          uint32_t fb = full_bar(stage);
+          if (MODE != 2 || leader) {
+            mbar_arrive_expect_tx(fb, C::EXPECT_BYTES);
+            armed |= 1u << stage;
+            armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          }
+          // In a pair, every load is counted on the leader's barrier.
+          if (MODE == 2) fb = leader ? fb : mapa_shared(fb, crank & ~1u);
           const int k0 = kb * C::BK;
           for (int part = 0; part < C::NPART; ++part) {
             const uint32_t sA = sbase + stage * C::STAGE_BYTES + part * (C::A_BYTES + C::B_BYTES);
             const uint32_t sB = sA + C::A_BYTES;
             const CUtensorMap* ma = part ? &tAl : &tA;
             const CUtensorMap* mb = part ? &tBl : &tB;
+            if (MODE == 2) {
+              if (!p.a_mn) {
+                tma_load_3d_pair(sA, ma, fb, k0, m0, z);
+              } else {
+#pragma unroll
+                for (int i = 0; i < C::A_BOXES_MN; ++i)
+                  tma_load_3d_pair(sA + i * C::MN_BOX_BYTES, ma, fb, m0 + i * C::MN_ATOM, k0, z);
+              }
+              const int nb = n0 + static_cast<int>(crank) * C::B_ROWS;  // this CTA's half of N
+              if (!p.b_mn) {
+                tma_load_3d_pair(sB, mb, fb, k0, nb, z);
+              } else {
+#pragma unroll
+                for (int i = 0; i < C::B_BOXES_MN; ++i)
+                  tma_load_3d_pair(sB + i * C::MN_BOX_BYTES, mb, fb, nb + i * C::MN_ATOM, k0, z);
+              }
+              continue;
+            }
             if (!p.a_mn) {
               tma_load_3d(sA, ma, fb, k0, m0, z);
             } else {
@@ -285,13 +330,13 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
       if (!ok) {
-        // Wait for the copies this thread started so none lands after exit.
+        // Wait for the copies this CTA's barriers count so none lands after exit.
         for (int s = 0; s < C::STAGES; ++s)
           if (armed & (1u << s)) mbar_wait_drain(full_bar(s), (armed_par >> s) & 1u);
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && (MODE != 2 || leader)) {
       // ------------------------------------------------------------ MMA issuer
       int stage = 0;
       uint32_t phase = 0;
@@ -322,27 +367,42 @@ __global__ void __launch_bounds__(192, 1)
                 p.b_mn ? smem_desc(sB + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO, C::MN_LAYOUT)
                        : smem_desc_sw128(sB + kk * 32, 16, 1024);
             const uint32_t accum = (kb | kk) ? 1u : 0u;
-            if (KT == 0) {
-              mma_f16(d_tmem, da, db, p.idesc, accum);
-            } else if (KT == 1) {
-              mma_tf32(d_tmem, da, db, p.idesc, accum);
-            } else {
+            uint64_t dal = 0, dbl = 0;
+            if (KT == 2) {
               const uint32_t lo_off = C::A_BYTES + C::B_BYTES;
-              const uint64_t dal =
-                  p.a_mn ? smem_desc(sA + lo_off + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO,
-                                     C::MN_LAYOUT)
-                         : smem_desc_sw128(sA + lo_off + kk * 32, 16, 1024);
-              const uint64_t dbl =
-                  p.b_mn ? smem_desc(sB + lo_off + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO,
-                                     C::MN_LAYOUT)
-                         : smem_desc_sw128(sB + lo_off + kk * 32, 16, 1024);
-              mma_tf32(d_tmem, dal, db, p.idesc, accum);
-              mma_tf32(d_tmem, da, dbl, p.idesc, 1u);
-              mma_tf32(d_tmem, da, db, p.idesc, 1u);
+              dal = p.a_mn ? smem_desc(sA + lo_off + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO,
+                                       C::MN_LAYOUT)
+                           : smem_desc_sw128(sA + lo_off + kk * 32, 16, 1024);
+              dbl = p.b_mn ? smem_desc(sB + lo_off + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO,
+                                       C::MN_LAYOUT)
+                           : smem_desc_sw128(sB + lo_off + kk * 32, 16, 1024);
+            }
+            if (MODE == 2) {
+              if (KT == 0) {
+                mma_f16_pair(d_tmem, da, db, p.idesc, accum);
+              } else if (KT == 1) {
+                mma_tf32_pair(d_tmem, da, db, p.idesc, accum);
+              } else {
+                mma_tf32_pair(d_tmem, dal, db, p.idesc, accum);
+                mma_tf32_pair(d_tmem, da, dbl, p.idesc, 1u);
+                mma_tf32_pair(d_tmem, da, db, p.idesc, 1u);
+              }
+            } else {
+              if (KT == 0) {
+                mma_f16(d_tmem, da, db, p.idesc, accum);
+              } else if (KT == 1) {
+                mma_tf32(d_tmem, da, db, p.idesc, accum);
+              } else {
+                mma_tf32(d_tmem, dal, db, p.idesc, accum);
+                mma_tf32(d_tmem, da, dbl, p.idesc, 1u);
+                mma_tf32(d_tmem, da, db, p.idesc, 1u);
+              }
             }
           }
-          // The stage is free once every CTA that received the multicast is done.
-          if (CL > 1)
+          // The stage is free once every CTA whose shared memory fed it is done.
+          if (MODE == 2)
+            mma_commit_pair_mc(empty_bar(stage), kMask);
+          else if (MODE == 1)
             mma_commit_mc(empty_bar(stage), kMask);
           else
             mma_commit(empty_bar(stage));
@@ -352,12 +412,18 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
         if (!ok) break;
-        mma_commit(tfull_bar(acc));
+        if (MODE == 2)
+          mma_commit_pair_mc(tfull_bar(acc), kMask);  // both CTAs hold half the rows
+        else
+          mma_commit(tfull_bar(acc));
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
       // Every MMA issued above must be complete before TMEM is released.
-      mma_commit(fin_bar);
+      if (MODE == 2)
+        mma_commit_pair(fin_bar);
+      else
+        mma_commit(fin_bar);
       mbar_wait_drain(fin_bar, 0);
     }
   } else {
@@ -398,7 +464,12 @@ __global__ void __launch_bounds__(192, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      if (lane == 0) {
+        if (MODE == 2)
+          mbar_arrive_cluster(mapa_shared(tempty_bar(acc), crank & ~1u));
+        else
+          mbar_arrive(tempty_bar(acc));
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
@@ -406,12 +477,15 @@ __global__ void __launch_bounds__(192, 1)
 
   tc_fence_before();
   __syncthreads();
-  // No CTA may leave while a peer can still multicast into it or arrive on it.
+  // No CTA may leave while a peer can still signal into it or use its TMEM.
   if (CL > 1) cluster_sync();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::TMEM_COLS);
+    if (MODE == 2)
+      tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
 }
 
@@ -469,14 +543,15 @@ int device_sm_count() {
   return cache[dev];
 }
 
-// Largest number of CL-CTA clusters of this kernel that can be resident at once.
-template <int BN, int KT, int CL>
+// Largest number of clusters of this kernel that can be resident at once.
+template <int BN, int KT, int MODE>
 static int max_active_clusters() {
   static int cache[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   if (cache[dev] == 0) {
-    using C = Cfg<BN, KT>;
+    using C = Cfg<BN, KT, MODE>;
+    constexpr int CL = C::CL;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -489,16 +564,17 @@ static int max_active_clusters() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, KT, CL>, &cfg) != cudaSuccess)
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, KT, MODE>, &cfg) != cudaSuccess)
       n = 0;
     cache[dev] = n > 0 ? n : -1;
   }
   return cache[dev];
 }
 
-template <int BN, int KT, int CL>
+template <int BN, int KT, int MODE>
 static dash_status run_gemm(const GemmLaunch& g, cudaStream_t st) {
-  using C = Cfg<BN, KT>;
+  using C = Cfg<BN, KT, MODE>;
+  constexpr int CL = C::CL;
   CUtensorMap tA, tB, tAl, tBl;
   const int a_mn = g.transA ? 1 : 0;
   const int b_mn = g.transB ? 0 : 1;
@@ -528,11 +604,11 @@ static dash_status run_gemm(const GemmLaunch& g, cudaStream_t st) {
   p.total_units = p.total_tiles / CL;
   p.nkb = g.dim / C::BK;
   const uint32_t fmt = (g.kind == KIND_BF16) ? 1u : (g.kind == KIND_F16 ? 0u : 2u);
-  p.idesc = make_idesc(fmt, a_mn, b_mn, 128, BN);
+  p.idesc = make_idesc(fmt, a_mn, b_mn, C::MMA_M, BN);
   p.a_mn = a_mn;
   p.b_mn = b_mn;
   p.epi = g.epi;
-  if (cudaFuncSetAttribute(gemm_tc_kernel<BN, KT, CL>,
+  if (cudaFuncSetAttribute(gemm_tc_kernel<BN, KT, MODE>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::SMEM_BYTES) != cudaSuccess)
     return DASH_ERR_CUDA;
@@ -541,7 +617,7 @@ static dash_status run_gemm(const GemmLaunch& g, cudaStream_t st) {
   // Persistent grid: one CTA per SM, or as many clusters as can be co-resident.
   long long slots = sms / CL;
   if (CL > 1) {
-    const int mac = max_active_clusters<BN, KT, CL>();
+    const int mac = max_active_clusters<BN, KT, MODE>();
     if (mac <= 0) return DASH_ERR_CUDA;
     if (mac < slots) slots = mac;
   }
@@ -559,7 +635,7 @@ static dash_status run_gemm(const GemmLaunch& g, cudaStream_t st) {
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t err = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, KT, CL>, tA, tB, tAl, tBl, p);
+  cudaError_t err = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, KT, MODE>, tA, tB, tAl, tBl, p);
   if (err == cudaSuccess) err = cudaGetLastError();
   if (rec >= 0) {
     const double bb = static_cast<double>(g.dim) * g.dim * g.nblocks;
@@ -579,15 +655,18 @@ dash_status launch_gemm(const GemmLaunch& g, cudaStream_t st) {
   if (g.nblocks <= 0) return DASH_OK;
   if (g.dim % 128 != 0 || g.dim < 128 || g.dim > 2048) return DASH_ERR_INVALID_ARG;
   const bool wide = (g.dim % 256) == 0;
+
   switch (g.kind) {
-    // B a multiple of 256: 128x256 tiles, clusters of two CTAs sharing the N tile.
+    // B a multiple of 256: CTA pairs on 256 x 256 tiles (cta_group::2); otherwise
+    // one CTA per 128 x 128 tile.  (MODE 1, clusters multicasting the shared B
+    // tile, measured equal or slower at B = 1024 and is not dispatched.)
     case KIND_F16:
     case KIND_BF16:
-      return wide ? run_gemm<256, 0, 2>(g, st) : run_gemm<128, 0, 1>(g, st);
+      return wide ? run_gemm<256, 0, 2>(g, st) : run_gemm<128, 0, 0>(g, st);
     case KIND_TF32:
-      return wide ? run_gemm<256, 1, 2>(g, st) : run_gemm<128, 1, 1>(g, st);
+      return wide ? run_gemm<256, 1, 2>(g, st) : run_gemm<128, 1, 0>(g, st);
     case KIND_TF32X3:
-      return wide ? run_gemm<256, 2, 2>(g, st) : run_gemm<128, 2, 1>(g, st);
+      return wide ? run_gemm<256, 2, 2>(g, st) : run_gemm<128, 2, 0>(g, st);
     default:
       return DASH_ERR_INVALID_ARG;
   }
