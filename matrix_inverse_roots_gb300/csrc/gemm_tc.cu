@@ -114,11 +114,8 @@ __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
 // Epilogue for 16 consecutive columns of one row.  Stores and the optional
 // E read are 256-bit (one whole L2 sector per thread) when the base pointers
 // allow it, 128-bit otherwise.
-__device__ __forceinline__ void epilogue16(const EpiParams& e, long long blk, int rg, int cg0,
-                                           long long idx, const uint32_t (&r)[16], float& rsum) {
-  float c[16];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) c[j] = __uint_as_float(r[j]);
+__device__ __forceinline__ void epilogue16f(const EpiParams& e, long long blk, int rg, int cg0,
+                                            long long idx, const float (&c)[16], float& rsum) {
   if (e.resid_acc != nullptr) {
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
@@ -170,6 +167,14 @@ __device__ __forceinline__ void epilogue16(const EpiParams& e, long long blk, in
       }
     }
   }
+}
+
+__device__ __forceinline__ void epilogue16(const EpiParams& e, long long blk, int rg, int cg0,
+                                           long long idx, const uint32_t (&r)[16], float& rsum) {
+  float c[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) c[j] = __uint_as_float(r[j]);
+  epilogue16f(e, blk, rg, cg0, idx, c, rsum);
 }
 
 template <int BN, int KT, int MODE>
@@ -489,6 +494,262 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
+// ---------------------------------------------------------------- accurate 3xTF32
+// The tensor core's fp32 accumulation truncates: a K-long product picks up a
+// relative bias of about -(K/8) 2^-24.  This variant of the pair kernel for
+// 3xTF32 bounds it: the MMA warp starts a fresh TMEM partial accumulator every
+// ACC_KB k-blocks (two partials alternate), and eight reducer warps -- two per
+// TMEM lane quarter, 128 columns each -- add the partials into fp32 registers
+// with round-to-nearest.  The fused epilogue then runs on those register sums.
+constexpr int ACC_KB = 2;  // k-blocks (of 32) per TMEM partial
+
+template <int KT>
+__global__ void __launch_bounds__(320, 1)
+    gemm_tc_acc_kernel(const __grid_constant__ CUtensorMap tA,
+                       const __grid_constant__ CUtensorMap tB,
+                       const __grid_constant__ CUtensorMap tAl,
+                       const __grid_constant__ CUtensorMap tBl, const __grid_constant__ KParams p) {
+  constexpr int BN = 256;
+  using C = Cfg<BN, KT, 2>;
+  constexpr int CL = 2;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw_base & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sbase = raw_base + pad;
+  uint8_t* bar_area = smem + C::STAGES * C::STAGE_BYTES;
+  const uint32_t bar0 = sbase + C::STAGES * C::STAGE_BYTES;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
+  auto pfull_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
+  auto pempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + 2 + a); };
+  const uint32_t fin_bar = bar0 + 8u * (2 * C::STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * (2 * C::STAGES + 5));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * (2 * C::STAGES + 5) + 8);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t crank = cluster_ctarank();
+  const bool leader = (crank == 0);
+  const long long cid = blockIdx.x / CL;
+  const long long ncl = gridDim.x / CL;
+  constexpr uint16_t kMask = 3;
+  const int ngroups = p.nkb / ACC_KB;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(pfull_bar(a), 1);
+      mbar_init(pempty_bar(a), 16);  // eight reducer warps in each CTA of the pair
+    }
+    mbar_init(fin_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tA);
+    tma_prefetch_desc(&tB);
+    tma_prefetch_desc(&tAl);
+    tma_prefetch_desc(&tBl);
+  }
+  if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), C::TMEM_COLS);
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_par = 0;
+      bool ok = true;
+      for (long long u = cid; u < p.total_units && ok; u += ncl) {
+        long long blk;
+        int m0, n0;
+        decode_unit<CL>(u, p, crank, blk, m0, n0, BN);
+        const int z = static_cast<int>(blk);
+        for (int kb = 0; kb < p.nkb; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint32_t fb = full_bar(stage);
+          if (leader) {
+            mbar_arrive_expect_tx(fb, C::EXPECT_BYTES);
+            armed |= 1u << stage;
+            armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          }
+          fb = leader ? fb : mapa_shared(fb, 0);
+          const int k0 = kb * C::BK;
+          for (int part = 0; part < C::NPART; ++part) {
+            const uint32_t sA = sbase + stage * C::STAGE_BYTES + part * (C::A_BYTES + C::B_BYTES);
+            const uint32_t sB = sA + C::A_BYTES;
+            const CUtensorMap* ma = part ? &tAl : &tA;
+            const CUtensorMap* mb = part ? &tBl : &tB;
+            if (!p.a_mn) {
+              tma_load_3d_pair(sA, ma, fb, k0, m0, z);
+            } else {
+#pragma unroll
+              for (int i = 0; i < C::A_BOXES_MN; ++i)
+                tma_load_3d_pair(sA + i * C::MN_BOX_BYTES, ma, fb, m0 + i * C::MN_ATOM, k0, z);
+            }
+            const int nb = n0 + static_cast<int>(crank) * C::B_ROWS;
+            if (!p.b_mn) {
+              tma_load_3d_pair(sB, mb, fb, k0, nb, z);
+            } else {
+#pragma unroll
+              for (int i = 0; i < C::B_BOXES_MN; ++i)
+                tma_load_3d_pair(sB + i * C::MN_BOX_BYTES, mb, fb, nb + i * C::MN_ATOM, k0, z);
+            }
+          }
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < C::STAGES; ++s)
+          if (armed & (1u << s)) mbar_wait_drain(full_bar(s), (armed_par >> s) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ------------------------------------------------------------ MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      long long gidx = 0;  // partials issued so far: buffer gidx & 1
+      bool ok = true;
+      for (long long u = cid; u < p.total_units && ok; u += ncl) {
+        for (int kg = 0; kg < ngroups && ok; ++kg, ++gidx) {
+          const int buf = static_cast<int>(gidx & 1);
+          const uint32_t par = static_cast<uint32_t>((gidx >> 1) & 1);
+          if (!mbar_wait(pempty_bar(buf), par ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+          for (int kq = 0; kq < ACC_KB; ++kq) {
+            if (!mbar_wait(full_bar(stage), phase, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sA = sbase + stage * C::STAGE_BYTES;
+            const uint32_t sB = sA + C::A_BYTES;
+            const uint32_t lo_off = C::A_BYTES + C::B_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < C::NSUB; ++kk) {
+              const uint64_t da =
+                  p.a_mn ? smem_desc(sA + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO, C::MN_LAYOUT)
+                         : smem_desc_sw128(sA + kk * 32, 16, 1024);
+              const uint64_t db =
+                  p.b_mn ? smem_desc(sB + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO, C::MN_LAYOUT)
+                         : smem_desc_sw128(sB + kk * 32, 16, 1024);
+              const uint64_t dal =
+                  p.a_mn ? smem_desc(sA + lo_off + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO,
+                                     C::MN_LAYOUT)
+                         : smem_desc_sw128(sA + lo_off + kk * 32, 16, 1024);
+              const uint64_t dbl =
+                  p.b_mn ? smem_desc(sB + lo_off + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO,
+                                     C::MN_LAYOUT)
+                         : smem_desc_sw128(sB + lo_off + kk * 32, 16, 1024);
+              const uint32_t accum = (kq | kk) ? 1u : 0u;  // fresh partial per group
+              mma_tf32_pair(d_tmem, dal, db, p.idesc, accum);
+              mma_tf32_pair(d_tmem, da, dbl, p.idesc, 1u);
+              mma_tf32_pair(d_tmem, da, db, p.idesc, 1u);
+            }
+            mma_commit_pair_mc(empty_bar(stage), kMask);
+            if (++stage == C::STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          mma_commit_pair_mc(pfull_bar(buf), kMask);
+        }
+      }
+      mma_commit_pair(fin_bar);
+      mbar_wait_drain(fin_bar, 0);
+    }
+  } else {
+    // ------------------------------------------------- reducers + epilogue
+    const int q = warp & 3;          // TMEM lane quarter
+    const int h = (warp - 2) >> 2;   // column half: 0 -> 0..127, 1 -> 128..255
+    const int row = q * 32 + lane;
+    const long long dd = static_cast<long long>(p.dim) * p.dim;
+    long long gidx = 0;
+    bool ok = true;
+    for (long long u = cid; u < p.total_units && ok; u += ncl) {
+      long long blk;
+      int m0, n0;
+      decode_unit<CL>(u, p, crank, blk, m0, n0, BN);
+      float sum[128];
+#pragma unroll
+      for (int j = 0; j < 128; ++j) sum[j] = 0.0f;
+      for (int kg = 0; kg < ngroups; ++kg, ++gidx) {
+        const int buf = static_cast<int>(gidx & 1);
+        const uint32_t par = static_cast<uint32_t>((gidx >> 1) & 1);
+        if (!mbar_wait(pfull_bar(buf), par, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                               static_cast<uint32_t>(buf * BN + h * 128);
+#pragma unroll
+        for (int c = 0; c < 8; c += 2) {
+          uint32_t ra[16], rb[16];
+          tmem_ld16(taddr + c * 16, ra);
+          tmem_ld16(taddr + (c + 1) * 16, rb);
+          tmem_wait_ld(ra);
+          tmem_fence_regs(rb);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            sum[c * 16 + j] = __fadd_rn(sum[c * 16 + j], __uint_as_float(ra[j]));
+            sum[(c + 1) * 16 + j] = __fadd_rn(sum[(c + 1) * 16 + j], __uint_as_float(rb[j]));
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(pempty_bar(buf), 0));
+      }
+      if (!ok) break;
+      const int rg = m0 + row;
+      const int cbase = n0 + h * 128;
+      const long long rbase = blk * dd + static_cast<long long>(rg) * p.dim;
+      float rsum = 0.0f;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = sum[c * 16 + j];
+        epilogue16f(p.epi, blk, rg, cbase + c * 16, rbase + cbase + c * 16, v, rsum);
+      }
+      if (p.epi.resid_acc != nullptr) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) rsum += __shfl_xor_sync(0xffffffffu, rsum, off);
+        if (lane == 0) atomicAdd(p.epi.resid_acc + blk * p.epi.resid_stride, rsum);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+  }
+}
+
 // ---------------------------------------------------------------- host side
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -543,8 +804,20 @@ int device_sm_count() {
   return cache[dev];
 }
 
+// Kernel entry of a configuration (ACC: the accurate 3xTF32 pair variant).
+template <int BN, int KT, int MODE, bool ACC>
+struct KernelOf {
+  static constexpr int THREADS = ACC ? 320 : 192;
+  static auto get() {
+    if constexpr (ACC)
+      return gemm_tc_acc_kernel<KT>;
+    else
+      return gemm_tc_kernel<BN, KT, MODE>;
+  }
+};
+
 // Largest number of clusters of this kernel that can be resident at once.
-template <int BN, int KT, int MODE>
+template <int BN, int KT, int MODE, bool ACC = false>
 static int max_active_clusters() {
   static int cache[64] = {0};
   int dev = 0;
@@ -559,19 +832,20 @@ static int max_active_clusters() {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(CL * 256, 1, 1);
-    cfg.blockDim = dim3(192, 1, 1);
+    cfg.blockDim = dim3(KernelOf<BN, KT, MODE, ACC>::THREADS, 1, 1);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, KT, MODE>, &cfg) != cudaSuccess)
+    if (cudaOccupancyMaxActiveClusters(&n, KernelOf<BN, KT, MODE, ACC>::get(), &cfg) !=
+        cudaSuccess)
       n = 0;
     cache[dev] = n > 0 ? n : -1;
   }
   return cache[dev];
 }
 
-template <int BN, int KT, int MODE>
+template <int BN, int KT, int MODE, bool ACC = false>
 static dash_status run_gemm(const GemmLaunch& g, cudaStream_t st) {
   using C = Cfg<BN, KT, MODE>;
   constexpr int CL = C::CL;
@@ -608,7 +882,7 @@ static dash_status run_gemm(const GemmLaunch& g, cudaStream_t st) {
   p.a_mn = a_mn;
   p.b_mn = b_mn;
   p.epi = g.epi;
-  if (cudaFuncSetAttribute(gemm_tc_kernel<BN, KT, MODE>,
+  if (cudaFuncSetAttribute(KernelOf<BN, KT, MODE, ACC>::get(),
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::SMEM_BYTES) != cudaSuccess)
     return DASH_ERR_CUDA;
@@ -617,7 +891,7 @@ static dash_status run_gemm(const GemmLaunch& g, cudaStream_t st) {
   // Persistent grid: one CTA per SM, or as many clusters as can be co-resident.
   long long slots = sms / CL;
   if (CL > 1) {
-    const int mac = max_active_clusters<BN, KT, MODE>();
+    const int mac = max_active_clusters<BN, KT, MODE, ACC>();
     if (mac <= 0) return DASH_ERR_CUDA;
     if (mac < slots) slots = mac;
   }
@@ -630,12 +904,12 @@ static dash_status run_gemm(const GemmLaunch& g, cudaStream_t st) {
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(nclusters * CL), 1, 1);
-  cfg.blockDim = dim3(192, 1, 1);
+  cfg.blockDim = dim3(KernelOf<BN, KT, MODE, ACC>::THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t err = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<BN, KT, MODE>, tA, tB, tAl, tBl, p);
+  cudaError_t err = cudaLaunchKernelEx(&cfg, KernelOf<BN, KT, MODE, ACC>::get(), tA, tB, tAl, tBl, p);
   if (err == cudaSuccess) err = cudaGetLastError();
   if (rec >= 0) {
     const double bb = static_cast<double>(g.dim) * g.dim * g.nblocks;
@@ -666,7 +940,8 @@ dash_status launch_gemm(const GemmLaunch& g, cudaStream_t st) {
     case KIND_TF32:
       return wide ? run_gemm<256, 1, 2>(g, st) : run_gemm<128, 1, 0>(g, st);
     case KIND_TF32X3:
-      return wide ? run_gemm<256, 2, 2>(g, st) : run_gemm<128, 2, 0>(g, st);
+      // fp32-accurate products: partial sums reduced with round-to-nearest.
+      return wide ? run_gemm<256, 2, 2, true>(g, st) : run_gemm<128, 2, 0>(g, st);
     default:
       return DASH_ERR_INVALID_ARG;
   }
