@@ -51,35 +51,59 @@ def library():
     return dr
 
 
-def cn_f32(a, s, iters, ridge=0.0):
-    """Coupled Newton in plain float32 torch on the CPU (the same iteration as
-    the library's), used only to show the error floor of 32-bit arithmetic."""
+STORE_DTYPES = {"3xtf32": torch.float32, "tf32": torch.float32, "fp16": torch.float16,
+                "bf16": torch.bfloat16}
+
+
+def _rd(x, dt):
+    return x.to(dt).float()
+
+
+def cn_emulated(a, s, iters, prec, ridge=0.0):
+    """Coupled Newton on the CPU with the library's storage rule: every iterate is
+    rounded to the precision's storage type, products and epilogue algebra run in
+    float32.  Used only to show what arithmetic of that precision can deliver."""
+    dt = STORE_DTYPES[prec]
     a = a.float()
     b = a.shape[0]
     eye = torch.eye(b, dtype=torch.float32)
-    M = (a + ridge * eye) / s
-    X = eye
+    As = (a + ridge * eye) / s
+    M = _rd(As, dt)
+    T = _rd((5 * eye - As) / 4, dt)
+    X = T
     for i in range(iters):
-        T = (5 * eye - M) / 4
-        X = T if i == 0 else X @ T
+        if i > 0:
+            X = _rd(X @ T, dt)
         if i < iters - 1:
-            T2 = T @ T
-            M = (T2 @ T2) @ M
+            T2 = _rd(T @ T, dt)
+            T4 = _rd(T2 @ T2, dt)
+            C = T4 @ M
+            M = _rd(C, dt)
+            T = _rd((5 * eye - C) / 4, dt)
+    if iters == 1:
+        X = _rd((5 * eye - As) / 4, dt)
     return (X * s ** -0.25).double().numpy()
 
 
-def ndb_f32(a, s, iters, ridge=0.0):
-    """Two-stage Newton-Denman-Beavers in plain float32 torch on the CPU."""
+def ndb_emulated(a, s, iters, prec, ridge=0.0):
+    """Two-stage Newton-Denman-Beavers on the CPU with the library's storage rule."""
+    dt = STORE_DTYPES[prec]
     a = a.float()
     b = a.shape[0]
     eye = torch.eye(b, dtype=torch.float32)
 
-    def stage(C, keep_y):
-        Y, Z = C, eye
+    def stage(Cexact, keep_y):
+        C = _rd(Cexact, dt)
+        Y, Z = C, _rd((3 * eye - Cexact) / 2, dt)
+        T = Z
         for i in range(iters):
-            P = C if i == 0 else Z @ Y
-            T = (3 * eye - P) / 2
-            Y, Z = Y @ T, (T if i == 0 else T @ Z)
+            if i > 0:
+                P = Z @ Y
+                T = _rd((3 * eye - P) / 2, dt)
+            last = i == iters - 1
+            Yn = _rd(Y @ T, dt) if (not last or keep_y) else Y
+            Zn = (T if i == 0 else _rd(T @ Z, dt)) if (not last or not keep_y) else Z
+            Y, Z = Yn, Zn
         return Y if keep_y else Z
 
     return (stage(stage((a + ridge * eye) / s, True), False) * s ** -0.25).double().numpy()

@@ -9,10 +9,13 @@ NDB is reported, not gated.  Measured errors are printed (run with -s).
 Ill-conditioned stacks.  Configs 2-4 have scaled condition numbers of 1e6-1e7
 (a spectrum down to 1e-6, or rank-deficient Gram matrices plus a 1e-6 ridge).
 There the inverse 4th root of the smallest eigen-directions is so sensitive that
-a plain float32 CPU run of the same iteration already misses the 1e-4 gate; the
-tests pin exactly that, report the GPU error next to it, and bound it only
-against catastrophic failure (< 0.5).  Every other stage of those configs
-(accumulate, lambda, apply, padding) stays gated.
+arithmetic of the path's own precision may miss the stated gate.  Each such root
+is also computed on the CPU with the library's storage rule (iterates rounded to
+the precision's storage type, products and epilogues in float32).  The gate is
+then the stated tolerance if that emulation meets it, and otherwise R_EMUL times
+the emulation's own error (the tensor core's truncating fp32 accumulation is the
+documented excess).  Every other stage of those configs (accumulate, lambda,
+apply, padding) keeps its stated gate.
 """
 
 import numpy as np
@@ -21,7 +24,7 @@ import torch
 
 import oracle
 import synth
-from tests.helpers import cn_f32, library, ndb_f32, rel_fro_blocks, require_gpu, to64
+from tests.helpers import cn_emulated, library, ndb_emulated, rel_fro_blocks, require_gpu, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -29,25 +32,28 @@ GATE = {"3xtf32": 1e-4, "tf32": 2e-3, "fp16": 1e-2, "bf16": 1e-2}
 RIDGE = 1e-6
 
 
-def check_root(name, X, A, lam, idx, ref_fn, gate, f32_fn=None):
+R_EMUL = 10.0
+
+
+def check_root(name, X, A, lam, idx, ref_fn, gate, emul_fn=None):
     """Relative Frobenius error of X[idx] against the oracle.
 
-    With f32_fn (ill-conditioned stacks) the same iteration also runs in float32
-    on the CPU; the test then pins that float32 misses the 3xTF32 gate on this
-    input and bounds the GPU error against catastrophic failure only."""
+    With emul_fn (ill-conditioned stacks) the same iteration is also run on the
+    CPU in the path's storage precision; the gate becomes R_EMUL times that
+    emulation's error whenever the emulation itself misses the stated gate."""
     Xs = to64(X[idx])
     A64 = to64(A[idx])
     ref = ref_fn(A64, to64(lam[idx]))
     err = rel_fro_blocks(Xs, ref)
     msg = "%s: blocks %s rel err max %.3e" % (name, [int(i) for i in idx], err.max())
-    if f32_fn is not None:
-        x32 = np.stack([f32_fn(A[int(i)].cpu(), float(lam[int(i)])) for i in idx])
-        e32 = rel_fro_blocks(x32, ref)
-        msg += " (float32 CPU run of the same iteration: %.3e)" % e32.max()
+    if emul_fn is not None:
+        xe = np.stack([emul_fn(A[int(i)].cpu(), float(lam[int(i)])) for i in idx])
+        ee = rel_fro_blocks(xe, ref)
+        g = gate if ee.max() <= gate else R_EMUL * ee.max()
+        msg += " (CPU emulation in the same precision: %.3e; gate %.1e)" % (ee.max(), g)
         print(msg)
         assert np.all(np.isfinite(Xs))
-        assert err.max() < 0.5, (name, err)
-        assert e32.max() > GATE["3xtf32"], "stack is not ill-conditioned for float32"
+        assert err.max() < g, (name, err, ee)
         return err
     print(msg)
     if gate is not None:
@@ -115,13 +121,13 @@ def test_config2_frobenius_vs_power_scaling():
     lam = scales["power"]
     X = dr.inv_root_cn(A, lam, k, "3xtf32")
     check_root("cfg2 CN 3xtf32 K=%d" % k, X, A, lam, np.array([0, 63]),
-               lambda a, s: oracle.cn_inv_root(a, s, k)[0], None,
-               lambda a, s: cn_f32(a, s, k))
+               lambda a, s: oracle.cn_inv_root(a, s, k)[0], GATE["3xtf32"],
+               lambda a, s: cn_emulated(a, s, k, "3xtf32"))
     kn = int(max(its[("ndb", "power")].max() // 2 + 2, 8))
     X = dr.inv_root_ndb(A, lam, kn, "3xtf32")
     check_root("cfg2 NDB 3xtf32 K=%d" % kn, X, A, lam, np.array([0, 63]),
-               lambda a, s: oracle.ndb_inv_root(a, s, kn)[0], None,
-               lambda a, s: ndb_f32(a, s, kn))
+               lambda a, s: oracle.ndb_inv_root(a, s, kn)[0], GATE["3xtf32"],
+               lambda a, s: ndb_emulated(a, s, kn, "3xtf32"))
     assert dr.device_status() == 0
 
 
@@ -157,9 +163,13 @@ def check_step(dr, tag, G, vr, vc, F, V0, lam, X, U, root, prec, fidx, gidx):
     assert errl.max() < 1e-5
     ref_fn = ((lambda a, s: oracle.ndb_inv_root(a, s, 10, ridge=RIDGE)[0]) if root == "ndb"
               else (lambda a, s: oracle.cn_inv_root(a, s, 10, ridge=RIDGE)[0]))
-    f32_fn = ((lambda a, s: ndb_f32(a, s, 10, RIDGE)) if root == "ndb"
-              else (lambda a, s: cn_f32(a, s, 10, RIDGE)))
-    check_root("%s %s %s" % (tag, root, prec), X, F, lam, fidx, ref_fn, None, f32_fn)
+    emul = ((lambda a, s: ndb_emulated(a, s, 10, prec, RIDGE)) if root == "ndb"
+            else (lambda a, s: cn_emulated(a, s, 10, prec, RIDGE)))
+    gate = GATE[prec] if (root == "cn" or prec in ("3xtf32", "tf32")) else None
+    if gate is None:  # half-precision NDB: reported only
+        check_root("%s %s %s" % (tag, root, prec), X, F, lam, fidx, ref_fn, None)
+    else:
+        check_root("%s %s %s" % (tag, root, prec), X, F, lam, fidx, ref_fn, gate, emul)
     Xs = torch.cat([X[gidx], X[ng + gidx]])
     Uref = oracle.apply_preconditioner(G64, to64(Xs))
     errU = rel_fro_blocks(to64(U[gidx]), Uref)
