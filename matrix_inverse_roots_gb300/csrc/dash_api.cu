@@ -232,8 +232,10 @@ dash_status dash_device_status(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return DASH_ERR_CUDA;
   const int a = gemm_read_clear_error();
   const int b = elementwise_read_clear_error();
-  if (a < 0 || b < 0) return DASH_ERR_CUDA;
-  if (a == DASH_ERR_TIMEOUT || b == DASH_ERR_TIMEOUT) return DASH_ERR_TIMEOUT;
+  const int c = power_tc_read_clear_error();
+  if (a < 0 || b < 0 || c < 0) return DASH_ERR_CUDA;
+  if (a == DASH_ERR_TIMEOUT || b == DASH_ERR_TIMEOUT || c == DASH_ERR_TIMEOUT)
+    return DASH_ERR_TIMEOUT;
   return DASH_OK;
 }
 
@@ -409,8 +411,8 @@ dash_status spectral_scale(const float* A, float ridge, int64_t N, int B, int mo
       const int last = (it == power_iters - 1);
       if (cudaMemsetAsync(nrm[cur], 0, acc_bytes, st) != cudaSuccess) return DASH_ERR_CUDA;
       if (last && cudaMemsetAsync(den, 0, acc_bytes, st) != cudaSuccess) return DASH_ERR_CUDA;
-      DASH_TRY(launch_power_step(Ac, ridge, B, nc, vin, vstride, n_vec, in_n, V[cur], nrm[cur],
-                                 den, last, st));
+      DASH_TRY(launch_power_step_tc(Ac, ridge, B, nc, vin, n_vec, in_n, V[cur], nrm[cur], den,
+                                    last, st));
       vin = V[cur];
       vstride = 32;
       in_n = nrm[cur];

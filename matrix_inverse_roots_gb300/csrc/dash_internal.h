@@ -85,15 +85,14 @@ dash_status launch_sqrt_scale(const float* acc, float* out, long long n, float m
 dash_status launch_frob_acc(const float* A, float ridge, int dim, long long nblocks, float* acc,
                             cudaStream_t st);
 
-// One power-iteration product W = (A + ridge I) V for every block; V is read as
-// Vin[blk][row][c] / sqrt(in_nrm2[blk][c]) (in_nrm2 null = unscaled); Vin has
-// row stride 32 (vin_stride is ignored).
-// Not last: writes W (stride 32) and acc0[blk][c] += sum_r W^2.
+// One power-iteration product W = (A + ridge I) V for every block, on the tensor
+// cores in 3xTF32 (A and V split into TF32 hi/lo in shared memory).  V is read as
+// Vin[blk][row][c] / sqrt(in_nrm2[blk][c]) (in_nrm2 null = unscaled), row stride 32.
+// Not last: writes W and acc0[blk][c] += sum_r W^2.
 // Last: acc0[blk][c] += sum_r v w, acc1[blk][c] += sum_r v v (W not written).
-dash_status launch_power_step(const float* A, float ridge, int dim, long long nblocks,
-                              const float* Vin, int vin_stride, int nv, const float* in_nrm2,
-                              float* Wout, float* acc0, float* acc1, int last,
-                              cudaStream_t st);
+dash_status launch_power_step_tc(const float* A, float ridge, int dim, long long nblocks,
+                                 const float* Vin, int nv, const float* in_nrm2, float* Wout,
+                                 float* acc0, float* acc1, int last, cudaStream_t st);
 
 // V (nblocks, dim, 32) = V0 (nblocks, dim, nv) with columns nv..31 zero.
 dash_status launch_pad_vectors(const float* V0, int nv, int dim, long long nblocks, float* V,
@@ -108,6 +107,7 @@ int trace_begin(cudaStream_t st);
 void trace_end(int rec, cudaStream_t st, int kind, double flops, double bytes);
 
 int gemm_read_clear_error();
+int power_tc_read_clear_error();
 int elementwise_read_clear_error();
 
 int device_sm_count();

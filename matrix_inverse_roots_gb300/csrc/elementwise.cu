@@ -1,7 +1,7 @@
 // Memory-bound kernels of the preconditioner step: the element-wise prologue
 // that scales a block and writes the first iterates in operand format, the
-// Frobenius reduction, per-block scale factors, and the multi-vector power
-// iteration.  All are HBM-bound: 16-byte vector accesses along rows, warp-shuffle
+// Frobenius reduction, per-block scale factors, and the bookkeeping kernels of
+// the multi-vector power iteration.  All are HBM-bound: 16-byte vector accesses along rows, warp-shuffle
 // reductions, one atomic per CTA and block for the per-block sums.
 #include <cmath>
 
@@ -181,178 +181,9 @@ dash_status launch_frob_acc(const float* A, float ridge, int dim, long long nblo
 }
 
 // ---------------------------------------------------------------- power iteration
-// W = (A + ridge I) V for every block, V being B x 32 (n_v <= 32 used columns,
-// stored with a row stride of 32; the previous step's column norms are applied
-// as W = (A V_raw) D + ridge V_raw D, D = diag(1/||column||)).
-// One CTA owns R = min(B, 512) rows of one block (rows a multiple of R/8 apart
-// share a thread), R/2 threads, each with an 8 rows x 8 vectors register tile.
-// A and V stream through shared memory in 16-column chunks with cp.async,
-// double-buffered.  Per column of A a thread does 8 scalar shared loads
-// (conflict-free: its warp's 8 rows are consecutive and the staged row stride is
-// 20 words) and two float4 loads of V for 64 FMAs.
+// The products themselves run on the tensor cores (power_tc.cu); here are the
+// start-vector layout change and the final Rayleigh-quotient maximum.
 constexpr int PW_NV = 32;
-constexpr int PW_KC = 16;
-constexpr int PW_STRIDE = 20;  // words per staged row of A (16 used, 16-byte aligned)
-
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all_but_one() {
-  asm volatile("cp.async.wait_group 1;" ::: "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
-}
-
-__global__ void __launch_bounds__(256)
-    power_step_kernel(const float* A, float ridge, int dim, long long nblocks, const float* Vin,
-                      int vin_stride, int nv, const float* in_nrm2, float* Wout, float* acc0,
-                      float* acc1, int last, int rows) {
-  extern __shared__ __align__(16) float pw_smem[];
-  float* As = pw_smem;                                    // [2][rows][PW_STRIDE]
-  float* Vs = pw_smem + 2 * rows * PW_STRIDE;             // [2][PW_KC][PW_NV]
-  __shared__ float vscale[PW_NV];
-  __shared__ float red0[8][PW_NV];
-  __shared__ float red1[8][PW_NV];
-
-  const long long blk = blockIdx.y;
-  const int r0 = blockIdx.x * rows;
-  const int tid = threadIdx.x;
-  const int nthreads = blockDim.x;  // rows / 2
-  const int groups = rows / 8;      // row groups; group g owns rows g + groups * i
-  const int cg = tid & 3;           // vector columns 8cg .. 8cg+7
-  const int g = tid >> 2;
-  const long long dd = static_cast<long long>(dim) * dim;
-  const float* Ab = A + blk * dd + static_cast<long long>(r0) * dim;
-  const float* Vb = Vin + blk * static_cast<long long>(dim) * PW_NV;
-  (void)vin_stride;
-
-  if (tid < PW_NV) {
-    float sc = 0.0f;
-    if (tid < nv) sc = (in_nrm2 != nullptr) ? 1.0f / sqrtf(in_nrm2[blk * PW_NV + tid]) : 1.0f;
-    vscale[tid] = sc;
-  }
-  __syncthreads();
-
-  // Stage chunk kc into buffer b: A rows r0..r0+rows-1 and V rows kc..kc+15,
-  // columns kc..kc+15 of A; all with 16-byte cp.async.
-  auto stage = [&](int b, int kc) {
-    float* Ad = As + b * rows * PW_STRIDE;
-    const int nvec = rows * (PW_KC / 4);
-    for (int f = tid; f < nvec; f += nthreads) {
-      const int r = f >> 2, q = f & 3;
-      cp_async16(Ad + r * PW_STRIDE + 4 * q, Ab + static_cast<long long>(r) * dim + kc + 4 * q);
-    }
-    float* Vd = Vs + b * PW_KC * PW_NV;
-    for (int f = tid; f < PW_KC * PW_NV / 4; f += nthreads)
-      cp_async16(Vd + 4 * f, Vb + static_cast<long long>(kc) * PW_NV + 4 * f);
-    cp_async_commit();
-  };
-
-  float acc[8][8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
-
-  const int nchunks = dim / PW_KC;
-  stage(0, 0);
-  for (int ch = 0; ch < nchunks; ++ch) {
-    const int b = ch & 1;
-    if (ch + 1 < nchunks) {
-      stage(b ^ 1, (ch + 1) * PW_KC);
-      cp_async_wait_all_but_one();
-    } else {
-      cp_async_wait_all();
-    }
-    __syncthreads();
-    const float* Ac = As + b * rows * PW_STRIDE;
-    const float* Vc = Vs + b * PW_KC * PW_NV;
-#pragma unroll
-    for (int k = 0; k < PW_KC; ++k) {
-      float a[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) a[i] = Ac[(g + groups * i) * PW_STRIDE + k];
-      const float4 v0 = *reinterpret_cast<const float4*>(Vc + k * PW_NV + 8 * cg);
-      const float4 v1 = *reinterpret_cast<const float4*>(Vc + k * PW_NV + 8 * cg + 4);
-      const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], v[j], acc[i][j]);
-    }
-    __syncthreads();
-  }
-
-  // Ridge term, output and per-column statistics.
-  float s0[8], s1[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    s0[j] = 0.0f;
-    s1[j] = 0.0f;
-  }
-  float sc[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) sc[j] = vscale[8 * cg + j];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int row = r0 + g + groups * i;
-    const float* vr = Vb + static_cast<long long>(row) * PW_NV + 8 * cg;
-    const float4 va = *reinterpret_cast<const float4*>(vr);
-    const float4 vb = *reinterpret_cast<const float4*>(vr + 4);
-    const float vraw[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
-    float w[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float v = vraw[j] * sc[j];
-      w[j] = fmaf(ridge, v, acc[i][j] * sc[j]);
-      if (last) {
-        s0[j] = fmaf(v, w[j], s0[j]);
-        s1[j] = fmaf(v, v, s1[j]);
-      } else {
-        s0[j] = fmaf(w[j], w[j], s0[j]);
-      }
-    }
-    if (!last) {
-      float* o = Wout + blk * static_cast<long long>(dim) * PW_NV +
-                 static_cast<long long>(row) * PW_NV + 8 * cg;
-      *reinterpret_cast<float4*>(o) = make_float4(w[0], w[1], w[2], w[3]);
-      *reinterpret_cast<float4*>(o + 4) = make_float4(w[4], w[5], w[6], w[7]);
-    }
-  }
-  // Lanes cg, cg+4, ..., cg+28 hold the same columns.
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      s0[j] += __shfl_xor_sync(0xffffffffu, s0[j], off);
-      s1[j] += __shfl_xor_sync(0xffffffffu, s1[j], off);
-    }
-  }
-  const int w = tid >> 5, l = tid & 31;
-  const int nwarps = nthreads >> 5;
-  if (l < 4) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      red0[w][8 * l + j] = s0[j];
-      red1[w][8 * l + j] = s1[j];
-    }
-  }
-  __syncthreads();
-  if (tid < PW_NV && tid < nv) {
-    float a = 0.f, b = 0.f;
-    for (int i = 0; i < nwarps; ++i) {
-      a += red0[i][tid];
-      b += red1[i][tid];
-    }
-    atomicAdd(acc0 + blk * PW_NV + tid, a);
-    if (last) atomicAdd(acc1 + blk * PW_NV + tid, b);
-  }
-}
 
 // V[blk][r][c] = V0[blk][r][c] for c < nv, 0 for nv <= c < 32.
 __global__ void pad_vectors_kernel(const float* V0, int nv, long long rows_total, float* V) {
@@ -372,33 +203,6 @@ dash_status launch_pad_vectors(const float* V0, int nv, int dim, long long nbloc
       V0, nv, static_cast<long long>(dim) * nblocks, V);
   const cudaError_t err = cudaGetLastError();
   trace_end(rec, st, DASH_TRACE_ELEMENTWISE, 0.0, 4.0 * static_cast<double>(dim) * nblocks * (nv + 32));
-  return err == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
-}
-
-static int power_rows(int dim) {
-  if (dim % 512 == 0) return 512;
-  if (dim % 256 == 0) return 256;
-  return 128;
-}
-
-dash_status launch_power_step(const float* A, float ridge, int dim, long long nblocks,
-                              const float* Vin, int vin_stride, int nv, const float* in_nrm2,
-                              float* Wout, float* acc0, float* acc1, int last, cudaStream_t st) {
-  if (nblocks <= 0) return DASH_OK;
-  if (nblocks > 65535) return DASH_ERR_INVALID_ARG;
-  const int rows = power_rows(dim);
-  const size_t smem = (2 * static_cast<size_t>(rows) * PW_STRIDE + 2 * PW_KC * PW_NV) * 4;
-  if (cudaFuncSetAttribute(power_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem)) != cudaSuccess)
-    return DASH_ERR_CUDA;
-  dim3 grid(dim / rows, static_cast<unsigned>(nblocks), 1);
-  const int rec = trace_begin(st);
-  power_step_kernel<<<grid, rows / 2, smem, st>>>(A, ridge, dim, nblocks, Vin, vin_stride, nv,
-                                                  in_nrm2, Wout, acc0, acc1, last, rows);
-  const cudaError_t err = cudaGetLastError();
-  const double bb = static_cast<double>(dim) * dim * nblocks;
-  const double vb = static_cast<double>(dim) * nblocks * 4.0;
-  trace_end(rec, st, DASH_TRACE_POWER, 2.0 * bb * nv, 4.0 * bb + vb * (32 + (last ? 0 : 32)));
   return err == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
 }
 
