@@ -269,6 +269,14 @@ dash_status dash_trace_stop(void);
  * (DASH_OK or DASH_ERR_TIMEOUT).  Synchronises the device. */
 dash_status dash_device_status(void);
 
+/* Failure-detection self-test (no counterpart on the pages): enqueues one
+ * kernel whose bounded device wait, on a barrier nothing arrives on, runs out
+ * after limit_us microseconds (1 .. 1e6).  It takes the same time-out path as
+ * every pipeline wait of the library: the kernel records DASH_ERR_TIMEOUT and
+ * returns, so the next dash_device_status() reports DASH_ERR_TIMEOUT and the
+ * CUDA context stays usable.  Nothing else is touched. */
+dash_status dash_selftest_wait_timeout(int limit_us, void* stream);
+
 const char* dash_status_string(int status);
 
 /* Library version, e.g. "dashroot 0.1 sm_103a". */

@@ -49,6 +49,7 @@ SYMBOLS = (
     "precondition_apply", "dash_gemm", "dash_workspace_size", "dash_op_matmuls",
     "dash_device_status", "dash_status_string", "dash_version", "dash_trace_start",
     "dash_trace_count", "dash_trace_read", "dash_trace_stop", "spectral_scale_noalloc",
+    "dash_selftest_wait_timeout",
 )
 
 _lib = None
@@ -88,6 +89,8 @@ def load_library(path=None):
     lib.dash_version.restype = ctypes.c_char_p
     lib.spectral_scale_noalloc.argtypes = [vp, f32, i64, i32, i32, i32, i32, vp, vp, vp]
     lib.spectral_scale_noalloc.restype = ctypes.c_int
+    lib.dash_selftest_wait_timeout.argtypes = [i32, vp]
+    lib.dash_selftest_wait_timeout.restype = ctypes.c_int
     lib.dash_trace_start.argtypes = [i32]
     lib.dash_trace_count.argtypes = []
     lib.dash_trace_count.restype = i32
@@ -203,6 +206,12 @@ def op_matmuls(op, param):
 
 def device_status():
     return int(load_library().dash_device_status())
+
+
+def selftest_wait_timeout(limit_us=50000):
+    """Run the bounded-wait self-test kernel (its wait times out on purpose)."""
+    _check(load_library().dash_selftest_wait_timeout(int(limit_us), _stream()),
+           "dash_selftest_wait_timeout")
 
 
 def shampoo_accumulate(G, F, beta, valid_rows=None, valid_cols=None, ws=None):

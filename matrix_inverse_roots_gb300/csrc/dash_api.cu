@@ -239,6 +239,11 @@ dash_status dash_device_status(void) {
   return DASH_OK;
 }
 
+dash_status dash_selftest_wait_timeout(int limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000) return DASH_ERR_INVALID_ARG;
+  return launch_wait_selftest(limit_us, static_cast<cudaStream_t>(stream));
+}
+
 int64_t dash_op_matmuls(int op, int param) {
   switch (op) {
     case DASH_OP_ACCUMULATE: return 2;  // one per factor, L and R

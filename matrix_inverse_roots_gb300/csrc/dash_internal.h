@@ -106,6 +106,9 @@ dash_status launch_power_finish(const float* num, const float* den, int nv, long
 int trace_begin(cudaStream_t st);
 void trace_end(int rec, cudaStream_t st, int kind, double flops, double bytes);
 
+// Bounded-wait self-test: a wait on a barrier nothing arrives on.
+dash_status launch_wait_selftest(int limit_us, cudaStream_t st);
+
 int gemm_read_clear_error();
 int power_tc_read_clear_error();
 int elementwise_read_clear_error();

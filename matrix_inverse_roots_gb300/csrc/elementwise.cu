@@ -226,4 +226,27 @@ dash_status launch_power_finish(const float* num, const float* den, int nv, long
   return err == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------- wait self-test
+// One thread waits, with the given limit, on an mbarrier that nothing arrives
+// on; when the limit runs out it records DEV_ERR_TIMEOUT and returns -- the
+// same path every pipeline wait of the library takes.
+__global__ void wait_selftest_kernel(unsigned long long limit_ns) {
+  __shared__ __align__(8) unsigned long long bar;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 1);
+  fence_barrier_init();
+  const unsigned long long t0 = globaltimer_ns();
+  while (!mbar_try_wait(b, 0)) {
+    if (globaltimer_ns() - t0 > limit_ns) {
+      atomicExch(&g_dash_error, DEV_ERR_TIMEOUT);
+      return;
+    }
+  }
+}
+
+dash_status launch_wait_selftest(int limit_us, cudaStream_t st) {
+  wait_selftest_kernel<<<1, 1, 0, st>>>(static_cast<unsigned long long>(limit_us) * 1000ull);
+  return cudaGetLastError() == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
+}
+
 }  // namespace dash
