@@ -12,10 +12,12 @@
 //   warp 1      allocates TMEM and issues tcgen05.mma from one thread into one of
 //               two TMEM accumulators (128 x BN fp32 each), so the epilogue of
 //               tile i overlaps the MMAs of tile i+1.
-//   warps 2..5  epilogue: tcgen05.ld the accumulator (one TMEM lane = one row per
-//               thread), apply D = mult*(alpha C + gamma I + eps E), optional
-//               residual sum (C - I)^2 and identity padding, and store in the
-//               requested format (fp32, TF32-rounded, hi/lo split, fp16, bf16).
+//   warps 2..9  epilogue, two warps per TMEM lane quarter, each taking half of
+//               the tile's columns: tcgen05.ld the accumulator (one TMEM lane =
+//               one row per thread), apply D = mult*(alpha C + gamma I + eps E),
+//               optional residual sum (C - I)^2 and identity padding, and store
+//               in the requested format (fp32, TF32-rounded, hi/lo split, fp16,
+//               bf16).  Chunks away from the diagonal take a branch-free path.
 // Tiles are ordered block-major so that concurrently running CTAs share the
 // operands of a few blocks in L2.
 // Precisions: kind::f16 (fp16 / bf16 operands), kind::tf32, and 3xTF32, which
@@ -115,12 +117,20 @@ __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
 // E read are 256-bit (one whole L2 sector per thread) when the base pointers
 // allow it, 128-bit otherwise.
 __device__ __forceinline__ void epilogue16f(const EpiParams& e, long long blk, int rg, int cg0,
-                                            long long idx, const float (&c)[16], float& rsum) {
+                                            long long idx, const float (&c)[16], float& rsum,
+                                            bool diag) {
+  // diag: this warp's rows and these 16 columns share a diagonal element (a
+  // warp-uniform flag: off-diagonal chunks skip every identity term).
   if (e.resid_acc != nullptr) {
+    if (diag) {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float d = c[j] - ((rg == cg0 + j) ? 1.0f : 0.0f);
-      rsum = fmaf(d, d, rsum);
+      for (int j = 0; j < 16; ++j) {
+        const float d = c[j] - ((rg == cg0 + j) ? 1.0f : 0.0f);
+        rsum = fmaf(d, d, rsum);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) rsum = fmaf(c[j], c[j], rsum);
     }
   }
   float ev[16];
@@ -140,21 +150,27 @@ __device__ __forceinline__ void epilogue16f(const EpiParams& e, long long blk, i
 #pragma unroll
     for (int j = 0; j < 16; ++j) ev[j] = 0.0f;
   }
-  const int pv = (e.pad_valid != nullptr) ? e.pad_valid[blk] : 0x7fffffff;
+  const bool pad = (e.pad_valid != nullptr);
+  const int pv = pad ? e.pad_valid[blk] : 0x7fffffff;
 #pragma unroll
   for (int o = 0; o < 3; ++o) {
     if (o < e.nout) {
       const EpiOut& O = e.out[o];
       const float m = (O.mult != nullptr) ? O.mult[blk] : 1.0f;
       float d[16];
+      if (!diag && !pad) {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int col = cg0 + j;
-        float v = fmaf(O.alpha, c[j], O.eps * ev[j]);
-        if (rg == col) v += O.gamma;
-        v *= m;
-        if (rg >= pv || col >= pv) v = (rg == col) ? 1.0f : 0.0f;
-        d[j] = v;
+        for (int j = 0; j < 16; ++j) d[j] = m * fmaf(O.alpha, c[j], O.eps * ev[j]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int col = cg0 + j;
+          float v = fmaf(O.alpha, c[j], O.eps * ev[j]);
+          if (rg == col) v += O.gamma;
+          v *= m;
+          if (rg >= pv || col >= pv) v = (rg == col) ? 1.0f : 0.0f;
+          d[j] = v;
+        }
       }
       if (aligned32(O.hi) && (O.fmt != FMT_SPLIT || aligned32(O.lo))) {
         store16_v8(O.fmt, O.hi, O.lo, idx, d);
@@ -170,15 +186,21 @@ __device__ __forceinline__ void epilogue16f(const EpiParams& e, long long blk, i
 }
 
 __device__ __forceinline__ void epilogue16(const EpiParams& e, long long blk, int rg, int cg0,
-                                           long long idx, const uint32_t (&r)[16], float& rsum) {
+                                           long long idx, const uint32_t (&r)[16], float& rsum,
+                                           bool diag) {
   float c[16];
 #pragma unroll
   for (int j = 0; j < 16; ++j) c[j] = __uint_as_float(r[j]);
-  epilogue16f(e, blk, rg, cg0, idx, c, rsum);
+  epilogue16f(e, blk, rg, cg0, idx, c, rsum, diag);
+}
+
+// Whether rows [r0, r0 + 32) and columns [c0, c0 + 16) contain a diagonal element.
+__device__ __forceinline__ bool chunk_on_diag(int r0, int c0) {
+  return c0 < r0 + 32 && r0 < c0 + 16;
 }
 
 template <int BN, int KT, int MODE>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tB,
                    const __grid_constant__ CUtensorMap tAl,
                    const __grid_constant__ CUtensorMap tBl, const __grid_constant__ KParams p) {
@@ -218,8 +240,9 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      // MODE 2: the leader's accumulator is freed by the epilogues of both CTAs.
-      mbar_init(tempty_bar(a), MODE == 2 ? 8 : 4);
+      // Eight epilogue warps per CTA; in MODE 2 the leader's accumulator is freed
+      // by the epilogues of both CTAs.
+      mbar_init(tempty_bar(a), MODE == 2 ? 16 : 8);
     }
     mbar_init(fin_bar, 1);
     *abort_flag = 0;
@@ -433,7 +456,10 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // -------------------------------------------------------------- epilogue
+    // Eight warps: two per TMEM lane quarter, each owning half of the columns.
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int h = (warp - 2) >> 2;
+    constexpr int HALF = BN / 2;
     const int row = q * 32 + lane;
     const long long dd = static_cast<long long>(p.dim) * p.dim;
     int acc = 0;
@@ -445,22 +471,25 @@ __global__ void __launch_bounds__(192, 1)
       int m0, n0;
       decode_unit<CL>(u, p, crank, blk, m0, n0, BN);
       const int rg = m0 + row;
+      const int r0w = m0 + q * 32;  // first row of this warp
+      const int nh = n0 + h * HALF;
       const long long rbase = blk * dd + static_cast<long long>(rg) * p.dim;
       float rsum = 0.0f;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                             static_cast<uint32_t>(acc * BN);
+                             static_cast<uint32_t>(acc * BN + h * HALF);
       // Two register sets: the TMEM load of chunk c+1 is in flight while chunk c
       // is processed.
       uint32_t ra[16], rb[16];
       tmem_ld16(taddr, ra);
 #pragma unroll 1
-      for (int c = 0; c < BN / 16; c += 2) {
+      for (int c = 0; c < HALF / 16; c += 2) {
         tmem_wait_ld(ra);
         tmem_ld16(taddr + (c + 1) * 16, rb);
-        epilogue16(p.epi, blk, rg, n0 + c * 16, rbase + n0 + c * 16, ra, rsum);
+        const int ca = nh + c * 16, cb = ca + 16;
+        epilogue16(p.epi, blk, rg, ca, rbase + ca, ra, rsum, chunk_on_diag(r0w, ca));
         tmem_wait_ld(rb);
-        if (c + 2 < BN / 16) tmem_ld16(taddr + (c + 2) * 16, ra);
-        epilogue16(p.epi, blk, rg, n0 + (c + 1) * 16, rbase + n0 + (c + 1) * 16, rb, rsum);
+        if (c + 2 < HALF / 16) tmem_ld16(taddr + (c + 2) * 16, ra);
+        epilogue16(p.epi, blk, rg, cb, rbase + cb, rb, rsum, chunk_on_diag(r0w, cb));
       }
       if (p.epi.resid_acc != nullptr) {
 #pragma unroll
@@ -730,7 +759,9 @@ __global__ void __launch_bounds__(320, 1)
         float v[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) v[j] = sum[c * 16 + j];
-        epilogue16f(p.epi, blk, rg, cbase + c * 16, rbase + cbase + c * 16, v, rsum);
+        // The generic (diagonal-aware) path for every chunk: the branch-free
+        // variants would add live registers to a kernel already holding sum[128].
+        epilogue16f(p.epi, blk, rg, cbase + c * 16, rbase + cbase + c * 16, v, rsum, true);
       }
       if (p.epi.resid_acc != nullptr) {
 #pragma unroll
@@ -807,7 +838,7 @@ int device_sm_count() {
 // Kernel entry of a configuration (ACC: the accurate 3xTF32 pair variant).
 template <int BN, int KT, int MODE, bool ACC>
 struct KernelOf {
-  static constexpr int THREADS = ACC ? 320 : 192;
+  static constexpr int THREADS = 320;
   static auto get() {
     if constexpr (ACC)
       return gemm_tc_acc_kernel<KT>;
