@@ -527,10 +527,11 @@ __global__ void __launch_bounds__(320, 1)
 // The tensor core's fp32 accumulation truncates: a K-long product picks up a
 // relative bias of about -(K/8) 2^-24.  This variant of the pair kernel for
 // 3xTF32 bounds it: the MMA warp starts a fresh TMEM partial accumulator every
-// ACC_KB k-blocks (two partials alternate), and eight reducer warps -- two per
-// TMEM lane quarter, 128 columns each -- add the partials into fp32 registers
-// with round-to-nearest.  The fused epilogue then runs on those register sums.
-constexpr int ACC_KB = 2;  // k-blocks (of 32) per TMEM partial
+// ACC_SUB sub-steps (one sub-step = the three MMAs of one K = 8 slice; two
+// partials alternate), and eight reducer warps -- two per TMEM lane quarter, 128
+// columns each -- add the partials into fp32 registers with round-to-nearest.
+// The fused epilogue then runs on those register sums.
+constexpr int ACC_SUB = 8;  // K = 8 sub-steps per TMEM partial
 
 template <int KT>
 __global__ void __launch_bounds__(320, 1)
@@ -563,7 +564,7 @@ __global__ void __launch_bounds__(320, 1)
   const long long cid = blockIdx.x / CL;
   const long long ncl = gridDim.x / CL;
   constexpr uint16_t kMask = 3;
-  const int ngroups = p.nkb / ACC_KB;
+  const int ngroups = p.nkb * C::NSUB / ACC_SUB;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -653,55 +654,60 @@ __global__ void __launch_bounds__(320, 1)
       int stage = 0;
       uint32_t phase = 0;
       long long gidx = 0;  // partials issued so far: buffer gidx & 1
+      int nsub = 0;        // sub-steps issued into the current partial
+      uint32_t d_tmem = 0;
       bool ok = true;
       for (long long u = cid; u < p.total_units && ok; u += ncl) {
-        for (int kg = 0; kg < ngroups && ok; ++kg, ++gidx) {
-          const int buf = static_cast<int>(gidx & 1);
-          const uint32_t par = static_cast<uint32_t>((gidx >> 1) & 1);
-          if (!mbar_wait(pempty_bar(buf), par ^ 1u, abort_flag)) {
+        for (int kb = 0; kb < p.nkb && ok; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
-          for (int kq = 0; kq < ACC_KB; ++kq) {
-            if (!mbar_wait(full_bar(stage), phase, abort_flag)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t sA = sbase + stage * C::STAGE_BYTES;
-            const uint32_t sB = sA + C::A_BYTES;
-            const uint32_t lo_off = C::A_BYTES + C::B_BYTES;
+          const uint32_t sA = sbase + stage * C::STAGE_BYTES;
+          const uint32_t sB = sA + C::A_BYTES;
+          const uint32_t lo_off = C::A_BYTES + C::B_BYTES;
 #pragma unroll
-            for (int kk = 0; kk < C::NSUB; ++kk) {
-              const uint64_t da =
-                  p.a_mn ? smem_desc(sA + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO, C::MN_LAYOUT)
-                         : smem_desc_sw128(sA + kk * 32, 16, 1024);
-              const uint64_t db =
-                  p.b_mn ? smem_desc(sB + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO, C::MN_LAYOUT)
-                         : smem_desc_sw128(sB + kk * 32, 16, 1024);
-              const uint64_t dal =
-                  p.a_mn ? smem_desc(sA + lo_off + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO,
-                                     C::MN_LAYOUT)
-                         : smem_desc_sw128(sA + lo_off + kk * 32, 16, 1024);
-              const uint64_t dbl =
-                  p.b_mn ? smem_desc(sB + lo_off + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO,
-                                     C::MN_LAYOUT)
-                         : smem_desc_sw128(sB + lo_off + kk * 32, 16, 1024);
-              const uint32_t accum = (kq | kk) ? 1u : 0u;  // fresh partial per group
-              mma_tf32_pair(d_tmem, dal, db, p.idesc, accum);
-              mma_tf32_pair(d_tmem, da, dbl, p.idesc, 1u);
-              mma_tf32_pair(d_tmem, da, db, p.idesc, 1u);
+          for (int kk = 0; kk < C::NSUB; ++kk) {
+            const int buf = static_cast<int>(gidx & 1);
+            if (nsub == 0) {
+              const uint32_t par = static_cast<uint32_t>((gidx >> 1) & 1);
+              if (!mbar_wait(pempty_bar(buf), par ^ 1u, abort_flag)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
             }
-            mma_commit_pair_mc(empty_bar(stage), kMask);
-            if (++stage == C::STAGES) {
-              stage = 0;
-              phase ^= 1u;
+            const uint64_t da =
+                p.a_mn ? smem_desc(sA + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO, C::MN_LAYOUT)
+                       : smem_desc_sw128(sA + kk * 32, 16, 1024);
+            const uint64_t db =
+                p.b_mn ? smem_desc(sB + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO, C::MN_LAYOUT)
+                       : smem_desc_sw128(sB + kk * 32, 16, 1024);
+            const uint64_t dal =
+                p.a_mn ? smem_desc(sA + lo_off + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO,
+                                   C::MN_LAYOUT)
+                       : smem_desc_sw128(sA + lo_off + kk * 32, 16, 1024);
+            const uint64_t dbl =
+                p.b_mn ? smem_desc(sB + lo_off + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO,
+                                   C::MN_LAYOUT)
+                       : smem_desc_sw128(sB + lo_off + kk * 32, 16, 1024);
+            mma_tf32_pair(d_tmem, dal, db, p.idesc, nsub ? 1u : 0u);  // fresh partial
+            mma_tf32_pair(d_tmem, da, dbl, p.idesc, 1u);
+            mma_tf32_pair(d_tmem, da, db, p.idesc, 1u);
+            if (++nsub == ACC_SUB) {
+              mma_commit_pair_mc(pfull_bar(buf), kMask);
+              nsub = 0;
+              ++gidx;
             }
           }
           if (!ok) break;
-          mma_commit_pair_mc(pfull_bar(buf), kMask);
+          mma_commit_pair_mc(empty_bar(stage), kMask);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
       }
       mma_commit_pair(fin_bar);

@@ -5,14 +5,20 @@
 // start-vector columns); D = diag(1 / ||previous column||) is applied to the
 // accumulator, since (A V) D = A (V D).  The product is a skinny GEMM
 // (M = B rows, N = 32, K = B) whose cost is reading A once, so the kernel is
-// built to stream A from HBM at full rate:
+// built to stream A from HBM at full rate, with as many bytes in flight as the
+// shared memory holds:
 //   warp 0      TMA producer: per k-block a 128 x 32 fp32 tile of A (K-major,
 //               128B swizzle) and the 32 x 32 tile of V (MN-major: the 32
-//               vectors are one 128-byte atom, 32-byte swizzle atoms).
-//   warps 2..5  converters: split both tiles in place into TF32 hi (overwriting
-//               the fp32 data) and lo (a second buffer), same swizzled layout.
-//   warp 1      one thread issues lo*hi, hi*lo and hi*hi (M = 128, N = 32, K = 8)
-//               into a TMEM accumulator; two accumulators alternate.
+//               vectors are one 128-byte atom, 32-byte swizzle atoms) into a
+//               ring of nine 24 KB stages.
+//   warps 2..5  converters: each thread reads one row of the A tile, splits it
+//               into TF32 hi and lo and writes both into a TMEM operand buffer
+//               (tcgen05.st), so the split costs no shared-memory writes and the
+//               ring holds only raw data; the small V tile is split in place
+//               (hi over the fp32 data, lo beside it).
+//   warp 1      one thread issues lo*hi, hi*lo and hi*hi (M = 128, N = 32, K = 8,
+//               A read from TMEM, V from shared memory) into a TMEM accumulator;
+//               two accumulators alternate.
 //   warps 6..9  epilogue: one accumulator row per thread; scale, ridge term,
 //               W stored as contiguous 128-byte rows; column sums (W^2, or v.w and
 //               v.v on the last product) reduced with a butterfly shuffle and one
@@ -39,12 +45,20 @@ constexpr int PT_BK = 32;                 // fp32 elements per 128-byte row
 constexpr int PT_NV = 32;
 constexpr int PT_A_BYTES = PT_BM * 128;   // 16 KB
 constexpr int PT_V_BYTES = PT_BK * 128;   // 4 KB
-// Stage: A (hi after conversion) | A lo | V (hi after conversion) | V lo.
-constexpr int PT_STAGE_BYTES = 2 * PT_A_BYTES + 2 * PT_V_BYTES;  // 40 KB
-constexpr int PT_STAGES = 5;
-constexpr int PT_TMEM_COLS = 64;          // two 32-column accumulators
+// Stage: A (raw fp32) | V (hi after conversion) | V lo.
+constexpr int PT_STAGE_BYTES = PT_A_BYTES + 2 * PT_V_BYTES;  // 24 KB
+constexpr int PT_STAGES = 9;
+// TMEM: two 32-column accumulators at column 0; PT_ABUFS A-operand buffers of
+// 64 columns (hi in the first 32, lo in the next 32) from column PT_ACOL.
+constexpr int PT_ABUFS = 4;
+constexpr int PT_ACOL = 256;
+constexpr int PT_TMEM_COLS = 512;
 constexpr int PT_THREADS = 320;
-constexpr int PT_SMEM_BYTES = PT_STAGES * PT_STAGE_BYTES + 1024 + 256;
+// mbarriers: full, conv, empty per stage; 2 + 2 accumulator; fin; one per A buffer.
+constexpr int PT_NBAR = 3 * PT_STAGES + 5 + PT_ABUFS;
+constexpr int PT_BAR_AREA = 512;
+static_assert(PT_NBAR * 8 + 16 <= PT_BAR_AREA, "barrier area");
+constexpr int PT_SMEM_BYTES = PT_STAGES * PT_STAGE_BYTES + 1024 + PT_BAR_AREA;
 static_assert(PT_SMEM_BYTES <= 232448, "shared memory budget");
 
 struct PowerParams {
@@ -105,9 +119,9 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
   auto tfull_bar = [&](int a) { return bar0 + 8u * (3 * PT_STAGES + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (3 * PT_STAGES + 2 + a); };
   const uint32_t fin_bar = bar0 + 8u * (3 * PT_STAGES + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * (3 * PT_STAGES + 5));
-  volatile int* abort_flag =
-      reinterpret_cast<volatile int*>(bar_area + 8 * (3 * PT_STAGES + 5) + 8);
+  auto aempty_bar = [&](int b) { return bar0 + 8u * (3 * PT_STAGES + 5 + b); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * PT_NBAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * PT_NBAR + 8);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -124,6 +138,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
       mbar_init(tempty_bar(a), 4);
     }
     mbar_init(fin_bar, 1);
+    for (int b = 0; b < PT_ABUFS; ++b) mbar_init(aempty_bar(b), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -158,7 +173,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
           const uint32_t s0 = sbase + stage * PT_STAGE_BYTES;
           tma_load_3d(s0, &tA, fb, kb * PT_BK, m0, blk);
-          tma_load_3d(s0 + 2 * PT_A_BYTES, &tV, fb, 0, kb * PT_BK, blk);
+          tma_load_3d(s0 + PT_A_BYTES, &tV, fb, 0, kb * PT_BK, blk);
           if (++stage == PT_STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -175,6 +190,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
       // ------------------------------------------------------------ MMA issuer
       int stage = 0;
       uint32_t phase = 0;
+      int abuf = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
@@ -191,28 +207,28 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t sA = sbase + stage * PT_STAGE_BYTES;
-          const uint32_t sAl = sA + PT_A_BYTES;
-          const uint32_t sV = sA + 2 * PT_A_BYTES;
+          const uint32_t sV = sbase + stage * PT_STAGE_BYTES + PT_A_BYTES;
           const uint32_t sVl = sV + PT_V_BYTES;
+          const uint32_t ta = tmem_base + static_cast<uint32_t>(PT_ACOL + abuf * 64);
 #pragma unroll
           for (int kk = 0; kk < PT_BK / 8; ++kk) {
-            const uint64_t da = smem_desc_sw128(sA + kk * 32, 16, 1024);
-            const uint64_t dal = smem_desc_sw128(sAl + kk * 32, 16, 1024);
             // V is MN-major TF32: 32-byte swizzle atoms, 4-row K slabs (SBO 512).
             const uint64_t dv = smem_desc(sV + kk * 8 * 128, PT_V_BYTES, 512, LAYOUT_SW128_BASE32);
             const uint64_t dvl =
                 smem_desc(sVl + kk * 8 * 128, PT_V_BYTES, 512, LAYOUT_SW128_BASE32);
+            const uint32_t a_hi = ta + kk * 8, a_lo = ta + 32 + kk * 8;
             const uint32_t accum = (kb | kk) ? 1u : 0u;
-            mma_tf32(d_tmem, dal, dv, p.idesc, accum);
-            mma_tf32(d_tmem, da, dvl, p.idesc, 1u);
-            mma_tf32(d_tmem, da, dv, p.idesc, 1u);
+            mma_tf32_ts(d_tmem, a_lo, dv, p.idesc, accum);
+            mma_tf32_ts(d_tmem, a_hi, dvl, p.idesc, 1u);
+            mma_tf32_ts(d_tmem, a_hi, dv, p.idesc, 1u);
           }
           mma_commit(empty_bar(stage));
+          mma_commit(aempty_bar(abuf));
           if (++stage == PT_STAGES) {
             stage = 0;
             phase ^= 1u;
           }
+          if (++abuf == PT_ABUFS) abuf = 0;
         }
         if (!ok) break;
         mma_commit(tfull_bar(acc));
@@ -225,36 +241,47 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
   } else if (warp < 6) {
     // -------------------------------------------------------------- converters
     const int ct = threadIdx.x - 64;  // 0..127
+    const int q = warp & 3;           // TMEM lane quarter this warp may write
+    const int r = q * 32 + lane;      // A-tile row this thread splits
     int stage = 0;
     uint32_t phase = 0;
+    int abuf = 0;
+    uint32_t aphase = 0;
     bool ok = true;
     for (long long sl = blockIdx.x; sl < p.slabs && ok; sl += gridDim.x) {
       for (int kb = 0; kb < p.nkb; ++kb) {
-        if (!mbar_wait(full_bar(stage), phase, abort_flag)) {
+        if (!mbar_wait(full_bar(stage), phase, abort_flag) ||
+            !mbar_wait(aempty_bar(abuf), aphase ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
+        tc_fence_after();
         uint8_t* st = smem + stage * PT_STAGE_BYTES;
-        // A: 1024 16-byte chunks; V: 256.  Element-wise, so the swizzle is kept.
+        // Row r of the 128B-swizzled tile: logical 16-byte chunk j sits at j ^ (r & 7).
+        uint32_t hi[32], lo[32];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int c = ct + 128 * i;
-          float4* hp = reinterpret_cast<float4*>(st + 16 * c);
-          float4* lp = reinterpret_cast<float4*>(st + PT_A_BYTES + 16 * c);
-          const float4 x = *hp;
-          float4 h, l;
-          h.x = rna_tf32(x.x); l.x = rna_tf32(x.x - h.x);
-          h.y = rna_tf32(x.y); l.y = rna_tf32(x.y - h.y);
-          h.z = rna_tf32(x.z); l.z = rna_tf32(x.z - h.z);
-          h.w = rna_tf32(x.w); l.w = rna_tf32(x.w - h.w);
-          *hp = h;
-          *lp = l;
+        for (int j = 0; j < 8; ++j) {
+          const float4 x = *reinterpret_cast<const float4*>(st + r * 128 + ((j ^ (r & 7)) << 4));
+          const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float h = rna_tf32(xs[e]);
+            hi[4 * j + e] = __float_as_uint(h);
+            lo[4 * j + e] = __float_as_uint(rna_tf32(xs[e] - h));
+          }
         }
+        const uint32_t ta = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                            static_cast<uint32_t>(PT_ACOL + abuf * 64);
+        tmem_st16(ta, reinterpret_cast<const uint32_t(&)[16]>(hi[0]));
+        tmem_st16(ta + 16, reinterpret_cast<const uint32_t(&)[16]>(hi[16]));
+        tmem_st16(ta + 32, reinterpret_cast<const uint32_t(&)[16]>(lo[0]));
+        tmem_st16(ta + 48, reinterpret_cast<const uint32_t(&)[16]>(lo[16]));
+        // V: 256 16-byte chunks, element-wise, so the swizzle is kept.
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           const int c = ct + 128 * i;
-          float4* hp = reinterpret_cast<float4*>(st + 2 * PT_A_BYTES + 16 * c);
-          float4* lp = reinterpret_cast<float4*>(st + 2 * PT_A_BYTES + PT_V_BYTES + 16 * c);
+          float4* hp = reinterpret_cast<float4*>(st + PT_A_BYTES + 16 * c);
+          float4* lp = reinterpret_cast<float4*>(st + PT_A_BYTES + PT_V_BYTES + 16 * c);
           const float4 x = *hp;
           float4 h, l;
           h.x = rna_tf32(x.x); l.x = rna_tf32(x.x - h.x);
@@ -264,12 +291,18 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
           *hp = h;
           *lp = l;
         }
+        tmem_wait_st();
         fence_async_shared();  // generic-proxy writes -> tensor-core reads
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(conv_bar(stage));
         if (++stage == PT_STAGES) {
           stage = 0;
           phase ^= 1u;
+        }
+        if (++abuf == PT_ABUFS) {
+          abuf = 0;
+          aphase ^= 1u;
         }
       }
     }

@@ -9,13 +9,19 @@ NDB is reported, not gated.  Measured errors are printed (run with -s).
 Ill-conditioned stacks.  Configs 2-4 have scaled condition numbers of 1e6-1e7
 (a spectrum down to 1e-6, or rank-deficient Gram matrices plus a 1e-6 ridge).
 There the inverse 4th root of the smallest eigen-directions is so sensitive that
-arithmetic of the path's own precision may miss the stated gate.  Each such root
-is also computed on the CPU with the library's storage rule (iterates rounded to
-the precision's storage type, products and epilogues in float32).  The gate is
-then the stated tolerance if that emulation meets it, and otherwise R_EMUL times
-the emulation's own error (the tensor core's truncating fp32 accumulation is the
-documented excess).  Every other stage of those configs (accumulate, lambda,
-apply, padding) keeps its stated gate.
+arithmetic of the path's own precision may miss the stated gate.
+  * 3xTF32 / TF32 roots: a sampled block that misses the stated gate is rerun
+    with the test-side model of the library's tensor-core arithmetic
+    (tests/tc_arith.py: alignment truncation with two guard bits, round toward
+    zero, the kernels' partial structure), in float64 on the GPU.  Its gate is
+    R_TC times the model's own error, and the GPU root must lie within
+    TRACK_TC times that error of the model's root.
+  * FP16 / BF16 roots: the root is also computed on the CPU with the library's
+    storage rule (iterates rounded to the storage type, products in float32);
+    the gate is R_EMUL times that emulation's error when the emulation itself
+    misses the stated gate.
+Every other stage of those configs (accumulate, lambda, apply, padding) keeps
+its stated gate.
 """
 
 import numpy as np
@@ -24,7 +30,9 @@ import torch
 
 import oracle
 import synth
-from tests.helpers import cn_emulated, library, ndb_emulated, rel_fro_blocks, require_gpu, to64
+from tests import tc_arith
+from tests.helpers import (cn_emulated, library, ndb_emulated, rel_fro, rel_fro_blocks,
+                           require_gpu, to64)
 
 pytestmark = pytest.mark.gpu
 
@@ -33,19 +41,43 @@ RIDGE = 1e-6
 
 
 R_EMUL = 10.0
+R_TC = 1.5
+TRACK_TC = 0.25
+MAX_TC_BLOCKS = 8
 
 
-def check_root(name, X, A, lam, idx, ref_fn, gate, emul_fn=None):
+def check_root(name, X, A, lam, idx, ref_fn, gate, emul_fn=None, tc_fn=None):
     """Relative Frobenius error of X[idx] against the oracle.
 
-    With emul_fn (ill-conditioned stacks) the same iteration is also run on the
-    CPU in the path's storage precision; the gate becomes R_EMUL times that
+    With tc_fn (3xTF32 / TF32 on ill-conditioned stacks) the blocks that miss the
+    stated gate are rerun with the tensor-core arithmetic model (at most
+    MAX_TC_BLOCKS of them, the worst first; any others must then stay below the
+    largest gate so found).  With emul_fn (half precision) the same iteration is
+    run on the CPU in the storage precision; the gate becomes R_EMUL times that
     emulation's error whenever the emulation itself misses the stated gate."""
     Xs = to64(X[idx])
     A64 = to64(A[idx])
     ref = ref_fn(A64, to64(lam[idx]))
     err = rel_fro_blocks(Xs, ref)
     msg = "%s: blocks %s rel err max %.3e" % (name, [int(i) for i in idx], err.max())
+    if tc_fn is not None:
+        print(msg)
+        assert np.all(np.isfinite(Xs))
+        miss = [t for t in np.argsort(-err) if err[t] >= gate]
+        gates = np.full(len(idx), gate)
+        for t in miss[:MAX_TC_BLOCKS]:
+            i = int(idx[t])
+            xm = to64(tc_fn(A[i], float(lam[i])))
+            em = rel_fro(xm, ref[t])
+            dm = rel_fro(Xs[t], xm)
+            gates[t] = max(gate, R_TC * em)
+            print("   block %d: gpu %.3e, tensor-core model %.3e, gpu vs model %.3e"
+                  % (i, err[t], em, dm))
+            assert dm < TRACK_TC * em, (name, i, dm, em)
+        for t in miss[MAX_TC_BLOCKS:]:
+            gates[t] = gates.max()
+        assert np.all(err < gates), (name, err, gates)
+        return err
     if emul_fn is not None:
         xe = np.stack([emul_fn(A[int(i)].cpu(), float(lam[int(i)])) for i in idx])
         ee = rel_fro_blocks(xe, ref)
@@ -122,12 +154,12 @@ def test_config2_frobenius_vs_power_scaling():
     X = dr.inv_root_cn(A, lam, k, "3xtf32")
     check_root("cfg2 CN 3xtf32 K=%d" % k, X, A, lam, np.array([0, 63]),
                lambda a, s: oracle.cn_inv_root(a, s, k)[0], GATE["3xtf32"],
-               lambda a, s: cn_emulated(a, s, k, "3xtf32"))
+               tc_fn=lambda a, s: tc_arith.cn_root(a, s, k, "3xtf32"))
     kn = int(max(its[("ndb", "power")].max() // 2 + 2, 8))
     X = dr.inv_root_ndb(A, lam, kn, "3xtf32")
     check_root("cfg2 NDB 3xtf32 K=%d" % kn, X, A, lam, np.array([0, 63]),
                lambda a, s: oracle.ndb_inv_root(a, s, kn)[0], GATE["3xtf32"],
-               lambda a, s: ndb_emulated(a, s, kn, "3xtf32"))
+               tc_fn=lambda a, s: tc_arith.ndb_root(a, s, kn, "3xtf32"))
     assert dr.device_status() == 0
 
 
@@ -165,11 +197,16 @@ def check_step(dr, tag, G, vr, vc, F, V0, lam, X, U, root, prec, fidx, gidx):
               else (lambda a, s: oracle.cn_inv_root(a, s, 10, ridge=RIDGE)[0]))
     emul = ((lambda a, s: ndb_emulated(a, s, 10, prec, RIDGE)) if root == "ndb"
             else (lambda a, s: cn_emulated(a, s, 10, prec, RIDGE)))
+    tc = ((lambda a, s: tc_arith.ndb_root(a, s, 10, prec, RIDGE)) if root == "ndb"
+          else (lambda a, s: tc_arith.cn_root(a, s, 10, prec, RIDGE)))
     gate = GATE[prec] if (root == "cn" or prec in ("3xtf32", "tf32")) else None
+    name = "%s %s %s" % (tag, root, prec)
     if gate is None:  # half-precision NDB: reported only
-        check_root("%s %s %s" % (tag, root, prec), X, F, lam, fidx, ref_fn, None)
+        check_root(name, X, F, lam, fidx, ref_fn, None)
+    elif prec in ("3xtf32", "tf32"):
+        check_root(name, X, F, lam, fidx, ref_fn, gate, tc_fn=tc)
     else:
-        check_root("%s %s %s" % (tag, root, prec), X, F, lam, fidx, ref_fn, gate, emul)
+        check_root(name, X, F, lam, fidx, ref_fn, gate, emul)
     Xs = torch.cat([X[gidx], X[ng + gidx]])
     Uref = oracle.apply_preconditioner(G64, to64(Xs))
     errU = rel_fro_blocks(to64(U[gidx]), Uref)

@@ -1,0 +1,144 @@
+"""Pins for the test-side tensor-core arithmetic model (tests/tc_arith.py), on the CPU.
+
+Each expected value below is worked out by hand from the stated rule (align to the
+largest exponent, truncate every addend toward zero two bits below the fp32 ulp,
+sum exactly, round the sum toward zero); a scalar restatement in exact rationals
+cross-checks the vectorised model on small random inputs."""
+
+import math
+import random
+from fractions import Fraction
+
+import pytest
+import torch
+
+from tests import tc_arith
+
+ULP1 = 2.0 ** -23  # fp32 ulp of [1, 2)
+
+
+def one_instr(terms, acc=0.0):
+    """Products of one instruction (each term times 1), added to acc."""
+    p = torch.zeros((8, 1, 1), dtype=torch.float64)
+    for k, v in enumerate(terms):
+        p[k, 0, 0] = v
+    return float(tc_arith.mma_accumulate(torch.full((1, 1), acc, dtype=torch.float32), p)[0, 0])
+
+
+@pytest.mark.parametrize("terms,acc,want", [
+    ([1.0, 0.75 * ULP1], 0.0, 1.0),                        # 0.75 ulp kept, then RZ
+    ([-1.0, -0.75 * ULP1], 0.0, -1.0),                     # RZ is symmetric
+    ([1.0, -1.25 * 2 ** -24], 0.0, 1.0 - 2 ** -24),        # addend truncated to -2^-24 first
+    ([-1.25 * 2 ** -24], 1.0, 1.0 - 2 ** -24),             # the accumulator sets E too
+    ([1.0] + [2.0 ** -25] * 4, 0.0, 1.0 + ULP1),           # 2^-25 is at the resolution
+    ([1.0] + [2.0 ** -26] * 4, 0.0, 1.0),                  # 2^-26 is below it
+    ([2.0 ** -24] * 4 + [1.0], 0.0, 1.0 + 2 * ULP1),       # order inside an instruction is irrelevant
+    ([1024.0, -1024.0, 3 * 2.0 ** -20], 0.0, 0.0),         # lost below 2^(10-25)
+    ([-1024.0, 3 * 2.0 ** -20], 1024.0, 0.0),
+    ([3.0, 5.0, -7.0, 11.0], 2.0, 14.0),                   # exact small integers stay exact
+])
+def test_single_instruction_rule(terms, acc, want):
+    assert one_instr(terms, acc) == want
+
+
+def _scalar_instr(acc, prods):
+    """The rule on one output element in exact rationals."""
+    vals = [Fraction(acc)] + [Fraction(p) for p in prods]
+    nz = [abs(v) for v in vals if v != 0]
+    if not nz:
+        return 0.0
+    e = math.floor(math.log2(max(nz)))
+    while Fraction(2) ** (e + 1) <= max(nz):
+        e += 1
+    while Fraction(2) ** e > max(nz):
+        e -= 1
+    res = Fraction(2) ** (e - tc_arith.GUARD)
+
+    def trunc(v):
+        q = abs(v) / res
+        return (1 if v >= 0 else -1) * (q.numerator // q.denominator) * res
+
+    s = sum(trunc(v) for v in vals)
+    if s == 0:
+        return 0.0
+    # round toward zero to 24 significant bits
+    es = math.floor(math.log2(abs(s)))
+    while Fraction(2) ** (es + 1) <= abs(s):
+        es += 1
+    while Fraction(2) ** es > abs(s):
+        es -= 1
+    q = Fraction(2) ** (es - 23)
+    r = abs(s) / q
+    return float((1 if s > 0 else -1) * (r.numerator // r.denominator) * q)
+
+
+def _scalar_gemm(a, b, passes, partial_sub):
+    n, K = len(a[0]), len(a[0][0])
+    m = len(b[0][0])
+    steps = K // 8
+    sub = steps if partial_sub is None else partial_sub
+    out = [[0.0] * m for _ in range(n)]
+    for i in range(n):
+        for j in range(m):
+            total = 0.0
+            for g in range(steps // sub):
+                acc = 0.0
+                for s in range(sub):
+                    k0 = (g * sub + s) * 8
+                    for x, y in passes:
+                        acc = _scalar_instr(acc, [a[x][i][k0 + t] * b[y][k0 + t][j] for t in range(8)])
+                total = float(torch.tensor(total, dtype=torch.float32) + torch.tensor(acc, dtype=torch.float32))
+            out[i][j] = total
+    return out
+
+
+@pytest.mark.parametrize("prec,partial_sub", [("tf32", None), ("3xtf32", None), ("3xtf32", 2)])
+def test_gemm_matches_scalar_restatement(prec, partial_sub):
+    g = torch.Generator().manual_seed(5)
+    a = torch.randn((3, 32), generator=g) * torch.exp(2 * torch.randn((3, 32), generator=g))
+    b = torch.randn((32, 2), generator=g)
+    got = tc_arith.gemm(a, b, prec, partial_sub)
+    if prec == "3xtf32":
+        ah, al = tc_arith.split_tf32(a)
+        bh, bl = tc_arith.split_tf32(b)
+        A = [al.double().tolist(), ah.double().tolist()]
+        B = [bh.double().tolist(), bl.double().tolist()]
+        passes = [(0, 0), (1, 1), (1, 0)]
+    else:
+        A = [tc_arith.rna_tf32(a).double().tolist()]
+        B = [tc_arith.rna_tf32(b).double().tolist()]
+        passes = [(0, 0)]
+    want = _scalar_gemm(A, B, passes, partial_sub)
+    assert got.tolist() == want
+
+
+def test_gemm_error_is_fp32_class_and_biased():
+    """On random data the modelled product is within a few fp32 ulps of exact; over
+    long positive sums the truncation shows as a negative bias growing with K."""
+    g = torch.Generator().manual_seed(6)
+    a = torch.rand((16, 512), generator=g)
+    b = torch.rand((512, 16), generator=g)
+    ex = a.double() @ b.double()
+    got = tc_arith.gemm(a, b, "tf32").double()
+    ex_tf = tc_arith.rna_tf32(a).double() @ tc_arith.rna_tf32(b).double()
+    rel = (got - ex_tf) / ex_tf
+    assert rel.max() <= 0.0                      # never above the exact sum of positives
+    assert -64 * 2.0 ** -24 < rel.mean() < -2.0 ** -24
+    got3 = tc_arith.gemm(a, b, "3xtf32").double()
+    assert ((got3 - ex).abs() / ex).max() < 128 * 2.0 ** -24
+    got3p = tc_arith.gemm(a, b, "3xtf32", partial_sub=8).double()
+    assert ((got3p - ex) / ex).mean() > ((got3 - ex) / ex).mean()   # shorter chains, less bias
+
+
+def test_roots_reduce_to_exact_on_identity():
+    eye = torch.eye(64)
+    for fn in (tc_arith.cn_root, tc_arith.ndb_root):
+        X = fn(4.0 * eye, 4.0, 6, "3xtf32")
+        assert torch.allclose(X, eye * 4.0 ** -0.25, rtol=0, atol=1e-6)
+
+
+def test_random_small_integers_are_exact():
+    rng = random.Random(7)
+    a = torch.tensor([[rng.randint(-8, 8) for _ in range(64)] for _ in range(4)], dtype=torch.float32)
+    b = torch.tensor([[rng.randint(-8, 8) for _ in range(3)] for _ in range(64)], dtype=torch.float32)
+    assert torch.equal(tc_arith.gemm(a, b, "tf32"), (a.double() @ b.double()).float())
