@@ -61,7 +61,11 @@ struct Cfg {
   static constexpr int STAGE_BYTES = (A_BYTES + B_BYTES) * NPART;
   // Bytes the barrier owner waits for per stage (both CTAs' loads for a pair).
   static constexpr int EXPECT_BYTES = (MODE == 2 ? 2 : 1) * STAGE_BYTES;
-  static constexpr int STAGES_RAW = (224 * 1024) / STAGE_BYTES;
+  // fp16/bf16-operand kernels stage 16-bit output tiles through shared memory
+  // (4 KB per epilogue warp) so that global stores cover whole rows.
+  static constexpr int EPI_WARP_BYTES = 4096;
+  static constexpr int EPI_BYTES = (KT == 0) ? 8 * EPI_WARP_BYTES : 0;
+  static constexpr int STAGES_RAW = (224 * 1024 - EPI_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int MMA_M = (MODE == 2) ? 256 : 128;
@@ -74,12 +78,13 @@ struct Cfg {
   static constexpr uint32_t MN_LAYOUT = (KT == 0) ? LAYOUT_SW128 : LAYOUT_SW128_BASE32;
   static constexpr uint32_t MN_SBO = (KT == 0) ? 1024 : 512;
   static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + BAR_BYTES;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + BAR_BYTES + EPI_BYTES;
   static_assert(STAGES >= 2, "need at least two pipeline stages");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
 struct KParams {
+  CUtensorMap tO[2];  // 16-bit outputs of the staged epilogue (TMA store maps)
   int dim;
   int tiles_m, tiles_n;
   long long total_tiles;
@@ -87,6 +92,7 @@ struct KParams {
   int nkb;
   uint32_t idesc;
   int a_mn, b_mn;
+  int staged;  // all outputs 16-bit (at most two): tiles leave through TMA stores
   EpiParams epi;
 };
 
@@ -113,12 +119,28 @@ __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
   }
 }
 
-// Epilogue for 16 consecutive columns of one row.  Stores and the optional
-// E read are 256-bit (one whole L2 sector per thread) when the base pointers
-// allow it, 128-bit otherwise.
-__device__ __forceinline__ void epilogue16f(const EpiParams& e, long long blk, int rg, int cg0,
-                                            long long idx, const float (&c)[16], float& rsum,
-                                            bool diag) {
+// Per-tile constants of the epilogue, read once per tile: the per-block output
+// multipliers and the valid size of a padded block.  (Read inside the chunk loop
+// they would be reloaded after every store, which may alias them.)
+struct TileEpi {
+  float m[3];
+  int pv;
+};
+
+__device__ __forceinline__ TileEpi tile_epi(const EpiParams& e, long long blk) {
+  TileEpi t;
+#pragma unroll
+  for (int o = 0; o < 3; ++o)
+    t.m[o] = (o < e.nout && e.out[o].mult != nullptr) ? e.out[o].mult[blk] : 1.0f;
+  t.pv = (e.pad_valid != nullptr) ? e.pad_valid[blk] : 0x7fffffff;
+  return t;
+}
+
+// Residual term and E operand for 16 consecutive columns of one row.  E reads are
+// 256-bit when the base pointers allow it, 128-bit otherwise.
+__device__ __forceinline__ void epi_pre16(const EpiParams& e, int rg, int cg0, long long idx,
+                                          const float (&c)[16], float& rsum, bool diag,
+                                          float (&ev)[16]) {
   // diag: this warp's rows and these 16 columns share a diagonal element (a
   // warp-uniform flag: off-diagonal chunks skip every identity term).
   if (e.resid_acc != nullptr) {
@@ -133,7 +155,6 @@ __device__ __forceinline__ void epilogue16f(const EpiParams& e, long long blk, i
       for (int j = 0; j < 16; ++j) rsum = fmaf(c[j], c[j], rsum);
     }
   }
-  float ev[16];
   if (e.E_hi != nullptr) {
     if (aligned32(e.E_hi) && (e.E_fmt != FMT_SPLIT || aligned32(e.E_lo))) {
       load16_v8(e.E_fmt, e.E_hi, e.E_lo, idx, ev);
@@ -150,28 +171,44 @@ __device__ __forceinline__ void epilogue16f(const EpiParams& e, long long blk, i
 #pragma unroll
     for (int j = 0; j < 16; ++j) ev[j] = 0.0f;
   }
-  const bool pad = (e.pad_valid != nullptr);
-  const int pv = pad ? e.pad_valid[blk] : 0x7fffffff;
+}
+
+// Output o's values D = mult (alpha C + gamma I + eps E), identity outside the
+// valid part of a padded block.
+__device__ __forceinline__ void epi_out16(const EpiParams& e, const TileEpi& te, int o, int rg,
+                                          int cg0, const float (&c)[16], const float (&ev)[16],
+                                          bool diag, float (&d)[16]) {
+  const EpiOut& O = e.out[o];
+  const float m = te.m[o];
+  if (!diag && e.pad_valid == nullptr) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) d[j] = m * fmaf(O.alpha, c[j], O.eps * ev[j]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int col = cg0 + j;
+      float v = fmaf(O.alpha, c[j], O.eps * ev[j]);
+      if (rg == col) v += O.gamma;
+      v *= m;
+      if (rg >= te.pv || col >= te.pv) v = (rg == col) ? 1.0f : 0.0f;
+      d[j] = v;
+    }
+  }
+}
+
+// Epilogue for 16 consecutive columns of one row, stored straight to global
+// memory (256-bit stores when the base pointers allow it, 128-bit otherwise).
+__device__ __forceinline__ void epilogue16f(const EpiParams& e, const TileEpi& te, int rg,
+                                            int cg0, long long idx, const float (&c)[16],
+                                            float& rsum, bool diag) {
+  float ev[16];
+  epi_pre16(e, rg, cg0, idx, c, rsum, diag, ev);
 #pragma unroll
   for (int o = 0; o < 3; ++o) {
     if (o < e.nout) {
       const EpiOut& O = e.out[o];
-      const float m = (O.mult != nullptr) ? O.mult[blk] : 1.0f;
       float d[16];
-      if (!diag && !pad) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) d[j] = m * fmaf(O.alpha, c[j], O.eps * ev[j]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int col = cg0 + j;
-          float v = fmaf(O.alpha, c[j], O.eps * ev[j]);
-          if (rg == col) v += O.gamma;
-          v *= m;
-          if (rg >= pv || col >= pv) v = (rg == col) ? 1.0f : 0.0f;
-          d[j] = v;
-        }
-      }
+      epi_out16(e, te, o, rg, cg0, c, ev, diag, d);
       if (aligned32(O.hi) && (O.fmt != FMT_SPLIT || aligned32(O.lo))) {
         store16_v8(O.fmt, O.hi, O.lo, idx, d);
       } else {
@@ -185,13 +222,61 @@ __device__ __forceinline__ void epilogue16f(const EpiParams& e, long long blk, i
   }
 }
 
-__device__ __forceinline__ void epilogue16(const EpiParams& e, long long blk, int rg, int cg0,
-                                           long long idx, const uint32_t (&r)[16], float& rsum,
-                                           bool diag) {
+// Position of 16-byte unit u of staging row r: the TMA store's swizzle (128-byte
+// rows: SWIZZLE_128B, unit ^ (r & 7); 64-byte rows: SWIZZLE_64B, unit ^ ((r >> 1)
+// & 3)).  Both spread a warp's row-wise writes over all banks.
+__device__ __forceinline__ int stage_unit(int u, int r, int U) {
+  return (U == 8) ? (u ^ (r & 7)) : (u ^ ((r >> 1) & 3));
+}
+
+// Staged variant for 16-bit outputs: chunk jr of the current round is packed and
+// written to this thread's row of the warp's staging buffer (per output a box of
+// 32 rows x U 16-byte units in the TMA store's swizzled layout).
+__device__ __forceinline__ void epilogue16s(const EpiParams& e, const TileEpi& te, int rg,
+                                            int cg0, long long idx, const float (&c)[16],
+                                            float& rsum, bool diag, uint8_t* wst, int lane,
+                                            int jr, int U) {
+  float ev[16];
+  epi_pre16(e, rg, cg0, idx, c, rsum, diag, ev);
+#pragma unroll
+  for (int o = 0; o < 2; ++o) {
+    if (o < e.nout) {
+      float d[16];
+      epi_out16(e, te, o, rg, cg0, c, ev, diag, d);
+      uint32_t r[8];
+      const bool half = (e.out[o].fmt == FMT_F16);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        r[j] = half ? pack_half2(d[2 * j], d[2 * j + 1]) : pack_bf162(d[2 * j], d[2 * j + 1]);
+      uint8_t* rowp = wst + o * 32 * U * 16 + lane * U * 16;
+      *reinterpret_cast<uint4*>(rowp + (stage_unit(2 * jr, lane, U) << 4)) =
+          make_uint4(r[0], r[1], r[2], r[3]);
+      *reinterpret_cast<uint4*>(rowp + (stage_unit(2 * jr + 1, lane, U) << 4)) =
+          make_uint4(r[4], r[5], r[6], r[7]);
+    }
+  }
+}
+
+// Hands one staged round to the TMA engine: a 32-row box per output at (col0,
+// row0) of block blk.  The buffer may be rewritten once the stores have read it.
+__device__ __forceinline__ void flush_round_tma(const KParams& p, uint32_t wst_s, int lane, int U,
+                                                int row0, long long blk, int col0) {
+  fence_async_shared();  // this thread's staging writes -> the TMA engine
+  __syncwarp();
+  if (lane == 0) {
+    for (int o = 0; o < p.epi.nout; ++o)
+      tma_store_3d(&p.tO[o], wst_s + o * 32 * U * 16, col0, row0, static_cast<int>(blk));
+    bulk_commit_group();
+  }
+}
+
+__device__ __forceinline__ void epilogue16(const EpiParams& e, const TileEpi& te, int rg,
+                                           int cg0, long long idx, const uint32_t (&r)[16],
+                                           float& rsum, bool diag) {
   float c[16];
 #pragma unroll
   for (int j = 0; j < 16; ++j) c[j] = __uint_as_float(r[j]);
-  epilogue16f(e, blk, rg, cg0, idx, c, rsum, diag);
+  epilogue16f(e, te, rg, cg0, idx, c, rsum, diag);
 }
 
 // Whether rows [r0, r0 + 32) and columns [c0, c0 + 16) contain a diagonal element.
@@ -212,8 +297,9 @@ __global__ void __launch_bounds__(320, 1)
   uint8_t* smem = smem_raw + pad;
   const uint32_t sbase = raw_base + pad;
 
-  uint8_t* bar_area = smem + C::STAGES * C::STAGE_BYTES;
-  const uint32_t bar0 = sbase + C::STAGES * C::STAGE_BYTES;
+  // Layout: stages | epilogue staging (1024-aligned) | barriers.
+  uint8_t* bar_area = smem + C::STAGES * C::STAGE_BYTES + C::EPI_BYTES;
+  const uint32_t bar0 = sbase + C::STAGES * C::STAGE_BYTES + C::EPI_BYTES;
   // barrier addresses
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
@@ -460,6 +546,8 @@ __global__ void __launch_bounds__(320, 1)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int h = (warp - 2) >> 2;
     constexpr int HALF = BN / 2;
+    uint8_t* wst = smem + C::STAGES * C::STAGE_BYTES + (warp - 2) * C::EPI_WARP_BYTES;
+    const uint32_t wst_s = sbase + C::STAGES * C::STAGE_BYTES + (warp - 2) * C::EPI_WARP_BYTES;
     const int row = q * 32 + lane;
     const long long dd = static_cast<long long>(p.dim) * p.dim;
     int acc = 0;
@@ -474,6 +562,7 @@ __global__ void __launch_bounds__(320, 1)
       const int r0w = m0 + q * 32;  // first row of this warp
       const int nh = n0 + h * HALF;
       const long long rbase = blk * dd + static_cast<long long>(rg) * p.dim;
+      const TileEpi te = tile_epi(p.epi, blk);
       float rsum = 0.0f;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * BN + h * HALF);
@@ -481,15 +570,45 @@ __global__ void __launch_bounds__(320, 1)
       // is processed.
       uint32_t ra[16], rb[16];
       tmem_ld16(taddr, ra);
+      if (p.staged) {
+        // Rounds of R chunks: 64 columns for one output, 32 for two (4 KB).
+        const int R = (p.epi.nout == 1) ? 4 : 2;
+        const int U = 2 * R;
 #pragma unroll 1
-      for (int c = 0; c < HALF / 16; c += 2) {
-        tmem_wait_ld(ra);
-        tmem_ld16(taddr + (c + 1) * 16, rb);
-        const int ca = nh + c * 16, cb = ca + 16;
-        epilogue16(p.epi, blk, rg, ca, rbase + ca, ra, rsum, chunk_on_diag(r0w, ca));
-        tmem_wait_ld(rb);
-        if (c + 2 < HALF / 16) tmem_ld16(taddr + (c + 2) * 16, ra);
-        epilogue16(p.epi, blk, rg, cb, rbase + cb, rb, rsum, chunk_on_diag(r0w, cb));
+        for (int c = 0; c < HALF / 16; c += 2) {
+          tmem_wait_ld(ra);
+          tmem_ld16(taddr + (c + 1) * 16, rb);
+          const int ca = nh + c * 16, cb = ca + 16;
+          if (c % R == 0) {
+            // The previous round's stores must have read the buffer.
+            if (lane == 0) bulk_wait_group_read<0>();
+            __syncwarp();
+          }
+          float fa[16], fb[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) fa[j] = __uint_as_float(ra[j]);
+          epilogue16s(p.epi, te, rg, ca, rbase + ca, fa, rsum, chunk_on_diag(r0w, ca), wst, lane,
+                      c % R, U);
+          tmem_wait_ld(rb);
+          if (c + 2 < HALF / 16) tmem_ld16(taddr + (c + 2) * 16, ra);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) fb[j] = __uint_as_float(rb[j]);
+          epilogue16s(p.epi, te, rg, cb, rbase + cb, fb, rsum, chunk_on_diag(r0w, cb), wst, lane,
+                      (c + 1) % R, U);
+          if ((c + 2) % R == 0)
+            flush_round_tma(p, wst_s, lane, U, r0w, blk, nh + (c + 2 - R) * 16);
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < HALF / 16; c += 2) {
+          tmem_wait_ld(ra);
+          tmem_ld16(taddr + (c + 1) * 16, rb);
+          const int ca = nh + c * 16, cb = ca + 16;
+          epilogue16(p.epi, te, rg, ca, rbase + ca, ra, rsum, chunk_on_diag(r0w, ca));
+          tmem_wait_ld(rb);
+          if (c + 2 < HALF / 16) tmem_ld16(taddr + (c + 2) * 16, ra);
+          epilogue16(p.epi, te, rg, cb, rbase + cb, rb, rsum, chunk_on_diag(r0w, cb));
+        }
       }
       if (p.epi.resid_acc != nullptr) {
 #pragma unroll
@@ -507,6 +626,9 @@ __global__ void __launch_bounds__(320, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
+    // Staged tiles: every TMA store has landed before the CTA exits.
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -547,8 +669,9 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t pad = (1024u - (raw_base & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
   const uint32_t sbase = raw_base + pad;
-  uint8_t* bar_area = smem + C::STAGES * C::STAGE_BYTES;
-  const uint32_t bar0 = sbase + C::STAGES * C::STAGE_BYTES;
+  // Layout: stages | epilogue staging (1024-aligned) | barriers.
+  uint8_t* bar_area = smem + C::STAGES * C::STAGE_BYTES + C::EPI_BYTES;
+  const uint32_t bar0 = sbase + C::STAGES * C::STAGE_BYTES + C::EPI_BYTES;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
   auto pfull_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
@@ -759,6 +882,7 @@ __global__ void __launch_bounds__(320, 1)
       const int rg = m0 + row;
       const int cbase = n0 + h * 128;
       const long long rbase = blk * dd + static_cast<long long>(rg) * p.dim;
+      const TileEpi te = tile_epi(p.epi, blk);
       float rsum = 0.0f;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
@@ -767,7 +891,7 @@ __global__ void __launch_bounds__(320, 1)
         for (int j = 0; j < 16; ++j) v[j] = sum[c * 16 + j];
         // The generic (diagonal-aware) path for every chunk: the branch-free
         // variants would add live registers to a kernel already holding sum[128].
-        epilogue16f(p.epi, blk, rg, cbase + c * 16, rbase + cbase + c * 16, v, rsum, true);
+        epilogue16f(p.epi, te, rg, cbase + c * 16, rbase + cbase + c * 16, v, rsum, true);
       }
       if (p.epi.resid_acc != nullptr) {
 #pragma unroll
@@ -919,6 +1043,22 @@ static dash_status run_gemm(const GemmLaunch& g, cudaStream_t st) {
   p.a_mn = a_mn;
   p.b_mn = b_mn;
   p.epi = g.epi;
+  p.staged = (C::EPI_BYTES > 0 && g.epi.nout >= 1 && g.epi.nout <= 2) ? 1 : 0;
+  for (int o = 0; o < g.epi.nout && p.staged; ++o) {
+    const EpiOut& O = g.epi.out[o];
+    if ((O.fmt != FMT_F16 && O.fmt != FMT_BF16) ||
+        (reinterpret_cast<uintptr_t>(O.hi) & 15u) != 0)
+      p.staged = 0;
+  }
+  if (p.staged) {
+    // Boxes of 32 rows x 64 columns (one output, 128-byte swizzle) or x 32
+    // columns (two outputs, 64-byte swizzle), matching the staging layout.
+    const bool one = (g.epi.nout == 1);
+    for (int o = 0; o < g.epi.nout; ++o)
+      if (!make_tmap(&p.tO[o], g.epi.out[o].hi, 2, g.dim, g.nblocks, one ? 64 : 32, 32,
+                     one ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
+        return DASH_ERR_CUDA;
+  }
   if (cudaFuncSetAttribute(KernelOf<BN, KT, MODE, ACC>::get(),
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::SMEM_BYTES) != cudaSuccess)
