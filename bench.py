@@ -47,6 +47,30 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # Nominal dense ratios to bf16 (GB300): tf32 1.1 / 2.25 PFLOP/s.
 TF32_RATIO = 1.1 / 2.25
 
+# DRAM bytes (read + write) per factor block per launch of the CTA-pair fp16 GEMM:
+# mean of the four Coupled Newton launches of the ncu capture summarised in
+# profiles/gemm_tc_f16_pair_cn_b1024_n64.md (64 blocks of 1024^2; traffic grows in
+# proportion to the blocks a launch processes).  Valid only for the kernel sources
+# it was taken on, identified by GEMM_TRAFFIC_SRC.
+GEMM_TRAFFIC_PER_BLOCK = 5.144e6
+GEMM_TRAFFIC_SRC = "b7d2761d0aa3d4f8"
+GEMM_SOURCES = ("matrix_inverse_roots_gb300/csrc/gemm_tc.cu",
+                "matrix_inverse_roots_gb300/csrc/dash_common.cuh")
+
+
+def gemm_traffic(flops_per_launch, b):
+    """Measured DRAM bytes of one dominant-GEMM launch, or None if the kernel changed."""
+    import hashlib
+
+    h = hashlib.sha256()
+    root = os.path.dirname(os.path.abspath(__file__))
+    for f in GEMM_SOURCES:
+        with open(os.path.join(root, f), "rb") as fh:
+            h.update(fh.read())
+    if h.hexdigest()[:16] != GEMM_TRAFFIC_SRC or b != 1024:
+        return None
+    return round(GEMM_TRAFFIC_PER_BLOCK * flops_per_launch / (2.0 * b ** 3))
+
 
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -214,7 +238,8 @@ def roofline_from_trace(records, peaks):
                     peaks["_source"], "" if dom in ("gemm_f16", "gemm_bf16")
                     else " x nominal tf32/bf16 ratio" + (" / 3" if dom == "gemm_3xtf32" else "")),
                 "launches": n, "avg_launch_ms": round(ms / n, 4),
-                "flops_per_launch": fl / n, "traffic": None}
+                "flops_per_launch": fl / n,
+                "traffic": gemm_traffic(fl / n, BS) if dom in ("gemm_f16", "gemm_bf16") else None}
     else:
         peak = peaks["hbm_gbs"]
         achieved = b / (ms * 1e-3) / 1e9
