@@ -16,9 +16,10 @@
 //               (tcgen05.st), so the split costs no shared-memory writes and the
 //               ring holds only raw data; the small V tile is split in place
 //               (hi over the fp32 data, lo beside it).
-//   warp 1      one thread issues lo*hi, hi*lo and hi*hi (M = 128, N = 32, K = 8,
-//               A read from TMEM, V from shared memory) into a TMEM accumulator;
-//               two accumulators alternate.
+//   warp 1      one thread issues, per K = 8 slice, A_hi [V_hi | V_lo] (N = 64:
+//               V_lo sits one operand atom after V_hi) and A_lo V_hi (N = 32) into
+//               a 64-column TMEM accumulator, A read from TMEM and V from shared
+//               memory; two accumulators alternate.  The epilogue adds the halves.
 //   warps 6..9  epilogue: one accumulator row per thread; scale, ridge term,
 //               W stored as contiguous 128-byte rows; column sums (W^2, or v.w and
 //               v.v on the last product) reduced with a butterfly shuffle and one
@@ -48,8 +49,10 @@ constexpr int PT_V_BYTES = PT_BK * 128;   // 4 KB
 // Stage: A (raw fp32) | V (hi after conversion) | V lo.
 constexpr int PT_STAGE_BYTES = PT_A_BYTES + 2 * PT_V_BYTES;  // 24 KB
 constexpr int PT_STAGES = 9;
-// TMEM: two 32-column accumulators at column 0; PT_ABUFS A-operand buffers of
-// 64 columns (hi in the first 32, lo in the next 32) from column PT_ACOL.
+// TMEM: two 64-column accumulators at column 0 (A_hi V_hi + A_lo V_hi | A_hi V_lo);
+// PT_ABUFS A-operand buffers of 64 columns (hi in the first 32, lo in the next 32)
+// from column PT_ACOL.
+constexpr int PT_ACC_COLS = 2 * PT_NV;
 constexpr int PT_ABUFS = 4;
 constexpr int PT_ACOL = 256;
 constexpr int PT_TMEM_COLS = 512;
@@ -66,7 +69,8 @@ struct PowerParams {
   long long nblocks;
   long long slabs;  // nblocks * dim / 128
   int nkb;          // dim / 32
-  uint32_t idesc;
+  uint32_t idesc;     // M = 128, N = 64
+  uint32_t idesc32;   // M = 128, N = 32
   float ridge;
   const float* Vin;       // (nblocks, dim, 32)
   const float* in_nrm2;   // (nblocks, 32) or null
@@ -200,7 +204,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * PT_NV);
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * PT_ACC_COLS);
         for (int kb = 0; kb < p.nkb; ++kb) {
           if (!mbar_wait(conv_bar(stage), phase, abort_flag)) {
             ok = false;
@@ -208,19 +212,16 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
           }
           tc_fence_after();
           const uint32_t sV = sbase + stage * PT_STAGE_BYTES + PT_A_BYTES;
-          const uint32_t sVl = sV + PT_V_BYTES;
           const uint32_t ta = tmem_base + static_cast<uint32_t>(PT_ACOL + abuf * 64);
 #pragma unroll
           for (int kk = 0; kk < PT_BK / 8; ++kk) {
-            // V is MN-major TF32: 32-byte swizzle atoms, 4-row K slabs (SBO 512).
+            // V is MN-major TF32: 32-byte swizzle atoms, 4-row K slabs (SBO 512);
+            // the next N atom (LBO) is V_lo, so N = 64 reads [V_hi | V_lo].
             const uint64_t dv = smem_desc(sV + kk * 8 * 128, PT_V_BYTES, 512, LAYOUT_SW128_BASE32);
-            const uint64_t dvl =
-                smem_desc(sVl + kk * 8 * 128, PT_V_BYTES, 512, LAYOUT_SW128_BASE32);
             const uint32_t a_hi = ta + kk * 8, a_lo = ta + 32 + kk * 8;
             const uint32_t accum = (kb | kk) ? 1u : 0u;
-            mma_tf32_ts(d_tmem, a_lo, dv, p.idesc, accum);
-            mma_tf32_ts(d_tmem, a_hi, dvl, p.idesc, 1u);
-            mma_tf32_ts(d_tmem, a_hi, dv, p.idesc, 1u);
+            mma_tf32_ts(d_tmem, a_hi, dv, p.idesc, accum);
+            mma_tf32_ts(d_tmem, a_lo, dv, p.idesc32, 1u);
           }
           mma_commit(empty_bar(stage));
           mma_commit(aempty_bar(abuf));
@@ -317,13 +318,17 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
       tc_fence_after();
       const long long blk = sl / slabs_per_blk;
       const int row = static_cast<int>(sl % slabs_per_blk) * PT_BM + row_in;
-      uint32_t r0[16], r1[16];
-      const uint32_t taddr =
-          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * PT_NV);
+      uint32_t r0[16], r1[16], r2[16], r3[16];
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(acc * PT_ACC_COLS);
       tmem_ld16(taddr, r0);
       tmem_ld16(taddr + 16, r1);
+      tmem_ld16(taddr + 32, r2);
+      tmem_ld16(taddr + 48, r3);
       tmem_wait_ld(r0);
       tmem_fence_regs(r1);
+      tmem_fence_regs(r2);
+      tmem_fence_regs(r3);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(acc));  // accumulator copied to registers
@@ -347,8 +352,10 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
       }
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
-        w[c] = fmaf(p.ridge, v[c], __uint_as_float(r0[c]) * sc[c]);
-        w[16 + c] = fmaf(p.ridge, v[16 + c], __uint_as_float(r1[c]) * sc[16 + c]);
+        const float a0 = __uint_as_float(r0[c]) + __uint_as_float(r2[c]);
+        const float a1 = __uint_as_float(r1[c]) + __uint_as_float(r3[c]);
+        w[c] = fmaf(p.ridge, v[c], a0 * sc[c]);
+        w[16 + c] = fmaf(p.ridge, v[16 + c], a1 * sc[16 + c]);
       }
       float s0[PT_NV], s1[PT_NV];
       if (p.last) {
@@ -432,7 +439,8 @@ dash_status launch_power_step_tc(const float* A, float ridge, int dim, long long
   p.nblocks = nblocks;
   p.slabs = nblocks * (dim / PT_BM);
   p.nkb = dim / PT_BK;
-  p.idesc = make_idesc(2, 0, 1, PT_BM, PT_NV);
+  p.idesc = make_idesc(2, 0, 1, PT_BM, PT_ACC_COLS);
+  p.idesc32 = make_idesc(2, 0, 1, PT_BM, PT_NV);
   p.ridge = ridge;
   p.Vin = Vin;
   p.in_nrm2 = in_nrm2;
