@@ -652,8 +652,12 @@ __global__ void __launch_bounds__(320, 1)
 // ACC_SUB sub-steps (one sub-step = the three MMAs of one K = 8 slice; two
 // partials alternate), and eight reducer warps -- two per TMEM lane quarter, 128
 // columns each -- add the partials into fp32 registers with round-to-nearest.
-// The fused epilogue then runs on those register sums.
-constexpr int ACC_SUB = 8;  // K = 8 sub-steps per TMEM partial
+// The fused epilogue then runs on those register sums.  The partial length trades
+// bias for speed: while the reducers run a tile's epilogue the MMA can only fill
+// the two partial buffers, so short partials leave it idle.  32 sub-steps (96
+// truncating instructions, a quarter of the single-accumulator chain at K = 1024)
+// keep the solvers above 60% of the 3xTF32 rate.
+constexpr int ACC_SUB = 32;  // K = 8 sub-steps per TMEM partial
 
 template <int KT>
 __global__ void __launch_bounds__(320, 1)
@@ -889,9 +893,8 @@ __global__ void __launch_bounds__(320, 1)
         float v[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) v[j] = sum[c * 16 + j];
-        // The generic (diagonal-aware) path for every chunk: the branch-free
-        // variants would add live registers to a kernel already holding sum[128].
-        epilogue16f(p.epi, te, rg, cbase + c * 16, rbase + cbase + c * 16, v, rsum, true);
+        epilogue16f(p.epi, te, rg, cbase + c * 16, rbase + cbase + c * 16, v, rsum,
+                    chunk_on_diag(m0 + q * 32, cbase + c * 16));
       }
       if (p.epi.resid_acc != nullptr) {
 #pragma unroll

@@ -25,7 +25,7 @@ Everything runs in float64 torch on whatever device the inputs live on.
 import torch
 
 GUARD = 25          # addend resolution: 2^(E - GUARD)
-PARTIAL_SUB = 8     # K = 8 slices per partial in the B % 256 == 0 3xTF32 kernel
+PARTIAL_SUB = 32    # K = 8 slices per partial in the B % 256 == 0 3xTF32 kernel
 
 
 def rna_tf32(t):
