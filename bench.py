@@ -150,7 +150,7 @@ class ClockSampler:
 
 
 class Workload:
-    def __init__(self, torch, dr, synth, device, root_prec, ndb=False):
+    def __init__(self, torch, dr, synth, device, root_prec, ndb=False, power="fp16"):
         self.torch = torch
         self.dr = dr
         dev = device
@@ -167,7 +167,11 @@ class Workload:
         self.apply_prec = dr.TF32 if root_prec in (dr.FP16, dr.BF16, dr.TF32) else dr.FP32_3XTF32
         self.ndb = ndb
         cap = 48 << 30
-        self.ws_scale = dr.workspace(dr.OP_SPECTRAL_SCALE, self.nf, BS, 0, NVEC, device=dev)
+        # The pages' power iteration runs in half precision; "3xtf32" keeps it fp32-accurate.
+        self.power_mode = {"3xtf32": dr.SCALE_POWER, "fp16": dr.SCALE_POWER_F16,
+                           "bf16": dr.SCALE_POWER_BF16}[power]
+        wprec = {"3xtf32": dr.FP32_3XTF32, "fp16": dr.FP16, "bf16": dr.BF16}[power]
+        self.ws_scale = dr.workspace(dr.OP_SPECTRAL_SCALE, self.nf, BS, wprec, NVEC, device=dev)
         op = dr.OP_INV_ROOT_NDB if ndb else dr.OP_INV_ROOT_CN
         self.ws_root = dr.workspace(op, self.nf, BS, root_prec, NDB_ITERS if ndb else CN_ITERS,
                                     device=dev, max_bytes=cap)
@@ -177,8 +181,8 @@ class Workload:
     def step(self):
         dr = self.dr
         dr.shampoo_accumulate(self.G, self.F, BETA, self.vr, self.vc)
-        dr.spectral_scale(self.F, dr.SCALE_POWER, self.V0, POWER_ITERS, ridge=RIDGE, out=self.lam,
-                          ws=self.ws_scale)
+        dr.spectral_scale(self.F, self.power_mode, self.V0, POWER_ITERS, ridge=RIDGE,
+                          out=self.lam, ws=self.ws_scale)
         if self.ndb:
             dr.inv_root_ndb(self.F, self.lam, NDB_ITERS, self.root_prec, ridge=RIDGE, X=self.Froot,
                             ws=self.ws_root)
@@ -322,7 +326,7 @@ def cpu_sample(ng_sample, rng_seed=SEED):
     return time.perf_counter() - t0
 
 
-def cpu_baseline(ng_sample=4):
+def cpu_baseline(ng_sample=32):
     secs = cpu_sample(ng_sample)
     blocks = 2 * ng_sample
     return {"value": round(blocks / secs, 4), "unit": "blocks/s", "cores": os.cpu_count(),
@@ -353,7 +357,7 @@ def run_gpu(args):
     dr.load_library()
     peaks = load_peaks()
 
-    wl = Workload(torch, dr, synth, dev, dr.FP16)
+    wl = Workload(torch, dr, synth, dev, dr.FP16, power=args.power)
     for _ in range(args.warmup):
         wl.step()
     torch.cuda.synchronize()
@@ -393,7 +397,7 @@ def run_gpu(args):
     # Same step with NDB in fp32 (3xTF32), a shorter run.
     ndb_ms = None
     if not args.no_ndb:
-        wn = Workload(torch, dr, synth, dev, dr.FP32_3XTF32, ndb=True)
+        wn = Workload(torch, dr, synth, dev, dr.FP32_3XTF32, ndb=True, power=args.power)
         wn.step()
         ndb_ms = timed_steps(torch, wn.step, 2, dist)
         wn.free()
@@ -414,8 +418,8 @@ def run_gpu(args):
         "data": "synthetic",
         "config": {
             "workload": "llama-d2048 x24 layers: 1248 bf16 gradient blocks, (2496,1024,1024) fp32 "
-                        "factor stack; step = accumulate(beta 0.95) + power scale(32 vec x10) + "
-                        "CN fp16 x10 + apply tf32, f=1",
+                        "factor stack; step = accumulate(beta 0.95) + power scale(32 vec x10, "
+                        + args.power + ") + CN fp16 x10 + apply tf32, f=1",
             "blocks": wl.nf, "block": BS, "root": "cn-fp16", "iters": CN_ITERS,
             "l2": "inputs 10.5 GB >> 129 MB L2, no flush",
         },
@@ -577,6 +581,8 @@ def main():
     ap.add_argument("--impl", default="dash", choices=["dash", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--no-ndb", action="store_true", help="skip the NDB fp32 step")
+    ap.add_argument("--power", choices=["fp16", "bf16", "3xtf32"], default="fp16",
+                    help="arithmetic of the power-iteration scaling (the pages: half precision)")
     ap.add_argument("--sweep", action="store_true",
                     help="inverse-root throughput sweep over block sizes and precisions")
     ap.add_argument("--sweep-b", type=int, nargs="*", default=None)

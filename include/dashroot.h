@@ -72,7 +72,12 @@ typedef enum {
 
 typedef enum { DASH_DT_F32 = 0, DASH_DT_BF16 = 1, DASH_DT_F16 = 2 } dash_dtype;
 
-typedef enum { DASH_SCALE_POWER = 0, DASH_SCALE_FROBENIUS = 1 } dash_scale_mode;
+typedef enum {
+  DASH_SCALE_POWER = 0,
+  DASH_SCALE_FROBENIUS = 1,
+  DASH_SCALE_POWER_F16 = 2,
+  DASH_SCALE_POWER_BF16 = 3
+} dash_scale_mode;
 
 typedef enum {
   DASH_OP_ACCUMULATE = 0,
@@ -117,10 +122,21 @@ dash_status shampoo_accumulate(const void* G, int gdt, int64_t Ng, int B, float 
  *     last, normalise each column of W to unit 2-norm and continue with it;
  *     after the last, lambda_out[k] = max_j (v_j . w_j) / (v_j . v_j).
  *     1 <= n_vec <= 32, power_iters >= 1, V0 (N, B, n_vec) fp32.
+ *   mode DASH_SCALE_POWER_F16 / _BF16: the same iteration in half precision
+ *     ([pt] Principais Contribuicoes item 4, "an efficient half-precision
+ *     Power-Iteration"): A_k is rounded once to fp16 / bf16, each product takes
+ *     16-bit A and 16-bit vectors with fp32 accumulation, the ridge term, the
+ *     column normalisation and the Rayleigh quotients are fp32, and the vectors
+ *     are stored in the 16-bit format between products.
  *   mode DASH_SCALE_FROBENIUS: lambda_out[k] = ||A_k + ridge I||_F
  *     (n_vec, power_iters, V0 ignored; may be 0 / NULL).
  *   A (N, B, B) fp32 symmetric blocks; lambda_out (N,) fp32.
- * Arithmetic: fp32 FMA with fp32 column sums (power); fp32 partial sums (Frobenius).
+ * Arithmetic: POWER runs the products on the tensor cores in 3xTF32 (fp32-level
+ *   accuracy) with fp32 column sums; the half modes as stated; FROBENIUS fp32
+ *   partial sums.
+ * Workspace: dash_workspace_size(DASH_OP_SPECTRAL_SCALE, N, B, prec, n_vec) with
+ *   prec DASH_FP16 / DASH_BF16 for the half modes (it then includes the 16-bit
+ *   copy of A, 2 B^2 bytes per block), any other prec for POWER and FROBENIUS.
  */
 dash_status spectral_scale(const float* A, float ridge, int64_t N, int B, int mode,
                            int n_vec, int power_iters, const float* V0,

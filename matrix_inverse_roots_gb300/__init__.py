@@ -34,6 +34,9 @@ DT_F16 = 2
 # dash_scale_mode
 SCALE_POWER = 0
 SCALE_FROBENIUS = 1
+SCALE_POWER_F16 = 2
+SCALE_POWER_BF16 = 3
+_HALF_SCALE = {SCALE_POWER_F16: FP16, SCALE_POWER_BF16: BF16}
 
 # dash_op
 OP_ACCUMULATE = 0
@@ -239,7 +242,7 @@ def spectral_scale(A, mode=SCALE_POWER, V0=None, power_iters=10, ridge=0.0, out=
     _stack(A, "A")
     n, b, _ = A.shape
     nv = 0
-    if mode == SCALE_POWER:
+    if mode != SCALE_FROBENIUS:
         _stack(V0, "V0")
         if V0.shape[0] != n or V0.shape[1] != b:
             raise ValueError("V0 must have shape (N, B, n_vec)")
@@ -247,7 +250,8 @@ def spectral_scale(A, mode=SCALE_POWER, V0=None, power_iters=10, ridge=0.0, out=
     if out is None:
         out = torch.empty(n, dtype=torch.float32, device=A.device)
     if ws is None:
-        ws = workspace(OP_SPECTRAL_SCALE, n, b, FP32_3XTF32, nv, device=A.device)
+        ws = workspace(OP_SPECTRAL_SCALE, n, b, _HALF_SCALE.get(mode, FP32_3XTF32), nv,
+                       device=A.device)
     _check(lib.spectral_scale(_ptr(A), float(ridge), n, b, int(mode), nv, int(power_iters),
                               _ptr(V0), _ptr(out), _ptr(ws), ws.numel(), _stream()),
            "spectral_scale")
@@ -268,7 +272,7 @@ def spectral_scale_noalloc(A, mode=SCALE_POWER, V0=None, power_iters=10, ridge=0
     _stack(A, "A")
     n, b, _ = A.shape
     nv = 0
-    if mode == SCALE_POWER:
+    if mode != SCALE_FROBENIUS:
         _stack(V0, "V0")
         if V0.shape[0] != n or V0.shape[1] != b:
             raise ValueError("V0 must have shape (N, B, n_vec)")

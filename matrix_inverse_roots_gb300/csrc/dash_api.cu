@@ -264,7 +264,11 @@ dash_status dash_workspace_size(int op, int64_t N, int B, int prec, int param, s
       s = (prec == DASH_FP32_3XTF32) ? bufs_bytes(DASH_FP32_3XTF32, B, N, 1) : 0;
       break;
     case DASH_OP_SPECTRAL_SCALE:
-      s = 2 * round256(static_cast<size_t>(N) * B * 32 * 4) + 3 * round256(N * 32 * 4) + 256;
+      if (prec == DASH_FP16 || prec == DASH_BF16)  // the half-precision power modes
+        s = round256(static_cast<size_t>(N) * B * B * 2) +
+            2 * round256(static_cast<size_t>(N) * B * 32 * 2) + 3 * round256(N * 32 * 4) + 256;
+      else
+        s = 2 * round256(static_cast<size_t>(N) * B * 32 * 4) + 3 * round256(N * 32 * 4) + 256;
       break;
     case DASH_OP_INV_ROOT_CN:
       s = root_small_bytes(N, N * (param > 0 ? param : 1)) + bufs_bytes(prec, B, N, CN_BUFS);
@@ -366,8 +370,11 @@ dash_status spectral_scale(const float* A, float ridge, int64_t N, int B, int mo
                            int power_iters, const float* V0, float* lambda_out, void* ws,
                            size_t ws_bytes, void* stream) {
   if (N < 0 || !valid_dim(B)) return DASH_ERR_INVALID_ARG;
-  if (mode != DASH_SCALE_POWER && mode != DASH_SCALE_FROBENIUS) return DASH_ERR_INVALID_ARG;
-  if (mode == DASH_SCALE_POWER && (n_vec < 1 || n_vec > 32 || power_iters < 1 || !V0))
+  const bool half = (mode == DASH_SCALE_POWER_F16 || mode == DASH_SCALE_POWER_BF16);
+  if (mode != DASH_SCALE_POWER && mode != DASH_SCALE_FROBENIUS && !half)
+    return DASH_ERR_INVALID_ARG;
+  if ((mode == DASH_SCALE_POWER || half) &&
+      (n_vec < 1 || n_vec > 32 || power_iters < 1 || !V0))
     return DASH_ERR_INVALID_ARG;
   if (N == 0) return DASH_OK;
   if (!A || !lambda_out || !aligned16(A)) return DASH_ERR_INVALID_ARG;
@@ -380,6 +387,60 @@ dash_status spectral_scale(const float* A, float ridge, int64_t N, int B, int mo
     if (cudaMemsetAsync(acc, 0, static_cast<size_t>(N) * 4, st) != cudaSuccess) return DASH_ERR_CUDA;
     DASH_TRY(launch_frob_acc(A, ridge, B, N, acc, st));
     return launch_sqrt_scale(acc, lambda_out, N, 1.0f, st);
+  }
+  if (half) {
+    // Half precision: a 16-bit copy of each block, vectors transposed (32, B).
+    const int bf = (mode == DASH_SCALE_POWER_BF16) ? 1 : 0;
+    const size_t per_blk = static_cast<size_t>(B) * B * 2 + 2 * static_cast<size_t>(B) * 32 * 2 +
+                           3 * 32 * 4;
+    long long chunk = static_cast<long long>(ws_bytes / per_blk);
+    if (chunk > N) chunk = N;
+    if (chunk > 65535) chunk = 65535;
+    while (chunk > 0) {
+      const size_t need = round256(static_cast<size_t>(chunk) * B * B * 2) +
+                          2 * round256(static_cast<size_t>(chunk) * B * 32 * 2) +
+                          3 * round256(static_cast<size_t>(chunk) * 32 * 4);
+      if (need <= ws_bytes) break;
+      --chunk;
+    }
+    if (chunk < 1) return DASH_ERR_WORKSPACE_TOO_SMALL;
+    Carver cv(ws, ws_bytes);
+    void* Ah = cv.take(static_cast<size_t>(chunk) * B * B * 2);
+    uint16_t* Vt[2];
+    Vt[0] = static_cast<uint16_t*>(cv.take(static_cast<size_t>(chunk) * B * 32 * 2));
+    Vt[1] = static_cast<uint16_t*>(cv.take(static_cast<size_t>(chunk) * B * 32 * 2));
+    float* nrm[2];
+    nrm[0] = static_cast<float*>(cv.take(static_cast<size_t>(chunk) * 32 * 4));
+    nrm[1] = static_cast<float*>(cv.take(static_cast<size_t>(chunk) * 32 * 4));
+    float* den = static_cast<float*>(cv.take(static_cast<size_t>(chunk) * 32 * 4));
+    if (!cv.ok) return DASH_ERR_WORKSPACE_TOO_SMALL;
+    const size_t acc_bytes = static_cast<size_t>(chunk) * 32 * 4;
+    for (long long c0 = 0; c0 < N; c0 += chunk) {
+      const long long nc = (N - c0 < chunk) ? N - c0 : chunk;
+      AffParams a = aff_from(offset_blocks(A, c0, B, 4), nullptr, FMT_F32, B, nc);
+      a.nout = 1;
+      Buf hb;
+      hb.hi = Ah;
+      a.out[0] = aout(hb, bf ? FMT_BF16 : FMT_F16, 1.0f, 0.0f);
+      DASH_TRY(launch_affine(a, st));
+      DASH_TRY(launch_pad_vectors_t(V0 + static_cast<size_t>(c0) * B * n_vec, n_vec, B, nc, bf,
+                                    Vt[1], st));
+      const uint16_t* vin = Vt[1];
+      const float* in_n = nullptr;
+      int cur = 0;
+      for (int it = 0; it < power_iters; ++it) {
+        const int last = (it == power_iters - 1);
+        if (cudaMemsetAsync(nrm[cur], 0, acc_bytes, st) != cudaSuccess) return DASH_ERR_CUDA;
+        if (last && cudaMemsetAsync(den, 0, acc_bytes, st) != cudaSuccess) return DASH_ERR_CUDA;
+        DASH_TRY(launch_power_step_half(Ah, bf, ridge, B, nc, vin, n_vec, in_n, Vt[cur],
+                                        nrm[cur], den, last, st));
+        vin = Vt[cur];
+        in_n = nrm[cur];
+        cur ^= 1;
+      }
+      DASH_TRY(launch_power_finish(nrm[cur ^ 1], den, n_vec, nc, lambda_out + c0, st));
+    }
+    return DASH_OK;
   }
   // Power iteration, chunked so each chunk's vectors fit in the workspace.
   const size_t per_blk = 2 * static_cast<size_t>(B) * 32 * 4 + 3 * 32 * 4;
@@ -409,7 +470,6 @@ dash_status spectral_scale(const float* A, float ridge, int64_t N, int B, int mo
     // Start vectors into the 32-column layout the product kernel streams.
     DASH_TRY(launch_pad_vectors(V0 + static_cast<size_t>(c0) * B * n_vec, n_vec, B, nc, V[1], st));
     const float* vin = V[1];
-    int vstride = 32;
     const float* in_n = nullptr;
     int cur = 0;
     for (int it = 0; it < power_iters; ++it) {
@@ -419,7 +479,6 @@ dash_status spectral_scale(const float* A, float ridge, int64_t N, int B, int mo
       DASH_TRY(launch_power_step_tc(Ac, ridge, B, nc, vin, n_vec, in_n, V[cur], nrm[cur], den,
                                     last, st));
       vin = V[cur];
-      vstride = 32;
       in_n = nrm[cur];
       cur ^= 1;
     }

@@ -90,6 +90,17 @@ dash_status launch_frob_acc(const float* A, float ridge, int dim, long long nblo
 // Vin[blk][row][c] / sqrt(in_nrm2[blk][c]) (in_nrm2 null = unscaled), row stride 32.
 // Not last: writes W and acc0[blk][c] += sum_r W^2.
 // Last: acc0[blk][c] += sum_r v w, acc1[blk][c] += sum_r v v (W not written).
+// One half-precision power product on (nblocks, dim, dim) 16-bit A (bf16 != 0:
+// bfloat16, else fp16); vectors transposed, (nblocks, 32, dim) 16-bit.
+dash_status launch_power_step_half(const void* Ah, int bf16, float ridge, int dim,
+                                   long long nblocks, const uint16_t* Vt_in, int nv,
+                                   const float* in_nrm2, uint16_t* Vt_out, float* acc0,
+                                   float* acc1, int last, cudaStream_t st);
+
+// V0 (nblocks, dim, nv) fp32 -> Vt (nblocks, 32, dim) 16-bit, rows c >= nv zero.
+dash_status launch_pad_vectors_t(const float* V0, int nv, int dim, long long nblocks, int bf16,
+                                 uint16_t* Vt, cudaStream_t st);
+
 dash_status launch_power_step_tc(const float* A, float ridge, int dim, long long nblocks,
                                  const float* Vin, int nv, const float* in_nrm2, float* Wout,
                                  float* acc0, float* acc1, int last, cudaStream_t st);

@@ -206,6 +206,31 @@ dash_status launch_pad_vectors(const float* V0, int nv, int dim, long long nbloc
   return err == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
 }
 
+__global__ void pad_vectors_t_kernel(const float* V0, int nv, int dim, long long nblocks, int bf16,
+                                     uint16_t* Vt) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= nblocks * PW_NV * dim) return;
+  const int r = static_cast<int>(i % dim);
+  const long long bc = i / dim;
+  const int c = static_cast<int>(bc % PW_NV);
+  const long long b = bc / PW_NV;
+  const float x = (c < nv) ? V0[(b * dim + r) * nv + c] : 0.0f;
+  Vt[i] = bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(x)) : __half_as_ushort(__float2half_rn(x));
+}
+
+dash_status launch_pad_vectors_t(const float* V0, int nv, int dim, long long nblocks, int bf16,
+                                 uint16_t* Vt, cudaStream_t st) {
+  if (nblocks <= 0) return DASH_OK;
+  const long long n = nblocks * PW_NV * dim;
+  const int rec = trace_begin(st);
+  pad_vectors_t_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(V0, nv, dim,
+                                                                               nblocks, bf16, Vt);
+  const cudaError_t err = cudaGetLastError();
+  trace_end(rec, st, DASH_TRACE_ELEMENTWISE, 0.0,
+            static_cast<double>(dim) * nblocks * (4.0 * nv + 2.0 * PW_NV));
+  return err == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
+}
+
 __global__ void power_finish_kernel(const float* num, const float* den, int nv, long long nblocks,
                                     float* lambda) {
   const long long k = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;

@@ -48,8 +48,10 @@ extern "C" dash_status spectral_scale_noalloc(const float* A, float ridge, int64
                                               const float* V0, float* lambda_out,
                                               void* stream) {
   size_t need = 0;
-  const dash_status s = dash_workspace_size(DASH_OP_SPECTRAL_SCALE, N, B, DASH_FP32_3XTF32,
-                                            n_vec, &need);
+  const int prec = (mode == DASH_SCALE_POWER_F16)    ? DASH_FP16
+                   : (mode == DASH_SCALE_POWER_BF16) ? DASH_BF16
+                                                     : DASH_FP32_3XTF32;
+  const dash_status s = dash_workspace_size(DASH_OP_SPECTRAL_SCALE, N, B, prec, n_vec, &need);
   if (s != DASH_OK) return s;
   if (mode == DASH_SCALE_FROBENIUS) need = (static_cast<size_t>(N) * 4 + 255) & ~size_t(255);
   // One pass over all N blocks must fit; larger stacks are refused, not chunked.

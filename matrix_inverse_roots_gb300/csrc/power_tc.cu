@@ -392,6 +392,256 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------- half precision
+// The power product in half precision ([pt] Principais Contribuicoes item 4: an
+// efficient half-precision power iteration).  A is a 16-bit copy of the block
+// (fp16 or bf16) and the 32 vectors are kept transposed, (32, B) per block, so
+// both operands are K-major 128-byte rows: TMA brings them straight into the
+// layout kind::f16 reads (no split, no converters), half the bytes of fp32.
+//   warp 0      TMA producer: per k-block (64 elements) a 128 x 64 tile of A and
+//               the 32 x 64 tile of V^T, ten 20 KB stages.
+//   warp 1      one thread issues four M = 128, N = 32, K = 16 MMAs per k-block
+//               into one of two 32-column TMEM accumulators (fp32).
+//   warps 2..5  epilogue: one accumulator row per thread; scale by the previous
+//               column norms, ridge term, W^T stored in the 16-bit format
+//               (coalesced across the warp), fp32 column sums of the stored values.
+constexpr int PH_BK = 64;                             // 16-bit elements per 128-byte row
+constexpr int PH_A_BYTES = PT_BM * 128;               // 16 KB
+constexpr int PH_V_BYTES = PT_NV * 128;               // 4 KB
+constexpr int PH_STAGE_BYTES = PH_A_BYTES + PH_V_BYTES;
+constexpr int PH_STAGES = 10;
+constexpr int PH_NBAR = 2 * PH_STAGES + 5;            // full, empty; tfull x2, tempty x2; fin
+constexpr int PH_THREADS = 192;
+constexpr int PH_TMEM_COLS = 64;
+constexpr int PH_SMEM_BYTES = PH_STAGES * PH_STAGE_BYTES + 1024 + PT_BAR_AREA;
+static_assert(PH_NBAR * 8 + 16 <= PT_BAR_AREA, "barrier area");
+static_assert(PH_SMEM_BYTES <= 232448, "shared memory budget");
+
+struct PowerHalfParams {
+  int dim;
+  long long slabs;
+  int nkb;
+  uint32_t idesc;
+  float ridge;
+  const uint16_t* Vt_in;  // (nblocks, 32, dim): previous vectors, transposed
+  const float* in_nrm2;   // (nblocks, 32) or null
+  uint16_t* Vt_out;       // (nblocks, 32, dim); unused on the last product
+  float* acc0;            // W.W per column, or v.w on the last product
+  float* acc1;            // v.v per column on the last product
+  int nv;
+  int last;
+};
+
+template <bool BF>
+__device__ __forceinline__ float h16_to_f(uint16_t x) {
+  if (BF) return __uint_as_float(static_cast<uint32_t>(x) << 16);
+  return __half2float(__ushort_as_half(x));
+}
+
+template <bool BF>
+__device__ __forceinline__ uint16_t f_to_h16(float x) {
+  if (BF) return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+  return __half_as_ushort(__float2half_rn(x));
+}
+
+template <bool BF>
+__global__ void __launch_bounds__(PH_THREADS, 1)
+    power_half_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tV,
+                      const __grid_constant__ PowerHalfParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw_base & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sbase = raw_base + pad;
+  uint8_t* bar_area = smem + PH_STAGES * PH_STAGE_BYTES;
+  const uint32_t bar0 = sbase + PH_STAGES * PH_STAGE_BYTES;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (PH_STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * PH_STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * PH_STAGES + 2 + a); };
+  const uint32_t fin_bar = bar0 + 8u * (2 * PH_STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * PH_NBAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * PH_NBAR + 8);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int slabs_per_blk = p.dim / PT_BM;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < PH_STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 4);
+    }
+    mbar_init(fin_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tA);
+    tma_prefetch_desc(&tV);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), PH_TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_par = 0;
+      bool ok = true;
+      for (long long sl = blockIdx.x; sl < p.slabs && ok; sl += gridDim.x) {
+        const int blk = static_cast<int>(sl / slabs_per_blk);
+        const int m0 = static_cast<int>(sl % slabs_per_blk) * PT_BM;
+        for (int kb = 0; kb < p.nkb; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full_bar(stage);
+          mbar_arrive_expect_tx(fb, PH_STAGE_BYTES);
+          armed |= 1u << stage;
+          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          const uint32_t s0 = sbase + stage * PH_STAGE_BYTES;
+          tma_load_3d(s0, &tA, fb, kb * PH_BK, m0, blk);
+          tma_load_3d(s0 + PH_A_BYTES, &tV, fb, kb * PH_BK, 0, blk);
+          if (++stage == PH_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < PH_STAGES; ++s)
+          if (armed & (1u << s)) drain_wait(full_bar(s), (armed_par >> s) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (long long sl = blockIdx.x; sl < p.slabs && ok; sl += gridDim.x) {
+        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * PT_NV);
+        for (int kb = 0; kb < p.nkb; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sA = sbase + stage * PH_STAGE_BYTES;
+          const uint32_t sV = sA + PH_A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < PH_BK / 16; ++kk) {
+            const uint64_t da = smem_desc_sw128(sA + kk * 32, 16, 1024);
+            const uint64_t dv = smem_desc_sw128(sV + kk * 32, 16, 1024);
+            mma_f16(d_tmem, da, dv, p.idesc, (kb | kk) ? 1u : 0u);
+          }
+          mma_commit(empty_bar(stage));
+          if (++stage == PH_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(tfull_bar(acc));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      mma_commit(fin_bar);
+      drain_wait(fin_bar, 0);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int q = warp & 3;
+    const int row_in = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (long long sl = blockIdx.x; sl < p.slabs; sl += gridDim.x) {
+      if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag)) break;
+      tc_fence_after();
+      const long long blk = sl / slabs_per_blk;
+      const int row = static_cast<int>(sl % slabs_per_blk) * PT_BM + row_in;
+      uint32_t r0[16], r1[16];
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * PT_NV);
+      tmem_ld16(taddr, r0);
+      tmem_ld16(taddr + 16, r1);
+      tmem_wait_ld(r0);
+      tmem_fence_regs(r1);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(acc));  // accumulator copied to registers
+      float sc[PT_NV];
+#pragma unroll
+      for (int c = 0; c < PT_NV; ++c) {
+        float s = 0.0f;
+        if (c < p.nv)
+          s = (p.in_nrm2 != nullptr) ? 1.0f / sqrtf(p.in_nrm2[blk * PT_NV + c]) : 1.0f;
+        sc[c] = s;
+      }
+      // Element (c, row) of this block's V^T; consecutive lanes read consecutive rows.
+      const uint16_t* vin = p.Vt_in + blk * PT_NV * static_cast<long long>(p.dim) + row;
+      float w[PT_NV], v[PT_NV];
+#pragma unroll
+      for (int c = 0; c < PT_NV; ++c) v[c] = h16_to_f<BF>(vin[static_cast<long long>(c) * p.dim]) * sc[c];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        w[c] = fmaf(p.ridge, v[c], __uint_as_float(r0[c]) * sc[c]);
+        w[16 + c] = fmaf(p.ridge, v[16 + c], __uint_as_float(r1[c]) * sc[16 + c]);
+      }
+      float s0[PT_NV], s1[PT_NV];
+      if (p.last) {
+#pragma unroll
+        for (int c = 0; c < PT_NV; ++c) {
+          s0[c] = v[c] * w[c];
+          s1[c] = v[c] * v[c];
+        }
+      } else {
+        uint16_t* wout = p.Vt_out + blk * PT_NV * static_cast<long long>(p.dim) + row;
+#pragma unroll
+        for (int c = 0; c < PT_NV; ++c) {
+          const uint16_t hw = f_to_h16<BF>(w[c]);
+          wout[static_cast<long long>(c) * p.dim] = hw;
+          const float wr = h16_to_f<BF>(hw);  // the next product sees the stored value
+          s0[c] = wr * wr;
+        }
+      }
+      const float t0 = butterfly_colsum(s0, lane);
+      if (lane < p.nv) atomicAdd(p.acc0 + blk * PT_NV + lane, t0);
+      if (p.last) {
+        const float t1 = butterfly_colsum(s1, lane);
+        if (lane < p.nv) atomicAdd(p.acc1 + blk * PT_NV + lane, t1);
+      }
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, PH_TMEM_COLS);
+  }
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -423,7 +673,57 @@ bool map_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, ui
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool map_3d_h16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t nblk,
+                uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t gdim[3] = {inner, outer, nblk};
+  cuuint64_t gstride[2] = {inner * 2, inner * outer * 2};
+  cuuint32_t box[3] = {box_inner, box_outer, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(base), gdim, gstride, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
+
+dash_status launch_power_step_half(const void* Ah, int bf16, float ridge, int dim,
+                                   long long nblocks, const uint16_t* Vt_in, int nv,
+                                   const float* in_nrm2, uint16_t* Vt_out, float* acc0,
+                                   float* acc1, int last, cudaStream_t st) {
+  if (nblocks <= 0) return DASH_OK;
+  CUtensorMap tA, tV;
+  if (!map_3d_h16(&tA, Ah, dim, dim, nblocks, PH_BK, PT_BM)) return DASH_ERR_CUDA;
+  if (!map_3d_h16(&tV, Vt_in, dim, PT_NV, nblocks, PH_BK, PT_NV)) return DASH_ERR_CUDA;
+  PowerHalfParams p;
+  p.dim = dim;
+  p.slabs = nblocks * (dim / PT_BM);
+  p.nkb = dim / PH_BK;
+  p.idesc = make_idesc(bf16 ? 1u : 0u, 0, 0, PT_BM, PT_NV);
+  p.ridge = ridge;
+  p.Vt_in = Vt_in;
+  p.in_nrm2 = in_nrm2;
+  p.Vt_out = Vt_out;
+  p.acc0 = acc0;
+  p.acc1 = acc1;
+  p.nv = nv;
+  p.last = last;
+  auto kern = bf16 ? power_half_kernel<true> : power_half_kernel<false>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PH_SMEM_BYTES) !=
+      cudaSuccess)
+    return DASH_ERR_CUDA;
+  const int sms = device_sm_count();
+  if (sms <= 0) return DASH_ERR_CUDA;
+  const long long grid = p.slabs < sms ? p.slabs : sms;
+  const int rec = trace_begin(st);
+  kern<<<static_cast<unsigned>(grid), PH_THREADS, PH_SMEM_BYTES, st>>>(tA, tV, p);
+  const cudaError_t err = cudaGetLastError();
+  const double bb = static_cast<double>(dim) * dim * nblocks;
+  const double vb = static_cast<double>(dim) * nblocks * 2.0 * PT_NV;
+  trace_end(rec, st, DASH_TRACE_POWER, 2.0 * bb * nv, 2.0 * bb + vb * (last ? 1 : 2));
+  return err == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
+}
 
 dash_status launch_power_step_tc(const float* A, float ridge, int dim, long long nblocks,
                                  const float* Vin, int nv, const float* in_nrm2, float* Wout,

@@ -63,6 +63,10 @@ def test_workspace_sizes():
     assert dr.workspace_size(dr.OP_INV_ROOT_CHEB, 10, b, dr.BF16, 16) >= 4 * 10 * mat * 2
     assert dr.workspace_size(dr.OP_ACCUMULATE, 10, b, dr.BF16, 0) == 0
     assert dr.workspace_size(dr.OP_SPECTRAL_SCALE, 10, b, 0, 32) >= 2 * 10 * b * 32 * 4
+    # Half-precision power modes also hold a 16-bit copy of A.
+    for prec in (dr.FP16, dr.BF16):
+        assert dr.workspace_size(dr.OP_SPECTRAL_SCALE, 10, b, prec, 32) >= (
+            10 * mat * 2 + 2 * 10 * b * 32 * 2)
 
 
 def test_bad_arguments_rejected_on_host():
@@ -86,6 +90,14 @@ def test_bad_arguments_rejected_on_host():
     # Null workspace where one is required.
     assert lib.spectral_scale(ctypes.c_void_p(256), 0.0, 2, 128, 0, 32, 10,
                               ctypes.c_void_p(512), ctypes.c_void_p(1024), null, 0, null) == 1
+    # Unknown scale mode; a half-precision power mode without start vectors.
+    assert lib.spectral_scale(ctypes.c_void_p(256), 0.0, 2, 128, 4, 32, 10,
+                              ctypes.c_void_p(512), ctypes.c_void_p(1024),
+                              ctypes.c_void_p(2048), 1 << 20, null) == 1
+    for mode in (dr.SCALE_POWER_F16, dr.SCALE_POWER_BF16):
+        assert lib.spectral_scale(ctypes.c_void_p(256), 0.0, 2, 128, mode, 32, 10, null,
+                                  ctypes.c_void_p(1024), ctypes.c_void_p(2048), 1 << 20,
+                                  null) == 1
     # beta outside [0, 1].
     assert lib.shampoo_accumulate(ctypes.c_void_p(256), 1, 2, 128, ctypes.c_float(1.5),
                                   ctypes.c_void_p(512), null, null, null, 0, null) == 1
@@ -102,3 +114,6 @@ def test_workspace_too_small_reported():
     assert lib.inv_root_cn(p, 0.0, p, 4, 1024, 10, 0, p, None, p, 4096, None) == 4
     assert lib.inv_root_ndb(p, 0.0, p, 4, 1024, 10, 2, p, None, p, 4096, None) == 4
     assert lib.precondition_apply(p, 1, p, 4, 1024, 0, p, p, 4096, None) == 4
+    # Half-precision power: one block's 16-bit copy (2 MiB at B = 1024) does not fit.
+    assert lib.spectral_scale(p, 0.0, 4, 1024, dr.SCALE_POWER_F16, 32, 10, p, p, p, 4096,
+                              None) == 4

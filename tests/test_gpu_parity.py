@@ -5,7 +5,9 @@ root solvers, the GPU's own fp32 scale), so every step is checked on its own.
 Gates (relative Frobenius error of the result, per block):
   3xTF32 1e-4, TF32 2e-3, FP16/BF16 Coupled Newton and Chebyshev 1e-2;
   NDB in half precision is reported, not gated (the pages call it unstable).
-Power-iteration lambda: relative error 1e-5.  Accumulate / apply: 1e-5 / 1e-4.
+Power-iteration lambda: relative error 1e-5 (3xTF32 products); the half-precision
+modes are checked against the oracle run on the same 16-bit A (see
+test_power_lambda_half).  Accumulate / apply: 1e-5 / 1e-4.
 """
 
 import numpy as np
@@ -38,6 +40,41 @@ def test_power_lambda(b):
         torch.cuda.synchronize()
         ref = oracle.power_lambda(to64(A), to64(V0[:, :, :nv]), iters, ridge=1e-3)
         assert np.max(np.abs(to64(lam) - ref) / ref) < 1e-5, (iters, nv)
+    assert dr.device_status() == 0
+
+
+HALF_MODES = [("fp16", torch.float16, 2.0 ** -11), ("bf16", torch.bfloat16, 2.0 ** -8)]
+
+
+@pytest.mark.parametrize("name,dt,u", HALF_MODES)
+@pytest.mark.parametrize("b,n", [(128, 8), (1024, 4)])
+def test_power_lambda_half(name, dt, u, b, n):
+    """Half-precision power iteration ([pt] Principais Contribuicoes item 4).
+
+    Against the oracle on the 16-bit A the GPU read, the differences are the
+    16-bit rounding of the vectors between products (relative u) and fp32 sums.
+    A perturbation dv of the final vector changes its Rayleigh quotient by at most
+    2 |dv| |(A - rho I) v| / |v|^2 <= 2u ||A||_2, so the gate is 4u.  The ridge,
+    0.2 here (about 7% of lambda), is large enough that dropping it fails that
+    gate in both formats.  Against the oracle on the fp32 A, the 16-bit rounding E
+    of A (|E_ij| <= u |A_ij|) moves every eigenvalue by at most
+    ||E||_2 <= u ||A||_F (Weyl), which bounds that difference."""
+    require_gpu()
+    dr = library()
+    mode = dr.SCALE_POWER_F16 if name == "fp16" else dr.SCALE_POWER_BF16
+    A, V0 = wishart_case(n, b, 1900 + b)
+    for iters, nv in ((10, 32), (3, 7)):
+        V = V0[:, :, :nv].contiguous()
+        lam = to64(dr.spectral_scale(A, mode, V, iters, ridge=0.2))
+        Ah = to64(A.to(dt))
+        ref_h = oracle.power_lambda(Ah, to64(V), iters, ridge=0.2)
+        err_h = np.abs(lam - ref_h) / ref_h
+        print("%s B=%d iters=%d nv=%d: vs oracle on the 16-bit A %.2e" % (
+            name, b, iters, nv, err_h.max()))
+        assert err_h.max() < 4 * u, (iters, nv, err_h)
+        ref = oracle.power_lambda(to64(A), to64(V), iters, ridge=0.2)
+        bound = u * np.linalg.norm(to64(A).reshape(n, -1), axis=1) / ref
+        assert np.all(np.abs(lam - ref) / ref <= bound + 4 * u)
     assert dr.device_status() == 0
 
 
