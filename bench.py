@@ -52,8 +52,8 @@ TF32_RATIO = 1.1 / 2.25
 # profiles/gemm_tc_f16_pair_cn_b1024_n64.md (64 blocks of 1024^2; traffic grows in
 # proportion to the blocks a launch processes).  Valid only for the kernel sources
 # it was taken on, identified by GEMM_TRAFFIC_SRC.
-GEMM_TRAFFIC_PER_BLOCK = 5.144e6
-GEMM_TRAFFIC_SRC = "b7d2761d0aa3d4f8"
+GEMM_TRAFFIC_PER_BLOCK = 5.152e6
+GEMM_TRAFFIC_SRC = "ad73f9a8d686a200"
 GEMM_SOURCES = ("matrix_inverse_roots_gb300/csrc/gemm_tc.cu",
                 "matrix_inverse_roots_gb300/csrc/dash_common.cuh")
 
@@ -516,8 +516,9 @@ def run_case(args):
     dr.load_library()
     n, b = args.case_n, args.case_b
     A = synth.wishart(n, b, seed=5, device="cuda")
-    if args.case_scale == "power":
-        s = dr.spectral_scale(A, dr.SCALE_POWER, synth.start_vectors(n, b, 32, seed=6, device="cuda"),
+    if args.case_scale in ("power", "power-fp16"):
+        mode = dr.SCALE_POWER if args.case_scale == "power" else dr.SCALE_POWER_F16
+        s = dr.spectral_scale(A, mode, synth.start_vectors(n, b, 32, seed=6, device="cuda"),
                               POWER_ITERS)
     else:
         s = dr.spectral_scale(A, dr.SCALE_FROBENIUS)
@@ -592,7 +593,7 @@ def main():
     ap.add_argument("--case-b", type=int, default=1024)
     ap.add_argument("--case-prec", default="fp16")
     ap.add_argument("--case-iters", type=int, default=3)
-    ap.add_argument("--case-scale", choices=["power", "frobenius"], default="power")
+    ap.add_argument("--case-scale", choices=["power", "power-fp16", "frobenius"], default="power")
     args = ap.parse_args()
     if args.case:
         run_case(args)
