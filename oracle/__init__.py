@@ -31,7 +31,8 @@ different algorithm, or brute force on tiny inputs.  No function here is
 "parity unpinned".
 """
 
-from .shampoo64 import accumulate, apply_preconditioner, frobenius_norm, power_lambda
+from .shampoo64 import (accumulate, apply_preconditioner, frobenius_norm, pack_blocks,
+                        power_lambda, unpack_blocks, update_weights)
 from .roots64 import (
     evd_inv_root,
     cn_inv_root,
@@ -50,4 +51,7 @@ __all__ = [
     "ndb_inv_root",
     "cheb_coeffs",
     "cheb_inv_root",
+    "pack_blocks",
+    "unpack_blocks",
+    "update_weights",
 ]

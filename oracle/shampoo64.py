@@ -30,6 +30,14 @@ Readings of the pages taken here (the pages give no formulas):
 
 * Preconditioned update.  U = L^{-1/4} G R^{-1/4}, the standard Shampoo
   update that the -1/4 roots of L and R exist for ([tg], second paragraph).
+
+* Blocks of a weight.  A weight-shaped gradient (rows x cols) is cut into B x B
+  blocks G_ij ([pt] Metodologia 1, "Empilhamento de Tensores 3D"), enumerated
+  row-block-major (i outer, j inner); the last block row / column of a dimension
+  that is not a multiple of B is zero-padded and its valid extent recorded.
+
+* Weight step.  The pages give no optimizer update rule; the plain reading is the
+  step along the preconditioned direction, W <- W - lr U, block by block.
 """
 
 import numpy as np
@@ -123,3 +131,48 @@ def apply_preconditioner(G, Froot):
     for j in range(ng):
         out[j] = Froot[j] @ G[j] @ Froot[ng + j]
     return out
+
+
+def pack_blocks(M, b):
+    """Cut a (rows, cols) matrix into row-block-major (b, b) blocks, zero-padded.
+
+    Returns (blocks (nbr * nbc, b, b), valid_rows (nbr * nbc,), valid_cols
+    (nbr * nbc,)) with nbr = ceil(rows / b), nbc = ceil(cols / b); block i * nbc + j
+    holds rows i*b.. and columns j*b.. of M ([pt] Metodologia 1).
+    """
+    M = _as64(M)
+    rows, cols = M.shape
+    nbr = -(-rows // b)
+    nbc = -(-cols // b)
+    blocks = np.zeros((nbr * nbc, b, b))
+    vr = np.zeros(nbr * nbc, dtype=np.int64)
+    vc = np.zeros(nbr * nbc, dtype=np.int64)
+    for i in range(nbr):
+        for j in range(nbc):
+            k = i * nbc + j
+            r = min(b, rows - i * b)
+            c = min(b, cols - j * b)
+            blocks[k, :r, :c] = M[i * b:i * b + r, j * b:j * b + c]
+            vr[k] = r
+            vc[k] = c
+    return blocks, vr, vc
+
+
+def unpack_blocks(blocks, rows, cols):
+    """Inverse of pack_blocks: the (rows, cols) matrix, padding dropped."""
+    blocks = _as64(blocks)
+    b = blocks.shape[1]
+    nbc = -(-cols // b)
+    M = np.empty((rows, cols))
+    for k in range(blocks.shape[0]):
+        i, j = divmod(k, nbc)
+        r = min(b, rows - i * b)
+        c = min(b, cols - j * b)
+        M[i * b:i * b + r, j * b:j * b + c] = blocks[k, :r, :c]
+    return M
+
+
+def update_weights(W, G, Froot, lr):
+    """W_j - lr U_j for every block, U from apply_preconditioner (the weight-step
+    reading in the module docstring)."""
+    return _as64(W) - lr * apply_preconditioner(G, Froot)

@@ -375,3 +375,38 @@ def test_planted_mistakes_are_caught():
     Fr = rng.standard_normal((2, 3, 3))
     U = oracle.apply_preconditioner(G, Fr)
     assert np.max(np.abs(U[0] - Fr[0] @ G[0].T @ Fr[1])) > 1e-3
+
+
+def test_pack_blocks_against_numpy_block():
+    """Cutting a weight into B x B blocks ([pt] Metodologia 1), pinned by numpy's own
+    block assembly and hand-counted extents on a ragged 5 x 7 matrix with B = 4."""
+    rng = np.random.default_rng(11)
+    M = rng.standard_normal((5, 7))
+    blocks, vr, vc = oracle.pack_blocks(M, 4)
+    assert blocks.shape == (4, 4, 4)
+    assert list(vr) == [4, 4, 1, 1] and list(vc) == [4, 3, 4, 3]  # row-block-major
+    padded = np.zeros((8, 8))
+    padded[:5, :7] = M
+    assert np.array_equal(np.block([[blocks[0], blocks[1]], [blocks[2], blocks[3]]]), padded)
+    assert np.array_equal(oracle.unpack_blocks(blocks, 5, 7), M)
+    one, vr1, vc1 = oracle.pack_blocks(M[:4, :4], 4)
+    assert one.shape == (1, 4, 4) and np.array_equal(one[0], M[:4, :4])
+    assert list(vr1) == [4] and list(vc1) == [4]
+    # A column-major enumeration (a plausible slip) puts block (1, 0) second.
+    assert not np.array_equal(np.block([[blocks[0], blocks[2]], [blocks[1], blocks[3]]]), padded)
+
+
+def test_update_weights_closed_forms():
+    """W - lr L^{-1/4} G R^{-1/4}: identity roots give W - lr G, diagonal roots scale
+    rows and columns, lr = 0 leaves W."""
+    rng = np.random.default_rng(12)
+    W = rng.standard_normal((2, 3, 3))
+    G = rng.standard_normal((2, 3, 3))
+    eye = np.broadcast_to(np.eye(3), (4, 3, 3))
+    assert np.allclose(oracle.update_weights(W, G, eye, 0.1), W - 0.1 * G, rtol=0, atol=1e-15)
+    assert np.array_equal(oracle.update_weights(W, G, eye, 0.0), W)
+    dl = rng.uniform(0.5, 2.0, (2, 3))
+    dr = rng.uniform(0.5, 2.0, (2, 3))
+    Fr = np.concatenate([np.stack([np.diag(x) for x in dl]), np.stack([np.diag(x) for x in dr])])
+    want = W - 0.25 * (dl[:, :, None] * G * dr[:, None, :])
+    assert np.allclose(oracle.update_weights(W, G, Fr, 0.25), want, rtol=0, atol=1e-14)
