@@ -269,6 +269,49 @@ def e2e_steps(torch, wl, G_host, U_host, steps, dist=None):
     return t0.elapsed_time(t1) / steps
 
 
+def full_optimizer_step(torch, dr, synth, wl, dev, steps, dist, peaks, lr=1e-3):
+    """Times pack + accumulate + scale + CN + fused weight step on the bench workload."""
+    shapes = synth.llama_weight_shapes(LAYERS)
+    g = torch.Generator(device=dev).manual_seed(SEED + 7)
+    Gw = [(0.1 * torch.randn((r, c), generator=g, device=dev)).to(torch.bfloat16)
+          for r, c in shapes]
+    offs, o = [], 0
+    for r, c in shapes:
+        offs.append(o)
+        o += -(-r // BS) * -(-c // BS)
+    assert o == wl.ng
+    W = torch.zeros((wl.ng, BS, BS), dtype=torch.float32, device=dev)
+
+    def step():
+        for Gi, off in zip(Gw, offs):
+            nb = -(-Gi.shape[0] // BS) * -(-Gi.shape[1] // BS)
+            dr.pack_blocks(Gi, BS, out=wl.G[off:off + nb], valid=False)
+        dr.shampoo_accumulate(wl.G, wl.F, BETA, wl.vr, wl.vc)
+        dr.spectral_scale(wl.F, wl.power_mode, wl.V0, POWER_ITERS, ridge=RIDGE, out=wl.lam,
+                          ws=wl.ws_scale)
+        dr.inv_root_cn(wl.F, wl.lam, CN_ITERS, wl.root_prec, ridge=RIDGE, X=wl.Froot,
+                       ws=wl.ws_root)
+        dr.precondition_update(wl.G, wl.Froot, W, lr, wl.apply_prec, ws=wl.ws_apply)
+
+    step()
+    dr.trace_start(400 * steps + 64)
+    ms = timed_steps(torch, step, steps, dist)
+    recs = dr.trace_records()
+    dr.trace_stop()
+    pack = [r for r in recs if r[0] == "pack"]
+    pack_bytes = sum(r[2] for r in pack)
+    pack_ms = sum(r[3] for r in pack)
+    gbs = pack_bytes / (pack_ms * 1e-3) / 1e9 if pack_ms else None
+    del Gw, W
+    return {"ms_per_step": round(ms, 3),
+            "blocks_per_s": round(wl.nf / (ms * 1e-3), 2),
+            "what": "pack %d bf16 weight gradients -> (%d,1024,1024) + accumulate + scale + CN "
+                    "fp16 x10 + fused W -= lr L^-1/4 G R^-1/4 (block layout)" % (len(shapes), wl.ng),
+            "pack_ms_per_step": round(pack_ms / steps, 3),
+            "pack_gbs": None if gbs is None else round(gbs, 1),
+            "pack_frac_hbm": None if gbs is None else round(gbs / peaks["hbm_gbs"], 4)}
+
+
 def roofline_from_trace(records, peaks):
     by = {}
     for kind, fl, b, ms in records:
@@ -391,6 +434,11 @@ def run_gpu(args):
     h2d = G_host.numel() * G_host.element_size()
     d2h = U_host.numel() * U_host.element_size()
     del G_host, U_host
+
+    # The whole optimizer step from weight-shaped gradients: every Llama weight's bf16
+    # gradient packed into the block stack, accumulate, scale, CN, and the weight step
+    # W <- W - lr U fused into the apply epilogue (W kept in the block layout).
+    full = full_optimizer_step(torch, dr, synth, wl, dev, args.steps, dist, peaks)
     wl.free()
     torch.cuda.empty_cache()
 
@@ -434,6 +482,7 @@ def run_gpu(args):
                           "G and U double-buffered so they overlap the neighbouring steps"},
         "root_only_blocks_per_s": round(wl.nf / (root_ms * 1e-3), 1),
         "ndb_fp32_step_ms": None if ndb_ms is None else round(ndb_ms, 2),
+        "optimizer_step": full,
         "peaks_source": peaks["_source"],
     }
     if rank == 0 and world == 1 and not args.no_cpu:

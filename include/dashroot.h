@@ -205,6 +205,40 @@ dash_status precondition_apply(const void* G, int gdt, const float* Froot, int64
                                void* stream);
 
 /*
+ * precondition_update -- the weight step along the preconditioned direction,
+ * W_j <- W_j - lr * L_j^{-1/4} G_j R_j^{-1/4}, fused into the second product of
+ * precondition_apply (its epilogue reads W_j and writes the stepped W_j in place).
+ * Source: [tg] second paragraph (the preconditioned gradient) for U; the pages
+ * give no optimizer update rule, and the reading taken is the plain step
+ * W - lr U.  W (Ng, B, B) fp32 weights in the block layout of G, updated IN
+ * PLACE (padded rows / columns of a block stay as they are: U is zero there);
+ * U (Ng, B, B) fp32 or NULL: when given, also receives U.  lr finite.  Workspace
+ * as for precondition_apply (DASH_OP_PRECONDITION_APPLY).
+ */
+dash_status precondition_update(const void* G, int gdt, const float* Froot, int64_t Ng,
+                                int B, int prec, float lr, float* W, float* U, void* ws,
+                                size_t ws_bytes, void* stream);
+
+/*
+ * pack_blocks / unpack_blocks -- a weight-shaped matrix <-> its stack of B x B
+ * blocks.  Source: [pt] Metodologia 1 ("Empilhamento de Tensores 3D": gradient
+ * blocks G_ij stacked into (N, B, B)).  M is row-major (rows, cols) with leading
+ * dimension ld >= cols, dtype dt (DASH_DT_F32, DASH_DT_BF16, DASH_DT_F16;
+ * element-aligned); blocks is (nbr * nbc, B, B) of the same dtype with
+ * nbr = ceil(rows / B), nbc = ceil(cols / B), enumerated row-block-major: block
+ * i * nbc + j holds rows i*B.. and columns j*B.. of M.
+ *   pack_blocks zero-fills each block beyond the matrix and, when valid_rows /
+ *   valid_cols (int32, nbr * nbc) are given, writes each block's valid extent
+ *   min(B, rows - i*B) / min(B, cols - j*B) -- the arrays shampoo_accumulate
+ *   takes.  unpack_blocks writes back the valid part only.  rows or cols = 0 is
+ *   a no-op.  Bit copies: no conversion.
+ */
+dash_status pack_blocks(const void* M, int dt, int64_t rows, int64_t cols, int64_t ld, int B,
+                        void* blocks, int32_t* valid_rows, int32_t* valid_cols, void* stream);
+dash_status unpack_blocks(const void* blocks, int dt, int64_t rows, int64_t cols, int64_t ld,
+                          int B, void* M, void* stream);
+
+/*
  * dash_gemm -- the batched tensor-core product the solvers are built from,
  * exposed for tests and roofline measurement (no counterpart on the pages).
  * C[k] = op(A[k]) op(B[k]) for k < N, op = transpose when trans_* != 0.
@@ -273,7 +307,8 @@ typedef enum {
   DASH_TRACE_GEMM_3XTF32 = 3,
   DASH_TRACE_ELEMENTWISE = 4,
   DASH_TRACE_POWER = 5,
-  DASH_TRACE_REDUCE = 6
+  DASH_TRACE_REDUCE = 6,
+  DASH_TRACE_PACK = 7
 } dash_trace_kind;
 
 dash_status dash_trace_start(int capacity);

@@ -52,7 +52,7 @@ SYMBOLS = (
     "precondition_apply", "dash_gemm", "dash_workspace_size", "dash_op_matmuls",
     "dash_device_status", "dash_status_string", "dash_version", "dash_trace_start",
     "dash_trace_count", "dash_trace_read", "dash_trace_stop", "spectral_scale_noalloc",
-    "dash_selftest_wait_timeout",
+    "dash_selftest_wait_timeout", "precondition_update", "pack_blocks", "unpack_blocks",
 )
 
 _lib = None
@@ -82,6 +82,9 @@ def load_library(path=None):
     lib.inv_root_ndb.argtypes = [vp, f32, vp, i64, i32, i32, i32, vp, vp, vp, sz, vp]
     lib.inv_root_cheb.argtypes = [vp, f32, vp, i64, i32, i32, f64, f64, i32, vp, vp, sz, vp]
     lib.precondition_apply.argtypes = [vp, i32, vp, i64, i32, i32, vp, vp, sz, vp]
+    lib.precondition_update.argtypes = [vp, i32, vp, i64, i32, i32, f32, vp, vp, vp, sz, vp]
+    lib.pack_blocks.argtypes = [vp, i32, i64, i64, i64, i32, vp, vp, vp, vp]
+    lib.unpack_blocks.argtypes = [vp, i32, i64, i64, i64, i32, vp, vp]
     lib.dash_gemm.argtypes = [vp, vp, i32, vp, vp, i32, i64, i32, i32, vp, vp]
     lib.dash_workspace_size.argtypes = [i32, i64, i32, i32, i32, ctypes.POINTER(sz)]
     lib.dash_op_matmuls.argtypes = [i32, i32]
@@ -101,7 +104,8 @@ def load_library(path=None):
                                     ctypes.POINTER(f64), ctypes.POINTER(f32)]
     lib.dash_trace_stop.argtypes = []
     for name in ("shampoo_accumulate", "spectral_scale", "inv_root_cn", "inv_root_ndb",
-                 "inv_root_cheb", "precondition_apply", "dash_gemm", "dash_workspace_size",
+                 "inv_root_cheb", "precondition_apply", "precondition_update", "pack_blocks",
+                 "unpack_blocks", "dash_gemm", "dash_workspace_size",
                  "dash_device_status", "dash_trace_start", "dash_trace_read", "dash_trace_stop"):
         getattr(lib, name).restype = ctypes.c_int
     if path is None:
@@ -176,7 +180,7 @@ def workspace(op, n, b, prec=FP32_3XTF32, param=0, device=None, max_bytes=None):
 
 # dash_trace_kind
 TRACE_KINDS = ("gemm_f16", "gemm_bf16", "gemm_tf32", "gemm_3xtf32", "elementwise", "power",
-               "reduce")
+               "reduce", "pack")
 
 
 def trace_start(capacity=4096):
@@ -353,6 +357,68 @@ def precondition_apply(G, Froot, prec=FP32_3XTF32, U=None, ws=None):
     _check(lib.precondition_apply(_ptr(G), _gdt(G), _ptr(Froot), ng, b, p, _ptr(U), _ptr(ws),
                                   ws.numel(), _stream()), "precondition_apply")
     return U
+
+
+def precondition_update(G, Froot, W, lr, prec=FP32_3XTF32, U=None, ws=None):
+    """W_j -= lr * Froot[j] G_j Froot[Ng + j], in place on W (Ng, B, B) fp32; U optional."""
+    lib = load_library()
+    _stack(G, "G", G.dtype)
+    ng, b, _ = G.shape
+    _stack(Froot, "Froot")
+    _stack(W, "W")
+    if Froot.shape != (2 * ng, b, b) or W.shape != (ng, b, b):
+        raise ValueError("Froot must be (2*Ng, B, B) and W (Ng, B, B)")
+    p = _prec(prec)
+    if U is not None:
+        _stack(U, "U")
+    if ws is None:
+        ws = workspace(OP_PRECONDITION_APPLY, ng, b, p, device=G.device)
+    _check(lib.precondition_update(_ptr(G), _gdt(G), _ptr(Froot), ng, b, p, float(lr), _ptr(W),
+                                   _ptr(U), _ptr(ws), ws.numel(), _stream()),
+           "precondition_update")
+    return W
+
+
+def _matrix(M, name):
+    if not isinstance(M, torch.Tensor) or not M.is_cuda or M.dim() != 2:
+        raise TypeError("%s must be a 2-D CUDA tensor" % name)
+    if M.stride(1) != 1:
+        raise ValueError("%s must have unit column stride" % name)
+    return M
+
+
+def pack_blocks(M, B, out=None, valid=True):
+    """Row-block-major (ceil(rows/B) * ceil(cols/B), B, B) blocks of the 2-D matrix M,
+    zero-padded; returns (blocks, valid_rows, valid_cols) (the last two None if
+    valid is False).  M may be a row-strided view."""
+    lib = load_library()
+    _matrix(M, "M")
+    rows, cols = M.shape
+    nb = -(-rows // B) * -(-cols // B)
+    if out is None:
+        out = torch.empty((nb, B, B), dtype=M.dtype, device=M.device)
+    _stack(out, "out", M.dtype)
+    vr = torch.empty(nb, dtype=torch.int32, device=M.device) if valid else None
+    vc = torch.empty(nb, dtype=torch.int32, device=M.device) if valid else None
+    _check(lib.pack_blocks(_ptr(M), _gdt(M), rows, cols, M.stride(0), B, _ptr(out), _ptr(vr),
+                           _ptr(vc), _stream()), "pack_blocks")
+    return out, vr, vc
+
+
+def unpack_blocks(blocks, rows, cols, out=None):
+    """The (rows, cols) matrix whose row-block-major blocks are `blocks` (padding
+    dropped); `out` may be a row-strided 2-D view."""
+    lib = load_library()
+    _stack(blocks, "blocks", blocks.dtype)
+    B = blocks.shape[1]
+    if out is None:
+        out = torch.empty((rows, cols), dtype=blocks.dtype, device=blocks.device)
+    _matrix(out, "out")
+    if out.dtype != blocks.dtype or tuple(out.shape) != (rows, cols):
+        raise ValueError("out must be (rows, cols) of the blocks' dtype")
+    _check(lib.unpack_blocks(_ptr(blocks), _gdt(blocks), rows, cols, out.stride(0), B, _ptr(out),
+                             _stream()), "unpack_blocks")
+    return out
 
 
 def gemm(A, B, prec=TF32, trans_a=False, trans_b=False, A_lo=None, B_lo=None, C=None):

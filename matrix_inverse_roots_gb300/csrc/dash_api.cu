@@ -838,14 +838,18 @@ dash_status inv_root_cheb(const float* A, float ridge, const float* scale, int64
 
 // ---------------------------------------------------------------- apply
 
-dash_status precondition_apply(const void* G, int gdt, const float* Froot, int64_t Ng, int B,
-                               int prec, float* U, void* ws, size_t ws_bytes, void* stream) {
+// The preconditioned direction U = L^{-1/4} G R^{-1/4}; with W, the second product's
+// epilogue also takes the weight step W <- W - lr U in place (E = W), and U is
+// written only when asked for.
+static dash_status apply_impl(const void* G, int gdt, const float* Froot, int64_t Ng, int B,
+                              int prec, float* U, float* W, float lr, void* ws, size_t ws_bytes,
+                              void* stream) {
   if (Ng < 0 || !valid_dim(B) || !valid_prec(prec) ||
       !(gdt == DASH_DT_F32 || gdt == DASH_DT_BF16 || gdt == DASH_DT_F16))
     return DASH_ERR_INVALID_ARG;
   if (Ng == 0) return DASH_OK;
-  if (!G || !Froot || !U || !aligned16(G) || !aligned16(Froot) || !aligned16(U))
-    return DASH_ERR_INVALID_ARG;
+  if (!G || !Froot || !aligned16(G) || !aligned16(Froot)) return DASH_ERR_INVALID_ARG;
+  if ((!U && !W) || (U && !aligned16(U)) || (W && !aligned16(W))) return DASH_ERR_INVALID_ARG;
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return DASH_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int fmt = prec_fmt(prec);
@@ -877,10 +881,62 @@ dash_status precondition_apply(const void* G, int gdt, const float* Froot, int64
     e.nout = 1;
     e.out[0] = eout(bT, fmt, 1.0f, 0.0f);
     DASH_TRY(gemm(prec, B, nc, bL, 0, bG, 0, e, st));
-    e.out[0] = eout_f32(offset_blocks(U, c0, B, 4), 1.0f, 0.0f, 0.0f, nullptr);
+    e.nout = 0;
+    if (W) {
+      float* Wc = offset_blocks(W, c0, B, 4);
+      e.out[e.nout++] = eout_f32(Wc, -lr, 0.0f, 1.0f, nullptr);
+      e.E_hi = Wc;
+      e.E_fmt = FMT_F32;
+    }
+    if (U) e.out[e.nout++] = eout_f32(offset_blocks(U, c0, B, 4), 1.0f, 0.0f, 0.0f, nullptr);
     DASH_TRY(gemm(prec, B, nc, bT, 0, bR, 0, e, st));
   }
   return DASH_OK;
+}
+
+dash_status precondition_apply(const void* G, int gdt, const float* Froot, int64_t Ng, int B,
+                               int prec, float* U, void* ws, size_t ws_bytes, void* stream) {
+  if (!U && Ng > 0) return DASH_ERR_INVALID_ARG;
+  return apply_impl(G, gdt, Froot, Ng, B, prec, U, nullptr, 0.0f, ws, ws_bytes, stream);
+}
+
+dash_status precondition_update(const void* G, int gdt, const float* Froot, int64_t Ng, int B,
+                                int prec, float lr, float* W, float* U, void* ws,
+                                size_t ws_bytes, void* stream) {
+  if (!W && Ng > 0) return DASH_ERR_INVALID_ARG;
+  if (!std::isfinite(lr)) return DASH_ERR_INVALID_ARG;
+  return apply_impl(G, gdt, Froot, Ng, B, prec, U, W, lr, ws, ws_bytes, stream);
+}
+
+// ---------------------------------------------------------------- block packing
+
+static int dt_size(int dt) {
+  return dt == DASH_DT_F32 ? 4 : (dt == DASH_DT_BF16 || dt == DASH_DT_F16) ? 2 : 0;
+}
+
+dash_status pack_blocks(const void* M, int dt, int64_t rows, int64_t cols, int64_t ld, int B,
+                        void* blocks, int32_t* valid_rows, int32_t* valid_cols, void* stream) {
+  const int es = dt_size(dt);
+  if (es == 0 || rows < 0 || cols < 0 || ld < cols || !valid_dim(B)) return DASH_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return DASH_OK;
+  if (!M || !blocks || (reinterpret_cast<uintptr_t>(M) % es) ||
+      (reinterpret_cast<uintptr_t>(blocks) % es) ||
+      (valid_rows && (reinterpret_cast<uintptr_t>(valid_rows) & 3u)) ||
+      (valid_cols && (reinterpret_cast<uintptr_t>(valid_cols) & 3u)))
+    return DASH_ERR_INVALID_ARG;
+  return launch_pack_blocks(M, es, rows, cols, ld, B, blocks, valid_rows, valid_cols,
+                            static_cast<cudaStream_t>(stream));
+}
+
+dash_status unpack_blocks(const void* blocks, int dt, int64_t rows, int64_t cols, int64_t ld,
+                          int B, void* M, void* stream) {
+  const int es = dt_size(dt);
+  if (es == 0 || rows < 0 || cols < 0 || ld < cols || !valid_dim(B)) return DASH_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return DASH_OK;
+  if (!M || !blocks || (reinterpret_cast<uintptr_t>(M) % es) ||
+      (reinterpret_cast<uintptr_t>(blocks) % es))
+    return DASH_ERR_INVALID_ARG;
+  return launch_unpack_blocks(blocks, es, rows, cols, ld, B, M, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

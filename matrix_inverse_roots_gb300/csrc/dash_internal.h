@@ -90,6 +90,14 @@ dash_status launch_frob_acc(const float* A, float ridge, int dim, long long nblo
 // Vin[blk][row][c] / sqrt(in_nrm2[blk][c]) (in_nrm2 null = unscaled), row stride 32.
 // Not last: writes W and acc0[blk][c] += sum_r W^2.
 // Last: acc0[blk][c] += sum_r v w, acc1[blk][c] += sum_r v v (W not written).
+// Weight-shaped (rows, cols, leading dimension ld) <-> row-block-major (b, b)
+// blocks, element size esize (2 or 4); vr / vc (nullable) get each block's extent.
+dash_status launch_pack_blocks(const void* M, int esize, long long rows, long long cols,
+                               long long ld, int b, void* out, int32_t* vr, int32_t* vc,
+                               cudaStream_t st);
+dash_status launch_unpack_blocks(const void* blocks, int esize, long long rows, long long cols,
+                                 long long ld, int b, void* M, cudaStream_t st);
+
 // One half-precision power product on (nblocks, dim, dim) 16-bit A (bf16 != 0:
 // bfloat16, else fp16); vectors transposed, (nblocks, 32, dim) 16-bit.
 dash_status launch_power_step_half(const void* Ah, int bf16, float ridge, int dim,

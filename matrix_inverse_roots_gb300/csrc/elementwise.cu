@@ -231,6 +231,128 @@ dash_status launch_pad_vectors_t(const float* V0, int nv, int dim, long long nbl
   return err == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------- block packing
+// A weight-shaped (rows, cols) matrix with leading dimension ld <-> its
+// row-block-major stack of b x b blocks (block i * nbc + j holds rows i*b.. and
+// columns j*b..), zero-padded beyond the matrix.  Copies of the raw 16- or 32-bit
+// words.  Each thread moves one 16-byte vector of V words when cols and ld are
+// multiples of V and both buffers are 16-byte aligned (a vector then never straddles
+// the matrix edge, since b is a multiple of V too); otherwise one word.
+template <typename T, int V>
+__global__ void pack_blocks_kernel(const T* M, long long rows, long long cols, long long ld, int b,
+                                   long long nbc, long long nb, T* out, int32_t* vr, int32_t* vc) {
+  for (long long k = blockIdx.z; k < nb; k += gridDim.z) {
+    const long long bi = k / nbc, bj = k - (k / nbc) * nbc;
+    const long long r0 = bi * b, c0 = bj * b;
+    for (int r = blockIdx.y; r < b; r += gridDim.y) {
+      const long long gr = r0 + r;
+      T* orow = out + (k * b + r) * static_cast<long long>(b);
+      for (int c = (blockIdx.x * blockDim.x + threadIdx.x) * V; c < b;
+           c += gridDim.x * blockDim.x * V) {
+        const long long gc = c0 + c;
+        if (V > 1) {
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          if (gr < rows && gc < cols) v = *reinterpret_cast<const uint4*>(M + gr * ld + gc);
+          *reinterpret_cast<uint4*>(orow + c) = v;
+        } else {
+          orow[c] = (gr < rows && gc < cols) ? M[gr * ld + gc] : T(0);
+        }
+      }
+    }
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+      if (vr) vr[k] = static_cast<int32_t>(rows - r0 < b ? rows - r0 : b);
+      if (vc) vc[k] = static_cast<int32_t>(cols - c0 < b ? cols - c0 : b);
+    }
+  }
+}
+
+template <typename T, int V>
+__global__ void unpack_blocks_kernel(const T* blocks, long long rows, long long cols, long long ld,
+                                     int b, long long nbc, T* M) {
+  for (long long gr = blockIdx.y; gr < rows; gr += gridDim.y) {
+    const long long bi = gr / b;
+    const long long r = gr - bi * b;
+    for (long long gc = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) * V;
+         gc < cols; gc += static_cast<long long>(gridDim.x) * blockDim.x * V) {
+      const long long bj = gc / b;
+      const T* src = blocks + ((bi * nbc + bj) * b + r) * b + (gc - bj * b);
+      if (V > 1)
+        *reinterpret_cast<uint4*>(M + gr * ld + gc) = *reinterpret_cast<const uint4*>(src);
+      else
+        M[gr * ld + gc] = *src;
+    }
+  }
+}
+
+static bool vec16_ok(const void* p, const void* q, long long cols, long long ld, int v) {
+  return ((reinterpret_cast<uintptr_t>(p) | reinterpret_cast<uintptr_t>(q)) & 15u) == 0 &&
+         cols % v == 0 && ld % v == 0;
+}
+
+dash_status launch_pack_blocks(const void* M, int esize, long long rows, long long cols,
+                               long long ld, int b, void* out, int32_t* vr, int32_t* vc,
+                               cudaStream_t st) {
+  const long long nbr = (rows + b - 1) / b, nbc = (cols + b - 1) / b, nb = nbr * nbc;
+  if (nb <= 0) return DASH_OK;
+  const int v = 16 / esize;
+  const bool vec = vec16_ok(M, out, cols, ld, v);
+  const int per_thread = vec ? v : 1;
+  dim3 grid(static_cast<unsigned>((b / per_thread + 127) / 128), b < 65535 ? b : 65535,
+            static_cast<unsigned>(nb < 65535 ? nb : 65535));
+  const int rec = trace_begin(st);
+  if (esize == 2) {
+    const uint16_t* m = static_cast<const uint16_t*>(M);
+    uint16_t* o = static_cast<uint16_t*>(out);
+    if (vec)
+      pack_blocks_kernel<uint16_t, 8><<<grid, 128, 0, st>>>(m, rows, cols, ld, b, nbc, nb, o, vr, vc);
+    else
+      pack_blocks_kernel<uint16_t, 1><<<grid, 128, 0, st>>>(m, rows, cols, ld, b, nbc, nb, o, vr, vc);
+  } else {
+    const uint32_t* m = static_cast<const uint32_t*>(M);
+    uint32_t* o = static_cast<uint32_t*>(out);
+    if (vec)
+      pack_blocks_kernel<uint32_t, 4><<<grid, 128, 0, st>>>(m, rows, cols, ld, b, nbc, nb, o, vr, vc);
+    else
+      pack_blocks_kernel<uint32_t, 1><<<grid, 128, 0, st>>>(m, rows, cols, ld, b, nbc, nb, o, vr, vc);
+  }
+  const cudaError_t err = cudaGetLastError();
+  trace_end(rec, st, DASH_TRACE_PACK, 0.0,
+            static_cast<double>(esize) * (static_cast<double>(rows) * cols +
+                                          static_cast<double>(nb) * b * b));
+  return err == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
+}
+
+dash_status launch_unpack_blocks(const void* blocks, int esize, long long rows, long long cols,
+                                 long long ld, int b, void* M, cudaStream_t st) {
+  const long long nbc = (cols + b - 1) / b;
+  if (rows <= 0 || cols <= 0) return DASH_OK;
+  const int v = 16 / esize;
+  const bool vec = vec16_ok(blocks, M, cols, ld, v);
+  const int per_thread = vec ? v : 1;
+  const long long gx = (cols / per_thread + 127) / 128;
+  dim3 grid(static_cast<unsigned>(gx < 65535 ? gx : 65535),
+            static_cast<unsigned>(rows < 65535 ? rows : 65535), 1);
+  const int rec = trace_begin(st);
+  if (esize == 2) {
+    const uint16_t* s = static_cast<const uint16_t*>(blocks);
+    uint16_t* m = static_cast<uint16_t*>(M);
+    if (vec)
+      unpack_blocks_kernel<uint16_t, 8><<<grid, 128, 0, st>>>(s, rows, cols, ld, b, nbc, m);
+    else
+      unpack_blocks_kernel<uint16_t, 1><<<grid, 128, 0, st>>>(s, rows, cols, ld, b, nbc, m);
+  } else {
+    const uint32_t* s = static_cast<const uint32_t*>(blocks);
+    uint32_t* m = static_cast<uint32_t*>(M);
+    if (vec)
+      unpack_blocks_kernel<uint32_t, 4><<<grid, 128, 0, st>>>(s, rows, cols, ld, b, nbc, m);
+    else
+      unpack_blocks_kernel<uint32_t, 1><<<grid, 128, 0, st>>>(s, rows, cols, ld, b, nbc, m);
+  }
+  const cudaError_t err = cudaGetLastError();
+  trace_end(rec, st, DASH_TRACE_PACK, 0.0, 2.0 * esize * static_cast<double>(rows) * cols);
+  return err == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
+}
+
 __global__ void power_finish_kernel(const float* num, const float* den, int nv, long long nblocks,
                                     float* lambda) {
   const long long k = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;

@@ -98,6 +98,22 @@ def test_bad_arguments_rejected_on_host():
         assert lib.spectral_scale(ctypes.c_void_p(256), 0.0, 2, 128, mode, 32, 10, null,
                                   ctypes.c_void_p(1024), ctypes.c_void_p(2048), 1 << 20,
                                   null) == 1
+    # Block packing: ld < cols, unknown dtype, B out of range; update without W.
+    assert lib.pack_blocks(ctypes.c_void_p(256), 0, 4, 8, 7, 128, ctypes.c_void_p(512), null,
+                           null, null) == 1
+    assert lib.pack_blocks(ctypes.c_void_p(256), 9, 4, 8, 8, 128, ctypes.c_void_p(512), null,
+                           null, null) == 1
+    assert lib.unpack_blocks(ctypes.c_void_p(256), 1, 4, 8, 8, 100, ctypes.c_void_p(512),
+                             null) == 1
+    assert lib.pack_blocks(null, 0, 0, 8, 8, 128, null, null, null, null) == 0  # empty
+    assert lib.precondition_update(ctypes.c_void_p(256), 1, ctypes.c_void_p(512), 2, 128, 1,
+                                   ctypes.c_float(0.1), null, null, ctypes.c_void_p(1024),
+                                   1 << 20, null) == 1
+    assert lib.precondition_update(ctypes.c_void_p(256), 1, ctypes.c_void_p(512), 2, 128, 1,
+                                   ctypes.c_float(float("nan")), ctypes.c_void_p(768), null,
+                                   ctypes.c_void_p(1024), 1 << 20, null) == 1
+    assert lib.precondition_apply(ctypes.c_void_p(256), 1, ctypes.c_void_p(512), 2, 128, 1,
+                                  null, ctypes.c_void_p(1024), 1 << 20, null) == 1
     # beta outside [0, 1].
     assert lib.shampoo_accumulate(ctypes.c_void_p(256), 1, 2, 128, ctypes.c_float(1.5),
                                   ctypes.c_void_p(512), null, null, null, 0, null) == 1

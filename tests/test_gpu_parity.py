@@ -241,3 +241,81 @@ def test_empty_stack_is_noop():
     s = torch.empty((0,), device="cuda")
     X = dr.inv_root_cn(A, s, iters=3, ws=torch.empty(256, dtype=torch.uint8, device="cuda"))
     assert X.shape == (0, 128, 128)
+
+
+PACK_CASES = [((2048, 5632), 5632, torch.bfloat16, 1024),   # a Llama MLP weight, ragged last column
+              ((300, 200), 256, torch.float32, 128),        # ragged both ways, row-strided view
+              ((128, 384), 384, torch.float16, 128),
+              ((300, 203), 210, torch.float32, 128)]         # word-by-word path (cols % 4 != 0)
+
+
+@pytest.mark.parametrize("shape,ld,dt,b", PACK_CASES)
+def test_pack_unpack_bit_exact(shape, ld, dt, b):
+    """Weight <-> block stack ([pt] Metodologia 1) against the oracle's cut, bit for bit."""
+    require_gpu()
+    dr = library()
+    rows, cols = shape
+    g = torch.Generator(device="cuda").manual_seed(rows + cols)
+    base = torch.randn((rows, ld), generator=g, device="cuda").to(dt)
+    M = base[:, :cols]
+    blocks, vr, vc = dr.pack_blocks(M, b)
+    ref, rvr, rvc = oracle.pack_blocks(to64(M), b)
+    assert torch.equal(blocks.cpu(), torch.from_numpy(ref).to(dt))  # values are exact in dt
+    assert vr.cpu().tolist() == list(rvr) and vc.cpu().tolist() == list(rvc)
+    sentinel = torch.full((rows, ld), -7.0, dtype=dt, device="cuda")
+    dr.unpack_blocks(blocks, rows, cols, out=sentinel[:, :cols])
+    assert torch.equal(sentinel[:, :cols], M)
+    assert bool((sentinel[:, cols:] == -7.0).all())  # the gap beyond cols is untouched
+
+
+def test_pack_llama_layer_layout():
+    """Packing one layer's seven weights gives the block layout of the Llama cut."""
+    require_gpu()
+    dr = library()
+    vrs, vcs = [], []
+    for rows, cols in synth.llama_weight_shapes(1):
+        _, vr, vc = dr.pack_blocks(torch.zeros((rows, cols), dtype=torch.bfloat16, device="cuda"),
+                                   1024)
+        vrs += vr.cpu().tolist()
+        vcs += vc.cpu().tolist()
+    assert (vrs, vcs) == tuple(map(list, synth.llama_block_layout(1)))
+
+
+@pytest.mark.parametrize("prec", ["3xtf32", "tf32"])
+def test_precondition_update(prec):
+    """W <- W - lr U fused into the apply epilogue, against the oracle's weight step."""
+    require_gpu()
+    dr = library()
+    G, vr, vc = synth.llama_layer_blocks(1, seed=2100, var=1e-2, device="cuda")
+    G = G[40:48].contiguous()  # includes zero-padded blocks of the MLP weights
+    vr, vc = vr[40:48], vc[40:48]
+    ng, b = G.shape[0], G.shape[1]
+    g = torch.Generator(device="cuda").manual_seed(2101)
+    Q = torch.randn((2 * ng, b, b), generator=g, device="cuda") / b ** 0.5
+    Froot = Q @ Q.transpose(1, 2) + torch.eye(b, device="cuda")  # SPD stand-ins for the roots
+    # Roots of padded factors are the identity on the padded part (accumulate keeps
+    # the factors so), which is what leaves the padding of U zero.
+    valid = torch.cat([vr, vc]).tolist()
+    for k in range(2 * ng):
+        v = int(valid[k])
+        Froot[k, v:, :] = 0
+        Froot[k, :, v:] = 0
+        Froot[k, v:, v:] = torch.eye(b - v, device="cuda")
+    W0 = torch.randn((ng, b, b), generator=g, device="cuda")
+    for j in range(ng):
+        W0[j, int(vr[j]):, :] = 0
+        W0[j, :, int(vc[j]):] = 0
+    W = W0.clone()
+    U = torch.empty_like(W)
+    lr = 0.01
+    dr.precondition_update(G, Froot, W, lr, prec, U=U)
+    U_apply = dr.precondition_apply(G, Froot, prec)
+    torch.cuda.synchronize()
+    assert torch.equal(U, U_apply)  # same products, same epilogue arithmetic
+    ref = oracle.update_weights(to64(W0), to64(G), to64(Froot), lr)
+    step = to64(W) - to64(W0)
+    err = rel_fro_blocks(step, ref - to64(W0))
+    print("update %s: step rel err max %.3e" % (prec, err.max()))
+    assert err.max() < GATE[prec]
+    for j in range(ng):  # padded parts of W stay exactly as they were
+        assert bool((W[j, int(vr[j]):, :] == 0).all()) and bool((W[j, :, int(vc[j]):] == 0).all())
