@@ -166,9 +166,13 @@ AffParams aff_from(const void* src_hi, const void* src_lo, int src_fmt, int B, l
 }
 
 // One GEMM launch C = X * Y over nc blocks in precision prec.
+// sym: 0 plain; 1 symmetric operands (only their tiles on or above the diagonal
+// are read); 2 also a symmetric result (only those tiles computed and stored).
 dash_status gemm(int prec, int B, long long nc, const Buf& X, int tX, const Buf& Y, int tY,
-                 const EpiParams& e, cudaStream_t st) {
+                 const EpiParams& e, cudaStream_t st, int sym = 0) {
   GemmLaunch g;
+  g.sym_in = (sym >= 1) ? 1 : 0;
+  g.sym_out = (sym >= 2) ? 1 : 0;
   g.kind = prec_kind(prec);
   g.dim = B;
   g.nblocks = nc;
@@ -180,6 +184,14 @@ dash_status gemm(int prec, int B, long long nc, const Buf& X, int tX, const Buf&
   g.transB = tY;
   g.epi = e;
   return launch_gemm(g, st);
+}
+
+// Whether a root solver may keep its iterates as symmetric halves: every iterate
+// is a polynomial in the symmetric A, so each product of two is symmetric.  The
+// CTA-pair kernels (B a multiple of 256) of fp16 / bf16 / TF32 honour it; the
+// reduced-bias 3xTF32 kernel computes full products.
+int sym_mode(int prec, int B) {
+  return (B % 256 == 0 && (prec == DASH_FP16 || prec == DASH_BF16 || prec == DASH_TF32)) ? 2 : 0;
 }
 
 // Small per-call arrays shared by the root solvers.
@@ -499,6 +511,7 @@ dash_status inv_root_cn(const float* A, float ridge, const float* scale, int64_t
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int K = iters;
   const int fmt = prec_fmt(prec);
+  const int S = sym_mode(prec, B), SI = S ? 1 : 0;  // symmetric-half iterates
   Carver cv(ws, ws_bytes);
   RootSmall sm;
   sm.inv_s = static_cast<float*>(cv.take(N * 4));
@@ -557,22 +570,22 @@ dash_status inv_root_cn(const float* A, float ridge, const float* scale, int64_t
         EpiParams e = epi_none();
         e.nout = 1;
         e.out[0] = eout_f32(Xc, 1.0f, 0.0f, 0.0f, m14);
-        DASH_TRY(gemm(prec, B, nc, bx[xc], 0, bT, 0, e, st));
+        DASH_TRY(gemm(prec, B, nc, bx[xc], 0, bT, 0, e, st, SI));
         break;
       }
       if (k >= 1) {
         EpiParams e = epi_none();
         e.nout = 1;
         e.out[0] = eout(bx[xc ^ 1], fmt, 1.0f, 0.0f);
-        DASH_TRY(gemm(prec, B, nc, bx[xc], 0, bT, 0, e, st));
+        DASH_TRY(gemm(prec, B, nc, bx[xc], 0, bT, 0, e, st, S));
         xc ^= 1;
       }
       EpiParams e2 = epi_none();
       e2.nout = 1;
       e2.out[0] = eout(bT2, fmt, 1.0f, 0.0f);
-      DASH_TRY(gemm(prec, B, nc, bT, 0, bT, 0, e2, st));
+      DASH_TRY(gemm(prec, B, nc, bT, 0, bT, 0, e2, st, S));
       e2.out[0] = eout(bT4, fmt, 1.0f, 0.0f);
-      DASH_TRY(gemm(prec, B, nc, bT2, 0, bT2, 0, e2, st));
+      DASH_TRY(gemm(prec, B, nc, bT2, 0, bT2, 0, e2, st, S));
       // M_{k+1} = T^4 M_k; the same epilogue forms T_{k+1} and the residual of M_{k+1}.
       EpiParams em = epi_none();
       em.nout = 2;
@@ -580,7 +593,7 @@ dash_status inv_root_cn(const float* A, float ridge, const float* scale, int64_t
       em.out[1] = eout(bT, fmt, -0.25f, 1.25f);
       em.resid_acc = racc ? racc + (k + 1) : nullptr;
       em.resid_stride = K;
-      DASH_TRY(gemm(prec, B, nc, bT4, 0, bm[mc], 0, em, st));
+      DASH_TRY(gemm(prec, B, nc, bT4, 0, bm[mc], 0, em, st, S));
       mc ^= 1;
     }
   }
@@ -600,6 +613,7 @@ dash_status inv_root_ndb(const float* A, float ridge, const float* scale, int64_
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int K = iters;
   const int fmt = prec_fmt(prec);
+  const int S = sym_mode(prec, B), SI = S ? 1 : 0;  // symmetric-half iterates
   Carver cv(ws, ws_bytes);
   RootSmall sm;
   sm.inv_s = static_cast<float*>(cv.take(N * 4));
@@ -659,21 +673,21 @@ dash_status inv_root_ndb(const float* A, float ridge, const float* scale, int64_
           ep.out[0] = eout(pool[iT], fmt, -0.5f, 1.5f);
           ep.resid_acc = racc_s ? racc_s + k : nullptr;
           ep.resid_stride = rstride;
-          DASH_TRY(gemm(prec, B, nc, pool[iZ], 0, pool[iY], 0, ep, st));
+          DASH_TRY(gemm(prec, B, nc, pool[iZ], 0, pool[iY], 0, ep, st, S));
         }
         if (!lastk) {
           const int iYn = free_buf(iY, iZ, iT);
           EpiParams ey = epi_none();
           ey.nout = 1;
           ey.out[0] = eout(pool[iYn], fmt, 1.0f, 0.0f);
-          DASH_TRY(gemm(prec, B, nc, pool[iY], 0, pool[iT], 0, ey, st));
+          DASH_TRY(gemm(prec, B, nc, pool[iY], 0, pool[iT], 0, ey, st, S));
           iY = iYn;
           if (k >= 1) {
             const int iZn = free_buf(iY, iZ, iT);
             EpiParams ez = epi_none();
             ez.nout = 1;
             ez.out[0] = eout(pool[iZn], fmt, 1.0f, 0.0f);
-            DASH_TRY(gemm(prec, B, nc, pool[iT], 0, pool[iZ], 0, ez, st));
+            DASH_TRY(gemm(prec, B, nc, pool[iT], 0, pool[iZ], 0, ez, st, S));
             iZ = iZn;
           }
           continue;
@@ -698,13 +712,13 @@ dash_status inv_root_ndb(const float* A, float ridge, const float* scale, int64_
             ey.nout = 1;
             ey.out[0] = eout(Xout, FMT_F32, -0.5f, 1.5f, 0.0f, m14);
             // residual of C' = product itself
-            DASH_TRY(gemm(prec, B, nc, pool[iY], 0, pool[iT], 0, ey, st));
+            DASH_TRY(gemm(prec, B, nc, pool[iY], 0, pool[iT], 0, ey, st, SI));
           } else {
             ey.nout = 3;
             ey.out[0] = eout(pool[iCn], fmt, 1.0f, 0.0f);
             ey.out[1] = eout(pool[iTn], fmt, -0.5f, 1.5f);
             ey.out[2] = eout(pool[iZn], fmt, -0.5f, 1.5f);
-            DASH_TRY(gemm(prec, B, nc, pool[iY], 0, pool[iT], 0, ey, st));
+            DASH_TRY(gemm(prec, B, nc, pool[iY], 0, pool[iT], 0, ey, st, S));
           }
           iC = iCn;
           iT = iTn;
@@ -714,7 +728,7 @@ dash_status inv_root_ndb(const float* A, float ridge, const float* scale, int64_
           EpiParams ez = epi_none();
           ez.nout = 1;
           ez.out[0] = eout(Xout, FMT_F32, 1.0f, 0.0f, 0.0f, m14);
-          DASH_TRY(gemm(prec, B, nc, pool[iT], 0, pool[iZ], 0, ez, st));
+          DASH_TRY(gemm(prec, B, nc, pool[iT], 0, pool[iZ], 0, ez, st, SI));
         }
       }
       if (stage == 0 && K == 1) break;  // stage 2 finished inside stage 1's epilogue
@@ -738,6 +752,7 @@ dash_status inv_root_cheb(const float* A, float ridge, const float* scale, int64
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int d = degree;
   const int fmt = prec_fmt(prec);
+  const int S = sym_mode(prec, B), SI = S ? 1 : 0;  // symmetric-half iterates
   // Coefficients of the degree-d interpolant of x^{-1/4} at the first-kind
   // Chebyshev points of [lo, hi], in the Chebyshev basis of t in [-1, 1].
   std::vector<double> c(d + 1);
@@ -799,7 +814,7 @@ dash_status inv_root_cheb(const float* A, float ridge, const float* scale, int64
       EpiParams e = epi_none();
       e.nout = 1;
       e.out[0] = eout(xb, FMT_F32, 1.0f, static_cast<float>(c[0] - c[2]), 0.0f, m14);
-      DASH_TRY(gemm(prec, B, nc, bS, 0, bb[0], 0, e, st));
+      DASH_TRY(gemm(prec, B, nc, bS, 0, bb[0], 0, e, st, SI));
       continue;
     }
     // b_{d-2} = 2 S b_{d-1} + (c_{d-2} - c_d) I
@@ -808,7 +823,7 @@ dash_status inv_root_cheb(const float* A, float ridge, const float* scale, int64
       EpiParams e = epi_none();
       e.nout = 1;
       e.out[0] = eout(bb[i0], fmt, 2.0f, static_cast<float>(c[d - 2] - c[d]));
-      DASH_TRY(gemm(prec, B, nc, bS, 0, bb[i1], 0, e, st));
+      DASH_TRY(gemm(prec, B, nc, bS, 0, bb[i1], 0, e, st, S));
       i2 = i1;
       i1 = i0;
     }
@@ -820,7 +835,7 @@ dash_status inv_root_cheb(const float* A, float ridge, const float* scale, int64
       e.E_hi = bb[i2].hi;
       e.E_lo = bb[i2].lo;
       e.E_fmt = fmt;
-      DASH_TRY(gemm(prec, B, nc, bS, 0, bb[i1], 0, e, st));
+      DASH_TRY(gemm(prec, B, nc, bS, 0, bb[i1], 0, e, st, S));
       i2 = i1;
       i1 = i0;
     }
@@ -831,7 +846,7 @@ dash_status inv_root_cheb(const float* A, float ridge, const float* scale, int64
     e.E_hi = bb[i2].hi;
     e.E_lo = bb[i2].lo;
     e.E_fmt = fmt;
-    DASH_TRY(gemm(prec, B, nc, bS, 0, bb[i1], 0, e, st));
+    DASH_TRY(gemm(prec, B, nc, bS, 0, bb[i1], 0, e, st, SI));
   }
   return DASH_OK;
 }

@@ -42,6 +42,11 @@ struct GemmLaunch {
   const void* B_lo;
   int transB;
   EpiParams epi;
+  // Symmetric-half iterates (honoured for CTA-pair tiles of fp16 / bf16 / TF32):
+  // sym_in -- A and B symmetric, only their 256-tiles on or above the diagonal
+  // are read; sym_out -- only C's 256-tiles on or above the diagonal are computed.
+  int sym_in = 0;
+  int sym_out = 0;
 };
 
 dash_status launch_gemm(const GemmLaunch& g, cudaStream_t st);

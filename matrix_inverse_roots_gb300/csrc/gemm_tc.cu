@@ -85,6 +85,9 @@ struct Cfg {
 
 struct KParams {
   CUtensorMap tO[2];  // 16-bit outputs of the staged epilogue (TMA store maps)
+  // Symmetric operands (sym_in): the other-major views of A and B, used for the
+  // k-blocks that lie in the unstored lower triangle (A(m,k) = A(k,m)).
+  CUtensorMap tAm, tBm;
   int dim;
   int tiles_m, tiles_n;
   long long total_tiles;
@@ -93,6 +96,12 @@ struct KParams {
   uint32_t idesc;
   int a_mn, b_mn;
   int staged;  // all outputs 16-bit (at most two): tiles leave through TMA stores
+  // Symmetric-half iterates (CTA pairs only).  sym_in: A and B are symmetric and
+  // only their 256 x 256 tiles on or above the diagonal are read.  sym_out: only
+  // those tiles of C are computed and written (C symmetric by construction).
+  int sym_in, sym_out;
+  int t256;         // dim / 256
+  uint32_t idesc0;  // instruction descriptor without the operand-major bits
   EpiParams epi;
 };
 
@@ -101,6 +110,21 @@ struct KParams {
 template <int CL>
 __device__ __forceinline__ void decode_unit(long long u, const KParams& p, uint32_t crank,
                                             long long& blk, int& m0, int& n0, int bn) {
+  if (p.sym_out) {
+    // Pair tiles (mt, nt) with nt >= mt, row by row: T(T+1)/2 per block.
+    const int T = p.t256;
+    const long long per = static_cast<long long>(T) * (T + 1) / 2;
+    blk = u / per;
+    int t = static_cast<int>(u - blk * per);
+    int mt = 0;
+    while (t >= T - mt) {
+      t -= T - mt;
+      ++mt;
+    }
+    m0 = mt * 256 + static_cast<int>(crank) * 128;
+    n0 = (mt + t) * 256;
+    return;
+  }
   const long long per = static_cast<long long>(p.tiles_m / CL) * p.tiles_n;
   blk = u / per;
   const int r = static_cast<int>(u - blk * per);
@@ -389,7 +413,13 @@ __global__ void __launch_bounds__(320, 1)
             const CUtensorMap* ma = part ? &tAl : &tA;
             const CUtensorMap* mb = part ? &tBl : &tB;
             if (MODE == 2) {
-              if (!p.a_mn) {
+              // Symmetric operands: a k-block left of A's (below B's) diagonal tile is
+              // read as the transpose of the stored tile, i.e. in the other major.
+              const bool amir = p.sym_in && (k0 >> 8) < (m0 >> 8);
+              const bool bmir = p.sym_in && (k0 >> 8) > (n0 >> 8);
+              if (amir) ma = &p.tAm;
+              if (bmir) mb = &p.tBm;
+              if (!(p.a_mn ^ amir)) {
                 tma_load_3d_pair(sA, ma, fb, k0, m0, z);
               } else {
 #pragma unroll
@@ -397,7 +427,7 @@ __global__ void __launch_bounds__(320, 1)
                   tma_load_3d_pair(sA + i * C::MN_BOX_BYTES, ma, fb, m0 + i * C::MN_ATOM, k0, z);
               }
               const int nb = n0 + static_cast<int>(crank) * C::B_ROWS;  // this CTA's half of N
-              if (!p.b_mn) {
+              if (!(p.b_mn ^ bmir)) {
                 tma_load_3d_pair(sB, mb, fb, k0, nb, z);
               } else {
 #pragma unroll
@@ -463,6 +493,10 @@ __global__ void __launch_bounds__(320, 1)
           break;
         }
         tc_fence_after();
+        // The pair tile's position, for the operand-major choice of symmetric operands.
+        long long ublk;
+        int um0 = 0, un0 = 0;
+        if (p.sym_in) decode_unit<CL>(u, p, 0u, ublk, um0, un0, BN);
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = 0; kb < p.nkb; ++kb) {
           if (!mbar_wait(full_bar(stage), phase, abort_flag)) {
@@ -472,34 +506,41 @@ __global__ void __launch_bounds__(320, 1)
           tc_fence_after();
           const uint32_t sA = sbase + stage * C::STAGE_BYTES;
           const uint32_t sB = sA + C::A_BYTES;
+          const int k0 = kb * C::BK;
+          const int amn = p.a_mn ^ ((p.sym_in && (k0 >> 8) < (um0 >> 8)) ? 1 : 0);
+          const int bmn = p.b_mn ^ ((p.sym_in && (k0 >> 8) > (un0 >> 8)) ? 1 : 0);
+          const uint32_t idesc =
+              p.sym_in ? (p.idesc0 | (static_cast<uint32_t>(amn) << 15) |
+                          (static_cast<uint32_t>(bmn) << 16))
+                       : p.idesc;
 #pragma unroll
           for (int kk = 0; kk < C::NSUB; ++kk) {
             const uint64_t da =
-                p.a_mn ? smem_desc(sA + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO, C::MN_LAYOUT)
-                       : smem_desc_sw128(sA + kk * 32, 16, 1024);
+                amn ? smem_desc(sA + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO, C::MN_LAYOUT)
+                    : smem_desc_sw128(sA + kk * 32, 16, 1024);
             const uint64_t db =
-                p.b_mn ? smem_desc(sB + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO, C::MN_LAYOUT)
-                       : smem_desc_sw128(sB + kk * 32, 16, 1024);
+                bmn ? smem_desc(sB + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO, C::MN_LAYOUT)
+                    : smem_desc_sw128(sB + kk * 32, 16, 1024);
             const uint32_t accum = (kb | kk) ? 1u : 0u;
             uint64_t dal = 0, dbl = 0;
             if (KT == 2) {
               const uint32_t lo_off = C::A_BYTES + C::B_BYTES;
-              dal = p.a_mn ? smem_desc(sA + lo_off + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO,
-                                       C::MN_LAYOUT)
-                           : smem_desc_sw128(sA + lo_off + kk * 32, 16, 1024);
-              dbl = p.b_mn ? smem_desc(sB + lo_off + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO,
-                                       C::MN_LAYOUT)
-                           : smem_desc_sw128(sB + lo_off + kk * 32, 16, 1024);
+              dal = amn ? smem_desc(sA + lo_off + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO,
+                                    C::MN_LAYOUT)
+                        : smem_desc_sw128(sA + lo_off + kk * 32, 16, 1024);
+              dbl = bmn ? smem_desc(sB + lo_off + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO,
+                                    C::MN_LAYOUT)
+                        : smem_desc_sw128(sB + lo_off + kk * 32, 16, 1024);
             }
             if (MODE == 2) {
               if (KT == 0) {
-                mma_f16_pair(d_tmem, da, db, p.idesc, accum);
+                mma_f16_pair(d_tmem, da, db, idesc, accum);
               } else if (KT == 1) {
-                mma_tf32_pair(d_tmem, da, db, p.idesc, accum);
+                mma_tf32_pair(d_tmem, da, db, idesc, accum);
               } else {
-                mma_tf32_pair(d_tmem, dal, db, p.idesc, accum);
-                mma_tf32_pair(d_tmem, da, dbl, p.idesc, 1u);
-                mma_tf32_pair(d_tmem, da, db, p.idesc, 1u);
+                mma_tf32_pair(d_tmem, dal, db, idesc, accum);
+                mma_tf32_pair(d_tmem, da, dbl, idesc, 1u);
+                mma_tf32_pair(d_tmem, da, db, idesc, 1u);
               }
             } else {
               if (KT == 0) {
@@ -611,6 +652,8 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
       if (p.epi.resid_acc != nullptr) {
+        // A symmetric output stores one of each mirrored pair of off-diagonal tiles.
+        if (p.sym_out && (m0 >> 8) != (n0 >> 8)) rsum *= 2.0f;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) rsum += __shfl_xor_sync(0xffffffffu, rsum, off);
         if (lane == 0) atomicAdd(p.epi.resid_acc + blk * p.epi.resid_stride, rsum);
@@ -1043,9 +1086,30 @@ static dash_status run_gemm(const GemmLaunch& g, cudaStream_t st) {
   p.nkb = g.dim / C::BK;
   const uint32_t fmt = (g.kind == KIND_BF16) ? 1u : (g.kind == KIND_F16 ? 0u : 2u);
   p.idesc = make_idesc(fmt, a_mn, b_mn, C::MMA_M, BN);
+  p.idesc0 = make_idesc(fmt, 0, 0, C::MMA_M, BN);
   p.a_mn = a_mn;
   p.b_mn = b_mn;
   p.epi = g.epi;
+  // Symmetric-half iterates: CTA-pair tiles of the plain kernels only.
+  const bool sym_ok = (MODE == 2 && KT != 2 && !ACC);
+  p.sym_in = (sym_ok && g.sym_in) ? 1 : 0;
+  p.sym_out = (sym_ok && g.sym_out) ? 1 : 0;
+  p.t256 = g.dim / 256;
+  if (p.sym_out) {
+    p.total_tiles = g.nblocks * p.t256 * (p.t256 + 1);  // CTA tiles: 2 per pair tile
+    p.total_units = p.total_tiles / CL;
+  }
+  if (p.sym_in) {
+    // The other-major view of each operand over the same memory.
+    const uint32_t am_in = !a_mn ? C::MN_ATOM : C::BK, am_out = !a_mn ? C::BK : 128;
+    const uint32_t bm_in = !b_mn ? C::MN_ATOM : C::BK, bm_out = !b_mn ? C::BK : BN / CL;
+    if (!make_tmap(&p.tAm, g.A, C::EB, g.dim, g.nblocks, am_in, am_out,
+                   !a_mn ? mn_swz : CU_TENSOR_MAP_SWIZZLE_128B))
+      return DASH_ERR_CUDA;
+    if (!make_tmap(&p.tBm, g.B, C::EB, g.dim, g.nblocks, bm_in, bm_out,
+                   !b_mn ? mn_swz : CU_TENSOR_MAP_SWIZZLE_128B))
+      return DASH_ERR_CUDA;
+  }
   p.staged = (C::EPI_BYTES > 0 && g.epi.nout >= 1 && g.epi.nout <= 2) ? 1 : 0;
   for (int o = 0; o < g.epi.nout && p.staged; ++o) {
     const EpiOut& O = g.epi.out[o];
@@ -1093,14 +1157,17 @@ static dash_status run_gemm(const GemmLaunch& g, cudaStream_t st) {
   if (err == cudaSuccess) err = cudaGetLastError();
   if (rec >= 0) {
     const double bb = static_cast<double>(g.dim) * g.dim * g.nblocks;
+    // A symmetric output computes and writes only the (T + 1) / 2T of C on or above
+    // the diagonal (T = dim / 256): those are the flops and output bytes it costs.
+    const double frac = p.sym_out ? (p.t256 + 1.0) / (2.0 * p.t256) : 1.0;
     double bytes = 2.0 * bb * (KT == 2 ? 8 : C::EB);
-    for (int o = 0; o < g.epi.nout; ++o) bytes += bb * fmt_bytes(g.epi.out[o].fmt);
-    if (g.epi.E_hi != nullptr) bytes += bb * fmt_bytes(g.epi.E_fmt);
+    for (int o = 0; o < g.epi.nout; ++o) bytes += frac * bb * fmt_bytes(g.epi.out[o].fmt);
+    if (g.epi.E_hi != nullptr) bytes += frac * bb * fmt_bytes(g.epi.E_fmt);
     const int kind = KT == 2 ? DASH_TRACE_GEMM_3XTF32
                              : (KT == 1 ? DASH_TRACE_GEMM_TF32
                                         : (g.kind == KIND_BF16 ? DASH_TRACE_GEMM_BF16
                                                                : DASH_TRACE_GEMM_F16));
-    trace_end(rec, st, kind, 2.0 * bb * g.dim, bytes);
+    trace_end(rec, st, kind, frac * 2.0 * bb * g.dim, bytes);
   }
   return err == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
 }
