@@ -188,10 +188,11 @@ dash_status gemm(int prec, int B, long long nc, const Buf& X, int tX, const Buf&
 
 // Whether a root solver may keep its iterates as symmetric halves: every iterate
 // is a polynomial in the symmetric A, so each product of two is symmetric.  The
-// CTA-pair kernels (B a multiple of 256) of fp16 / bf16 / TF32 honour it; the
-// reduced-bias 3xTF32 kernel computes full products.
+// CTA-pair kernels (B a multiple of 256) honour it in every precision.  Used by
+// Coupled Newton and Chebyshev; Newton-Denman-Beavers keeps full products.
 int sym_mode(int prec, int B) {
-  return (B % 256 == 0 && (prec == DASH_FP16 || prec == DASH_BF16 || prec == DASH_TF32)) ? 2 : 0;
+  (void)prec;
+  return (B % 256 == 0) ? 2 : 0;
 }
 
 // Small per-call arrays shared by the root solvers.
@@ -511,7 +512,7 @@ dash_status inv_root_cn(const float* A, float ridge, const float* scale, int64_t
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int K = iters;
   const int fmt = prec_fmt(prec);
-  const int S = sym_mode(prec, B), SI = S ? 1 : 0;  // symmetric-half iterates
+  const int S = sym_mode(prec, B);  // symmetric-half iterates
   Carver cv(ws, ws_bytes);
   RootSmall sm;
   sm.inv_s = static_cast<float*>(cv.take(N * 4));
@@ -570,7 +571,8 @@ dash_status inv_root_cn(const float* A, float ridge, const float* scale, int64_t
         EpiParams e = epi_none();
         e.nout = 1;
         e.out[0] = eout_f32(Xc, 1.0f, 0.0f, 0.0f, m14);
-        DASH_TRY(gemm(prec, B, nc, bx[xc], 0, bT, 0, e, st, SI));
+        DASH_TRY(gemm(prec, B, nc, bx[xc], 0, bT, 0, e, st, S));
+        if (S) DASH_TRY(launch_mirror_lower(Xc, B, nc, st));
         break;
       }
       if (k >= 1) {
@@ -613,7 +615,11 @@ dash_status inv_root_ndb(const float* A, float ridge, const float* scale, int64_
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int K = iters;
   const int fmt = prec_fmt(prec);
-  const int S = sym_mode(prec, B), SI = S ? 1 : 0;  // symmetric-half iterates
+  // No symmetric-half iterates here: forcing each product of the coupled iteration
+  // symmetric breaks the Y = A Z balance its left / right products keep, and on
+  // ill-conditioned blocks (scaled condition ~1e6) the iteration then diverges --
+  // in plain float32 as well -- where the full products converge.
+  const int S = 0, SI = 0;
   Carver cv(ws, ws_bytes);
   RootSmall sm;
   sm.inv_s = static_cast<float*>(cv.take(N * 4));
@@ -752,7 +758,7 @@ dash_status inv_root_cheb(const float* A, float ridge, const float* scale, int64
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int d = degree;
   const int fmt = prec_fmt(prec);
-  const int S = sym_mode(prec, B), SI = S ? 1 : 0;  // symmetric-half iterates
+  const int S = sym_mode(prec, B);  // symmetric-half iterates
   // Coefficients of the degree-d interpolant of x^{-1/4} at the first-kind
   // Chebyshev points of [lo, hi], in the Chebyshev basis of t in [-1, 1].
   std::vector<double> c(d + 1);
@@ -814,7 +820,8 @@ dash_status inv_root_cheb(const float* A, float ridge, const float* scale, int64
       EpiParams e = epi_none();
       e.nout = 1;
       e.out[0] = eout(xb, FMT_F32, 1.0f, static_cast<float>(c[0] - c[2]), 0.0f, m14);
-      DASH_TRY(gemm(prec, B, nc, bS, 0, bb[0], 0, e, st, SI));
+      DASH_TRY(gemm(prec, B, nc, bS, 0, bb[0], 0, e, st, S));
+      if (S) DASH_TRY(launch_mirror_lower(Xc, B, nc, st));
       continue;
     }
     // b_{d-2} = 2 S b_{d-1} + (c_{d-2} - c_d) I
@@ -846,7 +853,10 @@ dash_status inv_root_cheb(const float* A, float ridge, const float* scale, int64
     e.E_hi = bb[i2].hi;
     e.E_lo = bb[i2].lo;
     e.E_fmt = fmt;
-    DASH_TRY(gemm(prec, B, nc, bS, 0, bb[i1], 0, e, st, SI));
+    // All products keep symmetric halves (E is read only where it was written);
+    // the caller's X is completed below the diagonal afterwards.
+    DASH_TRY(gemm(prec, B, nc, bS, 0, bb[i1], 0, e, st, S));
+    if (S) DASH_TRY(launch_mirror_lower(Xc, B, nc, st));
   }
   return DASH_OK;
 }

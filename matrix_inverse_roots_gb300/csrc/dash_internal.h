@@ -42,7 +42,7 @@ struct GemmLaunch {
   const void* B_lo;
   int transB;
   EpiParams epi;
-  // Symmetric-half iterates (honoured for CTA-pair tiles of fp16 / bf16 / TF32):
+  // Symmetric-half iterates (honoured for CTA-pair tiles, B a multiple of 256):
   // sym_in -- A and B symmetric, only their 256-tiles on or above the diagonal
   // are read; sym_out -- only C's 256-tiles on or above the diagonal are computed.
   int sym_in = 0;
@@ -102,6 +102,10 @@ dash_status launch_pack_blocks(const void* M, int esize, long long rows, long lo
                                cudaStream_t st);
 dash_status launch_unpack_blocks(const void* blocks, int esize, long long rows, long long cols,
                                  long long ld, int b, void* M, cudaStream_t st);
+
+// Fills the 256-tiles below the diagonal of each (dim, dim) fp32 block with the
+// transposes of their mirror tiles (a symmetric result stored as its upper half).
+dash_status launch_mirror_lower(float* X, int dim, long long nblocks, cudaStream_t st);
 
 // One half-precision power product on (nblocks, dim, dim) 16-bit A (bf16 != 0:
 // bfloat16, else fp16); vectors transposed, (nblocks, 32, dim) 16-bit.

@@ -353,6 +353,47 @@ dash_status launch_unpack_blocks(const void* blocks, int esize, long long rows, 
   return err == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
 }
 
+// Completes a symmetric result stored as its 256 x 256 tiles on or above the
+// diagonal: every tile below it becomes the transpose of its mirror tile.  One
+// CTA per 32 x 32 sub-tile, transposed through padded shared memory so both the
+// read and the write are coalesced.
+__global__ void mirror_lower_kernel(float* X, int dim, int T, long long nblocks) {
+  __shared__ float t[32][33];
+  const int pair = blockIdx.y;  // lower tile (I, J), I > J, row by row
+  int I = 1, rem = pair;
+  while (rem >= I) {
+    rem -= I;
+    ++I;
+  }
+  const int J = rem;
+  const int sa = blockIdx.x >> 3, sb = blockIdx.x & 7;  // 32 x 32 sub-tile of the 256 tile
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  for (long long k = blockIdx.z; k < nblocks; k += gridDim.z) {
+    float* M = X + k * static_cast<long long>(dim) * dim;
+    // Source: upper tile (J, I), rows J*256 + sb*32.., columns I*256 + sa*32..
+    const long long r0 = static_cast<long long>(J) * 256 + sb * 32;
+    const long long c0 = static_cast<long long>(I) * 256 + sa * 32;
+    for (int y = ty; y < 32; y += 8) t[y][tx] = M[(r0 + y) * dim + c0 + tx];
+    __syncthreads();
+    // Destination: lower tile (I, J), rows I*256 + sa*32.., columns J*256 + sb*32..
+    for (int y = ty; y < 32; y += 8) M[(c0 + y) * dim + r0 + tx] = t[tx][y];
+    __syncthreads();
+  }
+}
+
+dash_status launch_mirror_lower(float* X, int dim, long long nblocks, cudaStream_t st) {
+  const int T = dim / 256;
+  if (nblocks <= 0 || T < 2) return DASH_OK;
+  dim3 grid(64, static_cast<unsigned>(T * (T - 1) / 2),
+            static_cast<unsigned>(nblocks < 65535 ? nblocks : 65535));
+  const int rec = trace_begin(st);
+  mirror_lower_kernel<<<grid, dim3(32, 8), 0, st>>>(X, dim, T, nblocks);
+  const cudaError_t err = cudaGetLastError();
+  trace_end(rec, st, DASH_TRACE_ELEMENTWISE, 0.0,
+            8.0 * 65536.0 * (T * (T - 1) / 2) * static_cast<double>(nblocks));
+  return err == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
+}
+
 __global__ void power_finish_kernel(const float* num, const float* den, int nv, long long nblocks,
                                     float* lambda) {
   const long long k = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;

@@ -88,6 +88,7 @@ struct KParams {
   // Symmetric operands (sym_in): the other-major views of A and B, used for the
   // k-blocks that lie in the unstored lower triangle (A(m,k) = A(k,m)).
   CUtensorMap tAm, tBm;
+  CUtensorMap tAlm, tBlm;  // the same for the lo parts of 3xTF32 operands
   int dim;
   int tiles_m, tiles_n;
   long long total_tiles;
@@ -786,12 +787,14 @@ __global__ void __launch_bounds__(320, 1)
           }
           fb = leader ? fb : mapa_shared(fb, 0);
           const int k0 = kb * C::BK;
+          const bool amir = p.sym_in && (k0 >> 8) < (m0 >> 8);
+          const bool bmir = p.sym_in && (k0 >> 8) > (n0 >> 8);
           for (int part = 0; part < C::NPART; ++part) {
             const uint32_t sA = sbase + stage * C::STAGE_BYTES + part * (C::A_BYTES + C::B_BYTES);
             const uint32_t sB = sA + C::A_BYTES;
-            const CUtensorMap* ma = part ? &tAl : &tA;
-            const CUtensorMap* mb = part ? &tBl : &tB;
-            if (!p.a_mn) {
+            const CUtensorMap* ma = amir ? (part ? &p.tAlm : &p.tAm) : (part ? &tAl : &tA);
+            const CUtensorMap* mb = bmir ? (part ? &p.tBlm : &p.tBm) : (part ? &tBl : &tB);
+            if (!(p.a_mn ^ amir)) {
               tma_load_3d_pair(sA, ma, fb, k0, m0, z);
             } else {
 #pragma unroll
@@ -799,7 +802,7 @@ __global__ void __launch_bounds__(320, 1)
                 tma_load_3d_pair(sA + i * C::MN_BOX_BYTES, ma, fb, m0 + i * C::MN_ATOM, k0, z);
             }
             const int nb = n0 + static_cast<int>(crank) * C::B_ROWS;
-            if (!p.b_mn) {
+            if (!(p.b_mn ^ bmir)) {
               tma_load_3d_pair(sB, mb, fb, k0, nb, z);
             } else {
 #pragma unroll
@@ -828,6 +831,9 @@ __global__ void __launch_bounds__(320, 1)
       uint32_t d_tmem = 0;
       bool ok = true;
       for (long long u = cid; u < p.total_units && ok; u += ncl) {
+        long long ublk;
+        int um0 = 0, un0 = 0;
+        if (p.sym_in) decode_unit<CL>(u, p, 0u, ublk, um0, un0, BN);
         for (int kb = 0; kb < p.nkb && ok; ++kb) {
           if (!mbar_wait(full_bar(stage), phase, abort_flag)) {
             ok = false;
@@ -837,6 +843,13 @@ __global__ void __launch_bounds__(320, 1)
           const uint32_t sA = sbase + stage * C::STAGE_BYTES;
           const uint32_t sB = sA + C::A_BYTES;
           const uint32_t lo_off = C::A_BYTES + C::B_BYTES;
+          const int k0 = kb * C::BK;
+          const int amn = p.a_mn ^ ((p.sym_in && (k0 >> 8) < (um0 >> 8)) ? 1 : 0);
+          const int bmn = p.b_mn ^ ((p.sym_in && (k0 >> 8) > (un0 >> 8)) ? 1 : 0);
+          const uint32_t idesc =
+              p.sym_in ? (p.idesc0 | (static_cast<uint32_t>(amn) << 15) |
+                          (static_cast<uint32_t>(bmn) << 16))
+                       : p.idesc;
 #pragma unroll
           for (int kk = 0; kk < C::NSUB; ++kk) {
             const int buf = static_cast<int>(gidx & 1);
@@ -850,22 +863,22 @@ __global__ void __launch_bounds__(320, 1)
               d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
             }
             const uint64_t da =
-                p.a_mn ? smem_desc(sA + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO, C::MN_LAYOUT)
-                       : smem_desc_sw128(sA + kk * 32, 16, 1024);
+                amn ? smem_desc(sA + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO, C::MN_LAYOUT)
+                    : smem_desc_sw128(sA + kk * 32, 16, 1024);
             const uint64_t db =
-                p.b_mn ? smem_desc(sB + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO, C::MN_LAYOUT)
-                       : smem_desc_sw128(sB + kk * 32, 16, 1024);
+                bmn ? smem_desc(sB + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO, C::MN_LAYOUT)
+                    : smem_desc_sw128(sB + kk * 32, 16, 1024);
             const uint64_t dal =
-                p.a_mn ? smem_desc(sA + lo_off + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO,
-                                   C::MN_LAYOUT)
-                       : smem_desc_sw128(sA + lo_off + kk * 32, 16, 1024);
+                amn ? smem_desc(sA + lo_off + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO,
+                                C::MN_LAYOUT)
+                    : smem_desc_sw128(sA + lo_off + kk * 32, 16, 1024);
             const uint64_t dbl =
-                p.b_mn ? smem_desc(sB + lo_off + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO,
-                                   C::MN_LAYOUT)
-                       : smem_desc_sw128(sB + lo_off + kk * 32, 16, 1024);
-            mma_tf32_pair(d_tmem, dal, db, p.idesc, nsub ? 1u : 0u);  // fresh partial
-            mma_tf32_pair(d_tmem, da, dbl, p.idesc, 1u);
-            mma_tf32_pair(d_tmem, da, db, p.idesc, 1u);
+                bmn ? smem_desc(sB + lo_off + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO,
+                                C::MN_LAYOUT)
+                    : smem_desc_sw128(sB + lo_off + kk * 32, 16, 1024);
+            mma_tf32_pair(d_tmem, dal, db, idesc, nsub ? 1u : 0u);  // fresh partial
+            mma_tf32_pair(d_tmem, da, dbl, idesc, 1u);
+            mma_tf32_pair(d_tmem, da, db, idesc, 1u);
             if (++nsub == ACC_SUB) {
               mma_commit_pair_mc(pfull_bar(buf), kMask);
               nsub = 0;
@@ -940,6 +953,7 @@ __global__ void __launch_bounds__(320, 1)
                     chunk_on_diag(m0 + q * 32, cbase + c * 16));
       }
       if (p.epi.resid_acc != nullptr) {
+        if (p.sym_out && (m0 >> 8) != (n0 >> 8)) rsum *= 2.0f;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) rsum += __shfl_xor_sync(0xffffffffu, rsum, off);
         if (lane == 0) atomicAdd(p.epi.resid_acc + blk * p.epi.resid_stride, rsum);
@@ -1091,7 +1105,7 @@ static dash_status run_gemm(const GemmLaunch& g, cudaStream_t st) {
   p.b_mn = b_mn;
   p.epi = g.epi;
   // Symmetric-half iterates: CTA-pair tiles of the plain kernels only.
-  const bool sym_ok = (MODE == 2 && KT != 2 && !ACC);
+  const bool sym_ok = (MODE == 2 && (KT != 2 || ACC));
   p.sym_in = (sym_ok && g.sym_in) ? 1 : 0;
   p.sym_out = (sym_ok && g.sym_out) ? 1 : 0;
   p.t256 = g.dim / 256;
@@ -1109,6 +1123,14 @@ static dash_status run_gemm(const GemmLaunch& g, cudaStream_t st) {
     if (!make_tmap(&p.tBm, g.B, C::EB, g.dim, g.nblocks, bm_in, bm_out,
                    !b_mn ? mn_swz : CU_TENSOR_MAP_SWIZZLE_128B))
       return DASH_ERR_CUDA;
+    if (KT == 2) {
+      if (!make_tmap(&p.tAlm, g.A_lo, C::EB, g.dim, g.nblocks, am_in, am_out,
+                     !a_mn ? mn_swz : CU_TENSOR_MAP_SWIZZLE_128B))
+        return DASH_ERR_CUDA;
+      if (!make_tmap(&p.tBlm, g.B_lo, C::EB, g.dim, g.nblocks, bm_in, bm_out,
+                     !b_mn ? mn_swz : CU_TENSOR_MAP_SWIZZLE_128B))
+        return DASH_ERR_CUDA;
+    }
   }
   p.staged = (C::EPI_BYTES > 0 && g.epi.nout >= 1 && g.epi.nout <= 2) ? 1 : 0;
   for (int o = 0; o < g.epi.nout && p.staged; ++o) {

@@ -18,6 +18,10 @@ The GEMM kernels issue, per K = 8 slice, lo*hi, hi*lo and hi*hi (3xTF32) or one
 hi*hi (TF32).  For B a multiple of 256 the 3xTF32 kernel starts a fresh partial
 accumulator every PARTIAL_SUB slices and adds the partials in fp32 with
 round-to-nearest, in order; other sizes accumulate over the whole K.
+For B a multiple of 256 Coupled Newton keeps symmetric-half iterates: a product
+reads each operand's 256 x 256 tiles on or above the diagonal and takes the
+tiles below it as the transposes of their mirror images (tile_sym).  NDB keeps
+full products.
 
 Everything runs in float64 torch on whatever device the inputs live on.
 """
@@ -99,8 +103,21 @@ def partial_sub_for(b, prec):
     return PARTIAL_SUB if (prec == "3xtf32" and b % 256 == 0) else None
 
 
-def _mm(prec, b):
+def tile_sym(m, t=256):
+    """m with every t x t tile below the diagonal replaced by the transpose of its
+    mirror tile above it (the tiles on the diagonal are kept whole)."""
+    out = m.clone()
+    n = m.shape[0] // t
+    for i in range(n):
+        for j in range(i):
+            out[i * t:(i + 1) * t, j * t:(j + 1) * t] = m[j * t:(j + 1) * t, i * t:(i + 1) * t].T
+    return out
+
+
+def _mm(prec, b, sym):
     sub = partial_sub_for(b, prec)
+    if sym and b % 256 == 0:
+        return lambda x, y: gemm(tile_sym(x), tile_sym(y), prec, sub)
     return lambda x, y: gemm(x, y, prec, sub)
 
 
@@ -108,7 +125,7 @@ def cn_root(a, s, iters, prec, ridge=0.0):
     """Coupled Newton (p = 4) with model products; iterates stored in fp32."""
     a = a.float()
     b = a.shape[0]
-    mm = _mm(prec, b)
+    mm = _mm(prec, b, sym=True)
     eye = torch.eye(b, dtype=torch.float32, device=a.device)
     As = (a + ridge * eye) / s
     M = As
@@ -130,7 +147,7 @@ def ndb_root(a, s, iters, prec, ridge=0.0):
     """Two-stage Newton-Denman-Beavers with model products; iterates in fp32."""
     a = a.float()
     b = a.shape[0]
-    mm = _mm(prec, b)
+    mm = _mm(prec, b, sym=False)
     eye = torch.eye(b, dtype=torch.float32, device=a.device)
 
     def stage(C, keep_y):

@@ -319,3 +319,25 @@ def test_precondition_update(prec):
     assert err.max() < GATE[prec]
     for j in range(ng):  # padded parts of W stay exactly as they were
         assert bool((W[j, int(vr[j]):, :] == 0).all()) and bool((W[j, :, int(vc[j]):] == 0).all())
+
+
+@pytest.mark.parametrize("prec", PRECS)
+@pytest.mark.parametrize("b", [512, 1024])
+def test_symmetric_half_iterates(prec, b):
+    """B a multiple of 256: CN and Chebyshev keep symmetric-half iterates (only the
+    256-tiles on or above the diagonal are computed).  Chebyshev degrees 3, 4 and 5
+    take b_2 from the prologue, the first product and the loop respectively; the
+    last product reads it whole."""
+    require_gpu()
+    dr = library()
+    A, _ = wishart_case(3, b, 2200 + b)
+    s = dr.spectral_scale(A, dr.SCALE_FROBENIUS)
+    X = dr.inv_root_cn(A, s, 8, prec)
+    err = rel_fro_blocks(to64(X), oracle.cn_inv_root(to64(A), to64(s), 8)[0])
+    assert err.max() < GATE[prec], ("cn", err)
+    for d in (3, 4, 5, 8):
+        X = dr.inv_root_cheb(A, s, d, 1e-2, 1.05, prec)
+        ref = oracle.cheb_inv_root(to64(A), to64(s), d, 1e-2, 1.05)[0]
+        err = rel_fro_blocks(to64(X), ref)
+        assert err.max() < GATE[prec], ("cheb", d, err)
+        assert np.all(np.isfinite(to64(X)))

@@ -142,3 +142,14 @@ def test_random_small_integers_are_exact():
     a = torch.tensor([[rng.randint(-8, 8) for _ in range(64)] for _ in range(4)], dtype=torch.float32)
     b = torch.tensor([[rng.randint(-8, 8) for _ in range(3)] for _ in range(64)], dtype=torch.float32)
     assert torch.equal(tc_arith.gemm(a, b, "tf32"), (a.double() @ b.double()).float())
+
+
+def test_tile_sym_mirrors_lower_tiles():
+    g = torch.Generator().manual_seed(9)
+    m = torch.randn((512, 512), generator=g)
+    s = tc_arith.tile_sym(m)
+    assert torch.equal(s[:256, :], m[:256, :])                 # upper block row kept
+    assert torch.equal(s[256:, 256:], m[256:, 256:])           # diagonal tile kept whole
+    assert torch.equal(s[256:, :256], m[:256, 256:].T)         # lower tile mirrored
+    sym = m + m.T
+    assert torch.equal(tc_arith.tile_sym(sym), sym)            # a symmetric matrix is unchanged
