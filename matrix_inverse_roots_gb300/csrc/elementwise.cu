@@ -384,8 +384,13 @@ __global__ void mirror_lower_kernel(float* X, int dim, int T, long long nblocks)
 dash_status launch_mirror_lower(float* X, int dim, long long nblocks, cudaStream_t st) {
   const int T = dim / 256;
   if (nblocks <= 0 || T < 2) return DASH_OK;
-  dim3 grid(64, static_cast<unsigned>(T * (T - 1) / 2),
-            static_cast<unsigned>(nblocks < 65535 ? nblocks : 65535));
+  // About 32 CTAs per SM in all; each walks the blocks with stride gridDim.z.
+  const long long per_block = 64LL * (T * (T - 1) / 2);
+  long long gz = (static_cast<long long>(device_sm_count()) * 32 + per_block - 1) / per_block;
+  if (gz > nblocks) gz = nblocks;
+  if (gz > 65535) gz = 65535;
+  if (gz < 1) gz = 1;
+  dim3 grid(64, static_cast<unsigned>(T * (T - 1) / 2), static_cast<unsigned>(gz));
   const int rec = trace_begin(st);
   mirror_lower_kernel<<<grid, dim3(32, 8), 0, st>>>(X, dim, T, nblocks);
   const cudaError_t err = cudaGetLastError();
