@@ -59,7 +59,11 @@ GEMM_SOURCES = ("matrix_inverse_roots_gb300/csrc/gemm_tc.cu",
 
 
 def gemm_traffic(flops_per_launch, b):
-    """Measured DRAM bytes of one dominant-GEMM launch, or None if the kernel changed."""
+    """Measured DRAM bytes of one dominant-GEMM launch, or None if the kernel changed.
+
+    The launch's block count comes from its executed flops: a Coupled Newton product
+    at B a multiple of 256 computes only the T(T+1)/2 upper 256-tiles of T^2
+    (T = B / 256), i.e. 2 B^3 (T + 1) / (2 T) flops per block."""
     import hashlib
 
     h = hashlib.sha256()
@@ -69,7 +73,9 @@ def gemm_traffic(flops_per_launch, b):
             h.update(fh.read())
     if h.hexdigest()[:16] != GEMM_TRAFFIC_SRC or b != 1024:
         return None
-    return round(GEMM_TRAFFIC_PER_BLOCK * flops_per_launch / (2.0 * b ** 3))
+    t = b // 256
+    per_block = 2.0 * b ** 3 * ((t + 1) / (2.0 * t) if b % 256 == 0 else 1.0)
+    return round(GEMM_TRAFFIC_PER_BLOCK * flops_per_launch / per_block)
 
 
 def load_peaks():
@@ -221,7 +227,10 @@ def e2e_steps(torch, wl, G_host, U_host, steps, dist=None):
     buffered: step k's read-back and step k+1's upload run on two copy streams while
     the neighbouring steps compute (the uploads wait until the step two back has
     finished reading that G buffer; a step waits until the read-back of the U buffer it
-    is about to overwrite has finished).  Returns ms per step."""
+    is about to overwrite has finished).  Each copy is bracketed by timing events on its
+    own stream, so the link's achieved bandwidth is known: when the uploads plus the
+    read-backs take longer than the compute, the step is bound by the host link.
+    Returns (ms per step, upload ms per step, read-back ms per step)."""
     comp = torch.cuda.current_stream()
     up, down = torch.cuda.Stream(), torch.cuda.Stream()
     Gb = [wl.G, torch.empty_like(wl.G)]
@@ -229,6 +238,15 @@ def e2e_steps(torch, wl, G_host, U_host, steps, dist=None):
     used = [torch.cuda.Event() for _ in range(2)]
     uploaded = [torch.cuda.Event() for _ in range(2)]
     read = [torch.cuda.Event() for _ in range(2)]
+    spans = {"up": [], "down": []}
+
+    def timed_copy(kind, stream, dst, src):
+        a = torch.cuda.Event(enable_timing=True)
+        z = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        dst.copy_(src, non_blocking=True)
+        z.record(stream)
+        spans[kind].append((a, z))
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
@@ -237,7 +255,7 @@ def e2e_steps(torch, wl, G_host, U_host, steps, dist=None):
     t0.record(comp)
     up.wait_stream(comp)
     with torch.cuda.stream(up):
-        Gb[0].copy_(G_host, non_blocking=True)
+        timed_copy("up", up, Gb[0], G_host)
         uploaded[0].record(up)
     for k in range(steps):
         b = k % 2
@@ -246,7 +264,7 @@ def e2e_steps(torch, wl, G_host, U_host, steps, dist=None):
             if k >= 1:
                 up.wait_event(used[nb])
             with torch.cuda.stream(up):
-                Gb[nb].copy_(G_host, non_blocking=True)
+                timed_copy("up", up, Gb[nb], G_host)
                 uploaded[nb].record(up)
         comp.wait_event(uploaded[b])
         if k >= 2:
@@ -256,7 +274,7 @@ def e2e_steps(torch, wl, G_host, U_host, steps, dist=None):
         used[b].record(comp)
         down.wait_event(used[b])
         with torch.cuda.stream(down):
-            U_host.copy_(Ub[b], non_blocking=True)
+            timed_copy("down", down, U_host, Ub[b])
             read[b].record(down)
     comp.wait_stream(up)
     comp.wait_stream(down)
@@ -266,7 +284,9 @@ def e2e_steps(torch, wl, G_host, U_host, steps, dist=None):
         dist.barrier()
     wl.G, wl.U = Gb[0], Ub[0]
     del Gb, Ub
-    return t0.elapsed_time(t1) / steps
+    up_ms = sum(a.elapsed_time(z) for a, z in spans["up"]) / steps
+    down_ms = sum(a.elapsed_time(z) for a, z in spans["down"]) / steps
+    return t0.elapsed_time(t1) / steps, up_ms, down_ms
 
 
 def full_optimizer_step(torch, dr, synth, wl, dev, steps, dist, peaks, lr=1e-3):
@@ -434,8 +454,8 @@ def run_gpu(args):
     U_host = torch.empty(wl.U.shape, dtype=wl.U.dtype, pin_memory=True)
 
     e2e_steps(torch, wl, G_host, U_host, 2)
-    e2e_ms = max_over_ranks(e2e_steps(torch, wl, G_host, U_host, max(4, args.steps), dist),
-                            dev)
+    e2e_ms, up_ms, down_ms = e2e_steps(torch, wl, G_host, U_host, max(4, args.steps), dist)
+    e2e_ms = max_over_ranks(e2e_ms, dev)
     h2d = G_host.numel() * G_host.element_size()
     d2h = U_host.numel() * U_host.element_size()
     del G_host, U_host
@@ -483,6 +503,8 @@ def run_gpu(args):
         "e2e": {"value": round(wl.nf * world / (e2e_ms * 1e-3), 2), "unit": "blocks/s",
                 "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
+                "h2d_ms_per_step": round(up_ms, 2), "d2h_ms_per_step": round(down_ms, 2),
+                "h2d_gbs": round(h2d / (up_ms * 1e6), 1), "d2h_gbs": round(d2h / (down_ms * 1e6), 1),
                 "copies": "pinned host buffers; uploads and read-backs on two copy streams, "
                           "G and U double-buffered so they overlap the neighbouring steps"},
         "root_only_blocks_per_s": round(wl.nf / (root_ms * 1e-3), 1),
