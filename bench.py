@@ -52,8 +52,8 @@ TF32_RATIO = 1.1 / 2.25
 # profiles/gemm_tc_f16_pair_cn_b1024_n64.md (64 blocks of 1024^2; traffic grows in
 # proportion to the blocks a launch processes).  Valid only for the kernel sources
 # it was taken on, identified by GEMM_TRAFFIC_SRC.
-GEMM_TRAFFIC_PER_BLOCK = 3.018e6
-GEMM_TRAFFIC_SRC = "4991dffb0bd8ff48"
+GEMM_TRAFFIC_PER_BLOCK = 2.975e6
+GEMM_TRAFFIC_SRC = "f70b79738d50bf44"
 GEMM_SOURCES = ("matrix_inverse_roots_gb300/csrc/gemm_tc.cu",
                 "matrix_inverse_roots_gb300/csrc/dash_common.cuh")
 

@@ -124,10 +124,15 @@ dash_status shampoo_accumulate(const void* G, int gdt, int64_t Ng, int B, float 
  *     1 <= n_vec <= 32, power_iters >= 1, V0 (N, B, n_vec) fp32.
  *   mode DASH_SCALE_POWER_F16 / _BF16: the same iteration in half precision
  *     ([pt] Principais Contribuicoes item 4, "an efficient half-precision
- *     Power-Iteration"): A_k is rounded once to fp16 / bf16, each product takes
- *     16-bit A and 16-bit vectors with fp32 accumulation, the ridge term, the
- *     column normalisation and the Rayleigh quotients are fp32, and the vectors
- *     are stored in the 16-bit format between products.
+ *     Power-Iteration"): sigma_k A_k is rounded once to fp16 / bf16, each product
+ *     takes 16-bit A and 16-bit vectors with fp32 accumulation, the ridge term
+ *     (sigma_k ridge), the column normalisation and the Rayleigh quotients are
+ *     fp32, the vectors are stored in the 16-bit format between products, and the
+ *     result is divided by sigma_k.  sigma_k is the power of two that brings
+ *     max(max_i |A_k[i][i]|, |ridge|) into [1/2, 1); it is exact, so a block whose
+ *     16-bit copy would neither overflow nor underflow gets the same lambda as
+ *     with sigma_k = 1, and a positive semidefinite block (|A_ij| <= max_i A_ii)
+ *     stays within fp16's range whatever its magnitude.
  *   mode DASH_SCALE_FROBENIUS: lambda_out[k] = ||A_k + ridge I||_F
  *     (n_vec, power_iters, V0 ignored; may be 0 / NULL).
  *   A (N, B, B) fp32 symmetric blocks; lambda_out (N,) fp32.

@@ -279,7 +279,8 @@ dash_status dash_workspace_size(int op, int64_t N, int B, int prec, int param, s
     case DASH_OP_SPECTRAL_SCALE:
       if (prec == DASH_FP16 || prec == DASH_BF16)  // the half-precision power modes
         s = round256(static_cast<size_t>(N) * B * B * 2) +
-            2 * round256(static_cast<size_t>(N) * B * 32 * 2) + 3 * round256(N * 32 * 4) + 256;
+            2 * round256(static_cast<size_t>(N) * B * 32 * 2) + 3 * round256(N * 32 * 4) +
+            round256(N * 4) + 256;
       else
         s = 2 * round256(static_cast<size_t>(N) * B * 32 * 4) + 3 * round256(N * 32 * 4) + 256;
       break;
@@ -405,14 +406,15 @@ dash_status spectral_scale(const float* A, float ridge, int64_t N, int B, int mo
     // Half precision: a 16-bit copy of each block, vectors transposed (32, B).
     const int bf = (mode == DASH_SCALE_POWER_BF16) ? 1 : 0;
     const size_t per_blk = static_cast<size_t>(B) * B * 2 + 2 * static_cast<size_t>(B) * 32 * 2 +
-                           3 * 32 * 4;
+                           3 * 32 * 4 + 4;
     long long chunk = static_cast<long long>(ws_bytes / per_blk);
     if (chunk > N) chunk = N;
     if (chunk > 65535) chunk = 65535;
     while (chunk > 0) {
       const size_t need = round256(static_cast<size_t>(chunk) * B * B * 2) +
                           2 * round256(static_cast<size_t>(chunk) * B * 32 * 2) +
-                          3 * round256(static_cast<size_t>(chunk) * 32 * 4);
+                          3 * round256(static_cast<size_t>(chunk) * 32 * 4) +
+                          round256(static_cast<size_t>(chunk) * 4);
       if (need <= ws_bytes) break;
       --chunk;
     }
@@ -426,11 +428,17 @@ dash_status spectral_scale(const float* A, float ridge, int64_t N, int B, int mo
     nrm[0] = static_cast<float*>(cv.take(static_cast<size_t>(chunk) * 32 * 4));
     nrm[1] = static_cast<float*>(cv.take(static_cast<size_t>(chunk) * 32 * 4));
     float* den = static_cast<float*>(cv.take(static_cast<size_t>(chunk) * 32 * 4));
+    float* sigma = static_cast<float*>(cv.take(static_cast<size_t>(chunk) * 4));
     if (!cv.ok) return DASH_ERR_WORKSPACE_TOO_SMALL;
     const size_t acc_bytes = static_cast<size_t>(chunk) * 32 * 4;
     for (long long c0 = 0; c0 < N; c0 += chunk) {
       const long long nc = (N - c0 < chunk) ? N - c0 : chunk;
+      // Each block is stored as sigma A with sigma an exact power of two, so that the
+      // 16-bit copy keeps fp16's range whatever the factor's magnitude; lambda of
+      // sigma (A + ridge I) is divided by sigma at the end.
+      DASH_TRY(launch_diag_pow2_scale(offset_blocks(A, c0, B, 4), ridge, B, nc, sigma, st));
       AffParams a = aff_from(offset_blocks(A, c0, B, 4), nullptr, FMT_F32, B, nc);
+      a.inv_s = sigma;
       a.nout = 1;
       Buf hb;
       hb.hi = Ah;
@@ -445,13 +453,13 @@ dash_status spectral_scale(const float* A, float ridge, int64_t N, int B, int mo
         const int last = (it == power_iters - 1);
         if (cudaMemsetAsync(nrm[cur], 0, acc_bytes, st) != cudaSuccess) return DASH_ERR_CUDA;
         if (last && cudaMemsetAsync(den, 0, acc_bytes, st) != cudaSuccess) return DASH_ERR_CUDA;
-        DASH_TRY(launch_power_step_half(Ah, bf, ridge, B, nc, vin, n_vec, in_n, Vt[cur],
+        DASH_TRY(launch_power_step_half(Ah, bf, ridge, sigma, B, nc, vin, n_vec, in_n, Vt[cur],
                                         nrm[cur], den, last, st));
         vin = Vt[cur];
         in_n = nrm[cur];
         cur ^= 1;
       }
-      DASH_TRY(launch_power_finish(nrm[cur ^ 1], den, n_vec, nc, lambda_out + c0, st));
+      DASH_TRY(launch_power_finish(nrm[cur ^ 1], den, n_vec, nc, sigma, lambda_out + c0, st));
     }
     return DASH_OK;
   }
@@ -496,7 +504,7 @@ dash_status spectral_scale(const float* A, float ridge, int64_t N, int B, int mo
       cur ^= 1;
     }
     // After the loop the last step's numerators sit in nrm[cur ^ 1].
-    DASH_TRY(launch_power_finish(nrm[cur ^ 1], den, n_vec, nc, lambda_out + c0, st));
+    DASH_TRY(launch_power_finish(nrm[cur ^ 1], den, n_vec, nc, nullptr, lambda_out + c0, st));
   }
   return DASH_OK;
 }
@@ -559,44 +567,52 @@ dash_status inv_root_cn(const float* A, float ridge, const float* scale, int64_t
       DASH_TRY(launch_affine(a, st));
       continue;
     }
-    a.nout = 3;
+    a.nout = 2;
     a.out[0] = aout(bm[0], fmt, 1.0f, 0.0f);
     a.out[1] = aout(bT, fmt, -0.25f, 1.25f);
-    a.out[2] = aout(bx[0], fmt, -0.25f, 1.25f);
     DASH_TRY(launch_affine(a, st));
-    int mc = 0, xc = 0;
+    // T_k and the scratch that takes T_k^2 and then T_{k+1} trade buffers every
+    // iteration.  X_1 = T_0 is not copied: it is read from T_0's buffer, which
+    // becomes scratch only after the first X product has consumed it.
+    Buf tk = bT, tsp = bT2, xk = bT;
+    int mc = 0, xn = 0;
     for (int k = 0; k < K; ++k) {
       if (k == K - 1) {
         // X_K = X_{K-1} T_{K-1}, scaled by s^{-1/4}, into the caller's fp32 output.
         EpiParams e = epi_none();
         e.nout = 1;
         e.out[0] = eout_f32(Xc, 1.0f, 0.0f, 0.0f, m14);
-        DASH_TRY(gemm(prec, B, nc, bx[xc], 0, bT, 0, e, st, S));
+        DASH_TRY(gemm(prec, B, nc, xk, 0, tk, 0, e, st, S));
         if (S) DASH_TRY(launch_mirror_lower(Xc, B, nc, st));
         break;
       }
       if (k >= 1) {
         EpiParams e = epi_none();
         e.nout = 1;
-        e.out[0] = eout(bx[xc ^ 1], fmt, 1.0f, 0.0f);
-        DASH_TRY(gemm(prec, B, nc, bx[xc], 0, bT, 0, e, st, S));
-        xc ^= 1;
+        e.out[0] = eout(bx[xn], fmt, 1.0f, 0.0f);
+        DASH_TRY(gemm(prec, B, nc, xk, 0, tk, 0, e, st, S));
+        xk = bx[xn];
+        xn ^= 1;
       }
       EpiParams e2 = epi_none();
       e2.nout = 1;
-      e2.out[0] = eout(bT2, fmt, 1.0f, 0.0f);
-      DASH_TRY(gemm(prec, B, nc, bT, 0, bT, 0, e2, st, S));
+      e2.out[0] = eout(tsp, fmt, 1.0f, 0.0f);
+      DASH_TRY(gemm(prec, B, nc, tk, 0, tk, 0, e2, st, S));
       e2.out[0] = eout(bT4, fmt, 1.0f, 0.0f);
-      DASH_TRY(gemm(prec, B, nc, bT2, 0, bT2, 0, e2, st, S));
-      // M_{k+1} = T^4 M_k; the same epilogue forms T_{k+1} and the residual of M_{k+1}.
+      DASH_TRY(gemm(prec, B, nc, tsp, 0, tsp, 0, e2, st, S));
+      // M_{k+1} = T^4 M_k; the same epilogue forms T_{k+1} (into the scratch, free
+      // once T^4 is formed) and the residual of M_{k+1}.
       EpiParams em = epi_none();
       em.nout = 2;
       em.out[0] = eout(bm[mc ^ 1], fmt, 1.0f, 0.0f);
-      em.out[1] = eout(bT, fmt, -0.25f, 1.25f);
+      em.out[1] = eout(tsp, fmt, -0.25f, 1.25f);
       em.resid_acc = racc ? racc + (k + 1) : nullptr;
       em.resid_stride = K;
       DASH_TRY(gemm(prec, B, nc, bT4, 0, bm[mc], 0, em, st, S));
       mc ^= 1;
+      const Buf t = tk;
+      tk = tsp;
+      tsp = t;
     }
   }
   if (resid_out)

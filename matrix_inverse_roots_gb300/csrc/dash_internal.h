@@ -108,9 +108,11 @@ dash_status launch_unpack_blocks(const void* blocks, int esize, long long rows, 
 dash_status launch_mirror_lower(float* X, int dim, long long nblocks, cudaStream_t st);
 
 // One half-precision power product on (nblocks, dim, dim) 16-bit A (bf16 != 0:
-// bfloat16, else fp16); vectors transposed, (nblocks, 32, dim) 16-bit.
-dash_status launch_power_step_half(const void* Ah, int bf16, float ridge, int dim,
-                                   long long nblocks, const uint16_t* Vt_in, int nv,
+// bfloat16, else fp16); vectors transposed, (nblocks, 32, dim) 16-bit.  When
+// blk_scale is given, block k of Ah holds sigma_k A_k and its ridge term is
+// sigma_k ridge.
+dash_status launch_power_step_half(const void* Ah, int bf16, float ridge, const float* blk_scale,
+                                   int dim, long long nblocks, const uint16_t* Vt_in, int nv,
                                    const float* in_nrm2, uint16_t* Vt_out, float* acc0,
                                    float* acc1, int last, cudaStream_t st);
 
@@ -126,9 +128,16 @@ dash_status launch_power_step_tc(const float* A, float ridge, int dim, long long
 dash_status launch_pad_vectors(const float* V0, int nv, int dim, long long nblocks, float* V,
                                cudaStream_t st);
 
-// lambda[k] = max_{c < nv} num[k][c] / den[k][c].
+// lambda[k] = max_{c < nv} num[k][c] / den[k][c], divided by blk_scale[k] when given.
 dash_status launch_power_finish(const float* num, const float* den, int nv, long long nblocks,
-                                float* lambda, cudaStream_t st);
+                                const float* blk_scale, float* lambda, cudaStream_t st);
+
+// sigma[k] = 2^-e with max(max_i |A_k[i][i]|, |ridge|) in [2^(e-1), 2^e), e clamped to
+// [-126, 126]; 1 for a zero or non-finite maximum.  For a symmetric positive
+// semidefinite block every |sigma A_k[i][j]| <= 1, so a 16-bit copy neither
+// overflows nor loses its large entries to underflow, and the scale is exact.
+dash_status launch_diag_pow2_scale(const float* A, float ridge, int dim, long long nblocks,
+                                   float* sigma, cudaStream_t st);
 
 // Kernel trace hooks (no-ops unless dash_trace_start was called).
 int trace_begin(cudaStream_t st);

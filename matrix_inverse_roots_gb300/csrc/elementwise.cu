@@ -399,21 +399,65 @@ dash_status launch_mirror_lower(float* X, int dim, long long nblocks, cudaStream
   return err == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
 }
 
+// One CTA per block (grid-strided): the largest |diagonal entry| and |ridge|, turned
+// into the power of two that brings it into [1/2, 1).
+__global__ void __launch_bounds__(EW_THREADS)
+    diag_pow2_kernel(const float* A, float ridge, int dim, long long nblocks, float* sigma) {
+  __shared__ float red[EW_THREADS / 32];
+  const long long dd = static_cast<long long>(dim) * dim;
+  for (long long blk = blockIdx.x; blk < nblocks; blk += gridDim.x) {
+    float m = fabsf(ridge);
+    for (int i = threadIdx.x; i < dim; i += EW_THREADS)
+      m = fmaxf(m, fabsf(A[blk * dd + static_cast<long long>(i) * (dim + 1)]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float mx = red[0];
+      for (int w = 1; w < EW_THREADS / 32; ++w) mx = fmaxf(mx, red[w]);
+      // mx = f 2^e, f in [1/2, 1): the biased exponent field E of a normal mx is e + 126.
+      const uint32_t E = (__float_as_uint(mx) >> 23) & 0xffu;
+      float s = 1.0f;
+      if (E != 0xffu && mx > 0.0f) {
+        int e = static_cast<int>(E) - 126;  // a subnormal mx (E = 0) clamps below
+        e = e < -126 ? -126 : (e > 126 ? 126 : e);
+        s = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e, a normal float
+      }
+      sigma[blk] = s;
+    }
+    __syncthreads();
+  }
+}
+
+dash_status launch_diag_pow2_scale(const float* A, float ridge, int dim, long long nblocks,
+                                   float* sigma, cudaStream_t st) {
+  if (nblocks <= 0) return DASH_OK;
+  const long long cap = static_cast<long long>(device_sm_count()) * 16;
+  const long long grid = nblocks < cap ? nblocks : (cap > 0 ? cap : 1);
+  const int rec = trace_begin(st);
+  diag_pow2_kernel<<<static_cast<unsigned>(grid), EW_THREADS, 0, st>>>(A, ridge, dim, nblocks, sigma);
+  const cudaError_t err = cudaGetLastError();
+  trace_end(rec, st, DASH_TRACE_REDUCE, 0.0, 4.0 * dim * nblocks + 4.0 * nblocks);
+  return err == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
+}
+
 __global__ void power_finish_kernel(const float* num, const float* den, int nv, long long nblocks,
-                                    float* lambda) {
+                                    const float* blk_scale, float* lambda) {
   const long long k = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (k >= nblocks) return;
   float best = -INFINITY;
   for (int c = 0; c < nv; ++c) best = fmaxf(best, num[k * PW_NV + c] / den[k * PW_NV + c]);
-  lambda[k] = best;
+  // A power-of-two scale divides out exactly.
+  lambda[k] = (blk_scale != nullptr) ? best / blk_scale[k] : best;
 }
 
 dash_status launch_power_finish(const float* num, const float* den, int nv, long long nblocks,
-                                float* lambda, cudaStream_t st) {
+                                const float* blk_scale, float* lambda, cudaStream_t st) {
   if (nblocks <= 0) return DASH_OK;
   const int rec = trace_begin(st);
-  power_finish_kernel<<<static_cast<unsigned>((nblocks + 127) / 128), 128, 0, st>>>(num, den, nv,
-                                                                                    nblocks, lambda);
+  power_finish_kernel<<<static_cast<unsigned>((nblocks + 127) / 128), 128, 0, st>>>(
+      num, den, nv, nblocks, blk_scale, lambda);
   const cudaError_t err = cudaGetLastError();
   trace_end(rec, st, DASH_TRACE_REDUCE, 0.0, 8.0 * 32 * nblocks);
   return err == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;

@@ -150,13 +150,22 @@ __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
 struct TileEpi {
   float m[3];
   int pv;
+  uint32_t plain;  // bit o: output o is the accumulator itself (D = C)
 };
 
 __device__ __forceinline__ TileEpi tile_epi(const EpiParams& e, long long blk) {
   TileEpi t;
+  t.plain = 0u;
 #pragma unroll
-  for (int o = 0; o < 3; ++o)
+  for (int o = 0; o < 3; ++o) {
     t.m[o] = (o < e.nout && e.out[o].mult != nullptr) ? e.out[o].mult[blk] : 1.0f;
+    if (o < e.nout) {
+      const EpiOut& O = e.out[o];
+      if (O.alpha == 1.0f && O.gamma == 0.0f && (O.eps == 0.0f || e.E_hi == nullptr) &&
+          t.m[o] == 1.0f && e.pad_valid == nullptr)
+        t.plain |= 1u << o;
+    }
+  }
   t.pv = (e.pad_valid != nullptr) ? e.pad_valid[blk] : 0x7fffffff;
   return t;
 }
@@ -205,6 +214,12 @@ __device__ __forceinline__ void epi_out16(const EpiParams& e, const TileEpi& te,
                                           bool diag, float (&d)[16]) {
   const EpiOut& O = e.out[o];
   const float m = te.m[o];
+  if ((te.plain >> o) & 1u) {
+    // alpha 1, no gamma, E or multiplier: the products' sum as it stands.
+#pragma unroll
+    for (int j = 0; j < 16; ++j) d[j] = c[j];
+    return;
+  }
   if (!diag && e.pad_valid == nullptr) {
 #pragma unroll
     for (int j = 0; j < 16; ++j) d[j] = m * fmaf(O.alpha, c[j], O.eps * ev[j]);

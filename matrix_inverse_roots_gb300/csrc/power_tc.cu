@@ -423,6 +423,7 @@ struct PowerHalfParams {
   int nkb;
   uint32_t idesc;
   float ridge;
+  const float* blk_scale;  // (nblocks) power-of-two scale of each 16-bit block, or null
   const uint16_t* Vt_in;  // (nblocks, 32, dim): previous vectors, transposed
   const float* in_nrm2;   // (nblocks, 32) or null
   uint16_t* Vt_out;       // (nblocks, 32, dim); unused on the last product
@@ -600,10 +601,12 @@ __global__ void __launch_bounds__(PH_THREADS, 1)
       float w[PT_NV], v[PT_NV];
 #pragma unroll
       for (int c = 0; c < PT_NV; ++c) v[c] = h16_to_f<BF>(vin[static_cast<long long>(c) * p.dim]) * sc[c];
+      // The 16-bit copy holds sigma A, so the ridge term is sigma ridge.
+      const float rb = (p.blk_scale != nullptr) ? p.ridge * p.blk_scale[blk] : p.ridge;
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
-        w[c] = fmaf(p.ridge, v[c], __uint_as_float(r0[c]) * sc[c]);
-        w[16 + c] = fmaf(p.ridge, v[16 + c], __uint_as_float(r1[c]) * sc[16 + c]);
+        w[c] = fmaf(rb, v[c], __uint_as_float(r0[c]) * sc[c]);
+        w[16 + c] = fmaf(rb, v[16 + c], __uint_as_float(r1[c]) * sc[16 + c]);
       }
       float s0[PT_NV], s1[PT_NV];
       if (p.last) {
@@ -688,8 +691,8 @@ bool map_3d_h16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer
 
 }  // namespace
 
-dash_status launch_power_step_half(const void* Ah, int bf16, float ridge, int dim,
-                                   long long nblocks, const uint16_t* Vt_in, int nv,
+dash_status launch_power_step_half(const void* Ah, int bf16, float ridge, const float* blk_scale,
+                                   int dim, long long nblocks, const uint16_t* Vt_in, int nv,
                                    const float* in_nrm2, uint16_t* Vt_out, float* acc0,
                                    float* acc1, int last, cudaStream_t st) {
   if (nblocks <= 0) return DASH_OK;
@@ -702,6 +705,7 @@ dash_status launch_power_step_half(const void* Ah, int bf16, float ridge, int di
   p.nkb = dim / PH_BK;
   p.idesc = make_idesc(bf16 ? 1u : 0u, 0, 0, PT_BM, PT_NV);
   p.ridge = ridge;
+  p.blk_scale = blk_scale;
   p.Vt_in = Vt_in;
   p.in_nrm2 = in_nrm2;
   p.Vt_out = Vt_out;

@@ -66,7 +66,8 @@ def test_power_lambda_half(name, dt, u, b, n):
     for iters, nv in ((10, 32), (3, 7)):
         V = V0[:, :, :nv].contiguous()
         lam = to64(dr.spectral_scale(A, mode, V, iters, ridge=0.2))
-        Ah = to64(A.to(dt))
+        sig = half_power_sigma(A, 0.2)
+        Ah = to64((A * sig[:, None, None]).to(dt)) / to64(sig)[:, None, None]
         ref_h = oracle.power_lambda(Ah, to64(V), iters, ridge=0.2)
         err_h = np.abs(lam - ref_h) / ref_h
         print("%s B=%d iters=%d nv=%d: vs oracle on the 16-bit A %.2e" % (
@@ -75,6 +76,45 @@ def test_power_lambda_half(name, dt, u, b, n):
         ref = oracle.power_lambda(to64(A), to64(V), iters, ridge=0.2)
         bound = u * np.linalg.norm(to64(A).reshape(n, -1), axis=1) / ref
         assert np.all(np.abs(lam - ref) / ref <= bound + 4 * u)
+    assert dr.device_status() == 0
+
+
+def half_power_sigma(A, ridge):
+    """The exact power of two the half modes scale each block by, as the header
+    states it: 2^-e with max(max_i |A_ii|, |ridge|) = f 2^e, f in [1/2, 1)."""
+    m = np.maximum(np.abs(np.diagonal(to64(A), axis1=1, axis2=2)).max(axis=1), abs(ridge))
+    _, e = np.frexp(m)
+    e = np.clip(e, -126, 126)
+    return torch.tensor(np.ldexp(1.0, -e), dtype=torch.float32, device=A.device)
+
+
+@pytest.mark.parametrize("name,dt,u", HALF_MODES)
+def test_power_half_scale_invariant(name, dt, u):
+    """The half modes store sigma A with sigma an exact power of two, so the 16-bit
+    copy of 2^k A (ridge 2^k r) is bit for bit that of A, and lambda scales by 2^k
+    up to the order of the fp32 column-sum atomics.  At k = -40 an unscaled fp16
+    copy of A would be all zeros (lambda = the ridge alone) and at k = 20 it would
+    overflow to inf, so each scaled run is checked against the oracle at its own
+    scale with the bound of test_power_lambda_half."""
+    require_gpu()
+    dr = library()
+    mode = dr.SCALE_POWER_F16 if name == "fp16" else dr.SCALE_POWER_BF16
+    A, V0 = wishart_case(4, 256, 2200)
+    ref0 = oracle.power_lambda(to64(A), to64(V0), 10, ridge=0.2)
+    bound = u * np.linalg.norm(to64(A).reshape(4, -1), axis=1) / ref0 + 4 * u
+    lam0 = to64(dr.spectral_scale(A, mode, V0, 10, ridge=0.2))
+    for k in (0, -40, -20, 20):
+        Ak = A * 2.0 ** k
+        if k == -40:
+            assert torch.count_nonzero(Ak.half()) == 0
+        if k == 20:
+            assert not torch.isfinite(Ak.half()).all()
+        lam = to64(dr.spectral_scale(Ak, mode, V0, 10, ridge=0.2 * 2.0 ** k))
+        ref = ref0 * 2.0 ** k
+        err = np.abs(lam - ref) / ref
+        print("%s k=%d: vs oracle %.2e, vs k=0 run %.2e" % (
+            name, k, err.max(), np.max(np.abs(lam / 2.0 ** k - lam0) / lam0)))
+        assert np.all(err <= bound), (k, err, bound)
     assert dr.device_status() == 0
 
 
