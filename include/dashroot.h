@@ -123,8 +123,8 @@ dash_status shampoo_accumulate(const void* G, int gdt, int64_t Ng, int B, float 
  *     after the last, lambda_out[k] = max_j (v_j . w_j) / (v_j . v_j).
  *     1 <= n_vec <= 32, power_iters >= 1, V0 (N, B, n_vec) fp32.
  *   mode DASH_SCALE_POWER_F16 / _BF16: the same iteration in half precision
- *     ([pt] Principais Contribuicoes item 4, "an efficient half-precision
- *     Power-Iteration"): sigma_k A_k is rounded once to fp16 / bf16, each product
+ *     ([pt] Principais Contribuicoes item 4, the half-precision power iteration
+ *     among the contributions): sigma_k A_k is rounded once to fp16 / bf16, each product
  *     takes 16-bit A and 16-bit vectors with fp32 accumulation, the ridge term
  *     (sigma_k ridge), the column normalisation and the Rayleigh quotients are
  *     fp32, the vectors are stored in the 16-bit format between products, and the

@@ -15,7 +15,7 @@ what the pages say about it):
 Scaling.  Every iterative solver works on A_s = (A + ridge I) / s, where s is
 the per-block scale (a power-iteration lambda_max estimate or the Frobenius
 norm), so that the spectrum sits near (0, 1] ([pt] Metodologia 2: the scale
-keeps eigenvalues "close to 1").  The result is s^{-1/4} times the solver's
+brings the eigenvalues near 1).  The result is s^{-1/4} times the solver's
 root of A_s.
 
 Coupled Newton, p = 4 (the coupled inverse p-th root iteration of Guo and
