@@ -102,7 +102,14 @@ typedef enum {
  *   G           (Ng, B, B) gradient blocks, dtype gdt (DASH_DT_BF16 runs
  *               bf16 tensor-core products, exact products with fp32
  *               accumulation; DASH_DT_F32 runs 3xTF32).
- *   F           (2*Ng, B, B) fp32 factors, updated IN PLACE.
+ *   F           (2*Ng, B, B) fp32 factors, updated IN PLACE.  Factors are
+ *               symmetric: for B a multiple of 256 only the 256 x 256 tiles on or
+ *               above the diagonal are computed (reading only those of the old
+ *               F), and each tile below is then written as the transpose of its
+ *               mirror (SYRK-style: 10 of 16 tiles at B = 1024).  With bf16 / fp16
+ *               gradients the result is exactly symmetric; with fp32 gradients
+ *               (3xTF32) the diagonal tiles, computed whole, are symmetric to
+ *               rounding.  Other B compute every element.
  *   valid_rows, valid_cols  (Ng,) int32 device arrays, or NULL (= B).
  *   ws/ws_bytes workspace; only DASH_DT_F32 needs one (see dash_workspace_size).
  */

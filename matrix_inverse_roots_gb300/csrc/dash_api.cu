@@ -167,11 +167,13 @@ AffParams aff_from(const void* src_hi, const void* src_lo, int src_fmt, int B, l
 
 // One GEMM launch C = X * Y over nc blocks in precision prec.
 // sym: 0 plain; 1 symmetric operands (only their tiles on or above the diagonal
-// are read); 2 also a symmetric result (only those tiles computed and stored).
+// are read); 2 also a symmetric result (only those tiles computed and stored);
+// 3 a symmetric result from operands read whole (X Y^T with Y = X, or X^T X).
+// Modes 1-3 take effect for B a multiple of 256 (CTA-pair kernels).
 dash_status gemm(int prec, int B, long long nc, const Buf& X, int tX, const Buf& Y, int tY,
                  const EpiParams& e, cudaStream_t st, int sym = 0) {
   GemmLaunch g;
-  g.sym_in = (sym >= 1) ? 1 : 0;
+  g.sym_in = (sym == 1 || sym == 2) ? 1 : 0;
   g.sym_out = (sym >= 2) ? 1 : 0;
   g.kind = prec_kind(prec);
   g.dim = B;
@@ -346,6 +348,10 @@ dash_status shampoo_accumulate(const void* G, int gdt, int64_t Ng, int B, float 
     if (!cv.ok) return DASH_ERR_WORKSPACE_TOO_SMALL;
   }
   const size_t gsz = (gdt == DASH_DT_F32) ? 4 : 2;
+  // G G^T and G^T G are symmetric, and so is every factor: for B a multiple of 256
+  // only the 256-tiles on or above the diagonal are computed (reading those of the
+  // old F), and the tiles below are then filled with their mirrors' transposes.
+  const int SO = (B % 256 == 0) ? 3 : 0;
   for (long long c0 = 0; c0 < Ng; c0 += chunk) {
     const long long nc = (Ng - c0 < chunk) ? Ng - c0 : chunk;
     Buf g;
@@ -368,12 +374,14 @@ dash_status shampoo_accumulate(const void* G, int gdt, int64_t Ng, int B, float 
     e.out[0] = eout_f32(FL, 1.0f - beta, 0.0f, beta, nullptr);
     e.E_hi = FL;
     e.pad_valid = valid_rows ? valid_rows + c0 : nullptr;
-    DASH_TRY(gemm(gprec, B, nc, g, 0, g, 1, e, st));
+    DASH_TRY(gemm(gprec, B, nc, g, 0, g, 1, e, st, SO));
+    if (SO) DASH_TRY(launch_mirror_lower(FL, B, nc, st));
     // R_j = beta R_j + (1 - beta) G^T G
     e.out[0] = eout_f32(FR, 1.0f - beta, 0.0f, beta, nullptr);
     e.E_hi = FR;
     e.pad_valid = valid_cols ? valid_cols + c0 : nullptr;
-    DASH_TRY(gemm(gprec, B, nc, g, 1, g, 0, e, st));
+    DASH_TRY(gemm(gprec, B, nc, g, 1, g, 0, e, st, SO));
+    if (SO) DASH_TRY(launch_mirror_lower(FR, B, nc, st));
   }
   return DASH_OK;
 }

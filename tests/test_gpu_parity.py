@@ -243,10 +243,11 @@ def test_accumulate_bf16_with_padding():
     assert dr.device_status() == 0
 
 
-def test_accumulate_fp32_gradients():
+@pytest.mark.parametrize("b", [128, 256, 512])
+def test_accumulate_fp32_gradients(b):
     require_gpu()
     dr = library()
-    ng, b = 3, 128
+    ng = 3
     G = torch.randn((ng, b, b), device="cuda")
     F = torch.zeros((2 * ng, b, b), device="cuda")
     dr.shampoo_accumulate(G, F, 0.9)
@@ -255,6 +256,49 @@ def test_accumulate_fp32_gradients():
     ref = oracle.accumulate(np.zeros((2 * ng, b, b)), to64(G), 0.9)
     ref = oracle.accumulate(ref, to64(G), 0.9)
     assert rel_fro_blocks(to64(F), ref).max() < 1e-5
+    # A 3xTF32 product adds its two cross terms in opposite orders for (i, j) and
+    # (j, i), so tiles computed whole are symmetric to rounding only; the lower
+    # 256-tiles of the mirrored path are their mirrors' transposes exactly.
+    assert torch.allclose(F, F.transpose(1, 2), rtol=1e-6, atol=1e-6 * float(F.abs().max()))
+    t = b // 256
+    for i in range(t):
+        for j in range(i):
+            lo = F[:, i * 256:(i + 1) * 256, j * 256:(j + 1) * 256]
+            up = F[:, j * 256:(j + 1) * 256, i * 256:(i + 1) * 256]
+            assert torch.equal(lo, up.transpose(1, 2)), (i, j)
+
+
+def test_accumulate_symmetric_tiles_with_padding():
+    """For B a multiple of 256 the factors' upper 256-tiles are computed and the
+    lower ones mirrored (SYRK-style).  Checked at B = 768 (3 x 3 tiles), with
+    padded rows / columns that cut across tile boundaries: oracle parity, exact
+    symmetry, and the identity on the padded part, below the diagonal too."""
+    require_gpu()
+    dr = library()
+    ng, b = 3, 768
+    g = torch.Generator(device="cuda")
+    g.manual_seed(78)
+    G = (0.1 * torch.randn((ng, b, b), generator=g, device="cuda")).to(torch.bfloat16)
+    vr = torch.tensor([768, 300, 520], dtype=torch.int32, device="cuda")
+    vc = torch.tensor([700, 768, 256], dtype=torch.int32, device="cuda")
+    for j in range(ng):
+        G[j, int(vr[j]):, :] = 0
+        G[j, :, int(vc[j]):] = 0
+    F0 = torch.randn((2 * ng, b, b), generator=g, device="cuda")
+    F0 = 0.5 * (F0 + F0.transpose(1, 2))
+    F = F0.clone()
+    for _ in range(2):
+        dr.shampoo_accumulate(G, F, 0.95, vr, vc)
+    torch.cuda.synchronize()
+    ref = oracle.accumulate(to64(F0), to64(G), 0.95, vr.tolist(), vc.tolist())
+    ref = oracle.accumulate(ref, to64(G), 0.95, vr.tolist(), vc.tolist())
+    assert rel_fro_blocks(to64(F), ref).max() < 1e-5
+    assert torch.equal(F, F.transpose(1, 2))
+    Fh = F.cpu()
+    assert torch.equal(Fh[1, 300:, 300:], torch.eye(468))
+    assert torch.equal(Fh[1, 300:, :300], torch.zeros(468, 300))
+    assert torch.equal(Fh[ng + 2, 256:, 256:], torch.eye(512))
+    assert dr.device_status() == 0
 
 
 @pytest.mark.parametrize("prec", PRECS)
