@@ -40,6 +40,8 @@ from .roots64 import (
     cheb_coeffs,
     cheb_inv_root,
 )
+from .select64 import (DEFAULT_TIERS, auto_inv_root, condition_estimate, lambda_min_estimate,
+                       select_tiers)
 
 __all__ = [
     "accumulate",
@@ -54,4 +56,9 @@ __all__ = [
     "pack_blocks",
     "unpack_blocks",
     "update_weights",
+    "DEFAULT_TIERS",
+    "lambda_min_estimate",
+    "condition_estimate",
+    "select_tiers",
+    "auto_inv_root",
 ]
