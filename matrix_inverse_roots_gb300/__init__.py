@@ -143,6 +143,23 @@ def _stack(t, name, dtype=torch.float32):
     return t
 
 
+def _shape(t, shape, name):
+    """Sizes the kernels will index: a wrong one would read or write past t."""
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+    return t
+
+
+def _blocks3(t, name):
+    if t.dim() != 3 or t.shape[1] != t.shape[2]:
+        raise ValueError("%s must be a (N, B, B) stack, got %s" % (name, tuple(t.shape)))
+    return t.shape[0], t.shape[1]
+
+
+def _nbytes(ws):
+    return 0 if ws is None else ws.numel() * ws.element_size()
+
+
 def _gdt(t):
     if t.dtype == torch.float32:
         return DT_F32
@@ -224,18 +241,18 @@ def selftest_wait_timeout(limit_us=50000):
 def shampoo_accumulate(G, F, beta, valid_rows=None, valid_cols=None, ws=None):
     """In place: F[j] <- beta F[j] + (1-beta) G_j G_j^T, F[Ng+j] likewise with G_j^T G_j."""
     lib = load_library()
-    ng, b, _ = G.shape
     _stack(G, "G", G.dtype)
-    _stack(F, "F")
-    if F.shape != (2 * ng, b, b):
-        raise ValueError("F must have shape (2*Ng, B, B)")
+    ng, b = _blocks3(G, "G")
+    _shape(_stack(F, "F"), (2 * ng, b, b), "F")
     gdt = _gdt(G)
     if ws is None and gdt == DT_F32:
         ws = workspace(OP_ACCUMULATE, ng, b, FP32_3XTF32, device=G.device)
-    vr = None if valid_rows is None else _stack(valid_rows, "valid_rows", torch.int32)
-    vc = None if valid_cols is None else _stack(valid_cols, "valid_cols", torch.int32)
+    vr = None if valid_rows is None else _shape(_stack(valid_rows, "valid_rows", torch.int32),
+                                                (ng,), "valid_rows")
+    vc = None if valid_cols is None else _shape(_stack(valid_cols, "valid_cols", torch.int32),
+                                                (ng,), "valid_cols")
     _check(lib.shampoo_accumulate(_ptr(G), gdt, ng, b, float(beta), _ptr(F), _ptr(vr), _ptr(vc),
-                                  _ptr(ws), 0 if ws is None else ws.numel(), _stream()),
+                                  _ptr(ws), _nbytes(ws), _stream()),
            "shampoo_accumulate")
     return F
 
@@ -244,20 +261,21 @@ def spectral_scale(A, mode=SCALE_POWER, V0=None, power_iters=10, ridge=0.0, out=
     """Per-block scale: multi-vector power-iteration lambda_max or Frobenius norm."""
     lib = load_library()
     _stack(A, "A")
-    n, b, _ = A.shape
+    n, b = _blocks3(A, "A")
     nv = 0
     if mode != SCALE_FROBENIUS:
         _stack(V0, "V0")
-        if V0.shape[0] != n or V0.shape[1] != b:
+        if V0.dim() != 3 or V0.shape[0] != n or V0.shape[1] != b:
             raise ValueError("V0 must have shape (N, B, n_vec)")
         nv = V0.shape[2]
     if out is None:
         out = torch.empty(n, dtype=torch.float32, device=A.device)
+    _shape(_stack(out, "out"), (n,), "out")
     if ws is None:
         ws = workspace(OP_SPECTRAL_SCALE, n, b, _HALF_SCALE.get(mode, FP32_3XTF32), nv,
                        device=A.device)
     _check(lib.spectral_scale(_ptr(A), float(ridge), n, b, int(mode), nv, int(power_iters),
-                              _ptr(V0), _ptr(out), _ptr(ws), ws.numel(), _stream()),
+                              _ptr(V0), _ptr(out), _ptr(ws), _nbytes(ws), _stream()),
            "spectral_scale")
     return out
 
@@ -274,15 +292,16 @@ def spectral_scale_noalloc(A, mode=SCALE_POWER, V0=None, power_iters=10, ridge=0
     concurrently.  `out` lets the caller avoid this wrapper's own allocation."""
     lib = load_library()
     _stack(A, "A")
-    n, b, _ = A.shape
+    n, b = _blocks3(A, "A")
     nv = 0
     if mode != SCALE_FROBENIUS:
         _stack(V0, "V0")
-        if V0.shape[0] != n or V0.shape[1] != b:
+        if V0.dim() != 3 or V0.shape[0] != n or V0.shape[1] != b:
             raise ValueError("V0 must have shape (N, B, n_vec)")
         nv = V0.shape[2]
     if out is None:
         out = torch.empty(n, dtype=torch.float32, device=A.device)
+    _shape(_stack(out, "out"), (n,), "out")
     _check(lib.spectral_scale_noalloc(_ptr(A), float(ridge), n, b, int(mode), nv,
                                       int(power_iters), _ptr(V0), _ptr(out), _stream()),
            "spectral_scale_noalloc")
@@ -291,13 +310,11 @@ def spectral_scale_noalloc(A, mode=SCALE_POWER, V0=None, power_iters=10, ridge=0
 
 def _root_common(A, scale, X):
     _stack(A, "A")
-    n, b, _ = A.shape
-    _stack(scale, "scale")
-    if scale.shape != (n,):
-        raise ValueError("scale must have shape (N,)")
+    n, b = _blocks3(A, "A")
+    _shape(_stack(scale, "scale"), (n,), "scale")
     if X is None:
         X = torch.empty_like(A)
-    _stack(X, "X")
+    _shape(_stack(X, "X"), (n, b, b), "X")
     return n, b, X
 
 
@@ -306,11 +323,11 @@ def inv_root_cn(A, scale, iters=10, prec=FP32_3XTF32, ridge=0.0, X=None, resid=F
     lib = load_library()
     n, b, X = _root_common(A, scale, X)
     p = _prec(prec)
-    r = torch.empty((n, iters), dtype=torch.float32, device=A.device) if resid else None
+    r = torch.empty((n, int(iters)), dtype=torch.float32, device=A.device) if resid else None
     if ws is None:
         ws = workspace(OP_INV_ROOT_CN, n, b, p, iters, device=A.device)
     _check(lib.inv_root_cn(_ptr(A), float(ridge), _ptr(scale), n, b, int(iters), p, _ptr(X),
-                           _ptr(r), _ptr(ws), ws.numel(), _stream()), "inv_root_cn")
+                           _ptr(r), _ptr(ws), _nbytes(ws), _stream()), "inv_root_cn")
     return (X, r) if resid else X
 
 
@@ -319,11 +336,11 @@ def inv_root_ndb(A, scale, iters=10, prec=FP32_3XTF32, ridge=0.0, X=None, resid=
     lib = load_library()
     n, b, X = _root_common(A, scale, X)
     p = _prec(prec)
-    r = torch.empty((n, 2, iters), dtype=torch.float32, device=A.device) if resid else None
+    r = torch.empty((n, 2, int(iters)), dtype=torch.float32, device=A.device) if resid else None
     if ws is None:
         ws = workspace(OP_INV_ROOT_NDB, n, b, p, iters, device=A.device)
     _check(lib.inv_root_ndb(_ptr(A), float(ridge), _ptr(scale), n, b, int(iters), p, _ptr(X),
-                            _ptr(r), _ptr(ws), ws.numel(), _stream()), "inv_root_ndb")
+                            _ptr(r), _ptr(ws), _nbytes(ws), _stream()), "inv_root_ndb")
     return (X, r) if resid else X
 
 
@@ -336,7 +353,7 @@ def inv_root_cheb(A, scale, degree=16, lo=1e-2, hi=1.05, prec=FP32_3XTF32, ridge
     if ws is None:
         ws = workspace(OP_INV_ROOT_CHEB, n, b, p, degree, device=A.device)
     _check(lib.inv_root_cheb(_ptr(A), float(ridge), _ptr(scale), n, b, int(degree), float(lo),
-                             float(hi), p, _ptr(X), _ptr(ws), ws.numel(), _stream()),
+                             float(hi), p, _ptr(X), _ptr(ws), _nbytes(ws), _stream()),
            "inv_root_cheb")
     return X
 
@@ -345,17 +362,16 @@ def precondition_apply(G, Froot, prec=FP32_3XTF32, U=None, ws=None):
     """U_j = Froot[j] G_j Froot[Ng + j]."""
     lib = load_library()
     _stack(G, "G", G.dtype)
-    ng, b, _ = G.shape
-    _stack(Froot, "Froot")
-    if Froot.shape != (2 * ng, b, b):
-        raise ValueError("Froot must have shape (2*Ng, B, B)")
+    ng, b = _blocks3(G, "G")
+    _shape(_stack(Froot, "Froot"), (2 * ng, b, b), "Froot")
     p = _prec(prec)
     if U is None:
         U = torch.empty((ng, b, b), dtype=torch.float32, device=G.device)
+    _shape(_stack(U, "U"), (ng, b, b), "U")
     if ws is None:
         ws = workspace(OP_PRECONDITION_APPLY, ng, b, p, device=G.device)
     _check(lib.precondition_apply(_ptr(G), _gdt(G), _ptr(Froot), ng, b, p, _ptr(U), _ptr(ws),
-                                  ws.numel(), _stream()), "precondition_apply")
+                                  _nbytes(ws), _stream()), "precondition_apply")
     return U
 
 
@@ -363,18 +379,16 @@ def precondition_update(G, Froot, W, lr, prec=FP32_3XTF32, U=None, ws=None):
     """W_j -= lr * Froot[j] G_j Froot[Ng + j], in place on W (Ng, B, B) fp32; U optional."""
     lib = load_library()
     _stack(G, "G", G.dtype)
-    ng, b, _ = G.shape
-    _stack(Froot, "Froot")
-    _stack(W, "W")
-    if Froot.shape != (2 * ng, b, b) or W.shape != (ng, b, b):
-        raise ValueError("Froot must be (2*Ng, B, B) and W (Ng, B, B)")
+    ng, b = _blocks3(G, "G")
+    _shape(_stack(Froot, "Froot"), (2 * ng, b, b), "Froot")
+    _shape(_stack(W, "W"), (ng, b, b), "W")
     p = _prec(prec)
     if U is not None:
-        _stack(U, "U")
+        _shape(_stack(U, "U"), (ng, b, b), "U")
     if ws is None:
         ws = workspace(OP_PRECONDITION_APPLY, ng, b, p, device=G.device)
     _check(lib.precondition_update(_ptr(G), _gdt(G), _ptr(Froot), ng, b, p, float(lr), _ptr(W),
-                                   _ptr(U), _ptr(ws), ws.numel(), _stream()),
+                                   _ptr(U), _ptr(ws), _nbytes(ws), _stream()),
            "precondition_update")
     return W
 
@@ -397,7 +411,7 @@ def pack_blocks(M, B, out=None, valid=True):
     nb = -(-rows // B) * -(-cols // B)
     if out is None:
         out = torch.empty((nb, B, B), dtype=M.dtype, device=M.device)
-    _stack(out, "out", M.dtype)
+    _shape(_stack(out, "out", M.dtype), (nb, B, B), "out")
     vr = torch.empty(nb, dtype=torch.int32, device=M.device) if valid else None
     vc = torch.empty(nb, dtype=torch.int32, device=M.device) if valid else None
     _check(lib.pack_blocks(_ptr(M), _gdt(M), rows, cols, M.stride(0), B, _ptr(out), _ptr(vr),
@@ -410,7 +424,11 @@ def unpack_blocks(blocks, rows, cols, out=None):
     dropped); `out` may be a row-strided 2-D view."""
     lib = load_library()
     _stack(blocks, "blocks", blocks.dtype)
-    B = blocks.shape[1]
+    _, B = _blocks3(blocks, "blocks")
+    nb = -(-rows // B) * -(-cols // B)
+    if blocks.shape[0] < nb:
+        raise ValueError("blocks holds %d blocks, a (%d, %d) matrix needs %d"
+                         % (blocks.shape[0], rows, cols, nb))
     if out is None:
         out = torch.empty((rows, cols), dtype=blocks.dtype, device=blocks.device)
     _matrix(out, "out")
@@ -425,9 +443,15 @@ def gemm(A, B, prec=TF32, trans_a=False, trans_b=False, A_lo=None, B_lo=None, C=
     """C[k] = op(A[k]) op(B[k]) on the tensor cores; operands already in prec's format."""
     lib = load_library()
     p = _prec(prec)
-    n, b, _ = A.shape
+    _stack(A, "A", A.dtype)
+    n, b = _blocks3(A, "A")
+    _shape(_stack(B, "B", A.dtype), (n, b, b), "B")
+    for t, name in ((A_lo, "A_lo"), (B_lo, "B_lo")):
+        if t is not None:
+            _shape(_stack(t, name, A.dtype), (n, b, b), name)
     if C is None:
         C = torch.empty((n, b, b), dtype=torch.float32, device=A.device)
+    _shape(_stack(C, "C"), (n, b, b), "C")
     _check(lib.dash_gemm(_ptr(A), _ptr(A_lo), int(bool(trans_a)), _ptr(B), _ptr(B_lo),
                          int(bool(trans_b)), n, b, p, _ptr(C), _stream()), "dash_gemm")
     return C

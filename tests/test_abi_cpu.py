@@ -133,3 +133,35 @@ def test_workspace_too_small_reported():
     # Half-precision power: one block's 16-bit copy (2 MiB at B = 1024) does not fit.
     assert lib.spectral_scale(p, 0.0, 4, 1024, dr.SCALE_POWER_F16, 32, 10, p, p, p, 4096,
                               None) == 4
+
+
+def test_binding_shape_checks():
+    """The binding rejects sizes the kernels would index past, before any call."""
+    import torch
+
+    dr = library()
+    t = torch.empty((3, 4, 4))
+    assert dr._shape(t, (3, 4, 4), "t") is t
+    with pytest.raises(ValueError, match="must have shape"):
+        dr._shape(t, (2, 4, 4), "t")
+    assert dr._blocks3(t, "t") == (3, 4)
+    for bad in (torch.empty((3, 4, 5)), torch.empty((4, 4))):
+        with pytest.raises(ValueError, match="stack"):
+            dr._blocks3(bad, "t")
+    assert dr._nbytes(None) == 0
+    assert dr._nbytes(torch.empty(10, dtype=torch.float32)) == 40
+    assert dr._nbytes(torch.empty(10, dtype=torch.uint8)) == 10
+
+
+def test_binding_requires_cuda_tensors():
+    import torch
+
+    dr = library()
+    G = torch.zeros((2, 128, 128), dtype=torch.bfloat16)
+    F = torch.zeros((4, 128, 128))
+    with pytest.raises(TypeError, match="CUDA"):
+        dr.shampoo_accumulate(G, F, 0.9)
+    with pytest.raises(TypeError, match="CUDA"):
+        dr.inv_root_cn(F, torch.ones(4), 3)
+    with pytest.raises(TypeError, match="CUDA"):
+        dr.gemm(F, F)
