@@ -162,8 +162,11 @@ dash_status spectral_scale(const float* A, float ridge, int64_t N, int B, int mo
  *   X_0 = I, M_0 = A_s;  T_i = (5I - M_i)/4;  X_{i+1} = X_i T_i;
  *   M_{i+1} = (T_i^2)^2 M_i;   X[k] = scale[k]^{-1/4} X_iters.
  * 4*iters - 4 products per block for iters >= 2, none for iters = 1 (iteration 0
- * needs no X product, the last no
- * M update).
+ * needs no X product, the last no M update).  Every iterate is a polynomial in
+ * the symmetric A_s, so for B a multiple of 256 each product computes and stores
+ * only its 256 x 256 tiles on or above the diagonal (10 of 16 at B = 1024); X's
+ * tiles below the diagonal are written as their mirrors' transposes.  A's tiles
+ * below the diagonal then do not affect X, so A must be symmetric, as a factor is.
  *   A (N, B, B) fp32; scale (N,) fp32 > 0 (e.g. from spectral_scale);
  *   iters >= 1; prec any dash_prec; X (N, B, B) fp32 output;
  *   resid_out (N, iters) fp32 or NULL: resid_out[k*iters + i] =
@@ -199,7 +202,8 @@ dash_status inv_root_ndb(const float* A, float ridge, const float* scale, int64_
  * the host in double); S = (2 A_s - (lo+hi) I)/(hi - lo);
  *   b_{d+1} = b_{d+2} = 0, b_j = c_j I + 2 S b_{j+1} - b_{j+2},
  *   P = c_0 I + S b_1 - b_2,  X[k] = scale[k]^{-1/4} P.
- * d - 1 products per block.  1 <= degree <= 64, 0 < lo < hi.
+ * d - 1 products per block.  1 <= degree <= 64, 0 < lo < hi.  For B a multiple
+ * of 256 every product keeps symmetric halves as in inv_root_cn.
  */
 dash_status inv_root_cheb(const float* A, float ridge, const float* scale, int64_t N, int B,
                           int degree, double lo, double hi, int prec, float* X, void* ws,
