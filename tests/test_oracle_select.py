@@ -95,3 +95,20 @@ def test_auto_root_picks_and_solves_per_block():
     # Each block is exactly its tier's solver with that tier's iteration count.
     assert np.array_equal(X[1], oracle.cn_inv_root(A[1:], lam[1:], 24)[0][0])
     assert np.array_equal(X[0], oracle.cn_inv_root(A[:1], lam[:1], 10)[0][0])
+
+
+def test_planted_mistakes_fail_the_pins():
+    """Slipped versions of the selection steps disagree with what the pins fix."""
+    a, b, ridge, c = 1.0, 0.25, 0.05, 1.2
+    A = np.diag([a, b])[None]
+    V0 = np.ones((1, 2, 1))
+    got = oracle.lambda_min_estimate(A, np.array([c]), V0, 3, ridge=ridge)[0]
+    # Dropping the ridge from the shift, or returning mu instead of c - mu.
+    no_ridge = oracle.lambda_min_estimate(A, np.array([c]), V0, 3, ridge=0.0)[0]
+    assert abs(no_ridge - got) > 1e-3
+    mu = c - got
+    assert abs(mu - got) > 1e-3
+    # kappa u / 2 instead of kappa u / 4 moves the tier boundary.
+    t0 = oracle.DEFAULT_TIERS[0]
+    edge = 4.0 * t0["gate"] / t0["u"]
+    assert edge * t0["u"] / 2.0 > t0["gate"] and oracle.select_tiers([edge])[0] == 0
