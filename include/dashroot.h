@@ -148,7 +148,8 @@ dash_status shampoo_accumulate(const void* G, int gdt, int64_t Ng, int B, float 
  *   partial sums.
  * Workspace: dash_workspace_size(DASH_OP_SPECTRAL_SCALE, N, B, prec, n_vec) with
  *   prec DASH_FP16 / DASH_BF16 for the half modes (it then includes the 16-bit
- *   copy of A, 2 B^2 bytes per block), any other prec for POWER and FROBENIUS.
+ *   copy of sigma A, 2 B^2 bytes per block, and sigma, 4 bytes per block), any
+ *   other prec for POWER and FROBENIUS.
  */
 dash_status spectral_scale(const float* A, float ridge, int64_t N, int B, int mode,
                            int n_vec, int power_iters, const float* V0,
