@@ -367,7 +367,8 @@ def roofline_from_trace(records, peaks):
                     else " x nominal tf32/bf16 ratio" + (" / 3" if dom == "gemm_3xtf32" else "")),
                 "launches": n, "avg_launch_ms": round(ms / n, 4),
                 "flops_per_launch": fl / n,
-                "traffic": gemm_traffic(fl / n, BS) if dom in ("gemm_f16", "gemm_bf16") else None}
+                # The capture measured the fp16 Coupled Newton products only.
+                "traffic": gemm_traffic(fl / n, BS) if dom == "gemm_f16" else None}
     else:
         peak = peaks["hbm_gbs"]
         achieved = b / (ms * 1e-3) / 1e9
