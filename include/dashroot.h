@@ -206,6 +206,16 @@ dash_status inv_root_ndb(const float* A, float ridge, const float* scale, int64_
  * d - 1 products per block.  1 <= degree <= 64, 0 < lo < hi.  For B a multiple
  * of 256 every product keeps symmetric halves as in inv_root_cn.
  */
+/*
+ * dash_cheb_coeffs -- the host-side coefficients inv_root_cheb uses (host code,
+ * no GPU needed): c[0..degree] of the degree-d interpolant of x^{-1/4} at the d+1
+ * first-kind Chebyshev points of [lo, hi], in the Chebyshev basis of
+ * t = (2x - lo - hi)/(hi - lo), computed in double.  c (degree + 1) is
+ * caller-owned host memory.  Same argument limits as inv_root_cheb;
+ * DASH_ERR_INVALID_ARG otherwise.
+ */
+dash_status dash_cheb_coeffs(int degree, double lo, double hi, double* c);
+
 dash_status inv_root_cheb(const float* A, float ridge, const float* scale, int64_t N, int B,
                           int degree, double lo, double hi, int prec, float* X, void* ws,
                           size_t ws_bytes, void* stream);

@@ -53,6 +53,7 @@ SYMBOLS = (
     "dash_device_status", "dash_status_string", "dash_version", "dash_trace_start",
     "dash_trace_count", "dash_trace_read", "dash_trace_stop", "spectral_scale_noalloc",
     "dash_selftest_wait_timeout", "precondition_update", "pack_blocks", "unpack_blocks",
+    "dash_cheb_coeffs",
 )
 
 _lib = None
@@ -95,6 +96,8 @@ def load_library(path=None):
     lib.dash_version.restype = ctypes.c_char_p
     lib.spectral_scale_noalloc.argtypes = [vp, f32, i64, i32, i32, i32, i32, vp, vp, vp]
     lib.spectral_scale_noalloc.restype = ctypes.c_int
+    lib.dash_cheb_coeffs.argtypes = [i32, f64, f64, ctypes.POINTER(f64)]
+    lib.dash_cheb_coeffs.restype = ctypes.c_int
     lib.dash_selftest_wait_timeout.argtypes = [i32, vp]
     lib.dash_selftest_wait_timeout.restype = ctypes.c_int
     lib.dash_trace_start.argtypes = [i32]
@@ -222,6 +225,14 @@ def trace_records():
                                    ctypes.byref(ms)), "dash_trace_read")
         out.append((TRACE_KINDS[k.value], fl.value, by.value, ms.value))
     return out
+
+
+def cheb_coeffs(degree, lo=1e-2, hi=1.05):
+    """The Chebyshev coefficients inv_root_cheb uses (computed on the host)."""
+    c = (ctypes.c_double * (int(degree) + 1))()
+    _check(load_library().dash_cheb_coeffs(int(degree), float(lo), float(hi), c),
+           "dash_cheb_coeffs")
+    return list(c)
 
 
 def op_matmuls(op, param):

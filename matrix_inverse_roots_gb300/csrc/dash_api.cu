@@ -772,20 +772,12 @@ dash_status inv_root_ndb(const float* A, float ridge, const float* scale, int64_
 
 // ---------------------------------------------------------------- Chebyshev / Clenshaw
 
-dash_status inv_root_cheb(const float* A, float ridge, const float* scale, int64_t N, int B,
-                          int degree, double lo, double hi, int prec, float* X, void* ws,
-                          size_t ws_bytes, void* stream) {
-  DASH_TRY(common_root_checks(A, scale, N, B, 1, prec, X, ws));
-  if (degree < 1 || degree > 64 || !(lo > 0.0) || !(hi > lo) || !std::isfinite(hi))
+dash_status dash_cheb_coeffs(int degree, double lo, double hi, double* c) {
+  if (degree < 1 || degree > 64 || !(lo > 0.0) || !(hi > lo) || !std::isfinite(hi) || !c)
     return DASH_ERR_INVALID_ARG;
-  if (N == 0) return DASH_OK;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int d = degree;
-  const int fmt = prec_fmt(prec);
-  const int S = sym_mode(prec, B);  // symmetric-half iterates
   // Coefficients of the degree-d interpolant of x^{-1/4} at the first-kind
   // Chebyshev points of [lo, hi], in the Chebyshev basis of t in [-1, 1].
-  std::vector<double> c(d + 1);
+  const int d = degree;
   const double pi = 3.14159265358979323846;
   for (int j = 0; j <= d; ++j) {
     double acc = 0.0;
@@ -797,6 +789,22 @@ dash_status inv_root_cheb(const float* A, float ridge, const float* scale, int64
     c[j] = 2.0 * acc / (d + 1);
   }
   c[0] *= 0.5;
+  return DASH_OK;
+}
+
+dash_status inv_root_cheb(const float* A, float ridge, const float* scale, int64_t N, int B,
+                          int degree, double lo, double hi, int prec, float* X, void* ws,
+                          size_t ws_bytes, void* stream) {
+  DASH_TRY(common_root_checks(A, scale, N, B, 1, prec, X, ws));
+  if (degree < 1 || degree > 64 || !(lo > 0.0) || !(hi > lo) || !std::isfinite(hi))
+    return DASH_ERR_INVALID_ARG;
+  if (N == 0) return DASH_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int d = degree;
+  const int fmt = prec_fmt(prec);
+  const int S = sym_mode(prec, B);  // symmetric-half iterates
+  std::vector<double> c(d + 1);
+  DASH_TRY(dash_cheb_coeffs(d, lo, hi, c.data()));
   const double aS = 2.0 / (hi - lo), gS = -(hi + lo) / (hi - lo);
 
   Carver cv(ws, ws_bytes);

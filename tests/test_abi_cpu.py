@@ -165,3 +165,25 @@ def test_binding_requires_cuda_tensors():
         dr.inv_root_cn(F, torch.ones(4), 3)
     with pytest.raises(TypeError, match="CUDA"):
         dr.gemm(F, F)
+
+
+@pytest.mark.parametrize("d,lo,hi", [(1, 0.01, 1.05), (8, 0.01, 1.05), (16, 0.05, 2.0),
+                                     (32, 0.01, 1.05), (64, 1e-3, 1.0)])
+def test_library_chebyshev_coefficients_match_oracle(d, lo, hi):
+    """The coefficients inv_root_cheb computes on the host, against the oracle's
+    (itself pinned to numpy's chebinterpolate)."""
+    import numpy as np
+
+    dr = library()
+    got = np.array(dr.cheb_coeffs(d, lo, hi))
+    want = oracle.cheb_coeffs(d, lo, hi)
+    assert got.shape == want.shape
+    assert np.max(np.abs(got - want)) <= 1e-12 * np.max(np.abs(want))
+
+
+def test_chebyshev_coefficients_bad_arguments():
+    dr = library()
+    for args in ((0, 0.01, 1.05), (65, 0.01, 1.05), (8, 0.0, 1.0), (8, 1.0, 0.5),
+                 (8, 0.01, float("inf"))):
+        with pytest.raises(dr.DashError):
+            dr.cheb_coeffs(*args)
