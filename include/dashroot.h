@@ -72,6 +72,20 @@ typedef enum {
 
 typedef enum { DASH_DT_F32 = 0, DASH_DT_BF16 = 1, DASH_DT_F16 = 2 } dash_dtype;
 
+/* Inverse-root solvers, for per-block solver selection. */
+typedef enum { DASH_SOLVER_CN = 0, DASH_SOLVER_NDB = 1, DASH_SOLVER_CHEB = 2 } dash_solver;
+
+/* One tier of per-block solver selection: a solver, its precision and iteration
+ * count (degree for Chebyshev), the unit roundoff u its iterates are stored at,
+ * and the relative error gate it is held to. */
+typedef struct {
+  int solver;  /* dash_solver */
+  int prec;    /* dash_prec */
+  int iters;   /* >= 1 */
+  double u;    /* > 0 */
+  double gate; /* > 0 */
+} dash_tier;
+
 typedef enum {
   DASH_SCALE_POWER = 0,
   DASH_SCALE_FROBENIUS = 1,
@@ -206,6 +220,24 @@ dash_status inv_root_ndb(const float* A, float ridge, const float* scale, int64_
  * d - 1 products per block.  1 <= degree <= 64, 0 < lo < hi.  For B a multiple
  * of 256 every product keeps symmetric halves as in inv_root_cn.
  */
+/*
+ * dash_select_tiers -- per-block solver selection by a condition estimate (host
+ * code, no GPU needed).  Source: [pt] Significancia e Alegacoes, item Direcoes
+ * Futuras (choosing the solver per block from its condition number, named as
+ * future work).  Reading: kappa_k = lam_max[k] / lam_min[k] in double (+inf when
+ * lam_min[k] <= 0 or either value is NaN); choice[k] = the first tier t, in the
+ * given order (cheapest first), with kappa_k * u_t / 4 <= gate_t, else the last
+ * tier.  (Storing the scaled block at roundoff u moves its smallest eigenvalue,
+ * about 1/kappa, by about kappa u relative, and its inverse 4th root by a quarter
+ * of that.)
+ *   lam_max, lam_min (n,) and choice (n,) are caller-owned HOST arrays; tiers
+ *   (ntiers >= 1) likewise.  DASH_ERR_INVALID_ARG for n < 0, null pointers (when
+ *   n > 0) or a tier with an unknown solver or precision, iters < 1, u <= 0 or
+ *   gate <= 0.
+ */
+dash_status dash_select_tiers(const float* lam_max, const float* lam_min, int64_t n,
+                              const dash_tier* tiers, int ntiers, int32_t* choice);
+
 /*
  * dash_cheb_coeffs -- the host-side coefficients inv_root_cheb uses (host code,
  * no GPU needed): c[0..degree] of the degree-d interpolant of x^{-1/4} at the d+1

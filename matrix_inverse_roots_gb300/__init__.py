@@ -38,6 +38,19 @@ SCALE_POWER_F16 = 2
 SCALE_POWER_BF16 = 3
 _HALF_SCALE = {SCALE_POWER_F16: FP16, SCALE_POWER_BF16: BF16}
 
+# dash_solver
+SOLVER_CN = 0
+SOLVER_NDB = 1
+SOLVER_CHEB = 2
+SOLVERS = {"cn": SOLVER_CN, "ndb": SOLVER_NDB, "cheb": SOLVER_CHEB}
+
+
+class Tier(ctypes.Structure):
+    """dash_tier: one tier of per-block solver selection."""
+    _fields_ = [("solver", ctypes.c_int), ("prec", ctypes.c_int), ("iters", ctypes.c_int),
+                ("u", ctypes.c_double), ("gate", ctypes.c_double)]
+
+
 # dash_op
 OP_ACCUMULATE = 0
 OP_SPECTRAL_SCALE = 1
@@ -53,7 +66,7 @@ SYMBOLS = (
     "dash_device_status", "dash_status_string", "dash_version", "dash_trace_start",
     "dash_trace_count", "dash_trace_read", "dash_trace_stop", "spectral_scale_noalloc",
     "dash_selftest_wait_timeout", "precondition_update", "pack_blocks", "unpack_blocks",
-    "dash_cheb_coeffs",
+    "dash_cheb_coeffs", "dash_select_tiers",
 )
 
 _lib = None
@@ -97,6 +110,9 @@ def load_library(path=None):
     lib.spectral_scale_noalloc.argtypes = [vp, f32, i64, i32, i32, i32, i32, vp, vp, vp]
     lib.spectral_scale_noalloc.restype = ctypes.c_int
     lib.dash_cheb_coeffs.argtypes = [i32, f64, f64, ctypes.POINTER(f64)]
+    lib.dash_select_tiers.argtypes = [ctypes.POINTER(f32), ctypes.POINTER(f32), i64,
+                                      ctypes.POINTER(Tier), i32, ctypes.POINTER(ctypes.c_int32)]
+    lib.dash_select_tiers.restype = ctypes.c_int
     lib.dash_cheb_coeffs.restype = ctypes.c_int
     lib.dash_selftest_wait_timeout.argtypes = [i32, vp]
     lib.dash_selftest_wait_timeout.restype = ctypes.c_int
@@ -233,6 +249,25 @@ def cheb_coeffs(degree, lo=1e-2, hi=1.05):
     _check(load_library().dash_cheb_coeffs(int(degree), float(lo), float(hi), c),
            "dash_cheb_coeffs")
     return list(c)
+
+
+def select_tiers(lam_max, lam_min, tiers):
+    """Tier index per block from host sequences of lambda_max / lambda_min estimates.
+
+    tiers: sequence of dicts with keys solver ("cn" | "ndb" | "cheb"), prec, iters,
+    u, gate (cheapest first).  Host-side: no GPU is used."""
+    lmax = [float(x) for x in lam_max]
+    lmin = [float(x) for x in lam_min]
+    if len(lmax) != len(lmin):
+        raise ValueError("lam_max and lam_min must have the same length")
+    n = len(lmax)
+    tt = (Tier * len(tiers))(*[Tier(SOLVERS[t["solver"]], _prec(t["prec"]), int(t["iters"]),
+                                    float(t["u"]), float(t["gate"])) for t in tiers])
+    a = (ctypes.c_float * max(n, 1))(*lmax)
+    b = (ctypes.c_float * max(n, 1))(*lmin)
+    out = (ctypes.c_int32 * max(n, 1))()
+    _check(load_library().dash_select_tiers(a, b, n, tt, len(tiers), out), "dash_select_tiers")
+    return list(out)[:n]
 
 
 def op_matmuls(op, param):

@@ -3,6 +3,7 @@
 // The arithmetic lives in gemm_tc.cu (dense products, fused epilogues) and
 // elementwise.cu (prologues, reductions, power iteration).
 #include <cmath>
+#include <limits>
 #include <cstring>
 #include <vector>
 
@@ -771,6 +772,35 @@ dash_status inv_root_ndb(const float* A, float ridge, const float* scale, int64_
 }
 
 // ---------------------------------------------------------------- Chebyshev / Clenshaw
+
+dash_status dash_select_tiers(const float* lam_max, const float* lam_min, int64_t n,
+                              const dash_tier* tiers, int ntiers, int32_t* choice) {
+  if (n < 0 || ntiers < 1 || !tiers) return DASH_ERR_INVALID_ARG;
+  for (int t = 0; t < ntiers; ++t) {
+    const dash_tier& T = tiers[t];
+    if (T.solver < DASH_SOLVER_CN || T.solver > DASH_SOLVER_CHEB || !valid_prec(T.prec) ||
+        T.iters < 1 || !(T.u > 0.0) || !(T.gate > 0.0))
+      return DASH_ERR_INVALID_ARG;
+  }
+  if (n == 0) return DASH_OK;
+  if (!lam_max || !lam_min || !choice) return DASH_ERR_INVALID_ARG;
+  for (int64_t k = 0; k < n; ++k) {
+    const double hi = lam_max[k], lo = lam_min[k];
+    double kappa = std::numeric_limits<double>::infinity();
+    if (lo > 0.0 && !std::isnan(hi)) kappa = hi / lo;
+    int32_t pick = ntiers - 1;
+    if (!std::isnan(kappa)) {
+      for (int t = 0; t < ntiers; ++t) {
+        if (kappa * tiers[t].u / 4.0 <= tiers[t].gate) {
+          pick = t;
+          break;
+        }
+      }
+    }
+    choice[k] = pick;
+  }
+  return DASH_OK;
+}
 
 dash_status dash_cheb_coeffs(int degree, double lo, double hi, double* c) {
   if (degree < 1 || degree > 64 || !(lo > 0.0) || !(hi > lo) || !std::isfinite(hi) || !c)

@@ -187,3 +187,41 @@ def test_chebyshev_coefficients_bad_arguments():
                  (8, 0.01, float("inf"))):
         with pytest.raises(dr.DashError):
             dr.cheb_coeffs(*args)
+
+
+def test_library_tier_selection_matches_oracle():
+    """The library's host-side tier rule against the oracle's, on float32 estimates
+    including the edge cases (a gate boundary, lambda_min <= 0, NaN, inf)."""
+    import numpy as np
+
+    dr = library()
+    rng = np.random.default_rng(40)
+    lmax = rng.uniform(0.5, 2.0, 200).astype(np.float32)
+    lmin = (lmax / 10.0 ** rng.uniform(0, 7, 200)).astype(np.float32)
+    t0 = oracle.DEFAULT_TIERS[0]
+    edge = 4.0 * t0["gate"] / t0["u"]
+    extra_max = np.array([1.0, 1.0, 1.0, 1.0, np.nan, np.inf, 1.0], dtype=np.float32)
+    extra_min = np.array([1.0 / edge, 0.0, -1.0, np.nan, 0.5, 0.5, 1e-30], dtype=np.float32)
+    lmax = np.concatenate([lmax, extra_max])
+    lmin = np.concatenate([lmin, extra_min])
+    got = dr.select_tiers(lmax, lmin, oracle.DEFAULT_TIERS)
+    want = oracle.select_tiers(oracle.condition_estimate(lmax.astype(np.float64),
+                                                         lmin.astype(np.float64)))
+    assert got == want.tolist()
+    assert set(got[:200]) == {0, 1}
+    tiers3 = [dict(t0), {"solver": "ndb", "prec": "tf32", "iters": 12, "u": 2.0 ** -24,
+                         "gate": 1.0}, dict(oracle.DEFAULT_TIERS[1])]
+    got3 = dr.select_tiers(lmax, lmin, tiers3)
+    assert got3 == oracle.select_tiers(oracle.condition_estimate(
+        lmax.astype(np.float64), lmin.astype(np.float64)), tiers3).tolist()
+    assert dr.select_tiers([], [], tiers3) == []
+
+
+def test_library_tier_selection_bad_tiers():
+    dr = library()
+    good = dict(oracle.DEFAULT_TIERS[0])
+    for bad in ({"iters": 0}, {"u": 0.0}, {"gate": -1.0}, {"prec": 9}):
+        t = dict(good)
+        t.update(bad)
+        with pytest.raises(dr.DashError):
+            dr.select_tiers([1.0], [0.5], [t])
