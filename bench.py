@@ -590,7 +590,10 @@ def run_sweep(args):
 
 
 def run_case(args):
-    """A small untimed case for ncu captures: Wishart blocks, a scale, one root call."""
+    """A small untimed case for ncu captures: Wishart blocks, a scale, one root call;
+    or, for --case accumulate, one accumulate of n bf16 Llama-like gradient blocks
+    into 2n factors (two GEMM launches, then two mirror launches when B is a multiple
+    of 256)."""
     import torch
 
     import matrix_inverse_roots_gb300 as dr
@@ -599,6 +602,14 @@ def run_case(args):
     torch.cuda.set_device(0)
     dr.load_library()
     n, b = args.case_n, args.case_b
+    if args.case == "accumulate":
+        g = torch.Generator(device="cuda").manual_seed(5)
+        G = (0.1 * torch.randn((n, b, b), generator=g, device="cuda")).to(torch.bfloat16)
+        F = torch.zeros((2 * n, b, b), dtype=torch.float32, device="cuda")
+        dr.shampoo_accumulate(G, F, BETA)
+        torch.cuda.synchronize()
+        print("case ok, device status", dr.device_status())
+        return
     A = synth.wishart(n, b, seed=5, device="cuda")
     if args.case_scale in ("power", "power-fp16"):
         mode = dr.SCALE_POWER if args.case_scale == "power" else dr.SCALE_POWER_F16
@@ -671,7 +682,7 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="inverse-root throughput sweep over block sizes and precisions")
     ap.add_argument("--sweep-b", type=int, nargs="*", default=None)
-    ap.add_argument("--case", choices=["cn", "ndb", "cheb"], default=None,
+    ap.add_argument("--case", choices=["cn", "ndb", "cheb", "accumulate"], default=None,
                     help="run one small untimed case (for profiler captures)")
     ap.add_argument("--case-n", type=int, default=64)
     ap.add_argument("--case-b", type=int, default=1024)
