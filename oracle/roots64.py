@@ -59,9 +59,10 @@ def _as64(x):
     return np.asarray(x, dtype=np.float64)
 
 
-def _scaled(a, s, ridge):
+def _scaled(a, s, ridge, dtype=np.float64):
     b = a.shape[0]
-    return (a + ridge * np.eye(b)) / s
+    a = np.asarray(a, dtype=dtype)
+    return (a + dtype(ridge) * np.eye(b, dtype=dtype)) / dtype(s)
 
 
 def _resid(m):
@@ -87,22 +88,25 @@ def evd_inv_root(A, ridge=0.0):
     return out
 
 
-def cn_inv_root(A, scale, iters, ridge=0.0):
+def cn_inv_root(A, scale, iters, ridge=0.0, dtype=np.float64):
     """Coupled Newton inverse 4th root of every block (reading in module docstring).
 
     Returns (X, resid, matmuls): X (N, B, B) ~ A^{-1/4}; resid (N, iters) with
     resid[k, i] = ||M_i - I||_F / sqrt(B); matmuls = products per block.
+    dtype np.float32 runs the same steps in plain round-to-nearest float32 (the
+    scaled block, every product and every iterate), which shows what ordinary
+    arithmetic of that precision can deliver on a given block.
     """
     A = _as64(A)
     scale = _as64(scale)
     n, b, _ = A.shape
     p = 4.0
-    eye = np.eye(b)
+    eye = np.eye(b, dtype=dtype)
     X_out = np.empty_like(A)
     resid = np.empty((n, iters))
     mm = 0
     for k in range(n):
-        M = _scaled(A[k], scale[k], ridge)
+        M = _scaled(A[k], scale[k], ridge, dtype)
         X = eye.copy()
         mm = 0
         for i in range(iters):
@@ -125,9 +129,9 @@ def cn_inv_root(A, scale, iters, ridge=0.0):
 def _ndb_stage(C, iters, keep):
     """One Newton-Schulz Denman-Beavers stage on C; keep is "Y" or "Z".
 
-    Returns (kept iterate, residual list, products used)."""
+    Runs in C's dtype.  Returns (kept iterate, residual list, products used)."""
     b = C.shape[0]
-    eye = np.eye(b)
+    eye = np.eye(b, dtype=C.dtype)
     Y = C
     Z = eye
     res = []
@@ -157,11 +161,11 @@ def _ndb_stage(C, iters, keep):
     return (Y if keep == "Y" else Z), res, mm
 
 
-def ndb_inv_root(A, scale, iters, ridge=0.0):
+def ndb_inv_root(A, scale, iters, ridge=0.0, dtype=np.float64):
     """Two-stage Newton-Denman-Beavers inverse 4th root (reading in module docstring).
 
     Returns (X, resid, matmuls): resid (N, 2, iters); matmuls per block for both
-    stages together.
+    stages together.  dtype as for cn_inv_root.
     """
     A = _as64(A)
     scale = _as64(scale)
@@ -170,7 +174,7 @@ def ndb_inv_root(A, scale, iters, ridge=0.0):
     resid = np.empty((n, 2, iters))
     mm = 0
     for k in range(n):
-        As = _scaled(A[k], scale[k], ridge)
+        As = _scaled(A[k], scale[k], ridge, dtype)
         Yh, r1, m1 = _ndb_stage(As, iters, "Y")  # ~ A_s^{1/2}
         Zq, r2, m2 = _ndb_stage(Yh, iters, "Z")  # ~ (A_s^{1/2})^{-1/2}
         resid[k, 0] = r1

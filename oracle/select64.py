@@ -15,8 +15,8 @@ step says which):
    quotient never exceeds the largest eigenvalue, so mu_hat <= c - lambda_min and
    lambda_min_hat >= lambda_min for every iteration count: the estimate errs
    towards a better-conditioned block, and kappa_hat = lambda_max_hat /
-   lambda_min_hat <= kappa.  A non-positive lambda_min_hat (no resolved gap) gives
-   kappa_hat = inf.
+   lambda_min_hat <= kappa.  A non-positive lambda_min_hat (no resolved gap) or
+   lambda_max_hat (no usable estimate of an SPD block) gives kappa_hat = inf.
 2. Tiers.  An ordered list, cheapest first, of (solver, precision, iterations,
    unit roundoff u, error gate).  Storing the scaled block at roundoff u moves its
    smallest eigenvalue, about 1/kappa, by about kappa u relative, and its inverse
@@ -67,11 +67,12 @@ def lambda_min_estimate(A, lam_max, V0, iters, ridge=0.0):
 
 
 def condition_estimate(lam_max, lam_min):
-    """kappa_hat = lam_max / lam_min per block, inf where lam_min <= 0 (reading 1)."""
+    """kappa_hat = lam_max / lam_min per block, inf unless both are positive
+    (reading 1)."""
     lam_max = _as64(lam_max)
     lam_min = _as64(lam_min)
     out = np.full(lam_max.shape, np.inf)
-    ok = lam_min > 0
+    ok = (lam_min > 0) & (lam_max > 0)
     out[ok] = lam_max[ok] / lam_min[ok]
     return out
 

@@ -174,6 +174,66 @@ def test_ndb_diagonal_is_scalar_recurrence():
             assert abs(resid[0, stage, i] - r) <= 1e-13 * max(1.0, r)
 
 
+def cn_scalar32(lam, s, iters, ridge):
+    """Coupled Newton on one eigenvalue in numpy float32 scalars (rounding after
+    every operation, as a float32 run of the matrix iteration does on a diagonal)."""
+    f = np.float32
+    m = (f(lam) + f(ridge)) / f(s)
+    x = None
+    for i in range(iters):
+        t = (f(5.0) - m) / f(4.0)
+        x = t if i == 0 else x * t
+        if i < iters - 1:
+            t2 = t * t
+            m = (t2 * t2) * m
+    return float(x) * s ** -0.25
+
+
+def ndb_scalar32(lam, s, iters, ridge):
+    """Two Newton-Schulz Denman-Beavers stages on one eigenvalue in float32 scalars."""
+    f = np.float32
+
+    def stage(c, keep_y):
+        y, z = c, f(1.0)
+        for i in range(iters):
+            q = c if i == 0 else z * y
+            t = (f(3.0) - q) / f(2.0)
+            last = i == iters - 1
+            yn = y * t if (not last or keep_y) else y
+            zn = (t if i == 0 else t * z) if (not last or not keep_y) else z
+            y, z = yn, zn
+        return y if keep_y else z
+
+    c = (f(lam) + f(ridge)) / f(s)
+    return float(stage(stage(c, True), False)) * s ** -0.25
+
+
+def test_float32_runs_are_float32_recurrences():
+    # On a diagonal block every product of the matrix iteration is one rounded
+    # scalar product, so the float32 run must reproduce the float32 scalar
+    # recurrence bit for bit -- and differ from the float64 run, or it is not a
+    # float32 run.
+    lam = np.array([1e-5, 3e-3, 0.05, 0.4, 0.9, 1.0])
+    s, ridge, K = 1.3, 1e-6, 9
+    A = np.diag(lam)[None]
+    x32 = oracle.cn_inv_root(A, np.array([s]), K, ridge=ridge, dtype=np.float32)[0][0]
+    want = [cn_scalar32(l, s, K, ridge) for l in lam]
+    np.testing.assert_array_equal(np.diag(x32), want)
+    assert np.max(np.abs(x32 - np.diag(np.diag(x32)))) == 0.0
+    x64 = oracle.cn_inv_root(A, np.array([s]), K, ridge=ridge)[0][0]
+    assert np.any(np.diag(x32) != np.diag(x64))
+    n32 = oracle.ndb_inv_root(A, np.array([s]), K, ridge=ridge, dtype=np.float32)[0][0]
+    np.testing.assert_array_equal(np.diag(n32), [ndb_scalar32(l, s, K, ridge) for l in lam])
+    n64 = oracle.ndb_inv_root(A, np.array([s]), K, ridge=ridge)[0][0]
+    assert np.any(np.diag(n32) != np.diag(n64))
+    # On a well-conditioned block the float32 run stays within float32 rounding of
+    # the float64 run.
+    W = synth.wishart(1, 64, seed=12).double().numpy()
+    sw = np.array([np.linalg.eigvalsh(W[0])[-1]])
+    for fn in (oracle.cn_inv_root, oracle.ndb_inv_root):
+        assert rel_fro(fn(W, sw, 10, dtype=np.float32)[0][0], fn(W, sw, 10)[0][0]) < 1e-5
+
+
 def test_ndb_commuting_family_converges_and_counts():
     lam = np.linspace(0.02, 1.0, 16)
     A, Q = sym_from_spectrum(lam, 2)

@@ -58,6 +58,10 @@ def test_lambda_min_converges_on_a_gapped_spectrum():
 def test_condition_estimate_and_tier_boundaries():
     assert np.array_equal(oracle.condition_estimate([2.0, 2.0, 2.0], [0.5, 0.0, -1.0]),
                           [4.0, np.inf, np.inf])
+    # A non-positive (or NaN) lambda_max is no estimate of an SPD block: inf, not a
+    # small or negative kappa that would pick the cheapest tier.
+    assert np.array_equal(oracle.condition_estimate([-2.0, 0.0, np.nan], [0.5, 0.5, 0.5]),
+                          [np.inf, np.inf, np.inf])
     t0 = oracle.DEFAULT_TIERS[0]
     edge = 4.0 * t0["gate"] / t0["u"]          # kappa u / 4 == gate: admissible
     got = oracle.select_tiers([1.0, edge, np.nextafter(edge, np.inf), 1e12, np.inf, np.nan])
