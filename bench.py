@@ -48,10 +48,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 TF32_RATIO = 1.1 / 2.25
 
 # DRAM bytes (read + write) per factor block per launch of the CTA-pair fp16 GEMM:
-# mean of the four Coupled Newton launches of the ncu capture summarised in
-# profiles/gemm_tc_f16_pair_cn_b1024_n64.md (64 blocks of 1024^2; traffic grows in
-# proportion to the blocks a launch processes).  Valid only for the kernel sources
-# it was taken on, identified by GEMM_TRAFFIC_SRC.
+# mean of the four Coupled Newton launches of an ncu capture of 64 blocks of 1024^2
+# (traffic grows in proportion to the blocks a launch processes).  Valid only for
+# the kernel sources it was taken on, identified by GEMM_TRAFFIC_SRC.
 GEMM_TRAFFIC_PER_BLOCK = 2.975e6
 GEMM_TRAFFIC_SRC = "f70b79738d50bf44"
 GEMM_SOURCES = ("matrix_inverse_roots_gb300/csrc/gemm_tc.cu",
@@ -641,7 +640,10 @@ def run_reference(args):
     secs = sum(times) / len(times)
     blocks = 2 * ng
     value = blocks / secs
-    nf = 2 * sum(1 for _ in range(1)) * 0 + 2496
+    # The GPU arm's stack: an L and an R factor per gradient block of the 24 layers.
+    import synth
+
+    nf = 2 * len(synth.llama_block_layout(LAYERS, BS)[0])
     line = {
         "impl": "reference",
         "metric": "B=1024 inverse-4th-root blocks/sec and optimizer-step ms; % tensor-core peak",

@@ -99,7 +99,8 @@ typedef enum {
   DASH_OP_INV_ROOT_CN = 2,
   DASH_OP_INV_ROOT_NDB = 3,
   DASH_OP_INV_ROOT_CHEB = 4,
-  DASH_OP_PRECONDITION_APPLY = 5
+  DASH_OP_PRECONDITION_APPLY = 5,
+  DASH_OP_LAMBDA_MIN = 6
 } dash_op;
 
 /*
@@ -224,8 +225,8 @@ dash_status inv_root_ndb(const float* A, float ridge, const float* scale, int64_
  * dash_select_tiers -- per-block solver selection by a condition estimate (host
  * code, no GPU needed).  Source: [pt] Significancia e Alegacoes, item Direcoes
  * Futuras (choosing the solver per block from its condition number, named as
- * future work).  Reading: kappa_k = lam_max[k] / lam_min[k] in double (+inf when
- * lam_min[k] <= 0 or either value is NaN); choice[k] = the first tier t, in the
+ * future work).  Reading: kappa_k = lam_max[k] / lam_min[k] in double (+inf
+ * unless both values are positive, NaN included); choice[k] = the first tier t, in the
  * given order (cheapest first), with kappa_k * u_t / 4 <= gate_t, else the last
  * tier.  (Storing the scaled block at roundoff u moves its smallest eigenvalue,
  * about 1/kappa, by about kappa u relative, and its inverse 4th root by a quarter
@@ -237,6 +238,58 @@ dash_status inv_root_ndb(const float* A, float ridge, const float* scale, int64_
  */
 dash_status dash_select_tiers(const float* lam_max, const float* lam_min, int64_t n,
                               const dash_tier* tiers, int ntiers, int32_t* choice);
+
+/*
+ * spectral_lambda_min -- a lambda_min estimate per block, for per-block solver
+ * selection.  Source: [pt] Significancia e Alegacoes, item Direcoes Futuras
+ * (solver choice from each block's condition number).  Reading: the power
+ * iteration of spectral_scale (mode DASH_SCALE_POWER, _POWER_F16 or _POWER_BF16,
+ * same n_vec, power_iters and V0 conventions) on the shifted block
+ * c_k I - (A_k + ridge I), c_k = lam_max[k], gives mu_k, and
+ * lam_min_out[k] = c_k - mu_k.  The shifted block's eigenvalues are c_k - lambda_i;
+ * a Rayleigh quotient never exceeds the largest, so (up to rounding)
+ * lam_min_out[k] >= lambda_min(A_k + ridge I): the estimate errs toward a
+ * better-conditioned block.
+ *   A (N, B, B) fp32 symmetric; lam_max (N,) fp32 > 0 (e.g. spectral_scale's
+ *   output); lam_min_out (N,) fp32.
+ * Workspace: dash_workspace_size(DASH_OP_LAMBDA_MIN, N, B, prec, n_vec) (prec
+ *   DASH_FP16 / DASH_BF16 for the half modes) holds the shifted stack (4 B^2 bytes
+ *   per block) and spectral_scale's workspace for all N blocks; a smaller one walks
+ *   the stack in chunks.
+ */
+dash_status spectral_lambda_min(const float* A, float ridge, const float* lam_max, int64_t N,
+                                int B, int mode, int n_vec, int power_iters, const float* V0,
+                                float* lam_min_out, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * inv_root_auto -- inverse 4th roots with the solver chosen per block.  Source:
+ * [pt] Significancia e Alegacoes, item Direcoes Futuras.  Reading: block k's tier
+ * is dash_select_tiers(lam_max, lam_min, tiers)[k]; the blocks of each tier are
+ * solved by that tier's solver (Coupled Newton or NDB with `iters` iterations,
+ * Chebyshev of degree `iters` on [cheb_lo, cheb_hi]) in its precision, scaled by
+ * lam_max exactly as inv_root_cn / _ndb / _cheb scale, and written to X[k].
+ *   A (N, B, B) fp32; lam_max, lam_min (N,) fp32 device arrays (spectral_scale,
+ *   spectral_lambda_min); tiers (ntiers >= 1, cheapest first) HOST array as for
+ *   dash_select_tiers; X (N, B, B) fp32 output; choice_out (N,) int32 HOST array
+ *   or NULL: receives each block's tier.
+ * Synchronisation: unlike every other entry point, this one reads lam_max and
+ *   lam_min back to the host and so synchronises `stream`, once; a tier whose
+ *   blocks are not one contiguous range is gathered into a sub-stack of the
+ *   workspace, solved and scattered back, and uploading its index list waits for
+ *   the stream again.  A tier that is one contiguous range is solved in place.
+ * Workspace: dash_auto_workspace_size (the worst case: every block in one
+ *   gathered tier); a smaller one walks each gathered tier in chunks.
+ * Errors: as dash_select_tiers for the tiers; DASH_ERR_INVALID_ARG for a
+ *   Chebyshev tier with degree > 64 or a bad interval.
+ */
+dash_status inv_root_auto(const float* A, float ridge, const float* lam_max,
+                          const float* lam_min, int64_t N, int B, const dash_tier* tiers,
+                          int ntiers, double cheb_lo, double cheb_hi, float* X,
+                          int32_t* choice_out, void* ws, size_t ws_bytes, void* stream);
+
+/* Workspace bytes of inv_root_auto on N blocks of order B with these tiers. */
+dash_status dash_auto_workspace_size(int64_t N, int B, const dash_tier* tiers, int ntiers,
+                                     size_t* bytes);
 
 /*
  * dash_cheb_coeffs -- the host-side coefficients inv_root_cheb uses (host code,
@@ -311,6 +364,21 @@ dash_status dash_gemm(const void* A, const void* A_lo, int trans_a, const void* 
                       void* stream);
 
 /*
+ * dash_gemm_ex -- dash_gemm with the two operand forms the root solvers use, for
+ * tests (no counterpart on the pages).
+ *   sym 0: as dash_gemm.  sym 1: A and B symmetric; only their 256 x 256 tiles on
+ *   or above the diagonal are read (a tile below is taken as its mirror's
+ *   transpose).  sym 2: as 1, and only C's tiles on or above the diagonal are
+ *   computed and written (C symmetric by construction).  Modes 1 and 2 apply for B
+ *   a multiple of 256 and act as 0 otherwise.
+ *   With prec DASH_FP16 / DASH_BF16, a non-NULL B_lo makes B a 16-bit pair:
+ *   C = A B + A B_lo, both products in that 16-bit type (A_lo ignored).
+ */
+dash_status dash_gemm_ex(const void* A, const void* A_lo, int trans_a, const void* Bm,
+                         const void* B_lo, int trans_b, int64_t N, int B, int prec, int sym,
+                         float* C, void* stream);
+
+/*
  * spectral_scale_noalloc -- spectral_scale for callers that cannot allocate
  * device memory when they run (work being captured into a CUDA graph, hooks
  * inside another framework's memory manager, fixed-budget or real-time loops).
@@ -319,10 +387,14 @@ dash_status dash_gemm(const void* A, const void* A_lo, int trans_a, const void* 
  * the library, which every GPU that loads the library keeps until the process
  * exits.  Arguments and results are those of spectral_scale without ws/ws_bytes.
  *   Limit: one pass over all N blocks must fit the array, i.e.
- *   dash_workspace_size(DASH_OP_SPECTRAL_SCALE, N, B, ...) <= 32 MiB in power
- *   mode (N <= 127 blocks at B = 1024, N <= 1012 at B = 128) and 4*N bytes in
- *   Frobenius mode; larger requests return DASH_ERR_WORKSPACE_TOO_SMALL before
- *   anything is enqueued.
+ *   dash_workspace_size(DASH_OP_SPECTRAL_SCALE, N, B, prec, n_vec) <= 32 MiB,
+ *   with prec DASH_FP16 / DASH_BF16 for the half modes.  With 32 vectors that is
+ *     DASH_SCALE_POWER            N <= 127 at B = 1024 (1012 at 128, 63 at 2048);
+ *     DASH_SCALE_POWER_F16 / BF16 N <= 15 at B = 1024 (677 at 128, 3 at 2048),
+ *       because these modes also keep a 16-bit copy of every block there;
+ *     DASH_SCALE_FROBENIUS        4*N bytes.
+ *   Larger requests return DASH_ERR_WORKSPACE_TOO_SMALL before anything is
+ *   enqueued.
  *   No cudaMalloc, cudaFree or other allocating call is made.  The first call on
  *   each device looks up the array's device address (cudaGetSymbolAddress), so
  *   make that first call before any stream capture.

@@ -58,6 +58,7 @@ OP_INV_ROOT_CN = 2
 OP_INV_ROOT_NDB = 3
 OP_INV_ROOT_CHEB = 4
 OP_PRECONDITION_APPLY = 5
+OP_LAMBDA_MIN = 6
 
 # Exported C symbols (kept in step with include/dashroot.h).
 SYMBOLS = (
@@ -66,7 +67,8 @@ SYMBOLS = (
     "dash_device_status", "dash_status_string", "dash_version", "dash_trace_start",
     "dash_trace_count", "dash_trace_read", "dash_trace_stop", "spectral_scale_noalloc",
     "dash_selftest_wait_timeout", "precondition_update", "pack_blocks", "unpack_blocks",
-    "dash_cheb_coeffs", "dash_select_tiers",
+    "dash_cheb_coeffs", "dash_select_tiers", "spectral_lambda_min", "inv_root_auto",
+    "dash_auto_workspace_size", "dash_gemm_ex",
 )
 
 _lib = None
@@ -113,6 +115,16 @@ def load_library(path=None):
     lib.dash_select_tiers.argtypes = [ctypes.POINTER(f32), ctypes.POINTER(f32), i64,
                                       ctypes.POINTER(Tier), i32, ctypes.POINTER(ctypes.c_int32)]
     lib.dash_select_tiers.restype = ctypes.c_int
+    lib.spectral_lambda_min.argtypes = [vp, f32, vp, i64, i32, i32, i32, i32, vp, vp, vp, sz, vp]
+    lib.spectral_lambda_min.restype = ctypes.c_int
+    lib.inv_root_auto.argtypes = [vp, f32, vp, vp, i64, i32, ctypes.POINTER(Tier), i32, f64, f64,
+                                  vp, ctypes.POINTER(ctypes.c_int32), vp, sz, vp]
+    lib.inv_root_auto.restype = ctypes.c_int
+    lib.dash_auto_workspace_size.argtypes = [i64, i32, ctypes.POINTER(Tier), i32,
+                                             ctypes.POINTER(sz)]
+    lib.dash_auto_workspace_size.restype = ctypes.c_int
+    lib.dash_gemm_ex.argtypes = [vp, vp, i32, vp, vp, i32, i64, i32, i32, i32, vp, vp]
+    lib.dash_gemm_ex.restype = ctypes.c_int
     lib.dash_cheb_coeffs.restype = ctypes.c_int
     lib.dash_selftest_wait_timeout.argtypes = [i32, vp]
     lib.dash_selftest_wait_timeout.restype = ctypes.c_int
@@ -155,6 +167,12 @@ def _stream():
 def _stack(t, name, dtype=torch.float32):
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError("%s must be a CUDA tensor" % name)
+    # The library launches on the current device's stream (and the no-allocation
+    # entry point uses that device's built-in scratch): a tensor elsewhere would be
+    # handed to kernels of the wrong device.
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError("%s is on %s but the current CUDA device is cuda:%d" % (
+            name, t.device, torch.cuda.current_device()))
     if t.dtype != dtype:
         raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
     if not t.is_contiguous():
@@ -261,13 +279,76 @@ def select_tiers(lam_max, lam_min, tiers):
     if len(lmax) != len(lmin):
         raise ValueError("lam_max and lam_min must have the same length")
     n = len(lmax)
-    tt = (Tier * len(tiers))(*[Tier(SOLVERS[t["solver"]], _prec(t["prec"]), int(t["iters"]),
-                                    float(t["u"]), float(t["gate"])) for t in tiers])
+    tt = _tiers(tiers)
     a = (ctypes.c_float * max(n, 1))(*lmax)
     b = (ctypes.c_float * max(n, 1))(*lmin)
     out = (ctypes.c_int32 * max(n, 1))()
     _check(load_library().dash_select_tiers(a, b, n, tt, len(tiers), out), "dash_select_tiers")
     return list(out)[:n]
+
+
+def _tiers(tiers):
+    return (Tier * len(tiers))(*[Tier(SOLVERS[t["solver"]], _prec(t["prec"]), int(t["iters"]),
+                                      float(t["u"]), float(t["gate"])) for t in tiers])
+
+
+def spectral_lambda_min(A, lam_max, mode=SCALE_POWER, V0=None, power_iters=10, ridge=0.0,
+                        out=None, ws=None):
+    """lambda_min estimate per block: power iteration on lam_max I - (A + ridge I)."""
+    lib = load_library()
+    _stack(A, "A")
+    n, b = _blocks3(A, "A")
+    _shape(_stack(lam_max, "lam_max"), (n,), "lam_max")
+    _stack(V0, "V0")
+    if V0.dim() != 3 or V0.shape[0] != n or V0.shape[1] != b:
+        raise ValueError("V0 must have shape (N, B, n_vec)")
+    nv = V0.shape[2]
+    if out is None:
+        out = torch.empty(n, dtype=torch.float32, device=A.device)
+    _shape(_stack(out, "out"), (n,), "out")
+    if ws is None:
+        ws = workspace(OP_LAMBDA_MIN, n, b, _HALF_SCALE.get(mode, FP32_3XTF32), nv,
+                       device=A.device)
+    _check(lib.spectral_lambda_min(_ptr(A), float(ridge), _ptr(lam_max), n, b, int(mode), nv,
+                                   int(power_iters), _ptr(V0), _ptr(out), _ptr(ws), _nbytes(ws),
+                                   _stream()), "spectral_lambda_min")
+    return out
+
+
+def auto_workspace_size(n, b, tiers):
+    out = ctypes.c_size_t(0)
+    tt = _tiers(tiers)
+    _check(load_library().dash_auto_workspace_size(int(n), int(b), tt, len(tiers),
+                                                   ctypes.byref(out)), "dash_auto_workspace_size")
+    return out.value
+
+
+def inv_root_auto(A, lam_max, lam_min, tiers, ridge=0.0, cheb=(1e-2, 1.05), X=None, ws=None,
+                  max_ws_bytes=None):
+    """A^{-1/4} with the solver chosen per block by its condition estimate.
+
+    tiers: sequence of dicts (solver, prec, iters, u, gate), cheapest first.  Returns
+    (X, choice) with choice the list of tier indices.  Synchronises the stream (the
+    estimates are read back to the host)."""
+    lib = load_library()
+    _stack(A, "A")
+    n, b = _blocks3(A, "A")
+    _shape(_stack(lam_max, "lam_max"), (n,), "lam_max")
+    _shape(_stack(lam_min, "lam_min"), (n,), "lam_min")
+    if X is None:
+        X = torch.empty_like(A)
+    _shape(_stack(X, "X"), (n, b, b), "X")
+    tt = _tiers(tiers)
+    if ws is None:
+        nbytes = auto_workspace_size(n, b, tiers)
+        if max_ws_bytes is not None:
+            nbytes = min(nbytes, int(max_ws_bytes))
+        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=A.device)
+    choice = (ctypes.c_int32 * max(n, 1))()
+    _check(lib.inv_root_auto(_ptr(A), float(ridge), _ptr(lam_max), _ptr(lam_min), n, b, tt,
+                             len(tiers), float(cheb[0]), float(cheb[1]), _ptr(X), choice,
+                             _ptr(ws), _nbytes(ws), _stream()), "inv_root_auto")
+    return X, list(choice)[:n]
 
 
 def op_matmuls(op, param):
@@ -500,4 +581,24 @@ def gemm(A, B, prec=TF32, trans_a=False, trans_b=False, A_lo=None, B_lo=None, C=
     _shape(_stack(C, "C"), (n, b, b), "C")
     _check(lib.dash_gemm(_ptr(A), _ptr(A_lo), int(bool(trans_a)), _ptr(B), _ptr(B_lo),
                          int(bool(trans_b)), n, b, p, _ptr(C), _stream()), "dash_gemm")
+    return C
+
+
+def gemm_ex(A, B, prec=TF32, sym=0, trans_a=False, trans_b=False, A_lo=None, B_lo=None, C=None):
+    """dash_gemm_ex: symmetric-half operand forms (sym 1, 2) and, for 16-bit prec,
+    a 16-bit pair B (B_lo given): C = A B + A B_lo."""
+    lib = load_library()
+    p = _prec(prec)
+    _stack(A, "A", A.dtype)
+    n, b = _blocks3(A, "A")
+    _shape(_stack(B, "B", A.dtype), (n, b, b), "B")
+    for t, name in ((A_lo, "A_lo"), (B_lo, "B_lo")):
+        if t is not None:
+            _shape(_stack(t, name, A.dtype), (n, b, b), name)
+    if C is None:
+        C = torch.empty((n, b, b), dtype=torch.float32, device=A.device)
+    _shape(_stack(C, "C"), (n, b, b), "C")
+    _check(lib.dash_gemm_ex(_ptr(A), _ptr(A_lo), int(bool(trans_a)), _ptr(B), _ptr(B_lo),
+                            int(bool(trans_b)), n, b, p, int(sym), _ptr(C), _stream()),
+           "dash_gemm_ex")
     return C

@@ -80,7 +80,17 @@ struct Carver {
     }
     return b;
   }
+  // A 16-bit precision's buffer with room for a lo part (the pair formats).
+  Buf take_pair16(int B, long long nblk) {
+    Buf b;
+    const size_t elems = static_cast<size_t>(B) * B * nblk;
+    b.hi = take(elems * 2);
+    b.lo = take(elems * 2);
+    return b;
+  }
 };
+
+bool is_half(int prec) { return prec == DASH_FP16 || prec == DASH_BF16; }
 
 // Per-block bytes of the operand buffers, rounded the way the carver rounds
 // them when a chunk holds nblk blocks (used to size chunks).
@@ -138,6 +148,13 @@ EpiOut eout(const Buf& b, int fmt, float alpha, float gamma, float eps = 0.0f,
   return o;
 }
 
+// Sets the epilogue's E operand to the buffer b (in format fmt).
+void with_e(EpiParams& e, const Buf& b, int fmt) {
+  e.E_hi = b.hi;
+  e.E_lo = b.lo;
+  e.E_fmt = fmt;
+}
+
 EpiOut eout_f32(float* p, float alpha, float gamma, float eps, const float* mult) {
   Buf b;
   b.hi = p;
@@ -171,12 +188,14 @@ AffParams aff_from(const void* src_hi, const void* src_lo, int src_fmt, int B, l
 // are read); 2 also a symmetric result (only those tiles computed and stored);
 // 3 a symmetric result from operands read whole (X Y^T with Y = X, or X^T X).
 // Modes 1-3 take effect for B a multiple of 256 (CTA-pair kernels).
+// pairB: Y is a 16-bit pair (FMT_F16X2 / FMT_BF16X2) of the 16-bit precision prec.
 dash_status gemm(int prec, int B, long long nc, const Buf& X, int tX, const Buf& Y, int tY,
-                 const EpiParams& e, cudaStream_t st, int sym = 0) {
+                 const EpiParams& e, cudaStream_t st, int sym = 0, bool pairB = false) {
   GemmLaunch g;
   g.sym_in = (sym == 1 || sym == 2) ? 1 : 0;
   g.sym_out = (sym >= 2) ? 1 : 0;
   g.kind = prec_kind(prec);
+  if (pairB) g.kind = (prec == DASH_BF16) ? KIND_BF16_SPLITB : KIND_F16_SPLITB;
   g.dim = B;
   g.nblocks = nc;
   g.A = X.hi;
@@ -193,9 +212,12 @@ dash_status gemm(int prec, int B, long long nc, const Buf& X, int tX, const Buf&
 // is a polynomial in the symmetric A, so each product of two is symmetric.  The
 // CTA-pair kernels (B a multiple of 256) honour it in every precision.  Used by
 // Coupled Newton and Chebyshev; Newton-Denman-Beavers keeps full products.
+#ifndef DASH_SYM_HALVES
+#define DASH_SYM_HALVES 1  // build-time: 0 computes every product whole
+#endif
 int sym_mode(int prec, int B) {
   (void)prec;
-  return (B % 256 == 0) ? 2 : 0;
+  return (DASH_SYM_HALVES && B % 256 == 0) ? 2 : 0;
 }
 
 // Small per-call arrays shared by the root solvers.
@@ -220,6 +242,20 @@ dash_status common_root_checks(const float* A, const float* scale, long long N, 
 }
 
 constexpr int CN_BUFS = 7;
+// The two M iterates of a 16-bit Coupled Newton carry a lo part: two more arrays.
+int cn_bufs(int prec) { return is_half(prec) ? CN_BUFS + 2 : CN_BUFS; }
+
+// M-update products of a 16-bit Coupled Newton of K iterations that read M as a
+// 16-bit pair (hi + lo); the last three read it plain.  The root is sensitive to
+// the rounding of M in proportion to how much the remaining iterations amplify
+// its small eigenvalues (about (5/4)^4 per iteration), so only the early updates
+// need M's extra bits.
+#ifndef DASH_CN_PAIR_TAIL
+#define DASH_CN_PAIR_TAIL 4  // M-updates at the end of the iteration that read M plain, + 1
+#endif
+int cn_pair_updates(int prec, int K) {
+  return is_half(prec) ? (K > DASH_CN_PAIR_TAIL ? K - DASH_CN_PAIR_TAIL : 0) : 0;
+}
 constexpr int NDB_BUFS = 6;
 constexpr int CHEB_BUFS = 4;
 constexpr int APPLY_BUFS = 4;
@@ -288,7 +324,7 @@ dash_status dash_workspace_size(int op, int64_t N, int B, int prec, int param, s
         s = 2 * round256(static_cast<size_t>(N) * B * 32 * 4) + 3 * round256(N * 32 * 4) + 256;
       break;
     case DASH_OP_INV_ROOT_CN:
-      s = root_small_bytes(N, N * (param > 0 ? param : 1)) + bufs_bytes(prec, B, N, CN_BUFS);
+      s = root_small_bytes(N, N * (param > 0 ? param : 1)) + bufs_bytes(prec, B, N, cn_bufs(prec));
       break;
     case DASH_OP_INV_ROOT_NDB:
       s = root_small_bytes(N, 2 * N * (param > 0 ? param : 1)) + bufs_bytes(prec, B, N, NDB_BUFS);
@@ -299,6 +335,13 @@ dash_status dash_workspace_size(int op, int64_t N, int B, int prec, int param, s
     case DASH_OP_PRECONDITION_APPLY:
       s = bufs_bytes(prec, B, N, APPLY_BUFS);
       break;
+    case DASH_OP_LAMBDA_MIN: {
+      // The shifted stack, 1/c_k and mu_k, and spectral_scale's workspace.
+      size_t sc = 0;
+      DASH_TRY(dash_workspace_size(DASH_OP_SPECTRAL_SCALE, N, B, prec, param, &sc));
+      s = round256(static_cast<size_t>(N) * B * B * 4) + 2 * round256(N * 4) + round256(sc) + 256;
+      break;
+    }
     default:
       return DASH_ERR_INVALID_ARG;
   }
@@ -324,6 +367,29 @@ dash_status dash_gemm(const void* A, const void* A_lo, int trans_a, const void* 
   e.nout = 1;
   e.out[0] = eout_f32(C, 1.0f, 0.0f, 0.0f, nullptr);
   return gemm(prec, B, N, X, trans_a, Y, trans_b, e, static_cast<cudaStream_t>(stream));
+}
+
+dash_status dash_gemm_ex(const void* A, const void* A_lo, int trans_a, const void* Bm,
+                         const void* B_lo, int trans_b, int64_t N, int B, int prec, int sym,
+                         float* C, void* stream) {
+  if (N < 0 || !valid_dim(B) || !valid_prec(prec) || sym < 0 || sym > 2)
+    return DASH_ERR_INVALID_ARG;
+  if (N == 0) return DASH_OK;
+  if (!A || !Bm || !C || !aligned16(A) || !aligned16(Bm) || !aligned16(C))
+    return DASH_ERR_INVALID_ARG;
+  if (prec == DASH_FP32_3XTF32 && (!A_lo || !B_lo || !aligned16(A_lo) || !aligned16(B_lo)))
+    return DASH_ERR_INVALID_ARG;
+  const bool pair = is_half(prec) && B_lo != nullptr;
+  if (pair && !aligned16(B_lo)) return DASH_ERR_INVALID_ARG;
+  Buf X, Y;
+  X.hi = const_cast<void*>(A);
+  X.lo = const_cast<void*>(A_lo);
+  Y.hi = const_cast<void*>(Bm);
+  Y.lo = const_cast<void*>(B_lo);
+  EpiParams e = epi_none();
+  e.nout = 1;
+  e.out[0] = eout_f32(C, 1.0f, 0.0f, 0.0f, nullptr);
+  return gemm(prec, B, N, X, trans_a, Y, trans_b, e, static_cast<cudaStream_t>(stream), sym, pair);
 }
 
 // ---------------------------------------------------------------- accumulate
@@ -536,15 +602,23 @@ dash_status inv_root_cn(const float* A, float ridge, const float* scale, int64_t
   sm.s_m14 = static_cast<float*>(cv.take(N * 4));
   sm.racc = static_cast<float*>(cv.take(static_cast<size_t>(N) * K * 4));
   if (!cv.ok) return DASH_ERR_WORKSPACE_TOO_SMALL;
-  const int nbufs = (K >= 2) ? CN_BUFS : 0;
+  const int nbufs = (K >= 2) ? cn_bufs(prec) : 0;
   const long long chunk = fit_chunk(prec, B, N, nbufs, cv.left);
   if (chunk < 1) return DASH_ERR_WORKSPACE_TOO_SMALL;
+  // 16-bit precisions: M_k is a 16-bit pair for the first jp M-updates.
+  const int jp = cn_pair_updates(prec, K);
+  // 3xTF32 runs the identity-shifted form of the same iteration (see inv_root_ndb):
+  // the T buffers hold D = T - I, D2 = T^2 - I and D4 = T^4 - I, and
+  //   X T = X + X D,  T^2 - I = D D + 2D,  T^4 - I = D2 D2 + 2 D2,  T^4 M = M + D4 M,
+  // each large term added exactly in the epilogue (E operand).
+  const bool shift = (prec == DASH_FP32_3XTF32);
+  const int pfmt = (prec == DASH_BF16) ? FMT_BF16X2 : FMT_F16X2;
   Buf bx[2], bm[2], bT, bT2, bT4;
   if (K >= 2) {
     bx[0] = cv.take_buf(prec, B, chunk);
     bx[1] = cv.take_buf(prec, B, chunk);
-    bm[0] = cv.take_buf(prec, B, chunk);
-    bm[1] = cv.take_buf(prec, B, chunk);
+    bm[0] = is_half(prec) ? cv.take_pair16(B, chunk) : cv.take_buf(prec, B, chunk);
+    bm[1] = is_half(prec) ? cv.take_pair16(B, chunk) : cv.take_buf(prec, B, chunk);
     bT = cv.take_buf(prec, B, chunk);
     bT2 = cv.take_buf(prec, B, chunk);
     bT4 = cv.take_buf(prec, B, chunk);
@@ -577,20 +651,26 @@ dash_status inv_root_cn(const float* A, float ridge, const float* scale, int64_t
       continue;
     }
     a.nout = 2;
-    a.out[0] = aout(bm[0], fmt, 1.0f, 0.0f);
-    a.out[1] = aout(bT, fmt, -0.25f, 1.25f);
+    a.out[0] = aout(bm[0], jp > 0 ? pfmt : fmt, 1.0f, 0.0f);
+    a.out[1] = aout(bT, fmt, -0.25f, shift ? 0.25f : 1.25f);
+    if (shift) {
+      a.nout = 3;  // X_1 = T_0 = I + D_0 gets its own buffer
+      a.out[2] = aout(bx[0], fmt, -0.25f, 1.25f);
+    }
     DASH_TRY(launch_affine(a, st));
     // T_k and the scratch that takes T_k^2 and then T_{k+1} trade buffers every
     // iteration.  X_1 = T_0 is not copied: it is read from T_0's buffer, which
     // becomes scratch only after the first X product has consumed it.
-    Buf tk = bT, tsp = bT2, xk = bT;
-    int mc = 0, xn = 0;
+    Buf tk = bT, tsp = bT2, xk = shift ? bx[0] : bT;
+    int mc = 0, xn = shift ? 1 : 0;
+    const float e1 = shift ? 1.0f : 0.0f, e2 = shift ? 2.0f : 0.0f;
     for (int k = 0; k < K; ++k) {
       if (k == K - 1) {
         // X_K = X_{K-1} T_{K-1}, scaled by s^{-1/4}, into the caller's fp32 output.
         EpiParams e = epi_none();
         e.nout = 1;
-        e.out[0] = eout_f32(Xc, 1.0f, 0.0f, 0.0f, m14);
+        e.out[0] = eout_f32(Xc, 1.0f, 0.0f, e1, m14);
+        if (shift) with_e(e, xk, fmt);
         DASH_TRY(gemm(prec, B, nc, xk, 0, tk, 0, e, st, S));
         if (S) DASH_TRY(launch_mirror_lower(Xc, B, nc, st));
         break;
@@ -598,26 +678,35 @@ dash_status inv_root_cn(const float* A, float ridge, const float* scale, int64_t
       if (k >= 1) {
         EpiParams e = epi_none();
         e.nout = 1;
-        e.out[0] = eout(bx[xn], fmt, 1.0f, 0.0f);
+        e.out[0] = eout(bx[xn], fmt, 1.0f, 0.0f, e1);
+        if (shift) with_e(e, xk, fmt);
         DASH_TRY(gemm(prec, B, nc, xk, 0, tk, 0, e, st, S));
         xk = bx[xn];
         xn ^= 1;
       }
-      EpiParams e2 = epi_none();
-      e2.nout = 1;
-      e2.out[0] = eout(tsp, fmt, 1.0f, 0.0f);
-      DASH_TRY(gemm(prec, B, nc, tk, 0, tk, 0, e2, st, S));
-      e2.out[0] = eout(bT4, fmt, 1.0f, 0.0f);
-      DASH_TRY(gemm(prec, B, nc, tsp, 0, tsp, 0, e2, st, S));
+      EpiParams ea = epi_none();
+      ea.nout = 1;
+      ea.out[0] = eout(tsp, fmt, 1.0f, 0.0f, e2);
+      if (shift) with_e(ea, tk, fmt);
+      DASH_TRY(gemm(prec, B, nc, tk, 0, tk, 0, ea, st, S));
+      EpiParams eb = epi_none();
+      eb.nout = 1;
+      eb.out[0] = eout(bT4, fmt, 1.0f, 0.0f, e2);
+      if (shift) with_e(eb, tsp, fmt);
+      DASH_TRY(gemm(prec, B, nc, tsp, 0, tsp, 0, eb, st, S));
       // M_{k+1} = T^4 M_k; the same epilogue forms T_{k+1} (into the scratch, free
       // once T^4 is formed) and the residual of M_{k+1}.
       EpiParams em = epi_none();
       em.nout = 2;
-      em.out[0] = eout(bm[mc ^ 1], fmt, 1.0f, 0.0f);
-      em.out[1] = eout(tsp, fmt, -0.25f, 1.25f);
+      em.out[0] = eout(bm[mc ^ 1], (k + 1 < jp) ? pfmt : fmt, 1.0f, 0.0f, e1);
+      em.out[1] = eout(tsp, fmt, -0.25f, shift ? 0.25f : 1.25f, shift ? -0.25f : 0.0f);
+      if (shift) {
+        with_e(em, bm[mc], fmt);
+        em.resid_plus_e = 1;
+      }
       em.resid_acc = racc ? racc + (k + 1) : nullptr;
       em.resid_stride = K;
-      DASH_TRY(gemm(prec, B, nc, bT4, 0, bm[mc], 0, em, st, S));
+      DASH_TRY(gemm(prec, B, nc, bT4, 0, bm[mc], 0, em, st, S, k < jp));
       mc ^= 1;
       const Buf t = tk;
       tk = tsp;
@@ -645,6 +734,14 @@ dash_status inv_root_ndb(const float* A, float ridge, const float* scale, int64_
   // ill-conditioned blocks (scaled condition ~1e6) the iteration then diverges --
   // in plain float32 as well -- where the full products converge.
   const int S = 0, SI = 0;
+  // 3xTF32 runs the identity-shifted form of the same iteration: the buffer of T
+  // holds D = T - I, and Y T = Y + Y D, T Z = Z + D Z add the large term exactly in
+  // the epilogue (E operand).  The products then only carry the iterates' deviation
+  // from identity scaling, so the tensor core's truncating accumulation and the
+  // TF32 split act on small numbers; and D keeps full relative precision where T
+  // would lose it next to its unit diagonal.
+  const bool shift = (prec == DASH_FP32_3XTF32);
+  const float gT = shift ? 0.5f : 1.5f;  // gamma of T (or D) = (3I - P) / 2 (- I)
   Carver cv(ws, ws_bytes);
   RootSmall sm;
   sm.inv_s = static_cast<float*>(cv.take(N * 4));
@@ -681,7 +778,7 @@ dash_status inv_root_ndb(const float* A, float ridge, const float* scale, int64_
     a.resid_stride = rstride;
     a.nout = 3;
     a.out[0] = aout(pool[iC], fmt, 1.0f, 0.0f);
-    a.out[1] = aout(pool[iT], fmt, -0.5f, 1.5f);
+    a.out[1] = aout(pool[iT], fmt, -0.5f, gT);
     a.out[2] = aout(pool[iZ], fmt, -0.5f, 1.5f);
     DASH_TRY(launch_affine(a, st));
 
@@ -698,10 +795,10 @@ dash_status inv_root_ndb(const float* A, float ridge, const float* scale, int64_
       for (int k = 0; k < K; ++k) {
         const bool lastk = (k == K - 1);
         if (k >= 1) {
-          // P = Z_k Y_k -> T_k = (3I - P)/2 and the residual of P.
+          // P = Z_k Y_k -> T_k = (3I - P)/2 (D_k = T_k - I) and the residual of P.
           EpiParams ep = epi_none();
           ep.nout = 1;
-          ep.out[0] = eout(pool[iT], fmt, -0.5f, 1.5f);
+          ep.out[0] = eout(pool[iT], fmt, -0.5f, gT);
           ep.resid_acc = racc_s ? racc_s + k : nullptr;
           ep.resid_stride = rstride;
           DASH_TRY(gemm(prec, B, nc, pool[iZ], 0, pool[iY], 0, ep, st, S));
@@ -710,14 +807,16 @@ dash_status inv_root_ndb(const float* A, float ridge, const float* scale, int64_
           const int iYn = free_buf(iY, iZ, iT);
           EpiParams ey = epi_none();
           ey.nout = 1;
-          ey.out[0] = eout(pool[iYn], fmt, 1.0f, 0.0f);
+          ey.out[0] = eout(pool[iYn], fmt, 1.0f, 0.0f, shift ? 1.0f : 0.0f);
+          if (shift) with_e(ey, pool[iY], fmt);  // Y + Y D
           DASH_TRY(gemm(prec, B, nc, pool[iY], 0, pool[iT], 0, ey, st, S));
           iY = iYn;
           if (k >= 1) {
             const int iZn = free_buf(iY, iZ, iT);
             EpiParams ez = epi_none();
             ez.nout = 1;
-            ez.out[0] = eout(pool[iZn], fmt, 1.0f, 0.0f);
+            ez.out[0] = eout(pool[iZn], fmt, 1.0f, 0.0f, shift ? 1.0f : 0.0f);
+            if (shift) with_e(ez, pool[iZ], fmt);  // Z + D Z
             DASH_TRY(gemm(prec, B, nc, pool[iT], 0, pool[iZ], 0, ez, st, S));
             iZ = iZn;
           }
@@ -739,16 +838,22 @@ dash_status inv_root_ndb(const float* A, float ridge, const float* scale, int64_
           EpiParams ey = epi_none();
           ey.resid_acc = racc ? racc + K : nullptr;
           ey.resid_stride = rstride;
+          // Shifted: C' = Y + Y D, so every output adds (a multiple of) E = Y.
+          const float e1 = shift ? 1.0f : 0.0f, eh = shift ? -0.5f : 0.0f;
+          if (shift) {
+            with_e(ey, pool[iY], fmt);
+            ey.resid_plus_e = 1;
+          }
           if (K == 1) {
             ey.nout = 1;
-            ey.out[0] = eout(Xout, FMT_F32, -0.5f, 1.5f, 0.0f, m14);
+            ey.out[0] = eout(Xout, FMT_F32, -0.5f, 1.5f, eh, m14);
             // residual of C' = product itself
             DASH_TRY(gemm(prec, B, nc, pool[iY], 0, pool[iT], 0, ey, st, SI));
           } else {
             ey.nout = 3;
-            ey.out[0] = eout(pool[iCn], fmt, 1.0f, 0.0f);
-            ey.out[1] = eout(pool[iTn], fmt, -0.5f, 1.5f);
-            ey.out[2] = eout(pool[iZn], fmt, -0.5f, 1.5f);
+            ey.out[0] = eout(pool[iCn], fmt, 1.0f, 0.0f, e1);
+            ey.out[1] = eout(pool[iTn], fmt, -0.5f, gT, eh);
+            ey.out[2] = eout(pool[iZn], fmt, -0.5f, 1.5f, eh);
             DASH_TRY(gemm(prec, B, nc, pool[iY], 0, pool[iT], 0, ey, st, S));
           }
           iC = iCn;
@@ -758,7 +863,8 @@ dash_status inv_root_ndb(const float* A, float ridge, const float* scale, int64_
           // Z_K = T_{K-1} Z_{K-1}, scaled by s^{-1/4}, into the caller's output.
           EpiParams ez = epi_none();
           ez.nout = 1;
-          ez.out[0] = eout(Xout, FMT_F32, 1.0f, 0.0f, 0.0f, m14);
+          ez.out[0] = eout(Xout, FMT_F32, 1.0f, 0.0f, shift ? 1.0f : 0.0f, m14);
+          if (shift) with_e(ez, pool[iZ], fmt);  // Z + D Z
           DASH_TRY(gemm(prec, B, nc, pool[iT], 0, pool[iZ], 0, ez, st, SI));
         }
       }
@@ -786,8 +892,10 @@ dash_status dash_select_tiers(const float* lam_max, const float* lam_min, int64_
   if (!lam_max || !lam_min || !choice) return DASH_ERR_INVALID_ARG;
   for (int64_t k = 0; k < n; ++k) {
     const double hi = lam_max[k], lo = lam_min[k];
+    // No usable estimate unless both are positive (NaN compares false): inf, the
+    // last (most accurate) tier.
     double kappa = std::numeric_limits<double>::infinity();
-    if (lo > 0.0 && !std::isnan(hi)) kappa = hi / lo;
+    if (lo > 0.0 && hi > 0.0) kappa = hi / lo;
     int32_t pick = ntiers - 1;
     if (!std::isnan(kappa)) {
       for (int t = 0; t < ntiers; ++t) {
@@ -919,6 +1027,185 @@ dash_status inv_root_cheb(const float* A, float ridge, const float* scale, int64
     // the caller's X is completed below the diagonal afterwards.
     DASH_TRY(gemm(prec, B, nc, bS, 0, bb[i1], 0, e, st, S));
     if (S) DASH_TRY(launch_mirror_lower(Xc, B, nc, st));
+  }
+  return DASH_OK;
+}
+
+// ---------------------------------------------------------------- per-block solver selection
+
+namespace {
+
+// Bytes spectral_scale needs for n blocks in `mode` (0 for Frobenius).
+size_t scale_ws_bytes(int mode, long long n, int B, int n_vec) {
+  size_t b = 0;
+  const int prec = (mode == DASH_SCALE_POWER_F16)    ? DASH_FP16
+                   : (mode == DASH_SCALE_POWER_BF16) ? DASH_BF16
+                                                     : DASH_FP32_3XTF32;
+  if (dash_workspace_size(DASH_OP_SPECTRAL_SCALE, n, B, prec, n_vec, &b) != DASH_OK) return 0;
+  return b;
+}
+
+// Workspace of one solve of n blocks by tier t (its solver's full one-pass size).
+size_t tier_ws_bytes(const dash_tier& t, long long n, int B) {
+  const int op = t.solver == DASH_SOLVER_CN    ? DASH_OP_INV_ROOT_CN
+                 : t.solver == DASH_SOLVER_NDB ? DASH_OP_INV_ROOT_NDB
+                                               : DASH_OP_INV_ROOT_CHEB;
+  size_t b = 0;
+  if (dash_workspace_size(op, n, B, t.prec, t.iters, &b) != DASH_OK) return 0;
+  return b;
+}
+
+dash_status solve_tier(const dash_tier& t, const float* A, float ridge, const float* lam, long long n,
+                       int B, double lo, double hi, float* X, void* ws, size_t ws_bytes,
+                       cudaStream_t st) {
+  switch (t.solver) {
+    case DASH_SOLVER_CN:
+      return inv_root_cn(A, ridge, lam, n, B, t.iters, t.prec, X, nullptr, ws, ws_bytes, st);
+    case DASH_SOLVER_NDB:
+      return inv_root_ndb(A, ridge, lam, n, B, t.iters, t.prec, X, nullptr, ws, ws_bytes, st);
+    default:
+      return inv_root_cheb(A, ridge, lam, n, B, t.iters, lo, hi, t.prec, X, ws, ws_bytes, st);
+  }
+}
+
+bool valid_tiers(const dash_tier* tiers, int ntiers) {
+  if (!tiers || ntiers < 1) return false;
+  for (int t = 0; t < ntiers; ++t) {
+    const dash_tier& T = tiers[t];
+    if (T.solver < DASH_SOLVER_CN || T.solver > DASH_SOLVER_CHEB || !valid_prec(T.prec) ||
+        T.iters < 1 || !(T.u > 0.0) || !(T.gate > 0.0) ||
+        (T.solver == DASH_SOLVER_CHEB && T.iters > 64))
+      return false;
+  }
+  return true;
+}
+
+}  // namespace
+
+dash_status spectral_lambda_min(const float* A, float ridge, const float* lam_max, int64_t N, int B,
+                                int mode, int n_vec, int power_iters, const float* V0,
+                                float* lam_min_out, void* ws, size_t ws_bytes, void* stream) {
+  if (N < 0 || !valid_dim(B)) return DASH_ERR_INVALID_ARG;
+  if (mode != DASH_SCALE_POWER && mode != DASH_SCALE_POWER_F16 && mode != DASH_SCALE_POWER_BF16)
+    return DASH_ERR_INVALID_ARG;
+  if (n_vec < 1 || n_vec > 32 || power_iters < 1 || !V0) return DASH_ERR_INVALID_ARG;
+  if (N == 0) return DASH_OK;
+  if (!A || !lam_max || !lam_min_out || !aligned16(A) || !aligned16(V0))
+    return DASH_ERR_INVALID_ARG;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return DASH_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t blk = static_cast<size_t>(B) * B * 4;
+  // Per chunk of c blocks: the shifted stack, 1/c_k, mu_k, and spectral_scale's workspace.
+  auto need = [&](long long c) {
+    return round256(c * blk) + 2 * round256(c * 4) + round256(scale_ws_bytes(mode, c, B, n_vec));
+  };
+  long long chunk = N;
+  while (chunk > 0 && need(chunk) > ws_bytes) chunk = (chunk > 64) ? chunk * 3 / 4 : chunk - 1;
+  if (chunk < 1) return DASH_ERR_WORKSPACE_TOO_SMALL;
+  Carver cv(ws, ws_bytes);
+  float* S = static_cast<float*>(cv.take(chunk * blk));
+  float* inv_c = static_cast<float*>(cv.take(chunk * 4));
+  float* mu = static_cast<float*>(cv.take(chunk * 4));
+  const size_t sws = cv.left;
+  void* sw = cv.take(sws > 256 ? sws - 256 : 0);
+  if (!cv.ok || !sw) return DASH_ERR_WORKSPACE_TOO_SMALL;
+  for (long long c0 = 0; c0 < N; c0 += chunk) {
+    const long long nc = (N - c0 < chunk) ? N - c0 : chunk;
+    // S_k = c_k I - (A_k + ridge I) = c_k (I - (A_k + ridge I) / c_k), c_k = lam_max[k].
+    DASH_TRY(launch_scale_factors(lam_max + c0, inv_c, mu, nc, st));  // mu: scratch here
+    AffParams a = aff_from(offset_blocks(A, c0, B, 4), nullptr, FMT_F32, B, nc);
+    a.ridge = ridge;
+    a.inv_s = inv_c;
+    a.nout = 1;
+    Buf sb;
+    sb.hi = S;
+    a.out[0] = aout(sb, FMT_F32, -1.0f, 1.0f, lam_max + c0);
+    DASH_TRY(launch_affine(a, st));
+    DASH_TRY(spectral_scale(S, 0.0f, nc, B, mode, n_vec, power_iters,
+                            V0 + static_cast<size_t>(c0) * B * n_vec, mu, sw, sws - 256, st));
+    DASH_TRY(launch_sub(lam_max + c0, mu, lam_min_out + c0, nc, st));
+  }
+  return DASH_OK;
+}
+
+dash_status dash_auto_workspace_size(int64_t N, int B, const dash_tier* tiers, int ntiers,
+                                     size_t* bytes) {
+  if (!bytes || N < 0 || !valid_dim(B) || !valid_tiers(tiers, ntiers)) return DASH_ERR_INVALID_ARG;
+  size_t worst = 0;
+  for (int t = 0; t < ntiers; ++t) {
+    const size_t w = tier_ws_bytes(tiers[t], N, B);
+    if (w > worst) worst = w;
+  }
+  const size_t blk = static_cast<size_t>(B) * B * 4;
+  // Index list, gathered scales, gathered blocks and their roots, the solver's workspace.
+  *bytes = round256(N * 4) + round256(N * 4) + 2 * round256(N * blk) + round256(worst);
+  return DASH_OK;
+}
+
+dash_status inv_root_auto(const float* A, float ridge, const float* lam_max, const float* lam_min,
+                          int64_t N, int B, const dash_tier* tiers, int ntiers, double cheb_lo,
+                          double cheb_hi, float* X, int32_t* choice_out, void* ws,
+                          size_t ws_bytes, void* stream) {
+  if (N < 0 || !valid_dim(B) || !valid_tiers(tiers, ntiers)) return DASH_ERR_INVALID_ARG;
+  for (int t = 0; t < ntiers; ++t)
+    if (tiers[t].solver == DASH_SOLVER_CHEB &&
+        (!(cheb_lo > 0.0) || !(cheb_hi > cheb_lo) || !std::isfinite(cheb_hi)))
+      return DASH_ERR_INVALID_ARG;
+  if (N == 0) return DASH_OK;
+  if (!A || !lam_max || !lam_min || !X || !aligned16(A) || !aligned16(X) || !aligned16(lam_max))
+    return DASH_ERR_INVALID_ARG;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return DASH_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The one synchronisation: both estimates come back to the host for the tier rule.
+  std::vector<float> hmax(N), hmin(N);
+  if (cudaMemcpyAsync(hmax.data(), lam_max, N * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemcpyAsync(hmin.data(), lam_min, N * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return DASH_ERR_CUDA;
+  std::vector<int32_t> choice(N);
+  DASH_TRY(dash_select_tiers(hmax.data(), hmin.data(), N, tiers, ntiers, choice.data()));
+  if (choice_out) std::memcpy(choice_out, choice.data(), N * sizeof(int32_t));
+  const size_t blk = static_cast<size_t>(B) * B * 4;
+  for (int t = 0; t < ntiers; ++t) {
+    std::vector<int32_t> idx;
+    for (int64_t k = 0; k < N; ++k)
+      if (choice[k] == t) idx.push_back(static_cast<int32_t>(k));
+    const long long n = static_cast<long long>(idx.size());
+    if (n == 0) continue;
+    if (idx.back() - idx.front() + 1 == n) {
+      // One contiguous range: solve in place, no copies.
+      const long long a = idx.front();
+      DASH_TRY(solve_tier(tiers[t], offset_blocks(A, a, B, 4), ridge, lam_max + a, n, B, cheb_lo,
+                          cheb_hi, offset_blocks(X, a, B, 4), ws, ws_bytes, st));
+      continue;
+    }
+    // Gather the tier's blocks (and scales) into a sub-stack, solve, scatter the roots.
+    Carver cv(ws, ws_bytes);
+    int32_t* didx = static_cast<int32_t*>(cv.take(n * 4));
+    float* dlam = static_cast<float*>(cv.take(n * 4));
+    if (!cv.ok) return DASH_ERR_WORKSPACE_TOO_SMALL;
+    long long chunk = n;
+    while (chunk > 0 && 2 * round256(chunk * blk) + round256(tier_ws_bytes(tiers[t], chunk, B)) >
+                            cv.left)
+      chunk = (chunk > 64) ? chunk * 3 / 4 : chunk - 1;
+    if (chunk < 1) return DASH_ERR_WORKSPACE_TOO_SMALL;
+    float* At = static_cast<float*>(cv.take(chunk * blk));
+    float* Xt = static_cast<float*>(cv.take(chunk * blk));
+    const size_t sws = cv.left;
+    void* sw = cv.take(sws > 256 ? sws - 256 : 0);
+    if (!cv.ok || !sw) return DASH_ERR_WORKSPACE_TOO_SMALL;
+    if (cudaMemcpyAsync(didx, idx.data(), n * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
+      return DASH_ERR_CUDA;
+    DASH_TRY(launch_copy_items(lam_max, dlam, didx, 0, 1, n, st));
+    for (long long c0 = 0; c0 < n; c0 += chunk) {
+      const long long nc = (n - c0 < chunk) ? n - c0 : chunk;
+      DASH_TRY(launch_copy_items(A, At, didx + c0, 0, static_cast<long long>(B) * B, nc, st));
+      DASH_TRY(solve_tier(tiers[t], At, ridge, dlam + c0, nc, B, cheb_lo, cheb_hi, Xt, sw,
+                          sws - 256, st));
+      DASH_TRY(launch_copy_items(Xt, X, didx + c0, 1, static_cast<long long>(B) * B, nc, st));
+    }
+    // The next tier's index upload reuses didx; it is ordered after these kernels
+    // on the stream (a copy from pageable host memory also waits for the stream).
   }
   return DASH_OK;
 }

@@ -18,10 +18,24 @@ enum Fmt : int {
   FMT_SPLIT = 2,  // two fp32 arrays: hi = rna_tf32(x), lo = rna_tf32(x - hi)
   FMT_F16 = 3,
   FMT_BF16 = 4,
+  // Unevaluated sum of two 16-bit numbers in two arrays: hi = rn16(x), lo =
+  // rn16(x - hi) (x - hi is exact in fp32).  About 22 significant bits (fp16) or
+  // 16 (bf16) in the range of the 16-bit type; a tensor-core operand of this
+  // format takes two products, one per part.
+  FMT_F16X2 = 5,
+  FMT_BF16X2 = 6,
 };
 
-// Tensor-core operand kinds.
-enum Kind : int { KIND_F16 = 0, KIND_BF16 = 1, KIND_TF32 = 2, KIND_TF32X3 = 3 };
+// Tensor-core operand kinds.  The _SPLITB kinds take B in FMT_F16X2 / FMT_BF16X2:
+// C = A B_hi + A B_lo, both products of one 16-bit type.
+enum Kind : int {
+  KIND_F16 = 0,
+  KIND_BF16 = 1,
+  KIND_TF32 = 2,
+  KIND_TF32X3 = 3,
+  KIND_F16_SPLITB = 4,
+  KIND_BF16_SPLITB = 5
+};
 
 // Device error codes recorded in g_dash_error (mirrors dash_status values).
 constexpr int DEV_ERR_TIMEOUT = 5;
@@ -108,17 +122,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, 
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
-
-// 3-D tiled load multicast to every CTA of the cluster named in cta_mask; dst and
-// bar are CTA-relative shared addresses, valid in each destination CTA.
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* m, uint32_t bar,
-                                               int x, int y, int z, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "r"(z), "h"(cta_mask)
       : "memory");
 }
 
@@ -247,15 +250,6 @@ __device__ __forceinline__ void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, ui
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-
-// As mma_commit, arriving on the barrier at the same offset in every CTA of cta_mask.
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
-      "h"(cta_mask)
       : "memory");
 }
 
@@ -389,9 +383,43 @@ __device__ __forceinline__ float rna_tf32(float x) {
   return __uint_as_float(r);
 }
 
-// Bytes per element of a storage format (both halves for the split format).
+// Bytes per element of a storage format (both halves for the split formats).
 __host__ __device__ constexpr int fmt_bytes(int fmt) {
   return fmt == FMT_SPLIT ? 8 : ((fmt == FMT_F16 || fmt == FMT_BF16) ? 2 : 4);
+}
+
+__host__ __device__ constexpr bool fmt_is_pair16(int fmt) {
+  return fmt == FMT_F16X2 || fmt == FMT_BF16X2;
+}
+
+// The two 16-bit parts of x: hi = rn16(x), lo = rn16(x - hi), packed two values
+// per 32-bit word (a in the low half).
+__device__ __forceinline__ void pair16_pack(bool bf, float a, float b, uint32_t& hi, uint32_t& lo) {
+  if (bf) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+  } else {
+    const __half2 h = __floats2half2_rn(a, b);
+    const float2 hf = __half22float2(h);
+    const __half2 l = __floats2half2_rn(a - hf.x, b - hf.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+  }
+}
+
+// Value of one packed word pair (two elements) of a pair format.
+__device__ __forceinline__ float2 pair16_unpack(bool bf, uint32_t hi, uint32_t lo) {
+  if (bf) {
+    const float2 h = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi));
+    const float2 l = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&lo));
+    return make_float2(h.x + l.x, h.y + l.y);
+  }
+  const float2 h = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+  const float2 l = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+  return make_float2(h.x + l.x, h.y + l.y);
 }
 
 // Element offset helpers use 64-bit arithmetic throughout.
@@ -403,6 +431,12 @@ __device__ __forceinline__ float load_elem(int fmt, const void* hi, const void* 
       return __bfloat162float(static_cast<const __nv_bfloat16*>(hi)[i]);
     case FMT_SPLIT:
       return static_cast<const float*>(hi)[i] + static_cast<const float*>(lo)[i];
+    case FMT_F16X2:
+      return __half2float(static_cast<const __half*>(hi)[i]) +
+             __half2float(static_cast<const __half*>(lo)[i]);
+    case FMT_BF16X2:
+      return __bfloat162float(static_cast<const __nv_bfloat16*>(hi)[i]) +
+             __bfloat162float(static_cast<const __nv_bfloat16*>(lo)[i]);
     default:
       return static_cast<const float*>(hi)[i];
   }
@@ -420,6 +454,13 @@ __device__ __forceinline__ void load4(int fmt, const void* hi, const void* lo, i
     const uint2 u = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(hi) + i);
     const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
     const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+  } else if (fmt_is_pair16(fmt)) {
+    const bool bf = (fmt == FMT_BF16X2);
+    const uint2 h = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(hi) + i);
+    const uint2 l = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(lo) + i);
+    const float2 a = pair16_unpack(bf, h.x, l.x);
+    const float2 b = pair16_unpack(bf, h.y, l.y);
     v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
   } else {
     const float4 a = *reinterpret_cast<const float4*>(static_cast<const float*>(hi) + i);
@@ -447,6 +488,13 @@ __device__ __forceinline__ void store4(int fmt, void* hi, void* lo, int64_t i, c
     u.x = *reinterpret_cast<uint32_t*>(&a);
     u.y = *reinterpret_cast<uint32_t*>(&b);
     *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(hi) + i) = u;
+  } else if (fmt_is_pair16(fmt)) {
+    const bool bf = (fmt == FMT_BF16X2);
+    uint2 h, l;
+    pair16_pack(bf, v[0], v[1], h.x, l.x);
+    pair16_pack(bf, v[2], v[3], h.y, l.y);
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(hi) + i) = h;
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(lo) + i) = l;
   } else if (fmt == FMT_TF32) {
     float4 a = make_float4(rna_tf32(v[0]), rna_tf32(v[1]), rna_tf32(v[2]), rna_tf32(v[3]));
     *reinterpret_cast<float4*>(static_cast<float*>(hi) + i) = a;
@@ -502,6 +550,14 @@ __device__ __forceinline__ void store16_v8(int fmt, void* hi, void* lo, int64_t 
     st_v8(static_cast<uint16_t*>(hi) + i, r);
     return;
   }
+  if (fmt_is_pair16(fmt)) {
+    uint32_t rh[8], rl[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) pair16_pack(fmt == FMT_BF16X2, v[2 * j], v[2 * j + 1], rh[j], rl[j]);
+    st_v8(static_cast<uint16_t*>(hi) + i, rh);
+    st_v8(static_cast<uint16_t*>(lo) + i, rl);
+    return;
+  }
   uint32_t h[16], l[16];
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
@@ -538,6 +594,18 @@ __device__ __forceinline__ void load16_v8(int fmt, const void* hi, const void* l
         v[2 * j] = f.x;
         v[2 * j + 1] = f.y;
       }
+    }
+    return;
+  }
+  if (fmt_is_pair16(fmt)) {
+    uint32_t rh[8], rl[8];
+    ld_v8(static_cast<const uint16_t*>(hi) + i, rh);
+    ld_v8(static_cast<const uint16_t*>(lo) + i, rl);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float2 f = pair16_unpack(fmt == FMT_BF16X2, rh[j], rl[j]);
+      v[2 * j] = f.x;
+      v[2 * j + 1] = f.y;
     }
     return;
   }

@@ -27,6 +27,7 @@ struct EpiParams {
   int E_fmt;
   float* resid_acc;        // if set: resid_acc[blk * resid_stride] += sum (C - I)^2
   long long resid_stride;
+  int resid_plus_e;        // residual of C + E instead of C (identity-shifted iterates)
   const int* pad_valid;    // if set: rows / cols >= pad_valid[blk] become the identity's
 };
 
@@ -102,6 +103,15 @@ dash_status launch_pack_blocks(const void* M, int esize, long long rows, long lo
                                cudaStream_t st);
 dash_status launch_unpack_blocks(const void* blocks, int esize, long long rows, long long cols,
                                  long long ld, int b, void* M, cudaStream_t st);
+
+// out[i] = a[i] - b[i].
+dash_status launch_sub(const float* a, const float* b, float* out, long long n, cudaStream_t st);
+
+// n items of `elems` floats: dst[j] = src[idx[j]] (scatter 0) or dst[idx[j]] = src[j]
+// (scatter 1), j < n; idx is a device array of n indices.  16-byte aligned pointers
+// when elems is a multiple of 4.
+dash_status launch_copy_items(const float* src, float* dst, const int32_t* idx, int scatter,
+                              long long elems, long long n, cudaStream_t st);
 
 // Fills the 256-tiles below the diagonal of each (dim, dim) fp32 block with the
 // transposes of their mirror tiles (a symmetric result stored as its upper half).

@@ -353,6 +353,62 @@ dash_status launch_unpack_blocks(const void* blocks, int esize, long long rows, 
   return err == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
 }
 
+__global__ void sub_kernel(const float* a, const float* b, float* out, long long n) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < n) out[i] = a[i] - b[i];
+}
+
+dash_status launch_sub(const float* a, const float* b, float* out, long long n, cudaStream_t st) {
+  if (n <= 0) return DASH_OK;
+  const int rec = trace_begin(st);
+  sub_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(a, b, out, n);
+  const cudaError_t err = cudaGetLastError();
+  trace_end(rec, st, DASH_TRACE_REDUCE, 0.0, 12.0 * n);
+  return err == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
+}
+
+// Item j of n items of `elems` floats each: dst[j] = src[idx[j]] (gather) or
+// dst[idx[j]] = src[j] (scatter).  grid.y walks the items, grid.x the 16-byte
+// vectors of one item (single floats when elems is not a multiple of 4).
+__global__ void __launch_bounds__(EW_THREADS)
+    copy_items_kernel(const float* src, float* dst, const int32_t* idx, int scatter,
+                      long long elems, long long n) {
+  for (long long j = blockIdx.y; j < n; j += gridDim.y) {
+    const long long k = idx[j];
+    const float* s = src + (scatter ? j : k) * elems;
+    float* d = dst + (scatter ? k : j) * elems;
+    if ((elems & 3) == 0) {
+      const long long nv = elems >> 2;
+      for (long long v = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; v < nv;
+           v += static_cast<long long>(gridDim.x) * blockDim.x)
+        reinterpret_cast<float4*>(d)[v] = reinterpret_cast<const float4*>(s)[v];
+    } else {
+      for (long long v = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+           v < elems; v += static_cast<long long>(gridDim.x) * blockDim.x)
+        d[v] = s[v];
+    }
+  }
+}
+
+dash_status launch_copy_items(const float* src, float* dst, const int32_t* idx, int scatter,
+                              long long elems, long long n, cudaStream_t st) {
+  if (n <= 0 || elems <= 0) return DASH_OK;
+  const long long nv = (elems & 3) == 0 ? elems / 4 : elems;
+  long long gx = (nv + EW_THREADS - 1) / EW_THREADS;
+  if (gx > 64) gx = 64;
+  // About 8 CTAs per SM over the whole launch.
+  long long gy = (static_cast<long long>(device_sm_count()) * 8 + gx - 1) / gx;
+  if (gy > n) gy = n;
+  if (gy > 65535) gy = 65535;
+  if (gy < 1) gy = 1;
+  const int rec = trace_begin(st);
+  copy_items_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), EW_THREADS, 0,
+                      st>>>(src, dst, idx, scatter, elems, n);
+  const cudaError_t err = cudaGetLastError();
+  trace_end(rec, st, DASH_TRACE_ELEMENTWISE, 0.0, 8.0 * static_cast<double>(elems) * n);
+  return err == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
+}
+
 // Completes a symmetric result stored as its 256 x 256 tiles on or above the
 // diagonal: every tile below it becomes the transpose of its mirror tile.  One
 // CTA per 32 x 32 sub-tile, transposed through padded shared memory so both the

@@ -39,32 +39,41 @@ int gemm_read_clear_error() {
   return v;
 }
 
-// KT: 0 = 16-bit operands (kind::f16), 1 = TF32, 2 = 3xTF32.
+// KT: 0 = 16-bit operands (kind::f16), 1 = TF32, 2 = 3xTF32, 3 = 16-bit A and a
+//     16-bit pair B (FMT_F16X2 / FMT_BF16X2): A B_lo, then A B_hi, per K slice
+//     into the same accumulator.
 // MODE: 0 = one CTA per 128 x BN tile;
-//       1 = clusters of two CTAs on adjacent 128-row tiles that share the N tile,
-//           each fetching half of B and multicasting it to both;
 //       2 = CTA pairs running one 256 x BN MMA (cta_group::2): each CTA stages
 //           its own 128 rows of A and half of B, the even CTA issues the MMA and
 //           both CTAs hold 128 rows of the accumulator.
+// Every CTA loads its own operand tiles; no load is shared between CTAs.
 template <int BN, int KT, int MODE>
 struct Cfg {
+  static_assert(MODE == 0 || MODE == 2, "MODE is 0 (single CTA) or 2 (CTA pair)");
   static constexpr int CL = MODE ? 2 : 1;       // CTAs per cluster
   static constexpr int BM = 128;                // accumulator rows per CTA
-  static constexpr int EB = (KT == 0) ? 2 : 4;  // operand element bytes
+  static constexpr bool H16 = (KT == 0 || KT == 3);  // 16-bit operands (kind::f16)
+  static constexpr int EB = H16 ? 2 : 4;        // operand element bytes
   static constexpr int BK = 128 / EB;           // elements per 128-byte row
-  static constexpr int UK = (KT == 0) ? 16 : 8; // K of one MMA
+  static constexpr int UK = H16 ? 16 : 8;       // K of one MMA
   static constexpr int NSUB = BK / UK;          // MMAs per k-block
   static constexpr int A_BYTES = BM * 128;
   static constexpr int B_ROWS = (MODE == 2) ? BN / 2 : BN;  // B rows staged per CTA
   static constexpr int B_BYTES = B_ROWS * 128;
-  static constexpr int NPART = (KT == 2) ? 2 : 1;
-  static constexpr int STAGE_BYTES = (A_BYTES + B_BYTES) * NPART;
+  // Operand parts staged per k-block: hi and lo of both operands for 3xTF32, of
+  // B alone for KT 3.  Stage layout: A | B | A_lo | B_lo (3xTF32), A | B | B_lo (KT 3).
+  static constexpr int NPART_A = (KT == 2) ? 2 : 1;
+  static constexpr int NPART_B = (KT == 2 || KT == 3) ? 2 : 1;
+  static constexpr int NPART = NPART_B;
+  static constexpr int LO_A = A_BYTES + B_BYTES;                     // A_lo after sA
+  static constexpr int LO_B = (KT == 2) ? A_BYTES + B_BYTES : B_BYTES;  // B_lo after sB
+  static constexpr int STAGE_BYTES = A_BYTES * NPART_A + B_BYTES * NPART_B;
   // Bytes the barrier owner waits for per stage (both CTAs' loads for a pair).
   static constexpr int EXPECT_BYTES = (MODE == 2 ? 2 : 1) * STAGE_BYTES;
   // fp16/bf16-operand kernels stage 16-bit output tiles through shared memory
   // (4 KB per epilogue warp) so that global stores cover whole rows.
   static constexpr int EPI_WARP_BYTES = 4096;
-  static constexpr int EPI_BYTES = (KT == 0) ? 8 * EPI_WARP_BYTES : 0;
+  static constexpr int EPI_BYTES = H16 ? 8 * EPI_WARP_BYTES : 0;
   static constexpr int STAGES_RAW = (224 * 1024 - EPI_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
   static constexpr int TMEM_COLS = 2 * BN;
@@ -75,8 +84,8 @@ struct Cfg {
   static constexpr int MN_BOX_BYTES = BK * 128;  // one MN-major box: BK rows of 128 B
   // MN-major 32-bit operands are read with 32-byte swizzle atoms; that layout
   // groups K in slabs of 4 rows (512 B), the 16-byte-atom layout in slabs of 8.
-  static constexpr uint32_t MN_LAYOUT = (KT == 0) ? LAYOUT_SW128 : LAYOUT_SW128_BASE32;
-  static constexpr uint32_t MN_SBO = (KT == 0) ? 1024 : 512;
+  static constexpr uint32_t MN_LAYOUT = H16 ? LAYOUT_SW128 : LAYOUT_SW128_BASE32;
+  static constexpr uint32_t MN_SBO = H16 ? 1024 : 512;
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + BAR_BYTES + EPI_BYTES;
   static_assert(STAGES >= 2, "need at least two pipeline stages");
@@ -112,18 +121,22 @@ template <int CL>
 __device__ __forceinline__ void decode_unit(long long u, const KParams& p, uint32_t crank,
                                             long long& blk, int& m0, int& n0, int bn) {
   if (p.sym_out) {
-    // Pair tiles (mt, nt) with nt >= mt, row by row: T(T+1)/2 per block.
+    // 256 x 256 tiles (mt, nt) with nt >= mt, row by row: T(T+1)/2 per block, each
+    // split into 256 / bn column tiles of width bn.
     const int T = p.t256;
-    const long long per = static_cast<long long>(T) * (T + 1) / 2;
+    const int nh = 256 / bn;
+    const long long per = static_cast<long long>(T) * (T + 1) / 2 * nh;
     blk = u / per;
     int t = static_cast<int>(u - blk * per);
+    const int h = t % nh;
+    t /= nh;
     int mt = 0;
     while (t >= T - mt) {
       t -= T - mt;
       ++mt;
     }
     m0 = mt * 256 + static_cast<int>(crank) * 128;
-    n0 = (mt + t) * 256;
+    n0 = (mt + t) * 256 + h * bn;
     return;
   }
   const long long per = static_cast<long long>(p.tiles_m / CL) * p.tiles_n;
@@ -177,18 +190,6 @@ __device__ __forceinline__ void epi_pre16(const EpiParams& e, int rg, int cg0, l
                                           float (&ev)[16]) {
   // diag: this warp's rows and these 16 columns share a diagonal element (a
   // warp-uniform flag: off-diagonal chunks skip every identity term).
-  if (e.resid_acc != nullptr) {
-    if (diag) {
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float d = c[j] - ((rg == cg0 + j) ? 1.0f : 0.0f);
-        rsum = fmaf(d, d, rsum);
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 16; ++j) rsum = fmaf(c[j], c[j], rsum);
-    }
-  }
   if (e.E_hi != nullptr) {
     if (aligned32(e.E_hi) && (e.E_fmt != FMT_SPLIT || aligned32(e.E_lo))) {
       load16_v8(e.E_fmt, e.E_hi, e.E_lo, idx, ev);
@@ -204,6 +205,23 @@ __device__ __forceinline__ void epi_pre16(const EpiParams& e, int rg, int cg0, l
   } else {
 #pragma unroll
     for (int j = 0; j < 16; ++j) ev[j] = 0.0f;
+  }
+  if (e.resid_acc != nullptr) {
+    // Residual of the iterate: C itself, or C + E when the iterate is stored as its
+    // deviation from a matrix the epilogue adds (E).
+    float x[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) x[j] = e.resid_plus_e ? c[j] + ev[j] : c[j];
+    if (diag) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float d = x[j] - ((rg == cg0 + j) ? 1.0f : 0.0f);
+        rsum = fmaf(d, d, rsum);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) rsum = fmaf(x[j], x[j], rsum);
+    }
   }
 }
 
@@ -361,8 +379,8 @@ __global__ void __launch_bounds__(320, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      // MODE 1: released by the MMA warp of both CTAs; MODE 2: by the leader's.
-      mbar_init(empty_bar(s), MODE == 1 ? 2 : 1);
+      // Released by the MMA warp (in a pair, the leader's).
+      mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
@@ -377,10 +395,8 @@ __global__ void __launch_bounds__(320, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tA);
     tma_prefetch_desc(&tB);
-    if (KT == 2) {
-      tma_prefetch_desc(&tAl);
-      tma_prefetch_desc(&tBl);
-    }
+    if (C::NPART_A == 2) tma_prefetch_desc(&tAl);
+    if (C::NPART_B == 2) tma_prefetch_desc(&tBl);
   }
   if (warp == 1) {
     if (MODE == 2)
@@ -423,9 +439,11 @@ __global__ void __launch_bounds__(320, 1)
           // In a pair, every load is counted on the leader's barrier.
           if (MODE == 2) fb = leader ? fb : mapa_shared(fb, crank & ~1u);
           const int k0 = kb * C::BK;
-          for (int part = 0; part < C::NPART; ++part) {
-            const uint32_t sA = sbase + stage * C::STAGE_BYTES + part * (C::A_BYTES + C::B_BYTES);
-            const uint32_t sB = sA + C::A_BYTES;
+          for (int part = 0; part < C::NPART_B; ++part) {
+            const uint32_t s0 = sbase + stage * C::STAGE_BYTES;
+            const uint32_t sA = s0 + part * C::LO_A;
+            const uint32_t sB = s0 + C::A_BYTES + part * C::LO_B;
+            const bool loadA = part < C::NPART_A;  // KT 3 has one A part
             const CUtensorMap* ma = part ? &tAl : &tA;
             const CUtensorMap* mb = part ? &tBl : &tB;
             if (MODE == 2) {
@@ -434,8 +452,9 @@ __global__ void __launch_bounds__(320, 1)
               const bool amir = p.sym_in && (k0 >> 8) < (m0 >> 8);
               const bool bmir = p.sym_in && (k0 >> 8) > (n0 >> 8);
               if (amir) ma = &p.tAm;
-              if (bmir) mb = &p.tBm;
-              if (!(p.a_mn ^ amir)) {
+              if (bmir) mb = part ? &p.tBlm : &p.tBm;
+              if (!loadA) {
+              } else if (!(p.a_mn ^ amir)) {
                 tma_load_3d_pair(sA, ma, fb, k0, m0, z);
               } else {
 #pragma unroll
@@ -452,35 +471,20 @@ __global__ void __launch_bounds__(320, 1)
               }
               continue;
             }
-            if (!p.a_mn) {
+            if (!loadA) {
+            } else if (!p.a_mn) {
               tma_load_3d(sA, ma, fb, k0, m0, z);
             } else {
 #pragma unroll
               for (int i = 0; i < C::A_BOXES_MN; ++i)
                 tma_load_3d(sA + i * C::MN_BOX_BYTES, ma, fb, m0 + i * C::MN_ATOM, k0, z);
             }
-            if (CL == 1) {
-              if (!p.b_mn) {
-                tma_load_3d(sB, mb, fb, k0, n0, z);
-              } else {
-#pragma unroll
-                for (int i = 0; i < C::B_BOXES_MN; ++i)
-                  tma_load_3d(sB + i * C::MN_BOX_BYTES, mb, fb, n0 + i * C::MN_ATOM, k0, z);
-              }
+            if (!p.b_mn) {
+              tma_load_3d(sB, mb, fb, k0, n0, z);
             } else {
-              // The shared N tile: each CTA fetches its share and multicasts it to all.
-              if (!p.b_mn) {
-                const int rows = BN / CL;
-                tma_load_3d_mc(sB + crank * rows * 128, mb, fb, k0, n0 + crank * rows, z, kMask);
-              } else {
-                constexpr int per = C::B_BOXES_MN / CL;
 #pragma unroll
-                for (int j = 0; j < per; ++j) {
-                  const int i = static_cast<int>(crank) * per + j;
-                  tma_load_3d_mc(sB + i * C::MN_BOX_BYTES, mb, fb, n0 + i * C::MN_ATOM, k0, z,
-                                 kMask);
-                }
-              }
+              for (int i = 0; i < C::B_BOXES_MN; ++i)
+                tma_load_3d(sB + i * C::MN_BOX_BYTES, mb, fb, n0 + i * C::MN_ATOM, k0, z);
             }
           }
           if (++stage == C::STAGES) {
@@ -539,18 +543,21 @@ __global__ void __launch_bounds__(320, 1)
                     : smem_desc_sw128(sB + kk * 32, 16, 1024);
             const uint32_t accum = (kb | kk) ? 1u : 0u;
             uint64_t dal = 0, dbl = 0;
-            if (KT == 2) {
-              const uint32_t lo_off = C::A_BYTES + C::B_BYTES;
-              dal = amn ? smem_desc(sA + lo_off + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO,
+            if (C::NPART_A == 2)
+              dal = amn ? smem_desc(sA + C::LO_A + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO,
                                     C::MN_LAYOUT)
-                        : smem_desc_sw128(sA + lo_off + kk * 32, 16, 1024);
-              dbl = bmn ? smem_desc(sB + lo_off + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO,
+                        : smem_desc_sw128(sA + C::LO_A + kk * 32, 16, 1024);
+            if (C::NPART_B == 2)
+              dbl = bmn ? smem_desc(sB + C::LO_B + kk * C::UK * 128, C::MN_BOX_BYTES, C::MN_SBO,
                                     C::MN_LAYOUT)
-                        : smem_desc_sw128(sB + lo_off + kk * 32, 16, 1024);
-            }
+                        : smem_desc_sw128(sB + C::LO_B + kk * 32, 16, 1024);
             if (MODE == 2) {
               if (KT == 0) {
                 mma_f16_pair(d_tmem, da, db, idesc, accum);
+              } else if (KT == 3) {
+                // The small part first, then the large one, into the same sum.
+                mma_f16_pair(d_tmem, da, dbl, idesc, accum);
+                mma_f16_pair(d_tmem, da, db, idesc, 1u);
               } else if (KT == 1) {
                 mma_tf32_pair(d_tmem, da, db, idesc, accum);
               } else {
@@ -561,6 +568,9 @@ __global__ void __launch_bounds__(320, 1)
             } else {
               if (KT == 0) {
                 mma_f16(d_tmem, da, db, p.idesc, accum);
+              } else if (KT == 3) {
+                mma_f16(d_tmem, da, dbl, p.idesc, accum);
+                mma_f16(d_tmem, da, db, p.idesc, 1u);
               } else if (KT == 1) {
                 mma_tf32(d_tmem, da, db, p.idesc, accum);
               } else {
@@ -573,8 +583,6 @@ __global__ void __launch_bounds__(320, 1)
           // The stage is free once every CTA whose shared memory fed it is done.
           if (MODE == 2)
             mma_commit_pair_mc(empty_bar(stage), kMask);
-          else if (MODE == 1)
-            mma_commit_mc(empty_bar(stage), kMask);
           else
             mma_commit(empty_bar(stage));
           if (++stage == C::STAGES) {
@@ -705,28 +713,37 @@ __global__ void __launch_bounds__(320, 1)
 }
 
 // ---------------------------------------------------------------- accurate 3xTF32
-// The tensor core's fp32 accumulation truncates: a K-long product picks up a
-// relative bias of about -(K/8) 2^-24.  This variant of the pair kernel for
-// 3xTF32 bounds it: the MMA warp starts a fresh TMEM partial accumulator every
-// ACC_SUB sub-steps (one sub-step = the three MMAs of one K = 8 slice; two
-// partials alternate), and eight reducer warps -- two per TMEM lane quarter, 128
-// columns each -- add the partials into fp32 registers with round-to-nearest.
-// The fused epilogue then runs on those register sums.  The partial length trades
-// bias for speed: while the reducers run a tile's epilogue the MMA can only fill
-// the two partial buffers, so short partials leave it idle.  32 sub-steps (96
-// truncating instructions, a quarter of the single-accumulator chain at K = 1024)
-// keep the solvers above 60% of the 3xTF32 rate.
-constexpr int ACC_SUB = 32;  // K = 8 sub-steps per TMEM partial
+// The tensor core's fp32 accumulation truncates: every MMA instruction aligns its
+// products and the running sum to their largest exponent, drops the bits below
+// (toward zero) and rounds the result toward zero.  Over a long K the losses add
+// up with one sign, a relative bias of order (K/8) 2^-24, which ill-conditioned
+// iterations amplify.  This variant of the pair kernel for 3xTF32 keeps the bias
+// at the level of a few instructions: the MMA warp starts a fresh TMEM partial
+// accumulator every ACC_SUB sub-steps (one sub-step = the three MMAs of one K = 8
+// slice), and eight reducer warps -- two per TMEM lane quarter, 64 columns each --
+// add the partials into fp32 registers with round-to-nearest.  The fused epilogue
+// then runs on those register sums.  Pair tiles are 256 x 128, so that TMEM holds
+// four partial buffers: the MMA runs up to four partials ahead while the reducers
+// run a tile's epilogue.
+#ifndef DASH_ACC_SUB
+#define DASH_ACC_SUB 2
+#endif
+constexpr int ACC_SUB = DASH_ACC_SUB;  // K = 8 sub-steps per TMEM partial
+constexpr int ACC_BN = 128;            // pair tile 256 x 128
+constexpr int ACC_NPB = 4;             // TMEM partial buffers (4 x 128 columns)
+constexpr int ACC_REDUCERS = 8;        // reducer / epilogue warps per CTA
+constexpr int ACC_THREADS = 32 * (2 + ACC_REDUCERS);
 
 template <int KT>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(ACC_THREADS, 1)
     gemm_tc_acc_kernel(const __grid_constant__ CUtensorMap tA,
                        const __grid_constant__ CUtensorMap tB,
                        const __grid_constant__ CUtensorMap tAl,
                        const __grid_constant__ CUtensorMap tBl, const __grid_constant__ KParams p) {
-  constexpr int BN = 256;
+  constexpr int BN = ACC_BN;
   using C = Cfg<BN, KT, 2>;
   constexpr int CL = 2;
+  constexpr int NPB = ACC_NPB;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw_base & 1023u)) & 1023u;
@@ -738,10 +755,14 @@ __global__ void __launch_bounds__(320, 1)
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
   auto pfull_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
-  auto pempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + 2 + a); };
-  const uint32_t fin_bar = bar0 + 8u * (2 * C::STAGES + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * (2 * C::STAGES + 5));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * (2 * C::STAGES + 5) + 8);
+  auto pempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + NPB + a); };
+  const uint32_t fin_bar = bar0 + 8u * (2 * C::STAGES + 2 * NPB);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * (2 * C::STAGES + 2 * NPB + 1));
+  volatile int* abort_flag =
+      reinterpret_cast<volatile int*>(bar_area + 8 * (2 * C::STAGES + 2 * NPB + 1) + 8);
+  static_assert(8 * (2 * C::STAGES + 2 * NPB + 1) + 16 <= C::BAR_BYTES, "barrier area");
+  constexpr uint32_t TMEM_ACC_COLS = NPB * BN;
+  static_assert(TMEM_ACC_COLS == 512, "partial buffers fill TMEM");
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -757,9 +778,9 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < NPB; ++a) {
       mbar_init(pfull_bar(a), 1);
-      mbar_init(pempty_bar(a), 16);  // eight reducer warps in each CTA of the pair
+      mbar_init(pempty_bar(a), 2 * ACC_REDUCERS);  // the reducer warps of both CTAs
     }
     mbar_init(fin_bar, 1);
     *abort_flag = 0;
@@ -771,7 +792,7 @@ __global__ void __launch_bounds__(320, 1)
     tma_prefetch_desc(&tAl);
     tma_prefetch_desc(&tBl);
   }
-  if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), C::TMEM_COLS);
+  if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), TMEM_ACC_COLS);
   tc_fence_before();
   cluster_sync();
   tc_fence_after();
@@ -841,7 +862,7 @@ __global__ void __launch_bounds__(320, 1)
       // ------------------------------------------------------------ MMA issuer
       int stage = 0;
       uint32_t phase = 0;
-      long long gidx = 0;  // partials issued so far: buffer gidx & 1
+      long long gidx = 0;  // partials issued so far: buffer gidx % NPB
       int nsub = 0;        // sub-steps issued into the current partial
       uint32_t d_tmem = 0;
       bool ok = true;
@@ -867,9 +888,9 @@ __global__ void __launch_bounds__(320, 1)
                        : p.idesc;
 #pragma unroll
           for (int kk = 0; kk < C::NSUB; ++kk) {
-            const int buf = static_cast<int>(gidx & 1);
+            const int buf = static_cast<int>(gidx % NPB);
             if (nsub == 0) {
-              const uint32_t par = static_cast<uint32_t>((gidx >> 1) & 1);
+              const uint32_t par = static_cast<uint32_t>((gidx / NPB) & 1);
               if (!mbar_wait(pempty_bar(buf), par ^ 1u, abort_flag)) {
                 ok = false;
                 break;
@@ -913,8 +934,10 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else {
     // ------------------------------------------------- reducers + epilogue
-    const int q = warp & 3;          // TMEM lane quarter
-    const int h = (warp - 2) >> 2;   // column half: 0 -> 0..127, 1 -> 128..255
+    // Warp w: TMEM lane quarter w & 3, column group (w - 2) >> 2 of COLS columns.
+    constexpr int COLS = BN / (ACC_REDUCERS / 4);
+    const int q = warp & 3;
+    const int cq = (warp - 2) >> 2;
     const int row = q * 32 + lane;
     const long long dd = static_cast<long long>(p.dim) * p.dim;
     long long gidx = 0;
@@ -923,21 +946,21 @@ __global__ void __launch_bounds__(320, 1)
       long long blk;
       int m0, n0;
       decode_unit<CL>(u, p, crank, blk, m0, n0, BN);
-      float sum[128];
+      float sum[COLS];
 #pragma unroll
-      for (int j = 0; j < 128; ++j) sum[j] = 0.0f;
+      for (int j = 0; j < COLS; ++j) sum[j] = 0.0f;
       for (int kg = 0; kg < ngroups; ++kg, ++gidx) {
-        const int buf = static_cast<int>(gidx & 1);
-        const uint32_t par = static_cast<uint32_t>((gidx >> 1) & 1);
+        const int buf = static_cast<int>(gidx % NPB);
+        const uint32_t par = static_cast<uint32_t>((gidx / NPB) & 1);
         if (!mbar_wait(pfull_bar(buf), par, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                               static_cast<uint32_t>(buf * BN + h * 128);
+                               static_cast<uint32_t>(buf * BN + cq * COLS);
 #pragma unroll
-        for (int c = 0; c < 8; c += 2) {
+        for (int c = 0; c < COLS / 16; c += 2) {
           uint32_t ra[16], rb[16];
           tmem_ld16(taddr + c * 16, ra);
           tmem_ld16(taddr + (c + 1) * 16, rb);
@@ -955,12 +978,12 @@ __global__ void __launch_bounds__(320, 1)
       }
       if (!ok) break;
       const int rg = m0 + row;
-      const int cbase = n0 + h * 128;
+      const int cbase = n0 + cq * COLS;
       const long long rbase = blk * dd + static_cast<long long>(rg) * p.dim;
       const TileEpi te = tile_epi(p.epi, blk);
       float rsum = 0.0f;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < COLS / 16; ++c) {
         float v[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) v[j] = sum[c * 16 + j];
@@ -982,7 +1005,7 @@ __global__ void __launch_bounds__(320, 1)
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    tmem_dealloc_pair(tmem_base, TMEM_ACC_COLS);
   }
 }
 
@@ -1043,7 +1066,7 @@ int device_sm_count() {
 // Kernel entry of a configuration (ACC: the accurate 3xTF32 pair variant).
 template <int BN, int KT, int MODE, bool ACC>
 struct KernelOf {
-  static constexpr int THREADS = 320;
+  static constexpr int THREADS = ACC ? ACC_THREADS : 320;
   static auto get() {
     if constexpr (ACC)
       return gemm_tc_acc_kernel<KT>;
@@ -1092,20 +1115,17 @@ static dash_status run_gemm(const GemmLaunch& g, cudaStream_t st) {
   const uint32_t b_in = b_mn ? C::MN_ATOM : C::BK, b_out = b_mn ? C::BK : BN / CL;
   // The TMA swizzle must produce the layout the MMA descriptor names.
   const CUtensorMapSwizzle mn_swz =
-      (KT == 0) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B;
+      C::H16 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B;
   const CUtensorMapSwizzle a_swz = a_mn ? mn_swz : CU_TENSOR_MAP_SWIZZLE_128B;
   const CUtensorMapSwizzle b_swz = b_mn ? mn_swz : CU_TENSOR_MAP_SWIZZLE_128B;
   if (!make_tmap(&tA, g.A, C::EB, g.dim, g.nblocks, a_in, a_out, a_swz)) return DASH_ERR_CUDA;
   if (!make_tmap(&tB, g.B, C::EB, g.dim, g.nblocks, b_in, b_out, b_swz)) return DASH_ERR_CUDA;
-  if (KT == 2) {
-    if (!make_tmap(&tAl, g.A_lo, C::EB, g.dim, g.nblocks, a_in, a_out, a_swz))
-      return DASH_ERR_CUDA;
-    if (!make_tmap(&tBl, g.B_lo, C::EB, g.dim, g.nblocks, b_in, b_out, b_swz))
-      return DASH_ERR_CUDA;
-  } else {
-    tAl = tA;
-    tBl = tB;
-  }
+  tAl = tA;
+  tBl = tB;
+  if (C::NPART_A == 2 && !make_tmap(&tAl, g.A_lo, C::EB, g.dim, g.nblocks, a_in, a_out, a_swz))
+    return DASH_ERR_CUDA;
+  if (C::NPART_B == 2 && !make_tmap(&tBl, g.B_lo, C::EB, g.dim, g.nblocks, b_in, b_out, b_swz))
+    return DASH_ERR_CUDA;
   KParams p;
   p.dim = g.dim;
   p.tiles_m = g.dim / 128;
@@ -1113,7 +1133,9 @@ static dash_status run_gemm(const GemmLaunch& g, cudaStream_t st) {
   p.total_tiles = g.nblocks * p.tiles_m * p.tiles_n;
   p.total_units = p.total_tiles / CL;
   p.nkb = g.dim / C::BK;
-  const uint32_t fmt = (g.kind == KIND_BF16) ? 1u : (g.kind == KIND_F16 ? 0u : 2u);
+  const uint32_t fmt = (g.kind == KIND_BF16 || g.kind == KIND_BF16_SPLITB)
+                           ? 1u
+                           : ((g.kind == KIND_F16 || g.kind == KIND_F16_SPLITB) ? 0u : 2u);
   p.idesc = make_idesc(fmt, a_mn, b_mn, C::MMA_M, BN);
   p.idesc0 = make_idesc(fmt, 0, 0, C::MMA_M, BN);
   p.a_mn = a_mn;
@@ -1125,7 +1147,8 @@ static dash_status run_gemm(const GemmLaunch& g, cudaStream_t st) {
   p.sym_out = (sym_ok && g.sym_out) ? 1 : 0;
   p.t256 = g.dim / 256;
   if (p.sym_out) {
-    p.total_tiles = g.nblocks * p.t256 * (p.t256 + 1);  // CTA tiles: 2 per pair tile
+    // CTA tiles: 2 per pair tile, 256 / BN pair tiles per upper 256 x 256 tile.
+    p.total_tiles = g.nblocks * p.t256 * (p.t256 + 1) / 2 * (256 / BN) * CL;
     p.total_units = p.total_tiles / CL;
   }
   if (p.sym_in) {
@@ -1138,16 +1161,19 @@ static dash_status run_gemm(const GemmLaunch& g, cudaStream_t st) {
     if (!make_tmap(&p.tBm, g.B, C::EB, g.dim, g.nblocks, bm_in, bm_out,
                    !b_mn ? mn_swz : CU_TENSOR_MAP_SWIZZLE_128B))
       return DASH_ERR_CUDA;
-    if (KT == 2) {
-      if (!make_tmap(&p.tAlm, g.A_lo, C::EB, g.dim, g.nblocks, am_in, am_out,
-                     !a_mn ? mn_swz : CU_TENSOR_MAP_SWIZZLE_128B))
-        return DASH_ERR_CUDA;
-      if (!make_tmap(&p.tBlm, g.B_lo, C::EB, g.dim, g.nblocks, bm_in, bm_out,
-                     !b_mn ? mn_swz : CU_TENSOR_MAP_SWIZZLE_128B))
-        return DASH_ERR_CUDA;
-    }
+    p.tAlm = p.tAm;
+    p.tBlm = p.tBm;
+    if (C::NPART_A == 2 && !make_tmap(&p.tAlm, g.A_lo, C::EB, g.dim, g.nblocks, am_in, am_out,
+                                      !a_mn ? mn_swz : CU_TENSOR_MAP_SWIZZLE_128B))
+      return DASH_ERR_CUDA;
+    if (C::NPART_B == 2 && !make_tmap(&p.tBlm, g.B_lo, C::EB, g.dim, g.nblocks, bm_in, bm_out,
+                                      !b_mn ? mn_swz : CU_TENSOR_MAP_SWIZZLE_128B))
+      return DASH_ERR_CUDA;
   }
-  p.staged = (C::EPI_BYTES > 0 && g.epi.nout >= 1 && g.epi.nout <= 2) ? 1 : 0;
+#ifndef DASH_STAGED_EPILOGUE
+#define DASH_STAGED_EPILOGUE 1  // build-time: 0 stores every output directly
+#endif
+  p.staged = (DASH_STAGED_EPILOGUE && C::EPI_BYTES > 0 && g.epi.nout >= 1 && g.epi.nout <= 2) ? 1 : 0;
   for (int o = 0; o < g.epi.nout && p.staged; ++o) {
     const EpiOut& O = g.epi.out[o];
     if ((O.fmt != FMT_F16 && O.fmt != FMT_BF16) ||
@@ -1197,14 +1223,16 @@ static dash_status run_gemm(const GemmLaunch& g, cudaStream_t st) {
     // A symmetric output computes and writes only the (T + 1) / 2T of C on or above
     // the diagonal (T = dim / 256): those are the flops and output bytes it costs.
     const double frac = p.sym_out ? (p.t256 + 1.0) / (2.0 * p.t256) : 1.0;
-    double bytes = 2.0 * bb * (KT == 2 ? 8 : C::EB);
+    double bytes = bb * C::EB * (C::NPART_A + C::NPART_B);
     for (int o = 0; o < g.epi.nout; ++o) bytes += frac * bb * fmt_bytes(g.epi.out[o].fmt);
     if (g.epi.E_hi != nullptr) bytes += frac * bb * fmt_bytes(g.epi.E_fmt);
+    const bool bf = (g.kind == KIND_BF16 || g.kind == KIND_BF16_SPLITB);
     const int kind = KT == 2 ? DASH_TRACE_GEMM_3XTF32
                              : (KT == 1 ? DASH_TRACE_GEMM_TF32
-                                        : (g.kind == KIND_BF16 ? DASH_TRACE_GEMM_BF16
-                                                               : DASH_TRACE_GEMM_F16));
-    trace_end(rec, st, kind, frac * 2.0 * bb * g.dim, bytes);
+                                        : (bf ? DASH_TRACE_GEMM_BF16 : DASH_TRACE_GEMM_F16));
+    // Tensor-core flops as issued: a pair-B product issues two 16-bit MMAs per slice
+    // (3xTF32 counts its fp32 product once against a third of the TF32 rate).
+    trace_end(rec, st, kind, frac * 2.0 * bb * g.dim * (KT == 3 ? 2 : 1), bytes);
   }
   return err == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
 }
@@ -1216,16 +1244,18 @@ dash_status launch_gemm(const GemmLaunch& g, cudaStream_t st) {
 
   switch (g.kind) {
     // B a multiple of 256: CTA pairs on 256 x 256 tiles (cta_group::2); otherwise
-    // one CTA per 128 x 128 tile.  (MODE 1, clusters multicasting the shared B
-    // tile, measured equal or slower at B = 1024 and is not dispatched.)
+    // one CTA per 128 x 128 tile.
     case KIND_F16:
     case KIND_BF16:
       return wide ? run_gemm<256, 0, 2>(g, st) : run_gemm<128, 0, 0>(g, st);
+    case KIND_F16_SPLITB:
+    case KIND_BF16_SPLITB:
+      return wide ? run_gemm<256, 3, 2>(g, st) : run_gemm<128, 3, 0>(g, st);
     case KIND_TF32:
       return wide ? run_gemm<256, 1, 2>(g, st) : run_gemm<128, 1, 0>(g, st);
     case KIND_TF32X3:
       // fp32-accurate products: partial sums reduced with round-to-nearest.
-      return wide ? run_gemm<256, 2, 2, true>(g, st) : run_gemm<128, 2, 0>(g, st);
+      return wide ? run_gemm<ACC_BN, 2, 2, true>(g, st) : run_gemm<128, 2, 0>(g, st);
     default:
       return DASH_ERR_INVALID_ARG;
   }

@@ -200,8 +200,10 @@ def test_library_tier_selection_matches_oracle():
     lmin = (lmax / 10.0 ** rng.uniform(0, 7, 200)).astype(np.float32)
     t0 = oracle.DEFAULT_TIERS[0]
     edge = 4.0 * t0["gate"] / t0["u"]
-    extra_max = np.array([1.0, 1.0, 1.0, 1.0, np.nan, np.inf, 1.0], dtype=np.float32)
-    extra_min = np.array([1.0 / edge, 0.0, -1.0, np.nan, 0.5, 0.5, 1e-30], dtype=np.float32)
+    extra_max = np.array([1.0, 1.0, 1.0, 1.0, np.nan, np.inf, 1.0, -1.0, 0.0],
+                         dtype=np.float32)
+    extra_min = np.array([1.0 / edge, 0.0, -1.0, np.nan, 0.5, 0.5, 1e-30, 0.5, 0.5],
+                         dtype=np.float32)
     lmax = np.concatenate([lmax, extra_max])
     lmin = np.concatenate([lmin, extra_min])
     got = dr.select_tiers(lmax, lmin, oracle.DEFAULT_TIERS)
@@ -209,6 +211,9 @@ def test_library_tier_selection_matches_oracle():
                                                          lmin.astype(np.float64)))
     assert got == want.tolist()
     assert set(got[:200]) == {0, 1}
+    # A block with no usable lambda_max estimate (negative or zero) goes to the
+    # last, most accurate tier, like one with no resolved lambda_min.
+    assert got[-2:] == [len(oracle.DEFAULT_TIERS) - 1] * 2
     tiers3 = [dict(t0), {"solver": "ndb", "prec": "tf32", "iters": 12, "u": 2.0 ** -24,
                          "gate": 1.0}, dict(oracle.DEFAULT_TIERS[1])]
     got3 = dr.select_tiers(lmax, lmin, tiers3)

@@ -5,6 +5,7 @@ MN-major shared-memory operands), the 128- and 256-wide tile paths and a ragged
 multi-tile size (B = 384: three M tiles, three 128-wide N tiles, twelve TF32
 k-blocks)."""
 
+import numpy as np
 import pytest
 import torch
 
@@ -65,3 +66,97 @@ def test_gemm_large_k_and_many_blocks():
         idx = [0, n // 2, n - 1]
         ref = to64(A[idx]) @ to64(B[idx])
         assert rel_fro_blocks(to64(C[idx]), ref).max() < 1e-5
+
+
+def sym_operand(b, n, seed):
+    """(n, b, b) fp32 symmetric matrices whose 256-tiles below the diagonal are NaN:
+    a symmetric-half product must never read them."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    S = torch.randn((n, b, b), generator=g, device="cuda") / b ** 0.5
+    S = 0.5 * (S + S.transpose(1, 2))
+    P = S.clone()
+    t = b // 256
+    for i in range(t):
+        for j in range(i):
+            P[:, i * 256:(i + 1) * 256, j * 256:(j + 1) * 256] = float("nan")
+    return S, P
+
+
+def upper_tiles(x, b):
+    """Mask of the 256-tiles on or above the diagonal."""
+    t = b // 256
+    m = torch.zeros((b, b), dtype=torch.bool)
+    for i in range(t):
+        m[i * 256:(i + 1) * 256, i * 256:] = True
+    return m.numpy()
+
+
+@pytest.mark.parametrize("prec", ["tf32", "3xtf32", "fp16", "bf16"])
+@pytest.mark.parametrize("sym", [1, 2])
+@pytest.mark.parametrize("b", [256, 512, 1024])
+def test_gemm_symmetric_halves(prec, sym, b):
+    """C = S S from the upper 256-tiles of S only (the lower ones hold NaN)."""
+    require_gpu()
+    dr = library()
+    n = 3
+    S, P = sym_operand(b, n, 7 * b + sym)
+    Ph, Pl, _ = operands(P, prec)
+    _, _, S64 = operands(S, prec)
+    C = torch.zeros((n, b, b), device="cuda")
+    dr.gemm_ex(Ph, Ph, prec=prec, sym=sym, A_lo=Pl, B_lo=Pl, C=C)
+    torch.cuda.synchronize()
+    assert dr.device_status() == 0
+    ref = S64 @ S64
+    got = to64(C)
+    mask = upper_tiles(got[0], b) if sym == 2 else np.ones((b, b), dtype=bool)
+    assert np.all(np.isfinite(got[:, mask]))
+    err = np.linalg.norm((got - ref)[:, mask]) / np.linalg.norm(ref[:, mask])
+    tol = 2e-5 if prec == "3xtf32" else 1e-5
+    assert err < tol, (prec, sym, b, err)
+
+
+@pytest.mark.parametrize("prec", ["fp16", "bf16"])
+@pytest.mark.parametrize("sym", [0, 1, 2])
+@pytest.mark.parametrize("b", [128, 256, 384, 512, 1024])
+def test_gemm_pair_b(prec, sym, b):
+    """16-bit A times a 16-bit pair B = hi + lo: C = A hi + A lo (the product Coupled
+    Newton uses for its M iterate), against float64 on the pair's exact value."""
+    require_gpu()
+    dr = library()
+    if sym and b % 256:
+        pytest.skip("symmetric halves need B a multiple of 256")
+    n = 3
+    dt = torch.float16 if prec == "fp16" else torch.bfloat16
+    S, P = sym_operand(b, n, 11 * b + sym) if b % 256 == 0 else (None, None)
+    if sym == 0 and S is not None:
+        P = S  # read whole: no NaN tiles
+    if S is None:
+        g = torch.Generator(device="cuda")
+        g.manual_seed(b)
+        S = torch.randn((n, b, b), generator=g, device="cuda") / b ** 0.5
+        P = S
+    # A = S^2 / 2 commutes with S, so A S is symmetric as sym 2 requires.
+    A = (torch.bmm(S, S) * 0.5).to(dt)
+    A64 = to64(A)
+    if sym:
+        A = A.clone()
+        for i in range(b // 256):
+            for j in range(i):
+                A[:, i * 256:(i + 1) * 256, j * 256:(j + 1) * 256] = float("nan")
+    hi = P.to(dt)
+    lo = (P - hi.float()).to(dt)
+    val = to64(S.to(dt)) + to64((S - S.to(dt).float()).to(dt))
+    C = torch.zeros((n, b, b), device="cuda")
+    dr.gemm_ex(A, hi, prec=prec, sym=sym, B_lo=lo, C=C)
+    torch.cuda.synchronize()
+    assert dr.device_status() == 0
+    ref = A64 @ val
+    got = to64(C)
+    mask = upper_tiles(got[0], b) if sym == 2 else np.ones((b, b), dtype=bool)
+    assert np.all(np.isfinite(got[:, mask]))
+    err = np.linalg.norm((got - ref)[:, mask]) / np.linalg.norm(ref[:, mask])
+    # The lo part must count: without it the error would be the 16-bit rounding of B.
+    plain = np.linalg.norm((A64 @ to64(S.to(dt)) - ref)[:, mask]) / np.linalg.norm(ref[:, mask])
+    print("pair-B %s sym %d B=%d: rel err %.3e (hi alone %.3e)" % (prec, sym, b, err, plain))
+    assert err < 1e-5 and err < 0.05 * plain, (prec, sym, b, err, plain)

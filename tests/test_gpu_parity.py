@@ -140,8 +140,46 @@ def test_cn_parity(prec, iters):
     Xr, rr, _ = oracle.cn_inv_root(to64(A), to64(lam), iters)
     err = rel_fro_blocks(to64(X), Xr)
     assert err.max() < GATE[prec], err
-    tol = 1e-4 if prec == "3xtf32" else 5e-2
-    assert np.max(np.abs(to64(r) - rr)) < tol * max(1.0, rr.max())
+    # Residuals are held to the precision's stated root tolerance.
+    rerr = np.max(np.abs(to64(r) - rr)) / max(1.0, rr.max())
+    print("CN %s iters=%d root err %.3e, residual err %.3e" % (prec, iters, err.max(), rerr))
+    assert rerr < GATE[prec]
+
+
+def rank_deficient_factors(n, b, seed):
+    """Factors G G^T (scaled by 1 - beta = 0.05) of bf16 gradient blocks whose right
+    half is zero padding: rank b / 2, so with a 1e-6 ridge the scaled condition
+    number is about 1e6 -- the padded factors of the Llama workload."""
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    G = (0.1 * torch.randn((n, b, b), generator=g, device="cuda")).to(torch.bfloat16).float()
+    G[:, :, b // 2:] = 0
+    return 0.05 * torch.bmm(G, G.transpose(1, 2))
+
+
+@pytest.mark.parametrize("b", [256, 512, 384])
+def test_cn_half_ill_conditioned(b):
+    """16-bit Coupled Newton on ill-conditioned factors against the oracle.
+
+    Rounding M to 16 bits moves the smallest scaled eigenvalues (about 1e-6) by
+    far more than themselves; the early M-updates therefore read M as a 16-bit
+    pair (hi + lo).  FP16 is held to its 1e-2 gate.  BF16's 8-bit iterates X and
+    T cannot reach it at this condition number: reported, not gated."""
+    require_gpu()
+    dr = library()
+    ridge = 1e-6
+    F = rank_deficient_factors(6, b, 5000 + b)
+    V0 = synth.start_vectors(6, b, 32, seed=5100 + b, device="cuda")
+    lam = dr.spectral_scale(F, dr.SCALE_POWER, V0, 10, ridge=ridge)
+    ref = oracle.cn_inv_root(to64(F), to64(lam), 10, ridge=ridge)[0]
+    for prec in ("fp16", "bf16"):
+        X = dr.inv_root_cn(F, lam, 10, prec, ridge=ridge)
+        torch.cuda.synchronize()
+        assert dr.device_status() == 0
+        err = rel_fro_blocks(to64(X), ref)
+        print("CN %s B=%d rank-deficient factors: max rel err %.3e" % (prec, b, err.max()))
+        assert np.all(np.isfinite(to64(X)))
+        if prec == "fp16":
+            assert err.max() < GATE[prec], err
 
 
 @pytest.mark.parametrize("prec", PRECS)
