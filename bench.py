@@ -155,13 +155,32 @@ class ClockSampler:
 
 
 class Workload:
-    def __init__(self, torch, dr, synth, device, root_prec, ndb=False, power="fp16"):
+    """The step on this rank's stack.  With world > 1 (data parallel, weak scaling)
+    the model is `world` copies of the 24-layer stack; every rank holds its own
+    data's gradients of all world x 1248 blocks (G_global), owns 1248 of them, and
+    each step reduce-scatters the gradients to their owners, runs the hot path on
+    the owned blocks and all-gathers the updates (shard.DataParallelStep)."""
+
+    def __init__(self, torch, dr, synth, device, root_prec, ndb=False, power="fp16", rank=0,
+                 world=1):
         self.torch = torch
         self.dr = dr
         dev = device
         G, vr, vc = synth.llama_layer_blocks(LAYERS, seed=SEED, var=1e-2, bs=BS, device=dev)
         self.G, self.vr, self.vc = G, vr, vc
         self.ng = G.shape[0]
+        self.dp = None
+        self.G_global = None
+        if world > 1:
+            from matrix_inverse_roots_gb300.shard import DataParallelStep
+
+            self.G_global = torch.empty((world * self.ng, BS, BS), dtype=G.dtype, device=dev)
+            for c in range(world):
+                Gc, _, _ = synth.llama_layer_blocks(LAYERS, seed=SEED + 100 * rank + c, var=1e-2,
+                                                    bs=BS, device=dev)
+                self.G_global[c * self.ng:(c + 1) * self.ng].copy_(Gc)
+                del Gc
+            self.dp = DataParallelStep(world * self.ng, self.local_step)
         self.nf = 2 * self.ng
         self.F = torch.zeros((self.nf, BS, BS), dtype=torch.float32, device=dev)
         self.Froot = torch.empty_like(self.F)
@@ -183,7 +202,19 @@ class Workload:
         self.ws_apply = dr.workspace(dr.OP_PRECONDITION_APPLY, self.ng, BS, self.apply_prec,
                                      device=dev, max_bytes=16 << 30)
 
+    def local_step(self, G_own):
+        """The hot path on the owned gradient blocks; returns their updates."""
+        self.G = G_own
+        self.step_local()
+        return self.U
+
     def step(self):
+        if self.dp is not None:
+            return self.dp(self.G_global)
+        self.step_local()
+        return self.U
+
+    def step_local(self):
         dr = self.dr
         dr.shampoo_accumulate(self.G, self.F, BETA, self.vr, self.vc)
         dr.spectral_scale(self.F, self.power_mode, self.V0, POWER_ITERS, ridge=RIDGE,
@@ -196,8 +227,25 @@ class Workload:
                            ws=self.ws_root)
         dr.precondition_apply(self.G, self.Froot, self.apply_prec, U=self.U, ws=self.ws_apply)
 
+    def tiered_step(self, tiers, ws_auto, lam_min):
+        """The step with the root solver chosen per block (inv_root_auto)."""
+        dr = self.dr
+        dr.shampoo_accumulate(self.G, self.F, BETA, self.vr, self.vc)
+        dr.spectral_scale(self.F, self.power_mode, self.V0, POWER_ITERS, ridge=RIDGE,
+                          out=self.lam, ws=self.ws_scale)
+        # lambda_min in the fp32-accurate mode: a 16-bit copy of the shifted block
+        # rounds lambda_max - lambda_min, so it cannot resolve lambda_min below about
+        # u lambda_max (every block would look well conditioned).
+        dr.spectral_lambda_min(self.F, self.lam, dr.SCALE_POWER, self.V0, POWER_ITERS,
+                               ridge=RIDGE, out=lam_min, ws=self.ws_lmin)
+        _, choice = dr.inv_root_auto(self.F, self.lam, lam_min, tiers, ridge=RIDGE,
+                                     X=self.Froot, ws=ws_auto)
+        dr.precondition_apply(self.G, self.Froot, self.apply_prec, U=self.U, ws=self.ws_apply)
+        return choice
+
     def free(self):
-        for k in ("G", "F", "Froot", "U", "V0", "ws_scale", "ws_root", "ws_apply"):
+        for k in ("G", "F", "Froot", "U", "V0", "ws_scale", "ws_root", "ws_apply", "G_global",
+                  "dp"):
             setattr(self, k, None)
 
 
@@ -232,7 +280,10 @@ def e2e_steps(torch, wl, G_host, U_host, steps, dist=None):
     Returns (ms per step, upload ms per step, read-back ms per step)."""
     comp = torch.cuda.current_stream()
     up, down = torch.cuda.Stream(), torch.cuda.Stream()
-    Gb = [wl.G, torch.empty_like(wl.G)]
+    # Data parallel: the input is this rank's gradients of every block, the result
+    # read back is the update of the blocks this rank owns.
+    gname = "G_global" if wl.dp is not None else "G"
+    Gb = [getattr(wl, gname), torch.empty_like(getattr(wl, gname))]
     Ub = [wl.U, torch.empty_like(wl.U)]
     used = [torch.cuda.Event() for _ in range(2)]
     uploaded = [torch.cuda.Event() for _ in range(2)]
@@ -268,7 +319,8 @@ def e2e_steps(torch, wl, G_host, U_host, steps, dist=None):
         comp.wait_event(uploaded[b])
         if k >= 2:
             comp.wait_event(read[b])
-        wl.G, wl.U = Gb[b], Ub[b]
+        setattr(wl, gname, Gb[b])
+        wl.U = Ub[b]
         wl.step()
         used[b].record(comp)
         down.wait_event(used[b])
@@ -281,7 +333,8 @@ def e2e_steps(torch, wl, G_host, U_host, steps, dist=None):
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
-    wl.G, wl.U = Gb[0], Ub[0]
+    setattr(wl, gname, Gb[0])
+    wl.U = Ub[0]
     del Gb, Ub
     up_ms = sum(a.elapsed_time(z) for a, z in spans["up"]) / steps
     down_ms = sum(a.elapsed_time(z) for a, z in spans["down"]) / steps
@@ -425,7 +478,7 @@ def run_gpu(args):
     dr.load_library()
     peaks = load_peaks()
 
-    wl = Workload(torch, dr, synth, dev, dr.FP16, power=args.power)
+    wl = Workload(torch, dr, synth, dev, dr.FP16, power=args.power, rank=rank, world=world)
     for _ in range(args.warmup):
         wl.step()
     torch.cuda.synchronize()
@@ -444,13 +497,22 @@ def run_gpu(args):
     # time is the slowest rank's and throughput counts the blocks of all ranks.
     value, ms = job_throughput(wl.nf, ms, device=dev)
 
+    # The data-parallel exchange, when there is one, as its share of the step.
+    exchange = None
+    if wl.dp is not None:
+        exchange = {"reduce_scatter_gb_per_rank": round(wl.G_global.numel() * 2 / 1e9, 2),
+                    "all_gather_gb_per_rank": round(wl.G_global.numel() * 4 / 1e9, 2),
+                    "what": "NCCL reduce-scatter of bf16 gradient blocks to their owners before "
+                            "accumulate, all-gather of fp32 U after apply"}
+
     # Root-only throughput of the same kernel chain (CN FP16 on the whole stack).
     root_ms = timed_steps(torch, lambda: dr.inv_root_cn(wl.F, wl.lam, CN_ITERS, dr.FP16, ridge=RIDGE,
                                                          X=wl.Froot, ws=wl.ws_root), 2)
 
     # End to end: gradients from pinned host memory in, update back to pinned host memory.
-    G_host = torch.empty(wl.G.shape, dtype=wl.G.dtype, pin_memory=True)
-    G_host.copy_(wl.G)
+    Gin = wl.G_global if wl.dp is not None else wl.G
+    G_host = torch.empty(Gin.shape, dtype=Gin.dtype, pin_memory=True)
+    G_host.copy_(Gin)
     U_host = torch.empty(wl.U.shape, dtype=wl.U.dtype, pin_memory=True)
 
     e2e_steps(torch, wl, G_host, U_host, 2)
@@ -464,6 +526,27 @@ def run_gpu(args):
     # gradient packed into the block stack, accumulate, scale, CN, and the weight step
     # W <- W - lr U fused into the apply epilogue (W kept in the block layout).
     full = full_optimizer_step(torch, dr, synth, wl, dev, args.steps, dist, peaks)
+
+    # The step with the root solver chosen per block by its condition estimate.
+    tiered = None
+    if not args.no_tiered:
+        wl.ws_root = None
+        torch.cuda.empty_cache()
+        wl.ws_lmin = dr.workspace(dr.OP_LAMBDA_MIN, wl.nf, BS, dr.FP32_3XTF32, NVEC, device=dev)
+        nb = min(dr.auto_workspace_size(wl.nf, BS, dr.DEFAULT_TIERS), 64 << 30)
+        ws_auto = torch.empty(nb, dtype=torch.uint8, device=dev)
+        lam_min = torch.empty_like(wl.lam)
+        choice = wl.tiered_step(dr.DEFAULT_TIERS, ws_auto, lam_min)
+        t_ms = timed_steps(torch, lambda: wl.tiered_step(dr.DEFAULT_TIERS, ws_auto, lam_min),
+                           2, dist)
+        counts = [choice.count(t) for t in range(len(dr.DEFAULT_TIERS))]
+        tiered = {"ms_per_step": round(t_ms, 2), "blocks_per_s": round(wl.nf / (t_ms * 1e-3), 1),
+                  "tiers": [dict(t) for t in dr.DEFAULT_TIERS], "blocks_per_tier": counts,
+                  "what": "accumulate + power scale + lambda_min (shifted power iteration, "
+                          "3xTF32) + per-block tier (inv_root_auto: gather, solve, scatter) + "
+                          "apply"}
+        del ws_auto, lam_min
+        wl.ws_lmin = None
     wl.free()
     torch.cuda.empty_cache()
 
@@ -508,6 +591,8 @@ def run_gpu(args):
                 "copies": "pinned host buffers; uploads and read-backs on two copy streams, "
                           "G and U double-buffered so they overlap the neighbouring steps"},
         "root_only_blocks_per_s": round(wl.nf / (root_ms * 1e-3), 1),
+        "tiered_step": tiered,
+        "exchange": exchange,
         "ndb_fp32_step_ms": None if ndb_ms is None else round(ndb_ms, 2),
         "optimizer_step": full,
         "peaks_source": peaks["_source"],
@@ -590,9 +675,11 @@ def run_sweep(args):
 
 def run_case(args):
     """A small untimed case for ncu captures: Wishart blocks, a scale, one root call;
-    or, for --case accumulate, one accumulate of n bf16 Llama-like gradient blocks
-    into 2n factors (two GEMM launches, then two mirror launches when B is a multiple
-    of 256)."""
+    --case accumulate: one accumulate of n bf16 Llama-like gradient blocks into 2n
+    factors (two GEMM launches, then two mirror launches when B is a multiple of
+    256); --case apply: one preconditioned update of n blocks (three conversions,
+    two GEMMs); --case pack: n stacked 2048 x 5632 bf16 gradients into blocks;
+    --case step: two steps of the benchmark workload (profile the second)."""
     import torch
 
     import matrix_inverse_roots_gb300 as dr
@@ -601,6 +688,30 @@ def run_case(args):
     torch.cuda.set_device(0)
     dr.load_library()
     n, b = args.case_n, args.case_b
+    if args.case == "step":
+        # One warm-up step of the benchmark workload, then the step a profiler
+        # captures (skip the first step's launches).
+        wl = Workload(torch, dr, synth, torch.device("cuda", 0), dr.FP16, power=args.power)
+        wl.step()
+        torch.cuda.synchronize()
+        wl.step()
+        torch.cuda.synchronize()
+        print("case ok, device status", dr.device_status())
+        return
+    if args.case in ("apply", "pack"):
+        g = torch.Generator(device="cuda").manual_seed(5)
+        G = (0.1 * torch.randn((n, b, b), generator=g, device="cuda")).to(torch.bfloat16)
+        if args.case == "apply":
+            R = synth.wishart(2 * n, b, seed=6, device="cuda")
+            dr.precondition_apply(G, R, args.case_prec)
+        else:
+            # n Llama MLP weights' gradients stacked (2048 n x 5632, row-major) into
+            # their blocks (184 MB at n = 8: more than L2).
+            M = (0.1 * torch.randn((2048 * n, 5632), generator=g, device="cuda")).to(torch.bfloat16)
+            dr.pack_blocks(M, b)
+        torch.cuda.synchronize()
+        print("case ok, device status", dr.device_status())
+        return
     if args.case == "accumulate":
         g = torch.Generator(device="cuda").manual_seed(5)
         G = (0.1 * torch.randn((n, b, b), generator=g, device="cuda")).to(torch.bfloat16)
@@ -679,12 +790,15 @@ def main():
     ap.add_argument("--impl", default="dash", choices=["dash", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--no-ndb", action="store_true", help="skip the NDB fp32 step")
+    ap.add_argument("--no-tiered", action="store_true",
+                    help="skip the step with per-block solver selection")
     ap.add_argument("--power", choices=["fp16", "bf16", "3xtf32"], default="fp16",
                     help="arithmetic of the power-iteration scaling (the pages: half precision)")
     ap.add_argument("--sweep", action="store_true",
                     help="inverse-root throughput sweep over block sizes and precisions")
     ap.add_argument("--sweep-b", type=int, nargs="*", default=None)
-    ap.add_argument("--case", choices=["cn", "ndb", "cheb", "accumulate"], default=None,
+    ap.add_argument("--case", choices=["cn", "ndb", "cheb", "accumulate", "apply", "pack", "step"],
+                    default=None,
                     help="run one small untimed case (for profiler captures)")
     ap.add_argument("--case-n", type=int, default=64)
     ap.add_argument("--case-b", type=int, default=1024)
@@ -692,6 +806,17 @@ def main():
     ap.add_argument("--case-iters", type=int, default=3)
     ap.add_argument("--case-scale", choices=["power", "power-fp16", "frobenius"], default="power")
     args = ap.parse_args()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ and not (args.case or args.sweep):
+        # One process per GPU: relaunch this command under torch.distributed.run.
+        import socket
+
+        with socket.socket() as s:
+            s.bind(("127.0.0.1", 0))
+            port = s.getsockname()[1]
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+               "--nproc-per-node=%d" % args.gpus, "--master-addr", "127.0.0.1",
+               "--master-port", str(port), os.path.abspath(__file__)] + sys.argv[1:]
+        sys.exit(subprocess.call(cmd))
     if args.case:
         run_case(args)
     elif args.sweep:

@@ -51,6 +51,17 @@ class Tier(ctypes.Structure):
                 ("u", ctypes.c_double), ("gate", ctypes.c_double)]
 
 
+# Default tiers of per-block solver selection, cheapest first: Coupled Newton in
+# FP16 (10 iterations, unit roundoff of fp16 storage, the 1e-2 FP16 tolerance),
+# else Coupled Newton in 3xTF32 with 24 iterations, enough for a smallest scaled
+# eigenvalue of 1e-6 to converge (each early iteration multiplies it by about
+# (5/4)^4), held to the 1e-4 fp32 tolerance.
+DEFAULT_TIERS = (
+    {"solver": "cn", "prec": "fp16", "iters": 10, "u": 2.0 ** -11, "gate": 1e-2},
+    {"solver": "cn", "prec": "3xtf32", "iters": 24, "u": 2.0 ** -24, "gate": 1e-4},
+)
+
+
 # dash_op
 OP_ACCUMULATE = 0
 OP_SPECTRAL_SCALE = 1

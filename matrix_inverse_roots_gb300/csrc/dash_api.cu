@@ -186,14 +186,16 @@ AffParams aff_from(const void* src_hi, const void* src_lo, int src_fmt, int B, l
 // One GEMM launch C = X * Y over nc blocks in precision prec.
 // sym: 0 plain; 1 symmetric operands (only their tiles on or above the diagonal
 // are read); 2 also a symmetric result (only those tiles computed and stored);
-// 3 a symmetric result from operands read whole (X Y^T with Y = X, or X^T X).
-// Modes 1-3 take effect for B a multiple of 256 (CTA-pair kernels).
+// 3 a symmetric result from operands read whole (X Y^T with Y = X, or X^T X);
+// 4 X symmetric (read from its upper tiles), Y and the result whole.
+// Modes 1-4 take effect for B a multiple of 256 (CTA-pair kernels).
 // pairB: Y is a 16-bit pair (FMT_F16X2 / FMT_BF16X2) of the 16-bit precision prec.
 dash_status gemm(int prec, int B, long long nc, const Buf& X, int tX, const Buf& Y, int tY,
                  const EpiParams& e, cudaStream_t st, int sym = 0, bool pairB = false) {
   GemmLaunch g;
-  g.sym_in = (sym == 1 || sym == 2) ? 1 : 0;
-  g.sym_out = (sym >= 2) ? 1 : 0;
+  g.sym_in = (sym == 1 || sym == 2 || sym == 4) ? 1 : 0;
+  g.sym_in_b = (sym == 1 || sym == 2) ? 1 : 0;
+  g.sym_out = (sym == 2 || sym == 3) ? 1 : 0;
   g.kind = prec_kind(prec);
   if (pairB) g.kind = (prec == DASH_BF16) ? KIND_BF16_SPLITB : KIND_F16_SPLITB;
   g.dim = B;
@@ -596,6 +598,27 @@ dash_status inv_root_cn(const float* A, float ridge, const float* scale, int64_t
   const int K = iters;
   const int fmt = prec_fmt(prec);
   const int S = sym_mode(prec, B);  // symmetric-half iterates
+  // 16-bit precisions (build-time modes, see gemm): the T^2 and T^4 products and the
+  // M-update run whole, only the X product keeps symmetric halves.  A product kept
+  // as its upper 256-tiles is symmetrised by a tile mask, which turns the
+  // antisymmetric part of a product of two rounded, not exactly commuting, iterates
+  // (of order u ||M|| at 16 bits) into a symmetric error of the same size.  An
+  // antisymmetric error moves eigenvalues only at second order; a symmetric one
+  // moves them at first order, and M's smallest eigenvalues (about 1e-6 of the
+  // largest on ill-conditioned factors) are what the root amplifies.  T comes from
+  // the (not exactly symmetric) M-update, so T, T^2, T^4 and M are all read whole;
+  // X only carries the result, whose absolute errors of order u |X| are harmless.
+#ifndef DASH_CN16_TSYM
+#define DASH_CN16_TSYM 0
+#endif
+#ifndef DASH_CN16_XSYM
+#define DASH_CN16_XSYM 2
+#endif
+#ifndef DASH_CN16_MSYM
+#define DASH_CN16_MSYM 0
+#endif
+  const int ST = (S && is_half(prec)) ? DASH_CN16_TSYM : S;
+  const int SX = (S && is_half(prec)) ? DASH_CN16_XSYM : S;
   Carver cv(ws, ws_bytes);
   RootSmall sm;
   sm.inv_s = static_cast<float*>(cv.take(N * 4));
@@ -671,8 +694,8 @@ dash_status inv_root_cn(const float* A, float ridge, const float* scale, int64_t
         e.nout = 1;
         e.out[0] = eout_f32(Xc, 1.0f, 0.0f, e1, m14);
         if (shift) with_e(e, xk, fmt);
-        DASH_TRY(gemm(prec, B, nc, xk, 0, tk, 0, e, st, S));
-        if (S) DASH_TRY(launch_mirror_lower(Xc, B, nc, st));
+        DASH_TRY(gemm(prec, B, nc, xk, 0, tk, 0, e, st, SX));
+        if (SX == 2) DASH_TRY(launch_mirror_lower(Xc, B, nc, st));
         break;
       }
       if (k >= 1) {
@@ -680,7 +703,7 @@ dash_status inv_root_cn(const float* A, float ridge, const float* scale, int64_t
         e.nout = 1;
         e.out[0] = eout(bx[xn], fmt, 1.0f, 0.0f, e1);
         if (shift) with_e(e, xk, fmt);
-        DASH_TRY(gemm(prec, B, nc, xk, 0, tk, 0, e, st, S));
+        DASH_TRY(gemm(prec, B, nc, xk, 0, tk, 0, e, st, SX));
         xk = bx[xn];
         xn ^= 1;
       }
@@ -688,12 +711,12 @@ dash_status inv_root_cn(const float* A, float ridge, const float* scale, int64_t
       ea.nout = 1;
       ea.out[0] = eout(tsp, fmt, 1.0f, 0.0f, e2);
       if (shift) with_e(ea, tk, fmt);
-      DASH_TRY(gemm(prec, B, nc, tk, 0, tk, 0, ea, st, S));
+      DASH_TRY(gemm(prec, B, nc, tk, 0, tk, 0, ea, st, ST));
       EpiParams eb = epi_none();
       eb.nout = 1;
       eb.out[0] = eout(bT4, fmt, 1.0f, 0.0f, e2);
       if (shift) with_e(eb, tsp, fmt);
-      DASH_TRY(gemm(prec, B, nc, tsp, 0, tsp, 0, eb, st, S));
+      DASH_TRY(gemm(prec, B, nc, tsp, 0, tsp, 0, eb, st, ST));
       // M_{k+1} = T^4 M_k; the same epilogue forms T_{k+1} (into the scratch, free
       // once T^4 is formed) and the residual of M_{k+1}.
       EpiParams em = epi_none();
@@ -706,7 +729,9 @@ dash_status inv_root_cn(const float* A, float ridge, const float* scale, int64_t
       }
       em.resid_acc = racc ? racc + (k + 1) : nullptr;
       em.resid_stride = K;
-      DASH_TRY(gemm(prec, B, nc, bT4, 0, bm[mc], 0, em, st, S, k < jp));
+      // 16-bit: T^4 and M read whole, M and T written whole (see ST above).
+      DASH_TRY(gemm(prec, B, nc, bT4, 0, bm[mc], 0, em, st,
+                    (S && is_half(prec)) ? DASH_CN16_MSYM : S, k < jp));
       mc ^= 1;
       const Buf t = tk;
       tk = tsp;

@@ -269,6 +269,14 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                : "memory");
 }
 
+// The same arrive with the default (release, CTA scope) semantics: no cluster-wide
+// memory fence.  For handing a tensor-memory buffer back to the peer that issues
+// the MMAs, where the only accesses to order are this thread's tcgen05.ld, already
+// completed (tcgen05.wait::ld) and ordered by tcgen05.fence::before_thread_sync.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 // 3-D tiled load into this CTA's shared memory whose completion is counted on
 // `bar`, which may be the peer CTA's barrier (shared::cluster address).
 __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar,

@@ -44,9 +44,11 @@ struct GemmLaunch {
   int transB;
   EpiParams epi;
   // Symmetric-half iterates (honoured for CTA-pair tiles, B a multiple of 256):
-  // sym_in -- A and B symmetric, only their 256-tiles on or above the diagonal
-  // are read; sym_out -- only C's 256-tiles on or above the diagonal are computed.
+  // sym_in -- A (sym_in_b: B) symmetric, only its 256-tiles on or above the
+  // diagonal are read; sym_out -- only C's 256-tiles on or above the diagonal are
+  // computed.
   int sym_in = 0;
+  int sym_in_b = 0;
   int sym_out = 0;
 };
 

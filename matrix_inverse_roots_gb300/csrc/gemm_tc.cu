@@ -106,10 +106,11 @@ struct KParams {
   uint32_t idesc;
   int a_mn, b_mn;
   int staged;  // all outputs 16-bit (at most two): tiles leave through TMA stores
-  // Symmetric-half iterates (CTA pairs only).  sym_in: A and B are symmetric and
-  // only their 256 x 256 tiles on or above the diagonal are read.  sym_out: only
-  // those tiles of C are computed and written (C symmetric by construction).
-  int sym_in, sym_out;
+  // Symmetric-half iterates (CTA pairs only).  sym_in / sym_in_b: A / B is
+  // symmetric and only its 256 x 256 tiles on or above the diagonal are read.
+  // sym_out: only those tiles of C are computed and written (C symmetric by
+  // construction).  sym_any = sym_in | sym_in_b.
+  int sym_in, sym_in_b, sym_out, sym_any;
   int t256;         // dim / 256
   uint32_t idesc0;  // instruction descriptor without the operand-major bits
   EpiParams epi;
@@ -450,7 +451,7 @@ __global__ void __launch_bounds__(320, 1)
               // Symmetric operands: a k-block left of A's (below B's) diagonal tile is
               // read as the transpose of the stored tile, i.e. in the other major.
               const bool amir = p.sym_in && (k0 >> 8) < (m0 >> 8);
-              const bool bmir = p.sym_in && (k0 >> 8) > (n0 >> 8);
+              const bool bmir = p.sym_in_b && (k0 >> 8) > (n0 >> 8);
               if (amir) ma = &p.tAm;
               if (bmir) mb = part ? &p.tBlm : &p.tBm;
               if (!loadA) {
@@ -516,7 +517,7 @@ __global__ void __launch_bounds__(320, 1)
         // The pair tile's position, for the operand-major choice of symmetric operands.
         long long ublk;
         int um0 = 0, un0 = 0;
-        if (p.sym_in) decode_unit<CL>(u, p, 0u, ublk, um0, un0, BN);
+        if (p.sym_any) decode_unit<CL>(u, p, 0u, ublk, um0, un0, BN);
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = 0; kb < p.nkb; ++kb) {
           if (!mbar_wait(full_bar(stage), phase, abort_flag)) {
@@ -528,9 +529,9 @@ __global__ void __launch_bounds__(320, 1)
           const uint32_t sB = sA + C::A_BYTES;
           const int k0 = kb * C::BK;
           const int amn = p.a_mn ^ ((p.sym_in && (k0 >> 8) < (um0 >> 8)) ? 1 : 0);
-          const int bmn = p.b_mn ^ ((p.sym_in && (k0 >> 8) > (un0 >> 8)) ? 1 : 0);
+          const int bmn = p.b_mn ^ ((p.sym_in_b && (k0 >> 8) > (un0 >> 8)) ? 1 : 0);
           const uint32_t idesc =
-              p.sym_in ? (p.idesc0 | (static_cast<uint32_t>(amn) << 15) |
+              p.sym_any ? (p.idesc0 | (static_cast<uint32_t>(amn) << 15) |
                           (static_cast<uint32_t>(bmn) << 16))
                        : p.idesc;
 #pragma unroll
@@ -686,7 +687,7 @@ __global__ void __launch_bounds__(320, 1)
       __syncwarp();
       if (lane == 0) {
         if (MODE == 2)
-          mbar_arrive_cluster(mapa_shared(tempty_bar(acc), crank & ~1u));
+          mbar_arrive_remote(mapa_shared(tempty_bar(acc), crank & ~1u));
         else
           mbar_arrive(tempty_bar(acc));
       }
@@ -824,7 +825,7 @@ __global__ void __launch_bounds__(ACC_THREADS, 1)
           fb = leader ? fb : mapa_shared(fb, 0);
           const int k0 = kb * C::BK;
           const bool amir = p.sym_in && (k0 >> 8) < (m0 >> 8);
-          const bool bmir = p.sym_in && (k0 >> 8) > (n0 >> 8);
+          const bool bmir = p.sym_in_b && (k0 >> 8) > (n0 >> 8);
           for (int part = 0; part < C::NPART; ++part) {
             const uint32_t sA = sbase + stage * C::STAGE_BYTES + part * (C::A_BYTES + C::B_BYTES);
             const uint32_t sB = sA + C::A_BYTES;
@@ -869,7 +870,7 @@ __global__ void __launch_bounds__(ACC_THREADS, 1)
       for (long long u = cid; u < p.total_units && ok; u += ncl) {
         long long ublk;
         int um0 = 0, un0 = 0;
-        if (p.sym_in) decode_unit<CL>(u, p, 0u, ublk, um0, un0, BN);
+        if (p.sym_any) decode_unit<CL>(u, p, 0u, ublk, um0, un0, BN);
         for (int kb = 0; kb < p.nkb && ok; ++kb) {
           if (!mbar_wait(full_bar(stage), phase, abort_flag)) {
             ok = false;
@@ -881,9 +882,9 @@ __global__ void __launch_bounds__(ACC_THREADS, 1)
           const uint32_t lo_off = C::A_BYTES + C::B_BYTES;
           const int k0 = kb * C::BK;
           const int amn = p.a_mn ^ ((p.sym_in && (k0 >> 8) < (um0 >> 8)) ? 1 : 0);
-          const int bmn = p.b_mn ^ ((p.sym_in && (k0 >> 8) > (un0 >> 8)) ? 1 : 0);
+          const int bmn = p.b_mn ^ ((p.sym_in_b && (k0 >> 8) > (un0 >> 8)) ? 1 : 0);
           const uint32_t idesc =
-              p.sym_in ? (p.idesc0 | (static_cast<uint32_t>(amn) << 15) |
+              p.sym_any ? (p.idesc0 | (static_cast<uint32_t>(amn) << 15) |
                           (static_cast<uint32_t>(bmn) << 16))
                        : p.idesc;
 #pragma unroll
@@ -974,7 +975,7 @@ __global__ void __launch_bounds__(ACC_THREADS, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(mapa_shared(pempty_bar(buf), 0));
+        if (lane == 0) mbar_arrive_remote(mapa_shared(pempty_bar(buf), 0));
       }
       if (!ok) break;
       const int rg = m0 + row;
@@ -1144,6 +1145,8 @@ static dash_status run_gemm(const GemmLaunch& g, cudaStream_t st) {
   // Symmetric-half iterates: CTA-pair tiles of the plain kernels only.
   const bool sym_ok = (MODE == 2 && (KT != 2 || ACC));
   p.sym_in = (sym_ok && g.sym_in) ? 1 : 0;
+  p.sym_in_b = (sym_ok && g.sym_in_b) ? 1 : 0;
+  p.sym_any = p.sym_in | p.sym_in_b;
   p.sym_out = (sym_ok && g.sym_out) ? 1 : 0;
   p.t256 = g.dim / 256;
   if (p.sym_out) {
@@ -1151,7 +1154,7 @@ static dash_status run_gemm(const GemmLaunch& g, cudaStream_t st) {
     p.total_tiles = g.nblocks * p.t256 * (p.t256 + 1) / 2 * (256 / BN) * CL;
     p.total_units = p.total_tiles / CL;
   }
-  if (p.sym_in) {
+  if (p.sym_any) {
     // The other-major view of each operand over the same memory.
     const uint32_t am_in = !a_mn ? C::MN_ATOM : C::BK, am_out = !a_mn ? C::BK : 128;
     const uint32_t bm_in = !b_mn ? C::MN_ATOM : C::BK, bm_out = !b_mn ? C::BK : BN / CL;

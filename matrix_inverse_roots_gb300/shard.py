@@ -103,6 +103,7 @@ class DataParallelStep:
         # Every rank must all-gather pieces of one dtype, also a rank owning none.
         self.u_dtype = u_dtype
         self._gpad = None
+        self._gown = None
         self._upad = None
         self._uall = None
 
@@ -123,7 +124,10 @@ class DataParallelStep:
             src = self._gpad
         else:
             src = G
-        G_own = torch.empty(shape, dtype=G.dtype, device=G.device)
+        if (self._gown is None or self._gown.dtype != G.dtype or self._gown.device != G.device
+                or tuple(self._gown.shape) != shape):
+            self._gown = torch.empty(shape, dtype=G.dtype, device=G.device)
+        G_own = self._gown
         dist.reduce_scatter_tensor(G_own, src, op=dist.ReduceOp.SUM)
         U_own = self.local_step(G_own[:n_own]) if n_own > 0 else None
         if U_own is not None and n_own == chunk and U_own.dtype == self.u_dtype:

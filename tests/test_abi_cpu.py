@@ -230,3 +230,11 @@ def test_library_tier_selection_bad_tiers():
         t.update(bad)
         with pytest.raises(dr.DashError):
             dr.select_tiers([1.0], [0.5], [t])
+
+
+def test_library_default_tiers_are_the_oracles():
+    """The binding's default tiers (used by bench.py and inv_root_auto callers) and
+    the oracle's are written separately; they must agree."""
+    import matrix_inverse_roots_gb300 as dr
+
+    assert [dict(t) for t in dr.DEFAULT_TIERS] == [dict(t) for t in oracle.DEFAULT_TIERS]

@@ -237,14 +237,6 @@ def test_config4_24_layer_step(root, prec):
     check_step(dr, "cfg4", *out, root, prec, fidx, gidx, power="fp16")
 
 
-# Per-block solver selection on the benchmarked stack.  The 16-bit Coupled Newton
-# keeps M as an fp16 pair (about 22 bits) through its early updates, so the scaled
-# block is stored at u = 2^-22 there; the fallback runs Coupled Newton in 3xTF32
-# long enough for a smallest scaled eigenvalue of 1e-6 to converge.
-TIERS = ({"solver": "cn", "prec": "fp16", "iters": 10, "u": 2.0 ** -22, "gate": 1e-2},
-         {"solver": "cn", "prec": "3xtf32", "iters": 24, "u": 2.0 ** -24, "gate": 1e-4})
-
-
 def test_config4_tiered_roots():
     """24 layers, roots with the solver chosen per block ([pt] Significancia e
     Alegacoes, Direcoes Futuras): lambda_min estimates, tier choice and each sampled
@@ -261,6 +253,7 @@ def test_config4_tiered_roots():
     # The lambda_min iteration in the fp32-accurate mode, so that it has an exact
     # oracle counterpart.
     lmin = dr.spectral_lambda_min(F, lam, dr.SCALE_POWER, V0, 10, ridge=RIDGE)
+    TIERS = dr.DEFAULT_TIERS
     X, choice = dr.inv_root_auto(F, lam, lmin, TIERS, ridge=RIDGE, max_ws_bytes=64 << 30)
     torch.cuda.synchronize()
     assert dr.device_status() == 0

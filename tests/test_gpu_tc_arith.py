@@ -1,7 +1,7 @@
 """The library's TF32 / 3xTF32 GEMM against the tensor-core arithmetic model.
 
-The model (tests/tc_arith.py) is what the ill-conditioned config tests gate
-against, so it has to describe the kernels: on crafted inputs the GEMM must give
+The model (tests/tc_arith.py) is a diagnostic description of the kernels'
+accumulation, so it has to describe them: on crafted inputs the GEMM must give
 the model's value exactly; on random inputs most elements agree bit for bit and
 the error norms agree closely."""
 

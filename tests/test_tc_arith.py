@@ -130,26 +130,8 @@ def test_gemm_error_is_fp32_class_and_biased():
     assert ((got3p - ex) / ex).mean() > ((got3 - ex) / ex).mean()   # shorter chains, less bias
 
 
-def test_roots_reduce_to_exact_on_identity():
-    eye = torch.eye(64)
-    for fn in (tc_arith.cn_root, tc_arith.ndb_root):
-        X = fn(4.0 * eye, 4.0, 6, "3xtf32")
-        assert torch.allclose(X, eye * 4.0 ** -0.25, rtol=0, atol=1e-6)
-
-
 def test_random_small_integers_are_exact():
     rng = random.Random(7)
     a = torch.tensor([[rng.randint(-8, 8) for _ in range(64)] for _ in range(4)], dtype=torch.float32)
     b = torch.tensor([[rng.randint(-8, 8) for _ in range(3)] for _ in range(64)], dtype=torch.float32)
     assert torch.equal(tc_arith.gemm(a, b, "tf32"), (a.double() @ b.double()).float())
-
-
-def test_tile_sym_mirrors_lower_tiles():
-    g = torch.Generator().manual_seed(9)
-    m = torch.randn((512, 512), generator=g)
-    s = tc_arith.tile_sym(m)
-    assert torch.equal(s[:256, :], m[:256, :])                 # upper block row kept
-    assert torch.equal(s[256:, 256:], m[256:, 256:])           # diagonal tile kept whole
-    assert torch.equal(s[256:, :256], m[:256, 256:].T)         # lower tile mirrored
-    sym = m + m.T
-    assert torch.equal(tc_arith.tile_sym(sym), sym)            # a symmetric matrix is unchanged
