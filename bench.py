@@ -47,22 +47,19 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # Nominal dense ratios to bf16 (GB300): tf32 1.1 / 2.25 PFLOP/s.
 TF32_RATIO = 1.1 / 2.25
 
-# DRAM bytes (read + write) per factor block per launch of the CTA-pair fp16 GEMM:
-# mean of the four Coupled Newton launches of an ncu capture of 64 blocks of 1024^2
-# (traffic grows in proportion to the blocks a launch processes).  Valid only for
-# the kernel sources it was taken on, identified by GEMM_TRAFFIC_SRC.
-GEMM_TRAFFIC_PER_BLOCK = 2.975e6
-GEMM_TRAFFIC_SRC = "f70b79738d50bf44"
+# DRAM bytes (read + write) per launch of the FP16 GEMM class, averaged over the
+# class's launches in one benchmark step at full size: an ncu capture of
+# `bench.py --case step` with gpu__time_duration.sum, dram__bytes_read.sum and
+# dram__bytes_write.sum (one pass).  Valid only for the sources it was taken on,
+# identified by GEMM_TRAFFIC_SRC (None: not measured for these sources).
+GEMM_TRAFFIC_PER_LAUNCH = None
+GEMM_TRAFFIC_SRC = None
 GEMM_SOURCES = ("matrix_inverse_roots_gb300/csrc/gemm_tc.cu",
-                "matrix_inverse_roots_gb300/csrc/dash_common.cuh")
+                "matrix_inverse_roots_gb300/csrc/dash_common.cuh",
+                "matrix_inverse_roots_gb300/csrc/dash_api.cu")
 
 
-def gemm_traffic(flops_per_launch, b):
-    """Measured DRAM bytes of one dominant-GEMM launch, or None if the kernel changed.
-
-    The launch's block count comes from its executed flops: a Coupled Newton product
-    at B a multiple of 256 computes only the T(T+1)/2 upper 256-tiles of T^2
-    (T = B / 256), i.e. 2 B^3 (T + 1) / (2 T) flops per block."""
+def gemm_source_hash():
     import hashlib
 
     h = hashlib.sha256()
@@ -70,11 +67,15 @@ def gemm_traffic(flops_per_launch, b):
     for f in GEMM_SOURCES:
         with open(os.path.join(root, f), "rb") as fh:
             h.update(fh.read())
-    if h.hexdigest()[:16] != GEMM_TRAFFIC_SRC or b != 1024:
+    return h.hexdigest()[:16]
+
+
+def gemm_traffic():
+    """Measured DRAM bytes of an average FP16-GEMM launch of the step, or None if the
+    sources changed since the capture."""
+    if GEMM_TRAFFIC_PER_LAUNCH is None or gemm_source_hash() != GEMM_TRAFFIC_SRC:
         return None
-    t = b // 256
-    per_block = 2.0 * b ** 3 * ((t + 1) / (2.0 * t) if b % 256 == 0 else 1.0)
-    return round(GEMM_TRAFFIC_PER_BLOCK * flops_per_launch / per_block)
+    return GEMM_TRAFFIC_PER_LAUNCH
 
 
 def load_peaks():
@@ -419,8 +420,8 @@ def roofline_from_trace(records, peaks):
                     else " x nominal tf32/bf16 ratio" + (" / 3" if dom == "gemm_3xtf32" else "")),
                 "launches": n, "avg_launch_ms": round(ms / n, 4),
                 "flops_per_launch": fl / n,
-                # The capture measured the fp16 Coupled Newton products only.
-                "traffic": gemm_traffic(fl / n, BS) if dom == "gemm_f16" else None}
+                # Average over the class's launches in one step (ncu capture).
+                "traffic": gemm_traffic() if dom == "gemm_f16" else None}
     else:
         peak = peaks["hbm_gbs"]
         achieved = b / (ms * 1e-3) / 1e9
@@ -469,6 +470,9 @@ def run_gpu(args):
     if world > 1:
         import torch.distributed as tdist
 
+        # NCCL's communicator set-up lines (rank count, transport) in the log.
+        os.environ.setdefault("NCCL_DEBUG", "INFO")
+        os.environ.setdefault("NCCL_DEBUG_SUBSYS", "INIT")
         torch.cuda.set_device(local)
         tdist.init_process_group("nccl", device_id=torch.device("cuda", local))
         dist = tdist

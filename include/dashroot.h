@@ -179,10 +179,23 @@ dash_status spectral_scale(const float* A, float ridge, int64_t N, int B, int mo
  *   M_{i+1} = (T_i^2)^2 M_i;   X[k] = scale[k]^{-1/4} X_iters.
  * 4*iters - 4 products per block for iters >= 2, none for iters = 1 (iteration 0
  * needs no X product, the last no M update).  Every iterate is a polynomial in
- * the symmetric A_s, so for B a multiple of 256 each product computes and stores
+ * the symmetric A_s, so for B a multiple of 256 a product may compute and store
  * only its 256 x 256 tiles on or above the diagonal (10 of 16 at B = 1024); X's
  * tiles below the diagonal are written as their mirrors' transposes.  A's tiles
  * below the diagonal then do not affect X, so A must be symmetric, as a factor is.
+ * Arithmetic by precision:
+ *   DASH_FP32_3XTF32: the identity-shifted form of the same iteration (T stored
+ *     as D = T - I; X T = X + X D, T^2 = I + D D + 2D, ..., each large term added
+ *     exactly in fp32), products with round-to-nearest partial sums, every
+ *     product in symmetric halves.
+ *   DASH_FP16 / DASH_BF16: M is carried as a 16-bit pair (hi + lo, about 22 bits
+ *     in fp16) through all but the last three M updates (two products per slice);
+ *     the T^2, T^4 and M products are computed whole (a symmetric-half product
+ *     would turn the antisymmetric part of their rounding into error in M's
+ *     smallest eigenvalues), except in the first iteration (T_0 exactly
+ *     symmetric: T^2, T^4 in halves) and the last M update (its error meets X
+ *     in one factor only: all three in halves); the X product in halves.
+ *   DASH_TF32: plain, every product in symmetric halves.
  *   A (N, B, B) fp32; scale (N,) fp32 > 0 (e.g. from spectral_scale);
  *   iters >= 1; prec any dash_prec; X (N, B, B) fp32 output;
  *   resid_out (N, iters) fp32 or NULL: resid_out[k*iters + i] =
@@ -204,7 +217,10 @@ dash_status inv_root_cn(const float* A, float ridge, const float* scale, int64_t
  * 6*iters - 6 products per block for iters >= 2 (one for iters = 1).
  *   resid_out (N, 2, iters) fp32 or NULL: ||Z_i Y_i - I||_F / sqrt(B) per stage.
  *   Other arguments as inv_root_cn.  Half precision runs but the pages report
- *   it unstable ([pt] Resultados, Precisao).
+ *   it unstable ([pt] Resultados, Precisao).  Every product is computed whole.
+ *   DASH_FP32_3XTF32 runs the identity-shifted form (T stored as D = T - I;
+ *   Y T = Y + Y D, T Z = Z + D Z, the large term added exactly in fp32) with
+ *   round-to-nearest partial sums.
  */
 dash_status inv_root_ndb(const float* A, float ridge, const float* scale, int64_t N, int B,
                          int iters, int prec, float* X, float* resid_out, void* ws,
@@ -369,8 +385,10 @@ dash_status dash_gemm(const void* A, const void* A_lo, int trans_a, const void* 
  *   sym 0: as dash_gemm.  sym 1: A and B symmetric; only their 256 x 256 tiles on
  *   or above the diagonal are read (a tile below is taken as its mirror's
  *   transpose).  sym 2: as 1, and only C's tiles on or above the diagonal are
- *   computed and written (C symmetric by construction).  Modes 1 and 2 apply for B
- *   a multiple of 256 and act as 0 otherwise.
+ *   computed and written (C symmetric by construction).  sym 3: A and B read whole,
+ *   only C's tiles on or above the diagonal computed and written.  sym 4: A
+ *   symmetric and read from its upper tiles as in 1, B read whole, C whole.
+ *   Modes 1-4 apply for B a multiple of 256 and act as 0 otherwise.
  *   With prec DASH_FP16 / DASH_BF16, a non-NULL B_lo makes B a 16-bit pair:
  *   C = A B + A B_lo, both products in that 16-bit type (A_lo ignored).
  */

@@ -596,8 +596,10 @@ def gemm(A, B, prec=TF32, trans_a=False, trans_b=False, A_lo=None, B_lo=None, C=
 
 
 def gemm_ex(A, B, prec=TF32, sym=0, trans_a=False, trans_b=False, A_lo=None, B_lo=None, C=None):
-    """dash_gemm_ex: symmetric-half operand forms (sym 1, 2) and, for 16-bit prec,
-    a 16-bit pair B (B_lo given): C = A B + A B_lo."""
+    """dash_gemm_ex: symmetric-half operand forms (sym 1-4: 1 both operands read from
+    their upper 256-tiles, 2 as 1 with only C's upper tiles written, 3 whole operands
+    with only C's upper tiles written, 4 only A read from its upper tiles) and, for
+    16-bit prec, a 16-bit pair B (B_lo given): C = A B + A B_lo."""
     lib = load_library()
     p = _prec(prec)
     _stack(A, "A", A.dtype)

@@ -374,7 +374,7 @@ dash_status dash_gemm(const void* A, const void* A_lo, int trans_a, const void* 
 dash_status dash_gemm_ex(const void* A, const void* A_lo, int trans_a, const void* Bm,
                          const void* B_lo, int trans_b, int64_t N, int B, int prec, int sym,
                          float* C, void* stream) {
-  if (N < 0 || !valid_dim(B) || !valid_prec(prec) || sym < 0 || sym > 2)
+  if (N < 0 || !valid_dim(B) || !valid_prec(prec) || sym < 0 || sym > 4)
     return DASH_ERR_INVALID_ARG;
   if (N == 0) return DASH_OK;
   if (!A || !Bm || !C || !aligned16(A) || !aligned16(Bm) || !aligned16(C))
@@ -599,7 +599,8 @@ dash_status inv_root_cn(const float* A, float ridge, const float* scale, int64_t
   const int fmt = prec_fmt(prec);
   const int S = sym_mode(prec, B);  // symmetric-half iterates
   // 16-bit precisions (build-time modes, see gemm): the T^2 and T^4 products and the
-  // M-update run whole, only the X product keeps symmetric halves.  A product kept
+  // M-update run whole (but in the two iterations below), the X product keeps
+  // symmetric halves.  A product kept
   // as its upper 256-tiles is symmetrised by a tile mask, which turns the
   // antisymmetric part of a product of two rounded, not exactly commuting, iterates
   // (of order u ||M|| at 16 bits) into a symmetric error of the same size.  An
@@ -619,6 +620,27 @@ dash_status inv_root_cn(const float* A, float ridge, const float* scale, int64_t
 #endif
   const int ST = (S && is_half(prec)) ? DASH_CN16_TSYM : S;
   const int SX = (S && is_half(prec)) ? DASH_CN16_XSYM : S;
+  // Per-iteration modes of the T^2 / T^4 products and the M-update in 16-bit
+  // precisions.  Whole products are needed while an error in M is amplified by the
+  // iterations that follow.  Two iterations keep halves:
+  //   k = 0: T_0 = (5I - A_s)/4 is exactly symmetric, so its squares keep halves;
+  //     the M-update (T_0^4 rounded does not commute with M_0) stays whole, reading
+  //     T^4 from its upper tiles (mode 4).
+  //   k = K - 2, the last M-update: its error reaches X only through T_{K-1}, one
+  //     factor of the final product, with no later iteration to amplify it (M is
+  //     plain there, K - 2 >= jp).
+  // Measured on rank-deficient factors (CN FP16, 10 iterations, B = 1024, against
+  // the float64 oracle): every M-chain product whole 3.1e-3; this schedule 3.3e-3;
+  // halves in all of the last three iterations 5.8e-3.
+  auto t_mode = [&](int k) {
+    if (!(S && is_half(prec))) return ST;
+    return (k == 0 || k == K - 2) ? S : ST;
+  };
+  auto m_mode = [&](int k) {
+    if (!(S && is_half(prec))) return S;
+    if (k == K - 2) return S;
+    return (k == 0) ? 4 : DASH_CN16_MSYM;
+  };
   Carver cv(ws, ws_bytes);
   RootSmall sm;
   sm.inv_s = static_cast<float*>(cv.take(N * 4));
@@ -711,12 +733,12 @@ dash_status inv_root_cn(const float* A, float ridge, const float* scale, int64_t
       ea.nout = 1;
       ea.out[0] = eout(tsp, fmt, 1.0f, 0.0f, e2);
       if (shift) with_e(ea, tk, fmt);
-      DASH_TRY(gemm(prec, B, nc, tk, 0, tk, 0, ea, st, ST));
+      DASH_TRY(gemm(prec, B, nc, tk, 0, tk, 0, ea, st, t_mode(k)));
       EpiParams eb = epi_none();
       eb.nout = 1;
       eb.out[0] = eout(bT4, fmt, 1.0f, 0.0f, e2);
       if (shift) with_e(eb, tsp, fmt);
-      DASH_TRY(gemm(prec, B, nc, tsp, 0, tsp, 0, eb, st, ST));
+      DASH_TRY(gemm(prec, B, nc, tsp, 0, tsp, 0, eb, st, t_mode(k)));
       // M_{k+1} = T^4 M_k; the same epilogue forms T_{k+1} (into the scratch, free
       // once T^4 is formed) and the residual of M_{k+1}.
       EpiParams em = epi_none();
@@ -730,8 +752,7 @@ dash_status inv_root_cn(const float* A, float ridge, const float* scale, int64_t
       em.resid_acc = racc ? racc + (k + 1) : nullptr;
       em.resid_stride = K;
       // 16-bit: T^4 and M read whole, M and T written whole (see ST above).
-      DASH_TRY(gemm(prec, B, nc, bT4, 0, bm[mc], 0, em, st,
-                    (S && is_half(prec)) ? DASH_CN16_MSYM : S, k < jp));
+      DASH_TRY(gemm(prec, B, nc, bT4, 0, bm[mc], 0, em, st, m_mode(k), k < jp));
       mc ^= 1;
       const Buf t = tk;
       tk = tsp;

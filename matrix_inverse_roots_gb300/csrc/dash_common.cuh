@@ -382,6 +382,24 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[16]) {
                  "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])::"memory");
 }
 
+// ---------------------------------------------------------------- packed fp32 pairs
+// Two fp32 values in one 64-bit register (lo = first), added lane by lane with
+// round-to-nearest: bit for bit two __fadd_rn, in one instruction.
+
+__device__ __forceinline__ uint64_t f32x2_pack(uint32_t lo, uint32_t hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+
+__device__ __forceinline__ void f32x2_unpack(uint64_t v, uint32_t& lo, uint32_t& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ void f32x2_add_rn(uint64_t& acc, uint64_t v) {
+  asm("add.rn.f32x2 %0, %0, %1;" : "+l"(acc) : "l"(v));
+}
+
 // ---------------------------------------------------------------- formats
 
 // Round an fp32 value to the nearest TF32 value (ties away from zero).

@@ -722,18 +722,21 @@ __global__ void __launch_bounds__(320, 1)
 // at the level of a few instructions: the MMA warp starts a fresh TMEM partial
 // accumulator every ACC_SUB sub-steps (one sub-step = the three MMAs of one K = 8
 // slice), and eight reducer warps -- two per TMEM lane quarter, 64 columns each --
-// add the partials into fp32 registers with round-to-nearest.  The fused epilogue
-// then runs on those register sums.  Pair tiles are 256 x 128, so that TMEM holds
-// four partial buffers: the MMA runs up to four partials ahead while the reducers
-// run a tile's epilogue.
+// add the partials into fp32 registers with round-to-nearest (two columns per
+// packed add.rn.f32x2, which halves the reducers' add issue).  Pair tiles are
+// 256 x 128, so TMEM holds three partial buffers and a fourth, final buffer: at a
+// tile's end the reducers store their sums there and go on with the next tile's
+// partials, while four epilogue warps (one per lane quarter) read the final buffer
+// and run the fused epilogue.  The MMA therefore never waits for a tile's stores.
 #ifndef DASH_ACC_SUB
 #define DASH_ACC_SUB 2
 #endif
 constexpr int ACC_SUB = DASH_ACC_SUB;  // K = 8 sub-steps per TMEM partial
 constexpr int ACC_BN = 128;            // pair tile 256 x 128
-constexpr int ACC_NPB = 4;             // TMEM partial buffers (4 x 128 columns)
-constexpr int ACC_REDUCERS = 8;        // reducer / epilogue warps per CTA
-constexpr int ACC_THREADS = 32 * (2 + ACC_REDUCERS);
+constexpr int ACC_NPB = 3;             // TMEM partial buffers (3 x 128 columns) + final
+constexpr int ACC_REDUCERS = 8;        // reducer warps per CTA
+constexpr int ACC_EPI = 4;             // epilogue warps per CTA
+constexpr int ACC_THREADS = 32 * (2 + ACC_REDUCERS + ACC_EPI);
 
 template <int KT>
 __global__ void __launch_bounds__(ACC_THREADS, 1)
@@ -757,13 +760,17 @@ __global__ void __launch_bounds__(ACC_THREADS, 1)
   auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
   auto pfull_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
   auto pempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + NPB + a); };
-  const uint32_t fin_bar = bar0 + 8u * (2 * C::STAGES + 2 * NPB);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * (2 * C::STAGES + 2 * NPB + 1));
-  volatile int* abort_flag =
-      reinterpret_cast<volatile int*>(bar_area + 8 * (2 * C::STAGES + 2 * NPB + 1) + 8);
-  static_assert(8 * (2 * C::STAGES + 2 * NPB + 1) + 16 <= C::BAR_BYTES, "barrier area");
-  constexpr uint32_t TMEM_ACC_COLS = NPB * BN;
-  static_assert(TMEM_ACC_COLS == 512, "partial buffers fill TMEM");
+  // The final buffer: filled by this CTA's reducers, emptied by its epilogue warps.
+  const uint32_t ffull_bar = bar0 + 8u * (2 * C::STAGES + 2 * NPB);
+  const uint32_t fempty_bar = ffull_bar + 8u;
+  const uint32_t fin_bar = fempty_bar + 8u;
+  constexpr int NBAR = 2 * C::STAGES + 2 * NPB + 3;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * NBAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * NBAR + 8);
+  static_assert(8 * NBAR + 16 <= C::BAR_BYTES, "barrier area");
+  constexpr uint32_t TMEM_ACC_COLS = (NPB + 1) * BN;
+  static_assert(TMEM_ACC_COLS == 512, "partial and final buffers fill TMEM");
+  constexpr uint32_t FINAL_COL = NPB * BN;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -783,6 +790,8 @@ __global__ void __launch_bounds__(ACC_THREADS, 1)
       mbar_init(pfull_bar(a), 1);
       mbar_init(pempty_bar(a), 2 * ACC_REDUCERS);  // the reducer warps of both CTAs
     }
+    mbar_init(ffull_bar, ACC_REDUCERS);
+    mbar_init(fempty_bar, ACC_EPI);
     mbar_init(fin_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -933,23 +942,20 @@ __global__ void __launch_bounds__(ACC_THREADS, 1)
       mma_commit_pair(fin_bar);
       mbar_wait_drain(fin_bar, 0);
     }
-  } else {
-    // ------------------------------------------------- reducers + epilogue
+  } else if (warp < 2 + ACC_REDUCERS) {
+    // ------------------------------------------------- reducers
     // Warp w: TMEM lane quarter w & 3, column group (w - 2) >> 2 of COLS columns.
     constexpr int COLS = BN / (ACC_REDUCERS / 4);
     const int q = warp & 3;
     const int cq = (warp - 2) >> 2;
-    const int row = q * 32 + lane;
-    const long long dd = static_cast<long long>(p.dim) * p.dim;
     long long gidx = 0;
+    uint32_t tcount = 0;
     bool ok = true;
-    for (long long u = cid; u < p.total_units && ok; u += ncl) {
-      long long blk;
-      int m0, n0;
-      decode_unit<CL>(u, p, crank, blk, m0, n0, BN);
-      float sum[COLS];
+    for (long long u = cid; u < p.total_units && ok; u += ncl, ++tcount) {
+      // Running sums as packed fp32 pairs: one add.rn.f32x2 per two columns.
+      uint64_t sum[COLS / 2];
 #pragma unroll
-      for (int j = 0; j < COLS; ++j) sum[j] = 0.0f;
+      for (int j = 0; j < COLS / 2; ++j) sum[j] = 0ull;
       for (int kg = 0; kg < ngroups; ++kg, ++gidx) {
         const int buf = static_cast<int>(gidx % NPB);
         const uint32_t par = static_cast<uint32_t>((gidx / NPB) & 1);
@@ -968,9 +974,9 @@ __global__ void __launch_bounds__(ACC_THREADS, 1)
           tmem_wait_ld(ra);
           tmem_fence_regs(rb);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            sum[c * 16 + j] = __fadd_rn(sum[c * 16 + j], __uint_as_float(ra[j]));
-            sum[(c + 1) * 16 + j] = __fadd_rn(sum[(c + 1) * 16 + j], __uint_as_float(rb[j]));
+          for (int j = 0; j < 8; ++j) {
+            f32x2_add_rn(sum[c * 8 + j], f32x2_pack(ra[2 * j], ra[2 * j + 1]));
+            f32x2_add_rn(sum[(c + 1) * 8 + j], f32x2_pack(rb[2 * j], rb[2 * j + 1]));
           }
         }
         tc_fence_before();
@@ -978,18 +984,59 @@ __global__ void __launch_bounds__(ACC_THREADS, 1)
         if (lane == 0) mbar_arrive_remote(mapa_shared(pempty_bar(buf), 0));
       }
       if (!ok) break;
+      // The tile's sums go to the final buffer once the epilogue warps have read
+      // the previous tile's.
+      if (!mbar_wait(fempty_bar, (tcount & 1u) ^ 1u, abort_flag)) break;
+      tc_fence_after();
+      const uint32_t tfin = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                            static_cast<uint32_t>(FINAL_COL + cq * COLS);
+#pragma unroll
+      for (int c = 0; c < COLS / 16; ++c) {
+        uint32_t r[16];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f32x2_unpack(sum[c * 8 + j], r[2 * j], r[2 * j + 1]);
+        tmem_st16(tfin + c * 16, r);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ffull_bar);
+    }
+  } else {
+    // ------------------------------------------------- epilogue
+    // Warp w reads its TMEM lane quarter (w & 3) of the final buffer: 32 rows of the
+    // CTA tile, all BN columns.
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const long long dd = static_cast<long long>(p.dim) * p.dim;
+    uint32_t tcount = 0;
+    for (long long u = cid; u < p.total_units; u += ncl, ++tcount) {
+      if (!mbar_wait(ffull_bar, tcount & 1u, abort_flag)) break;
+      tc_fence_after();
+      long long blk;
+      int m0, n0;
+      decode_unit<CL>(u, p, crank, blk, m0, n0, BN);
       const int rg = m0 + row;
-      const int cbase = n0 + cq * COLS;
+      const int r0w = m0 + q * 32;
       const long long rbase = blk * dd + static_cast<long long>(rg) * p.dim;
       const TileEpi te = tile_epi(p.epi, blk);
       float rsum = 0.0f;
-#pragma unroll
-      for (int c = 0; c < COLS / 16; ++c) {
-        float v[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = sum[c * 16 + j];
-        epilogue16f(p.epi, te, rg, cbase + c * 16, rbase + cbase + c * 16, v, rsum,
-                    chunk_on_diag(m0 + q * 32, cbase + c * 16));
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(FINAL_COL);
+      // Off the MMA's critical path: one TMEM load in flight at a time.
+#pragma unroll 1
+      for (int c = 0; c < BN / 16; ++c) {
+        uint32_t ra[16];
+        tmem_ld16(taddr + c * 16, ra);
+        tmem_wait_ld(ra);
+        if (c + 1 == BN / 16) {
+          // Every load of the final buffer has completed: hand it back.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(fempty_bar);
+        }
+        const int ca = n0 + c * 16;
+        epilogue16(p.epi, te, rg, ca, rbase + ca, ra, rsum, chunk_on_diag(r0w, ca));
       }
       if (p.epi.resid_acc != nullptr) {
         if (p.sym_out && (m0 >> 8) != (n0 >> 8)) rsum *= 2.0f;

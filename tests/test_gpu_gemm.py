@@ -93,23 +93,27 @@ def upper_tiles(x, b):
 
 
 @pytest.mark.parametrize("prec", ["tf32", "3xtf32", "fp16", "bf16"])
-@pytest.mark.parametrize("sym", [1, 2])
+@pytest.mark.parametrize("sym", [1, 2, 3, 4])
 @pytest.mark.parametrize("b", [256, 512, 1024])
 def test_gemm_symmetric_halves(prec, sym, b):
-    """C = S S from the upper 256-tiles of S only (the lower ones hold NaN)."""
+    """C = S S, each operand that the mode reads from its upper 256-tiles given
+    with NaN below them (A in modes 1, 2, 4; B in 1, 2); modes 2 and 3 write only
+    C's upper tiles (C is prefilled with NaN to show what was written)."""
     require_gpu()
     dr = library()
     n = 3
     S, P = sym_operand(b, n, 7 * b + sym)
     Ph, Pl, _ = operands(P, prec)
-    _, _, S64 = operands(S, prec)
-    C = torch.zeros((n, b, b), device="cuda")
-    dr.gemm_ex(Ph, Ph, prec=prec, sym=sym, A_lo=Pl, B_lo=Pl, C=C)
+    Sh, Sl, S64 = operands(S, prec)
+    Ah, Al = (Ph, Pl) if sym in (1, 2, 4) else (Sh, Sl)
+    Bh, Bl = (Ph, Pl) if sym in (1, 2) else (Sh, Sl)
+    C = torch.full((n, b, b), float("nan"), device="cuda")
+    dr.gemm_ex(Ah, Bh, prec=prec, sym=sym, A_lo=Al, B_lo=Bl, C=C)
     torch.cuda.synchronize()
     assert dr.device_status() == 0
     ref = S64 @ S64
     got = to64(C)
-    mask = upper_tiles(got[0], b) if sym == 2 else np.ones((b, b), dtype=bool)
+    mask = upper_tiles(got[0], b) if sym in (2, 3) else np.ones((b, b), dtype=bool)
     assert np.all(np.isfinite(got[:, mask]))
     err = np.linalg.norm((got - ref)[:, mask]) / np.linalg.norm(ref[:, mask])
     tol = 2e-5 if prec == "3xtf32" else 1e-5
