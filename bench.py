@@ -190,6 +190,11 @@ class Workload:
         self.lam = torch.empty(self.nf, dtype=torch.float32, device=dev)
         self.root_prec = root_prec
         self.apply_prec = dr.TF32 if root_prec in (dr.FP16, dr.BF16, dr.TF32) else dr.FP32_3XTF32
+        # With a TF32 apply the root solver writes its roots already rounded to TF32
+        # and apply reads them as they are (no conversion pass over both roots).
+        fuse = self.apply_prec == dr.TF32 and not ndb
+        self.root_out = root_prec | (dr.ROOT_TF32 if fuse else 0)
+        self.apply_in = self.apply_prec | (dr.ROOT_TF32 if fuse else 0)
         self.ndb = ndb
         cap = 48 << 30
         # The pages' power iteration runs in half precision; "3xtf32" keeps it fp32-accurate.
@@ -224,9 +229,9 @@ class Workload:
             dr.inv_root_ndb(self.F, self.lam, NDB_ITERS, self.root_prec, ridge=RIDGE, X=self.Froot,
                             ws=self.ws_root)
         else:
-            dr.inv_root_cn(self.F, self.lam, CN_ITERS, self.root_prec, ridge=RIDGE, X=self.Froot,
+            dr.inv_root_cn(self.F, self.lam, CN_ITERS, self.root_out, ridge=RIDGE, X=self.Froot,
                            ws=self.ws_root)
-        dr.precondition_apply(self.G, self.Froot, self.apply_prec, U=self.U, ws=self.ws_apply)
+        dr.precondition_apply(self.G, self.Froot, self.apply_in, U=self.U, ws=self.ws_apply)
 
     def tiered_step(self, tiers, ws_auto, lam_min):
         """The step with the root solver chosen per block (inv_root_auto)."""
@@ -363,9 +368,9 @@ def full_optimizer_step(torch, dr, synth, wl, dev, steps, dist, peaks, lr=1e-3):
         if refresh:
             dr.spectral_scale(wl.F, wl.power_mode, wl.V0, POWER_ITERS, ridge=RIDGE, out=wl.lam,
                               ws=wl.ws_scale)
-            dr.inv_root_cn(wl.F, wl.lam, CN_ITERS, wl.root_prec, ridge=RIDGE, X=wl.Froot,
+            dr.inv_root_cn(wl.F, wl.lam, CN_ITERS, wl.root_out, ridge=RIDGE, X=wl.Froot,
                            ws=wl.ws_root)
-        dr.precondition_update(wl.G, wl.Froot, W, lr, wl.apply_prec, ws=wl.ws_apply)
+        dr.precondition_update(wl.G, wl.Froot, W, lr, wl.apply_in, ws=wl.ws_apply)
 
     step()
     dr.trace_start(400 * steps + 64)
@@ -579,7 +584,7 @@ def run_gpu(args):
         "config": {
             "workload": "llama-d2048 x24 layers: 1248 bf16 gradient blocks, (2496,1024,1024) fp32 "
                         "factor stack; step = accumulate(beta 0.95) + power scale(32 vec x10, "
-                        + args.power + ") + CN fp16 x10 + apply tf32, f=1",
+                        + args.power + ") + CN fp16 x10 (roots stored TF32-rounded) + apply tf32, f=1",
             "blocks": wl.nf, "block": BS, "root": "cn-fp16", "iters": CN_ITERS,
             "l2": "inputs 10.5 GB >> 129 MB L2, no flush",
         },

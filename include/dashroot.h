@@ -70,6 +70,18 @@ typedef enum {
   DASH_BF16 = 3
 } dash_prec;
 
+/* Flag OR-ed into the prec argument (no counterpart on the pages: it only moves
+ * a rounding step).
+ *   inv_root_cn / inv_root_ndb / inv_root_cheb: X is written rounded to TF32
+ *     (round to nearest, ties away from zero; fp32 container), the operand form
+ *     of DASH_TF32 products.  The solver's arithmetic is unchanged.
+ *   precondition_apply / precondition_update, with DASH_TF32 only: Froot
+ *     already holds TF32-rounded roots (e.g. written with this flag) and the
+ *     products read it as it is, without the conversion pass they otherwise
+ *     make over both roots (results identical on such roots).
+ * Anywhere else: DASH_ERR_INVALID_ARG. */
+#define DASH_ROOT_TF32 0x100
+
 typedef enum { DASH_DT_F32 = 0, DASH_DT_BF16 = 1, DASH_DT_F16 = 2 } dash_dtype;
 
 /* Inverse-root solvers, for per-block solver selection. */

@@ -25,6 +25,9 @@ FP16 = 2
 BF16 = 3
 PRECISIONS = {"3xtf32": FP32_3XTF32, "fp32": FP32_3XTF32, "tf32": TF32, "fp16": FP16,
               "bf16": BF16}
+# Flag OR-ed into prec (DASH_ROOT_TF32): root solvers write X rounded to TF32;
+# precondition_apply / _update with TF32 then read such roots without converting.
+ROOT_TF32 = 0x100
 
 # dash_dtype
 DT_F32 = 0
@@ -219,8 +222,12 @@ def _gdt(t):
 
 
 def _prec(p):
+    """A precision name ("fp16", ...; "+root_tf32" adds ROOT_TF32) or a dash_prec value."""
     if isinstance(p, str):
-        return PRECISIONS[p.lower()]
+        name, _, flag = p.lower().partition("+")
+        if flag not in ("", "root_tf32"):
+            raise ValueError("unknown precision flag %r" % flag)
+        return PRECISIONS[name] | (ROOT_TF32 if flag else 0)
     return int(p)
 
 

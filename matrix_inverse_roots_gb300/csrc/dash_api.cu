@@ -21,6 +21,15 @@ bool valid_dim(int B) { return B >= 128 && B <= 2048 && (B % 128) == 0; }
 
 bool valid_prec(int prec) { return prec >= DASH_FP32_3XTF32 && prec <= DASH_BF16; }
 
+// Splits a root solver's prec argument into the arithmetic and the format of X
+// (DASH_ROOT_TF32: X rounded to TF32).  False for an unknown flag or precision.
+bool root_prec(int& prec, int& xfmt) {
+  if (prec & ~(0xff | DASH_ROOT_TF32)) return false;
+  xfmt = (prec & DASH_ROOT_TF32) ? FMT_TF32 : FMT_F32;
+  prec &= 0xff;
+  return valid_prec(prec);
+}
+
 int prec_fmt(int prec) {
   switch (prec) {
     case DASH_FP32_3XTF32: return FMT_SPLIT;
@@ -310,6 +319,7 @@ int64_t dash_op_matmuls(int op, int param) {
 }
 
 dash_status dash_workspace_size(int op, int64_t N, int B, int prec, int param, size_t* bytes) {
+  prec &= ~DASH_ROOT_TF32;  // moves a rounding step only: same workspace
   if (!bytes || N < 0 || !valid_dim(B) || !valid_prec(prec)) return DASH_ERR_INVALID_ARG;
   size_t s = 0;
   switch (op) {
@@ -419,7 +429,7 @@ dash_status shampoo_accumulate(const void* G, int gdt, int64_t Ng, int B, float 
   const size_t gsz = (gdt == DASH_DT_F32) ? 4 : 2;
   // G G^T and G^T G are symmetric, and so is every factor: for B a multiple of 256
   // only the 256-tiles on or above the diagonal are computed (reading those of the
-  // old F), and the tiles below are then filled with their mirrors' transposes.
+  // old F); the epilogue also stores each one transposed into its mirror below.
   const int SO = (B % 256 == 0) ? 3 : 0;
   for (long long c0 = 0; c0 < Ng; c0 += chunk) {
     const long long nc = (Ng - c0 < chunk) ? Ng - c0 : chunk;
@@ -441,16 +451,16 @@ dash_status shampoo_accumulate(const void* G, int gdt, int64_t Ng, int B, float 
     e.E_fmt = FMT_F32;
     // L_j = beta L_j + (1 - beta) G G^T
     e.out[0] = eout_f32(FL, 1.0f - beta, 0.0f, beta, nullptr);
+    e.out[0].mirror = 1;
     e.E_hi = FL;
     e.pad_valid = valid_rows ? valid_rows + c0 : nullptr;
     DASH_TRY(gemm(gprec, B, nc, g, 0, g, 1, e, st, SO));
-    if (SO) DASH_TRY(launch_mirror_lower(FL, B, nc, st));
     // R_j = beta R_j + (1 - beta) G^T G
     e.out[0] = eout_f32(FR, 1.0f - beta, 0.0f, beta, nullptr);
+    e.out[0].mirror = 1;
     e.E_hi = FR;
     e.pad_valid = valid_cols ? valid_cols + c0 : nullptr;
     DASH_TRY(gemm(gprec, B, nc, g, 1, g, 0, e, st, SO));
-    if (SO) DASH_TRY(launch_mirror_lower(FR, B, nc, st));
   }
   return DASH_OK;
 }
@@ -591,6 +601,8 @@ dash_status spectral_scale(const float* A, float ridge, int64_t N, int B, int mo
 dash_status inv_root_cn(const float* A, float ridge, const float* scale, int64_t N, int B,
                         int iters, int prec, float* X, float* resid_out, void* ws,
                         size_t ws_bytes, void* stream) {
+  int xfmt = FMT_F32;
+  if (!root_prec(prec, xfmt)) return DASH_ERR_INVALID_ARG;
   DASH_TRY(common_root_checks(A, scale, N, B, iters, prec, X, ws));
   if (N == 0) return DASH_OK;
   if (resid_out && !aligned16(resid_out)) return DASH_ERR_INVALID_ARG;
@@ -691,7 +703,7 @@ dash_status inv_root_cn(const float* A, float ridge, const float* scale, int64_t
       a.nout = 1;
       Buf xb;
       xb.hi = Xc;
-      a.out[0] = aout(xb, FMT_F32, -0.25f, 1.25f, m14);
+      a.out[0] = aout(xb, xfmt, -0.25f, 1.25f, m14);
       DASH_TRY(launch_affine(a, st));
       continue;
     }
@@ -714,10 +726,12 @@ dash_status inv_root_cn(const float* A, float ridge, const float* scale, int64_t
         // X_K = X_{K-1} T_{K-1}, scaled by s^{-1/4}, into the caller's fp32 output.
         EpiParams e = epi_none();
         e.nout = 1;
-        e.out[0] = eout_f32(Xc, 1.0f, 0.0f, e1, m14);
+        Buf xb;
+        xb.hi = Xc;
+        e.out[0] = eout(xb, xfmt, 1.0f, 0.0f, e1, m14);
+        e.out[0].mirror = 1;  // halves: the tiles below the diagonal by transposition
         if (shift) with_e(e, xk, fmt);
         DASH_TRY(gemm(prec, B, nc, xk, 0, tk, 0, e, st, SX));
-        if (SX == 2) DASH_TRY(launch_mirror_lower(Xc, B, nc, st));
         break;
       }
       if (k >= 1) {
@@ -769,6 +783,8 @@ dash_status inv_root_cn(const float* A, float ridge, const float* scale, int64_t
 dash_status inv_root_ndb(const float* A, float ridge, const float* scale, int64_t N, int B,
                          int iters, int prec, float* X, float* resid_out, void* ws,
                          size_t ws_bytes, void* stream) {
+  int xfmt = FMT_F32;
+  if (!root_prec(prec, xfmt)) return DASH_ERR_INVALID_ARG;
   DASH_TRY(common_root_checks(A, scale, N, B, iters, prec, X, ws));
   if (N == 0) return DASH_OK;
   if (resid_out && !aligned16(resid_out)) return DASH_ERR_INVALID_ARG;
@@ -892,7 +908,7 @@ dash_status inv_root_ndb(const float* A, float ridge, const float* scale, int64_
           }
           if (K == 1) {
             ey.nout = 1;
-            ey.out[0] = eout(Xout, FMT_F32, -0.5f, 1.5f, eh, m14);
+            ey.out[0] = eout(Xout, xfmt, -0.5f, 1.5f, eh, m14);
             // residual of C' = product itself
             DASH_TRY(gemm(prec, B, nc, pool[iY], 0, pool[iT], 0, ey, st, SI));
           } else {
@@ -909,7 +925,7 @@ dash_status inv_root_ndb(const float* A, float ridge, const float* scale, int64_
           // Z_K = T_{K-1} Z_{K-1}, scaled by s^{-1/4}, into the caller's output.
           EpiParams ez = epi_none();
           ez.nout = 1;
-          ez.out[0] = eout(Xout, FMT_F32, 1.0f, 0.0f, shift ? 1.0f : 0.0f, m14);
+          ez.out[0] = eout(Xout, xfmt, 1.0f, 0.0f, shift ? 1.0f : 0.0f, m14);
           if (shift) with_e(ez, pool[iZ], fmt);  // Z + D Z
           DASH_TRY(gemm(prec, B, nc, pool[iT], 0, pool[iZ], 0, ez, st, SI));
         }
@@ -979,6 +995,8 @@ dash_status dash_cheb_coeffs(int degree, double lo, double hi, double* c) {
 dash_status inv_root_cheb(const float* A, float ridge, const float* scale, int64_t N, int B,
                           int degree, double lo, double hi, int prec, float* X, void* ws,
                           size_t ws_bytes, void* stream) {
+  int xfmt = FMT_F32;
+  if (!root_prec(prec, xfmt)) return DASH_ERR_INVALID_ARG;
   DASH_TRY(common_root_checks(A, scale, N, B, 1, prec, X, ws));
   if (degree < 1 || degree > 64 || !(lo > 0.0) || !(hi > lo) || !std::isfinite(hi))
     return DASH_ERR_INVALID_ARG;
@@ -1019,7 +1037,7 @@ dash_status inv_root_cheb(const float* A, float ridge, const float* scale, int64
       Buf xb;
       xb.hi = Xc;
       a.nout = 1;
-      a.out[0] = aout(xb, FMT_F32, static_cast<float>(c[1] * aS),
+      a.out[0] = aout(xb, xfmt, static_cast<float>(c[1] * aS),
                       static_cast<float>(c[0] + c[1] * gS), m14);
       DASH_TRY(launch_affine(a, st));
       continue;
@@ -1035,9 +1053,9 @@ dash_status inv_root_cheb(const float* A, float ridge, const float* scale, int64
     if (d == 2) {
       EpiParams e = epi_none();
       e.nout = 1;
-      e.out[0] = eout(xb, FMT_F32, 1.0f, static_cast<float>(c[0] - c[2]), 0.0f, m14);
+      e.out[0] = eout(xb, xfmt, 1.0f, static_cast<float>(c[0] - c[2]), 0.0f, m14);
+      e.out[0].mirror = 1;
       DASH_TRY(gemm(prec, B, nc, bS, 0, bb[0], 0, e, st, S));
-      if (S) DASH_TRY(launch_mirror_lower(Xc, B, nc, st));
       continue;
     }
     // b_{d-2} = 2 S b_{d-1} + (c_{d-2} - c_d) I
@@ -1065,14 +1083,14 @@ dash_status inv_root_cheb(const float* A, float ridge, const float* scale, int64
     // P = S b_1 + c_0 I - b_2
     EpiParams e = epi_none();
     e.nout = 1;
-    e.out[0] = eout(xb, FMT_F32, 1.0f, static_cast<float>(c[0]), -1.0f, m14);
+    e.out[0] = eout(xb, xfmt, 1.0f, static_cast<float>(c[0]), -1.0f, m14);
+    e.out[0].mirror = 1;
     e.E_hi = bb[i2].hi;
     e.E_lo = bb[i2].lo;
     e.E_fmt = fmt;
     // All products keep symmetric halves (E is read only where it was written);
-    // the caller's X is completed below the diagonal afterwards.
+    // the caller's X is completed below the diagonal by the mirrored stores.
     DASH_TRY(gemm(prec, B, nc, bS, 0, bb[i1], 0, e, st, S));
-    if (S) DASH_TRY(launch_mirror_lower(Xc, B, nc, st));
   }
   return DASH_OK;
 }
@@ -1264,6 +1282,9 @@ dash_status inv_root_auto(const float* A, float ridge, const float* lam_max, con
 static dash_status apply_impl(const void* G, int gdt, const float* Froot, int64_t Ng, int B,
                               int prec, float* U, float* W, float lr, void* ws, size_t ws_bytes,
                               void* stream) {
+  // DASH_ROOT_TF32 (with DASH_TF32 only): Froot is read as it is.
+  const bool roots_ready = (prec == (DASH_TF32 | DASH_ROOT_TF32));
+  if (roots_ready) prec = DASH_TF32;
   if (Ng < 0 || !valid_dim(B) || !valid_prec(prec) ||
       !(gdt == DASH_DT_F32 || gdt == DASH_DT_BF16 || gdt == DASH_DT_F16))
     return DASH_ERR_INVALID_ARG;
@@ -1289,18 +1310,25 @@ static dash_status apply_impl(const void* G, int gdt, const float* Froot, int64_
     a.nout = 1;
     a.out[0] = aout(bG, fmt, 1.0f, 0.0f);
     DASH_TRY(launch_affine(a, st));
-    a = aff_from(offset_blocks(Froot, c0, B, 4), nullptr, FMT_F32, B, nc);
-    a.nout = 1;
-    a.out[0] = aout(bL, fmt, 1.0f, 0.0f);
-    DASH_TRY(launch_affine(a, st));
-    a = aff_from(offset_blocks(Froot, Ng + c0, B, 4), nullptr, FMT_F32, B, nc);
-    a.nout = 1;
-    a.out[0] = aout(bR, fmt, 1.0f, 0.0f);
-    DASH_TRY(launch_affine(a, st));
+    Buf opL = bL, opR = bR;
+    if (roots_ready) {
+      // TF32-rounded roots are the TF32 operands themselves.
+      opL.hi = const_cast<float*>(offset_blocks(Froot, c0, B, 4));
+      opR.hi = const_cast<float*>(offset_blocks(Froot, Ng + c0, B, 4));
+    } else {
+      a = aff_from(offset_blocks(Froot, c0, B, 4), nullptr, FMT_F32, B, nc);
+      a.nout = 1;
+      a.out[0] = aout(bL, fmt, 1.0f, 0.0f);
+      DASH_TRY(launch_affine(a, st));
+      a = aff_from(offset_blocks(Froot, Ng + c0, B, 4), nullptr, FMT_F32, B, nc);
+      a.nout = 1;
+      a.out[0] = aout(bR, fmt, 1.0f, 0.0f);
+      DASH_TRY(launch_affine(a, st));
+    }
     EpiParams e = epi_none();
     e.nout = 1;
     e.out[0] = eout(bT, fmt, 1.0f, 0.0f);
-    DASH_TRY(gemm(prec, B, nc, bL, 0, bG, 0, e, st));
+    DASH_TRY(gemm(prec, B, nc, opL, 0, bG, 0, e, st));
     e.nout = 0;
     if (W) {
       float* Wc = offset_blocks(W, c0, B, 4);
@@ -1309,7 +1337,7 @@ static dash_status apply_impl(const void* G, int gdt, const float* Froot, int64_
       e.E_fmt = FMT_F32;
     }
     if (U) e.out[e.nout++] = eout_f32(offset_blocks(U, c0, B, 4), 1.0f, 0.0f, 0.0f, nullptr);
-    DASH_TRY(gemm(prec, B, nc, bT, 0, bR, 0, e, st));
+    DASH_TRY(gemm(prec, B, nc, bT, 0, opR, 0, e, st));
   }
   return DASH_OK;
 }

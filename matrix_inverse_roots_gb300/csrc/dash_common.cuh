@@ -109,6 +109,33 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Bounded wait used only while draining after an abort: ignores the abort flag.
+__device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
+  const unsigned long long t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+      atomicExch(&g_dash_error, DEV_ERR_TIMEOUT);
+      return;
+    }
+  }
+}
+
+// Sum over the 32 lanes of x[c] for every c; lane l returns the total of column l.
+__device__ __forceinline__ float butterfly_colsum(float (&x)[32], int lane) {
+#pragma unroll
+  for (int half = 16; half >= 1; half >>= 1) {
+    const bool upper = (lane & half) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      // Keep the half of the columns this lane is responsible for, send the other.
+      const float send = upper ? x[i] : x[i + half];
+      const float keep = upper ? x[i + half] : x[i];
+      x[i] = keep + __shfl_xor_sync(0xffffffffu, send, half);
+    }
+  }
+  return x[0];
+}
+
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {

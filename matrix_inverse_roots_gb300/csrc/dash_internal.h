@@ -1,6 +1,7 @@
 // Host-side interfaces between the C-ABI layer (dash_api.cu) and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -11,12 +12,16 @@ namespace dash {
 // One output of a fused epilogue:
 //   D = mult[blk] * (alpha * C + gamma * I + eps * E)   stored in format fmt.
 // (mult may be null = 1; E is the launch's optional extra matrix.)
+// mirror (FMT_F32 outputs of a sym_out launch): each computed 256-tile above the
+// diagonal is also stored transposed into its mirror below the diagonal, so the
+// output holds the whole symmetric matrix.
 struct EpiOut {
   void* hi;
   void* lo;
   const float* mult;
   float alpha, gamma, eps;
   int fmt;
+  int mirror = 0;
 };
 
 struct EpiParams {
@@ -114,10 +119,6 @@ dash_status launch_sub(const float* a, const float* b, float* out, long long n, 
 // when elems is a multiple of 4.
 dash_status launch_copy_items(const float* src, float* dst, const int32_t* idx, int scatter,
                               long long elems, long long n, cudaStream_t st);
-
-// Fills the 256-tiles below the diagonal of each (dim, dim) fp32 block with the
-// transposes of their mirror tiles (a symmetric result stored as its upper half).
-dash_status launch_mirror_lower(float* X, int dim, long long nblocks, cudaStream_t st);
 
 // One half-precision power product on (nblocks, dim, dim) 16-bit A (bf16 != 0:
 // bfloat16, else fp16); vectors transposed, (nblocks, 32, dim) 16-bit.  When

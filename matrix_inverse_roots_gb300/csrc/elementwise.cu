@@ -409,72 +409,6 @@ dash_status launch_copy_items(const float* src, float* dst, const int32_t* idx, 
   return err == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
 }
 
-// Completes a symmetric result stored as its 256 x 256 tiles on or above the
-// diagonal: every tile below it becomes the transpose of its mirror tile.  One CTA
-// per 64 x 64 sub-tile: 16-byte loads along the source rows into padded shared
-// memory, then 16-byte stores along the destination rows (four values read down a
-// shared-memory column each), so both global sides move whole 256-byte row
-// segments per 16 threads.
-__global__ void __launch_bounds__(256) mirror_lower_kernel(float* X, int dim, int T,
-                                                           long long nblocks) {
-  __shared__ float t[64][65];
-  const int pair = blockIdx.y;  // lower tile (I, J), I > J, row by row
-  int I = 1, rem = pair;
-  while (rem >= I) {
-    rem -= I;
-    ++I;
-  }
-  const int J = rem;
-  const int sa = blockIdx.x >> 2, sb = blockIdx.x & 3;  // 64 x 64 sub-tile of the 256 tile
-  const int tid = threadIdx.x;
-  const int rr = tid >> 4, cc = (tid & 15) * 4;  // 16 rows x 64 columns per pass
-  for (long long k = blockIdx.z; k < nblocks; k += gridDim.z) {
-    float* M = X + k * static_cast<long long>(dim) * dim;
-    // Source: upper tile (J, I), rows J*256 + sb*64.., columns I*256 + sa*64..
-    const long long r0 = static_cast<long long>(J) * 256 + sb * 64;
-    const long long c0 = static_cast<long long>(I) * 256 + sa * 64;
-    float4 v[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      v[i] = *reinterpret_cast<const float4*>(M + (r0 + rr + 16 * i) * dim + c0 + cc);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      t[rr + 16 * i][cc] = v[i].x;
-      t[rr + 16 * i][cc + 1] = v[i].y;
-      t[rr + 16 * i][cc + 2] = v[i].z;
-      t[rr + 16 * i][cc + 3] = v[i].w;
-    }
-    __syncthreads();
-    // Destination: lower tile (I, J), rows I*256 + sa*64.., columns J*256 + sb*64..;
-    // destination (y, x) = source (x, y).
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int y = rr + 16 * i;
-      const float4 w = make_float4(t[cc][y], t[cc + 1][y], t[cc + 2][y], t[cc + 3][y]);
-      *reinterpret_cast<float4*>(M + (c0 + y) * dim + r0 + cc) = w;
-    }
-    __syncthreads();
-  }
-}
-
-dash_status launch_mirror_lower(float* X, int dim, long long nblocks, cudaStream_t st) {
-  const int T = dim / 256;
-  if (nblocks <= 0 || T < 2) return DASH_OK;
-  // About 16 CTAs per SM in all; each walks the blocks with stride gridDim.z.
-  const long long per_block = 16LL * (T * (T - 1) / 2);
-  long long gz = (static_cast<long long>(device_sm_count()) * 16 + per_block - 1) / per_block;
-  if (gz > nblocks) gz = nblocks;
-  if (gz > 65535) gz = 65535;
-  if (gz < 1) gz = 1;
-  dim3 grid(16, static_cast<unsigned>(T * (T - 1) / 2), static_cast<unsigned>(gz));
-  const int rec = trace_begin(st);
-  mirror_lower_kernel<<<grid, 256, 0, st>>>(X, dim, T, nblocks);
-  const cudaError_t err = cudaGetLastError();
-  trace_end(rec, st, DASH_TRACE_ELEMENTWISE, 0.0,
-            8.0 * 65536.0 * (T * (T - 1) / 2) * static_cast<double>(nblocks));
-  return err == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
-}
-
 // One CTA per block (grid-strided): the largest |diagonal entry| and |ridge|, turned
 // into the power of two that brings it into [1/2, 1).
 __global__ void __launch_bounds__(EW_THREADS)

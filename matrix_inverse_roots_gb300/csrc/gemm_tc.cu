@@ -147,17 +147,6 @@ __device__ __forceinline__ void decode_unit(long long u, const KParams& p, uint3
   n0 = (r % p.tiles_n) * bn;
 }
 
-// Bounded wait used only while draining after an abort: ignores the abort flag.
-__device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
-  const unsigned long long t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
-      atomicExch(&g_dash_error, DEV_ERR_TIMEOUT);
-      return;
-    }
-  }
-}
-
 // Per-tile constants of the epilogue, read once per tile: the per-block output
 // multipliers and the valid size of a padded block.  (Read inside the chunk loop
 // they would be reloaded after every store, which may alias them.)
@@ -257,9 +246,13 @@ __device__ __forceinline__ void epi_out16(const EpiParams& e, const TileEpi& te,
 
 // Epilogue for 16 consecutive columns of one row, stored straight to global
 // memory (256-bit stores when the base pointers allow it, 128-bit otherwise).
+// mir: the tile lies above the diagonal of a symmetric output, and element
+// (rg, cg0 + j) is also written to (cg0 + j, rg) for outputs flagged mirror.  The
+// lanes of a warp hold consecutive rows, so each of these stores covers 128
+// contiguous bytes of a row of the mirrored tile.
 __device__ __forceinline__ void epilogue16f(const EpiParams& e, const TileEpi& te, int rg,
                                             int cg0, long long idx, const float (&c)[16],
-                                            float& rsum, bool diag) {
+                                            float& rsum, bool diag, bool mir, int dim) {
   float ev[16];
   epi_pre16(e, rg, cg0, idx, c, rsum, diag, ev);
 #pragma unroll
@@ -275,6 +268,16 @@ __device__ __forceinline__ void epilogue16f(const EpiParams& e, const TileEpi& t
         for (int g = 0; g < 4; ++g) {
           const float q[4] = {d[4 * g], d[4 * g + 1], d[4 * g + 2], d[4 * g + 3]};
           store4(O.fmt, O.hi, O.lo, idx + 4 * g, q);
+        }
+      }
+      if (mir && O.mirror && (O.fmt == FMT_F32 || O.fmt == FMT_TF32)) {
+        // idx = blk dim^2 + rg dim + cg0  ->  blk dim^2 + cg0 dim + rg
+        float* mp = static_cast<float*>(O.hi) + (idx - cg0 + rg) +
+                    static_cast<long long>(cg0 - rg) * dim;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          *mp = (O.fmt == FMT_TF32) ? rna_tf32(d[j]) : d[j];
+          mp += dim;
         }
       }
     }
@@ -331,11 +334,11 @@ __device__ __forceinline__ void flush_round_tma(const KParams& p, uint32_t wst_s
 
 __device__ __forceinline__ void epilogue16(const EpiParams& e, const TileEpi& te, int rg,
                                            int cg0, long long idx, const uint32_t (&r)[16],
-                                           float& rsum, bool diag) {
+                                           float& rsum, bool diag, bool mir, int dim) {
   float c[16];
 #pragma unroll
   for (int j = 0; j < 16; ++j) c[j] = __uint_as_float(r[j]);
-  epilogue16f(e, te, rg, cg0, idx, c, rsum, diag);
+  epilogue16f(e, te, rg, cg0, idx, c, rsum, diag, mir, dim);
 }
 
 // Whether rows [r0, r0 + 32) and columns [c0, c0 + 16) contain a diagonal element.
@@ -343,7 +346,7 @@ __device__ __forceinline__ bool chunk_on_diag(int r0, int c0) {
   return c0 < r0 + 32 && r0 < c0 + 16;
 }
 
-template <int BN, int KT, int MODE>
+template <int BN, int KT, int MODE, bool MIR>
 __global__ void __launch_bounds__(320, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tB,
                    const __grid_constant__ CUtensorMap tAl,
@@ -665,15 +668,19 @@ __global__ void __launch_bounds__(320, 1)
             flush_round_tma(p, wst_s, lane, U, r0w, blk, nh + (c + 2 - R) * 16);
         }
       } else {
+        // A computed tile above the diagonal of a symmetric output: also stored
+        // transposed into its mirror (outputs flagged mirror).
+        // (Compiled only into the MIR instances, so the others keep their registers.)
+        const bool mir = MIR && p.sym_out && (m0 >> 8) != (n0 >> 8);
 #pragma unroll 1
         for (int c = 0; c < HALF / 16; c += 2) {
           tmem_wait_ld(ra);
           tmem_ld16(taddr + (c + 1) * 16, rb);
           const int ca = nh + c * 16, cb = ca + 16;
-          epilogue16(p.epi, te, rg, ca, rbase + ca, ra, rsum, chunk_on_diag(r0w, ca));
+          epilogue16(p.epi, te, rg, ca, rbase + ca, ra, rsum, chunk_on_diag(r0w, ca), mir, p.dim);
           tmem_wait_ld(rb);
           if (c + 2 < HALF / 16) tmem_ld16(taddr + (c + 2) * 16, ra);
-          epilogue16(p.epi, te, rg, cb, rbase + cb, rb, rsum, chunk_on_diag(r0w, cb));
+          epilogue16(p.epi, te, rg, cb, rbase + cb, rb, rsum, chunk_on_diag(r0w, cb), mir, p.dim);
         }
       }
       if (p.epi.resid_acc != nullptr) {
@@ -1020,6 +1027,7 @@ __global__ void __launch_bounds__(ACC_THREADS, 1)
       const int r0w = m0 + q * 32;
       const long long rbase = blk * dd + static_cast<long long>(rg) * p.dim;
       const TileEpi te = tile_epi(p.epi, blk);
+      const bool mir = p.sym_out && (m0 >> 8) != (n0 >> 8);  // see the plain kernel
       float rsum = 0.0f;
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(FINAL_COL);
@@ -1036,7 +1044,7 @@ __global__ void __launch_bounds__(ACC_THREADS, 1)
           if (lane == 0) mbar_arrive(fempty_bar);
         }
         const int ca = n0 + c * 16;
-        epilogue16(p.epi, te, rg, ca, rbase + ca, ra, rsum, chunk_on_diag(r0w, ca));
+        epilogue16(p.epi, te, rg, ca, rbase + ca, ra, rsum, chunk_on_diag(r0w, ca), mir, p.dim);
       }
       if (p.epi.resid_acc != nullptr) {
         if (p.sym_out && (m0 >> 8) != (n0 >> 8)) rsum *= 2.0f;
@@ -1112,19 +1120,19 @@ int device_sm_count() {
 }
 
 // Kernel entry of a configuration (ACC: the accurate 3xTF32 pair variant).
-template <int BN, int KT, int MODE, bool ACC>
+template <int BN, int KT, int MODE, bool ACC, bool MIR>
 struct KernelOf {
   static constexpr int THREADS = ACC ? ACC_THREADS : 320;
   static auto get() {
     if constexpr (ACC)
       return gemm_tc_acc_kernel<KT>;
     else
-      return gemm_tc_kernel<BN, KT, MODE>;
+      return gemm_tc_kernel<BN, KT, MODE, MIR>;
   }
 };
 
 // Largest number of clusters of this kernel that can be resident at once.
-template <int BN, int KT, int MODE, bool ACC = false>
+template <int BN, int KT, int MODE, bool ACC = false, bool MIR = false>
 static int max_active_clusters() {
   static int cache[64] = {0};
   int dev = 0;
@@ -1139,12 +1147,12 @@ static int max_active_clusters() {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(CL * 256, 1, 1);
-    cfg.blockDim = dim3(KernelOf<BN, KT, MODE, ACC>::THREADS, 1, 1);
+    cfg.blockDim = dim3(KernelOf<BN, KT, MODE, ACC, MIR>::THREADS, 1, 1);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, KernelOf<BN, KT, MODE, ACC>::get(), &cfg) !=
+    if (cudaOccupancyMaxActiveClusters(&n, KernelOf<BN, KT, MODE, ACC, MIR>::get(), &cfg) !=
         cudaSuccess)
       n = 0;
     cache[dev] = n > 0 ? n : -1;
@@ -1152,7 +1160,7 @@ static int max_active_clusters() {
   return cache[dev];
 }
 
-template <int BN, int KT, int MODE, bool ACC = false>
+template <int BN, int KT, int MODE, bool ACC = false, bool MIR = false>
 static dash_status run_gemm(const GemmLaunch& g, cudaStream_t st) {
   using C = Cfg<BN, KT, MODE>;
   constexpr int CL = C::CL;
@@ -1239,7 +1247,7 @@ static dash_status run_gemm(const GemmLaunch& g, cudaStream_t st) {
                      one ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
         return DASH_ERR_CUDA;
   }
-  if (cudaFuncSetAttribute(KernelOf<BN, KT, MODE, ACC>::get(),
+  if (cudaFuncSetAttribute(KernelOf<BN, KT, MODE, ACC, MIR>::get(),
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::SMEM_BYTES) != cudaSuccess)
     return DASH_ERR_CUDA;
@@ -1248,7 +1256,7 @@ static dash_status run_gemm(const GemmLaunch& g, cudaStream_t st) {
   // Persistent grid: one CTA per SM, or as many clusters as can be co-resident.
   long long slots = sms / CL;
   if (CL > 1) {
-    const int mac = max_active_clusters<BN, KT, MODE, ACC>();
+    const int mac = max_active_clusters<BN, KT, MODE, ACC, MIR>();
     if (mac <= 0) return DASH_ERR_CUDA;
     if (mac < slots) slots = mac;
   }
@@ -1261,12 +1269,12 @@ static dash_status run_gemm(const GemmLaunch& g, cudaStream_t st) {
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(nclusters * CL), 1, 1);
-  cfg.blockDim = dim3(KernelOf<BN, KT, MODE, ACC>::THREADS, 1, 1);
+  cfg.blockDim = dim3(KernelOf<BN, KT, MODE, ACC, MIR>::THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t err = cudaLaunchKernelEx(&cfg, KernelOf<BN, KT, MODE, ACC>::get(), tA, tB, tAl, tBl, p);
+  cudaError_t err = cudaLaunchKernelEx(&cfg, KernelOf<BN, KT, MODE, ACC, MIR>::get(), tA, tB, tAl, tBl, p);
   if (err == cudaSuccess) err = cudaGetLastError();
   if (rec >= 0) {
     const double bb = static_cast<double>(g.dim) * g.dim * g.nblocks;
@@ -1291,17 +1299,23 @@ dash_status launch_gemm(const GemmLaunch& g, cudaStream_t st) {
   if (g.nblocks <= 0) return DASH_OK;
   if (g.dim % 128 != 0 || g.dim < 128 || g.dim > 2048) return DASH_ERR_INVALID_ARG;
   const bool wide = (g.dim % 256) == 0;
+  // An fp32 output of a symmetric-half launch that is completed below the
+  // diagonal by transposed stores (the pair kernels' mirror instances).
+  bool mir = false;
+  for (int o = 0; o < g.epi.nout; ++o) mir = mir || (g.epi.out[o].mirror && g.sym_out);
 
   switch (g.kind) {
     // B a multiple of 256: CTA pairs on 256 x 256 tiles (cta_group::2); otherwise
     // one CTA per 128 x 128 tile.
     case KIND_F16:
     case KIND_BF16:
+      if (wide && mir) return run_gemm<256, 0, 2, false, true>(g, st);
       return wide ? run_gemm<256, 0, 2>(g, st) : run_gemm<128, 0, 0>(g, st);
     case KIND_F16_SPLITB:
     case KIND_BF16_SPLITB:
       return wide ? run_gemm<256, 3, 2>(g, st) : run_gemm<128, 3, 0>(g, st);
     case KIND_TF32:
+      if (wide && mir) return run_gemm<256, 1, 2, false, true>(g, st);
       return wide ? run_gemm<256, 1, 2>(g, st) : run_gemm<128, 1, 0>(g, st);
     case KIND_TF32X3:
       // fp32-accurate products: partial sums reduced with round-to-nearest.

@@ -81,32 +81,6 @@ struct PowerParams {
   int last;
 };
 
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
-  const unsigned long long t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
-      atomicExch(&g_dash_error, DEV_ERR_TIMEOUT);
-      return;
-    }
-  }
-}
-
-// Sum over the 32 lanes of x[c] for every c; lane l returns the total of column l.
-__device__ __forceinline__ float butterfly_colsum(float (&x)[32], int lane) {
-#pragma unroll
-  for (int half = 16; half >= 1; half >>= 1) {
-    const bool upper = (lane & half) != 0;
-#pragma unroll
-    for (int i = 0; i < half; ++i) {
-      // Keep the half of the columns this lane is responsible for, send the other.
-      const float send = upper ? x[i] : x[i + half];
-      const float keep = upper ? x[i + half] : x[i];
-      x[i] = keep + __shfl_xor_sync(0xffffffffu, send, half);
-    }
-  }
-  return x[0];
-}
-
 __global__ void __launch_bounds__(PT_THREADS, 1)
     power_tc_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tV,
                     const __grid_constant__ PowerParams p) {
@@ -186,7 +160,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
       }
       if (!ok) {
         for (int s = 0; s < PT_STAGES; ++s)
-          if (armed & (1u << s)) drain_wait(full_bar(s), (armed_par >> s) & 1u);
+          if (armed & (1u << s)) mbar_wait_drain(full_bar(s), (armed_par >> s) & 1u);
       }
     }
   } else if (warp == 1) {
@@ -237,7 +211,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
         if (acc == 0) acc_phase ^= 1u;
       }
       mma_commit(fin_bar);
-      drain_wait(fin_bar, 0);
+      mbar_wait_drain(fin_bar, 0);
     }
   } else if (warp < 6) {
     // -------------------------------------------------------------- converters
@@ -521,7 +495,7 @@ __global__ void __launch_bounds__(PH_THREADS, 1)
       }
       if (!ok) {
         for (int s = 0; s < PH_STAGES; ++s)
-          if (armed & (1u << s)) drain_wait(full_bar(s), (armed_par >> s) & 1u);
+          if (armed & (1u << s)) mbar_wait_drain(full_bar(s), (armed_par >> s) & 1u);
       }
     }
   } else if (warp == 1) {
@@ -565,7 +539,7 @@ __global__ void __launch_bounds__(PH_THREADS, 1)
         if (acc == 0) acc_phase ^= 1u;
       }
       mma_commit(fin_bar);
-      drain_wait(fin_bar, 0);
+      mbar_wait_drain(fin_bar, 0);
     }
   } else {
     // -------------------------------------------------------------- epilogue

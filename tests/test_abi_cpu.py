@@ -122,6 +122,30 @@ def test_bad_arguments_rejected_on_host():
     assert lib.dash_gemm(null, null, 0, null, null, 0, 0, 128, 1, null, null) == 0
 
 
+def test_root_tf32_flag_checked():
+    """DASH_ROOT_TF32 is accepted by the root solvers and, with TF32 only, by apply;
+    any other flag bit or combination is an argument error found on the host."""
+    dr = library()
+    lib = dr.load_library()
+    p = ctypes.c_void_p(1 << 20)  # never dereferenced: every call fails before a launch
+    f = dr.ROOT_TF32
+    for prec in (dr.FP16 | f, dr.TF32 | f, dr.FP32_3XTF32 | f):  # too small, not invalid
+        assert lib.inv_root_cn(p, 0.0, p, 4, 1024, 10, prec, p, None, p, 4096, None) == 4
+        assert lib.inv_root_ndb(p, 0.0, p, 4, 1024, 10, prec, p, None, p, 4096, None) == 4
+    assert lib.precondition_apply(p, 1, p, 4, 1024, dr.TF32 | f, p, p, 4096, None) == 4
+    for prec in (dr.FP16 | 0x200, dr.FP16 | f | 0x200, 4 | f):
+        assert lib.inv_root_cn(p, 0.0, p, 4, 1024, 10, prec, p, None, p, 4096, None) == 1
+        assert lib.inv_root_cheb(p, 0.0, p, 4, 1024, 8, ctypes.c_double(0.01),
+                                 ctypes.c_double(1.05), prec, p, p, 4096, None) == 1
+    for prec in (dr.FP16 | f, dr.BF16 | f, dr.FP32_3XTF32 | f, dr.TF32 | 0x200):
+        assert lib.precondition_apply(p, 1, p, 4, 1024, prec, p, p, 4096, None) == 1
+    assert dr._prec("tf32+root_tf32") == dr.TF32 | f
+    with pytest.raises(ValueError):
+        dr._prec("tf32+fast")
+    assert (dr.workspace_size(dr.OP_INV_ROOT_CN, 4, 1024, dr.FP16 | f, 10)
+            == dr.workspace_size(dr.OP_INV_ROOT_CN, 4, 1024, dr.FP16, 10))
+
+
 def test_workspace_too_small_reported():
     dr = library()
     lib = dr.load_library()

@@ -16,7 +16,7 @@ import torch
 
 import oracle
 import synth
-from tests.helpers import library, rel_fro_blocks, require_gpu, to64
+from tests.helpers import library, rel_fro_blocks, require_gpu, rna_tf32, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -47,7 +47,7 @@ HALF_MODES = [("fp16", torch.float16, 2.0 ** -11), ("bf16", torch.bfloat16, 2.0 
 
 
 @pytest.mark.parametrize("name,dt,u", HALF_MODES)
-@pytest.mark.parametrize("b,n", [(128, 8), (1024, 4)])
+@pytest.mark.parametrize("b,n", [(128, 8), (256, 200), (384, 9), (1024, 4), (1024, 40), (2048, 2)])
 def test_power_lambda_half(name, dt, u, b, n):
     """Half-precision power iteration ([pt] Principais Contribuicoes item 4).
 
@@ -354,6 +354,51 @@ def test_apply_parity(prec):
     err = rel_fro_blocks(to64(U), ref)
     gate = {"3xtf32": 1e-5, "tf32": 2e-3, "fp16": 5e-3, "bf16": 2e-2}[prec]
     assert err.max() < gate, err
+
+
+@pytest.mark.parametrize("b", [384, 512])
+def test_root_tf32_output(b):
+    """DASH_ROOT_TF32 rounds X to TF32 on the way out and changes nothing else: X
+    is bit for bit the host's round-to-nearest (ties away) TF32 rounding of the
+    plain X, also in the tiles a symmetric-half run completes by transposed
+    stores (B = 512)."""
+    require_gpu()
+    dr = library()
+    A, V0 = wishart_case(3, b, 3300 + b)
+    s = dr.spectral_scale(A, dr.SCALE_POWER, V0, 10, ridge=1e-3)
+    runs = [(dr.inv_root_cn, dict(iters=6), p) for p in ("fp16", "3xtf32", "tf32")]
+    runs += [(dr.inv_root_ndb, dict(iters=4), "3xtf32"), (dr.inv_root_cn, dict(iters=1), "fp16"),
+             (dr.inv_root_cheb, dict(degree=8, lo=0.02, hi=1.05), "fp16"),
+             (dr.inv_root_cheb, dict(degree=1, lo=0.02, hi=1.05), "tf32")]
+    for fn, kw, prec in runs:
+        X = fn(A, s, prec=prec, ridge=1e-3, **kw)
+        Xt = fn(A, s, prec=prec + "+root_tf32", ridge=1e-3, **kw)
+        torch.cuda.synchronize()
+        assert torch.equal(Xt, rna_tf32(X)), (fn.__name__, kw, prec)
+    assert dr.device_status() == 0
+
+
+def test_apply_reads_tf32_roots_as_they_are():
+    """precondition_apply / _update with TF32 | DASH_ROOT_TF32 skip the roots'
+    conversion pass: on TF32-rounded roots the results are bit for bit those of
+    plain TF32, and they meet the TF32 apply gate against the oracle."""
+    require_gpu()
+    dr = library()
+    ng, b = 3, 512
+    g = torch.Generator(device="cuda").manual_seed(3400)
+    G = torch.randn((ng, b, b), generator=g, device="cuda").to(torch.bfloat16)
+    Fr = rna_tf32(synth.wishart(2 * ng, b, seed=3401, device="cuda") / 2.0)
+    U = dr.precondition_apply(G, Fr, prec="tf32")
+    Ut = dr.precondition_apply(G, Fr, prec="tf32+root_tf32")
+    W0 = torch.randn((ng, b, b), generator=g, device="cuda")
+    W, Wt = W0.clone(), W0.clone()
+    dr.precondition_update(G, Fr, W, 0.01, "tf32")
+    dr.precondition_update(G, Fr, Wt, 0.01, "tf32+root_tf32")
+    torch.cuda.synchronize()
+    assert torch.equal(U, Ut) and torch.equal(W, Wt)
+    ref = oracle.apply_preconditioner(to64(G), to64(Fr))
+    assert rel_fro_blocks(to64(Ut), ref).max() < 2e-3
+    assert dr.device_status() == 0
 
 
 def test_empty_stack_is_noop():
