@@ -30,6 +30,10 @@
 #include "dash_common.cuh"
 #include "dash_internal.h"
 
+#ifndef DASH_STAGED_EPILOGUE
+#define DASH_STAGED_EPILOGUE 1  // build-time: 0 stores every output directly
+#endif
+
 namespace dash {
 
 int gemm_read_clear_error() {
@@ -73,7 +77,7 @@ struct Cfg {
   // fp16/bf16-operand kernels stage 16-bit output tiles through shared memory
   // (4 KB per epilogue warp) so that global stores cover whole rows.
   static constexpr int EPI_WARP_BYTES = 4096;
-  static constexpr int EPI_BYTES = H16 ? 8 * EPI_WARP_BYTES : 0;
+  static constexpr int EPI_BYTES = (H16 && DASH_STAGED_EPILOGUE) ? 8 * EPI_WARP_BYTES : 0;
   static constexpr int STAGES_RAW = (224 * 1024 - EPI_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
   static constexpr int TMEM_COLS = 2 * BN;
@@ -424,6 +428,34 @@ __global__ void __launch_bounds__(320, 1)
       uint32_t phase = 0;
       uint32_t armed = 0, armed_par = 0;
       bool ok = true;
+      // Pair kernels: the boxes of this CTA's part of the tile at (vm0, vn0) of
+      // block vz (A rows, its half of B), per k-block and operand part, handed to
+      // `op` with the map and the coordinates the loads use (the other-major view
+      // for a mirrored k-block).
+      auto for_boxes = [&](int vz, int vm0, int vn0, int kb, int part, auto&& op) {
+        const int k0 = kb * C::BK;
+        const bool amir = p.sym_in && (k0 >> 8) < (vm0 >> 8);
+        const bool bmir = p.sym_in_b && (k0 >> 8) > (vn0 >> 8);
+        const CUtensorMap* ma = amir ? &p.tAm : (part ? &tAl : &tA);
+        const CUtensorMap* mb = bmir ? (part ? &p.tBlm : &p.tBm) : (part ? &tBl : &tB);
+        if (part < C::NPART_A) {
+          if (!(p.a_mn ^ amir)) {
+            op(ma, 0, 0, k0, vm0, vz);
+          } else {
+#pragma unroll
+            for (int i = 0; i < C::A_BOXES_MN; ++i)
+              op(ma, 0, i * C::MN_BOX_BYTES, vm0 + i * C::MN_ATOM, k0, vz);
+          }
+        }
+        const int nb = vn0 + static_cast<int>(crank) * C::B_ROWS;  // this CTA's half of N
+        if (!(p.b_mn ^ bmir)) {
+          op(mb, 1, 0, k0, nb, vz);
+        } else {
+#pragma unroll
+          for (int i = 0; i < C::B_BOXES_MN; ++i)
+            op(mb, 1, i * C::MN_BOX_BYTES, nb + i * C::MN_ATOM, k0, vz);
+        }
+      };
       for (long long u = cid; u < p.total_units && ok; u += ncl) {
         long long blk;
         int m0, n0;
@@ -453,26 +485,10 @@ __global__ void __launch_bounds__(320, 1)
             if (MODE == 2) {
               // Symmetric operands: a k-block left of A's (below B's) diagonal tile is
               // read as the transpose of the stored tile, i.e. in the other major.
-              const bool amir = p.sym_in && (k0 >> 8) < (m0 >> 8);
-              const bool bmir = p.sym_in_b && (k0 >> 8) > (n0 >> 8);
-              if (amir) ma = &p.tAm;
-              if (bmir) mb = part ? &p.tBlm : &p.tBm;
-              if (!loadA) {
-              } else if (!(p.a_mn ^ amir)) {
-                tma_load_3d_pair(sA, ma, fb, k0, m0, z);
-              } else {
-#pragma unroll
-                for (int i = 0; i < C::A_BOXES_MN; ++i)
-                  tma_load_3d_pair(sA + i * C::MN_BOX_BYTES, ma, fb, m0 + i * C::MN_ATOM, k0, z);
-              }
-              const int nb = n0 + static_cast<int>(crank) * C::B_ROWS;  // this CTA's half of N
-              if (!(p.b_mn ^ bmir)) {
-                tma_load_3d_pair(sB, mb, fb, k0, nb, z);
-              } else {
-#pragma unroll
-                for (int i = 0; i < C::B_BOXES_MN; ++i)
-                  tma_load_3d_pair(sB + i * C::MN_BOX_BYTES, mb, fb, nb + i * C::MN_ATOM, k0, z);
-              }
+              for_boxes(z, m0, n0, kb, part, [&](const CUtensorMap* m, int isB, int off, int x,
+                                                 int y, int zz) {
+                tma_load_3d_pair((isB ? sB : sA) + off, m, fb, x, y, zz);
+              });
               continue;
             }
             if (!loadA) {
@@ -1228,9 +1244,6 @@ static dash_status run_gemm(const GemmLaunch& g, cudaStream_t st) {
                                       !b_mn ? mn_swz : CU_TENSOR_MAP_SWIZZLE_128B))
       return DASH_ERR_CUDA;
   }
-#ifndef DASH_STAGED_EPILOGUE
-#define DASH_STAGED_EPILOGUE 1  // build-time: 0 stores every output directly
-#endif
   p.staged = (DASH_STAGED_EPILOGUE && C::EPI_BYTES > 0 && g.epi.nout >= 1 && g.epi.nout <= 2) ? 1 : 0;
   for (int o = 0; o < g.epi.nout && p.staged; ++o) {
     const EpiOut& O = g.epi.out[o];
