@@ -1,4 +1,7 @@
-"""The five workload configurations at full size, against the float64 oracle.
+"""The five benchmark workloads at full size, against the float64 oracle: 8 Wishart
+blocks of 128; 64 blocks of 512 with a 1e-6 spectrum; one Llama-d2048 layer (NDB
+3xTF32); the 24-layer Llama step ((2496, 1024, 1024) factors); Wishart stacks of
+about 16 GB at B = 256 ... 2048.
 
 Each test runs the GPU path on the whole stack, in the launch configuration
 bench.py times, and checks sampled blocks against the oracle run on the exact fp32
@@ -7,7 +10,7 @@ block, against the float64 oracle running the same iteration): 3xTF32 1e-4, TF32
 2e-3, FP16/BF16 Coupled Newton 1e-2; half-precision NDB is reported, not gated.
 Every block's error and gate are printed (run with -s).
 
-Ill-conditioned stacks.  Configs 2-4 have scaled condition numbers of 1e6-1e7
+Ill-conditioned stacks.  The spectrum and Llama stacks have scaled condition numbers of 1e6-1e7
 (a spectrum down to 1e-6, or rank-deficient Gram matrices plus a 1e-6 ridge).  On
 such a block even a plain round-to-nearest float32 run of the same iteration (the
 oracle's own steps in float32: oracle.cn_inv_root / ndb_inv_root with
@@ -74,7 +77,7 @@ def ndb_f32(k, ridge=0.0):
     return lambda a, s: oracle.ndb_inv_root(a, s, k, ridge=ridge, dtype=np.float32)[0]
 
 
-def test_config1_small_all_solvers():
+def test_wishart8_b128_all_solvers():
     """N=8, B=128 Wishart + 1e-6 I: power scale (32 vectors), CN / NDB (10 its), Cheb 16."""
     require_gpu()
     dr = library()
@@ -87,16 +90,16 @@ def test_config1_small_all_solvers():
     idx = np.arange(8)
     for prec in ("3xtf32", "tf32", "fp16", "bf16"):
         X = dr.inv_root_cn(A, lam, 10, prec)
-        check_root("cfg1 CN %s" % prec, X, A, lam, idx,
+        check_root("wishart b128 CN %s" % prec, X, A, lam, idx,
                    lambda a, s: oracle.cn_inv_root(a, s, 10)[0], GATE[prec])
         print("   CN %s vs EVD %.3e" % (prec, rel_fro_blocks(to64(X), evd).max()))
         X = dr.inv_root_ndb(A, lam, 10, prec)
-        check_root("cfg1 NDB %s" % prec, X, A, lam, idx,
+        check_root("wishart b128 NDB %s" % prec, X, A, lam, idx,
                    lambda a, s: oracle.ndb_inv_root(a, s, 10)[0],
                    GATE[prec] if prec in ("3xtf32", "tf32") else None)
         print("   NDB %s vs EVD %.3e" % (prec, rel_fro_blocks(to64(X), evd).max()))
         X = dr.inv_root_cheb(A, lam, 16, 1e-2, 1.05, prec)
-        check_root("cfg1 Cheb16 %s" % prec, X, A, lam, idx,
+        check_root("wishart b128 Cheb16 %s" % prec, X, A, lam, idx,
                    lambda a, s: oracle.cheb_inv_root(a, s, 16, 1e-2, 1.05)[0], GATE[prec])
     assert dr.device_status() == 0
 
@@ -107,7 +110,7 @@ def iterations_to(resid, tol):
     return np.where(hit.any(axis=-1), hit.argmax(axis=-1), resid.shape[-1])
 
 
-def test_config2_frobenius_vs_power_scaling():
+def test_spectrum1e6_b512_power_vs_frobenius_scaling():
     """N=64, B=512, spectrum log-uniform in [1e-6, 1]: iterations to residual 1e-3."""
     require_gpu()
     dr = library()
@@ -124,7 +127,7 @@ def test_config2_frobenius_vs_power_scaling():
         r = to64(r)
         its[("ndb", name)] = iterations_to(r[:, 0], 1e-3) + iterations_to(r[:, 1], 1e-3)
     for k, v in its.items():
-        print("cfg2 %s %s: iterations to 1e-3 mean %.1f min %d max %d" % (k + (v.mean(), v.min(), v.max())))
+        print("spectrum1e6 b512 %s %s: iterations to 1e-3 mean %.1f min %d max %d" % (k + (v.mean(), v.min(), v.max())))
     # Frobenius scaling pushes the spectrum towards zero and needs more iterations.
     assert its[("cn", "power")].mean() < its[("cn", "frobenius")].mean()
     assert its[("ndb", "power")].mean() < its[("ndb", "frobenius")].mean()
@@ -133,11 +136,11 @@ def test_config2_frobenius_vs_power_scaling():
     k = int(its[("cn", "power")].max()) + 1
     lam = scales["power"]
     X = dr.inv_root_cn(A, lam, k, "3xtf32")
-    check_root("cfg2 CN 3xtf32 K=%d" % k, X, A, lam, np.array([0, 63]), cn_ref(k),
+    check_root("spectrum1e6 b512 CN 3xtf32 K=%d" % k, X, A, lam, np.array([0, 63]), cn_ref(k),
                GATE["3xtf32"], f32_fn=cn_f32(k))
     kn = int(max(its[("ndb", "power")].max() // 2 + 2, 8))
     X = dr.inv_root_ndb(A, lam, kn, "3xtf32")
-    check_root("cfg2 NDB 3xtf32 K=%d" % kn, X, A, lam, np.array([0, 63]), ndb_ref(kn),
+    check_root("spectrum1e6 b512 NDB 3xtf32 K=%d" % kn, X, A, lam, np.array([0, 63]), ndb_ref(kn),
                GATE["3xtf32"], f32_fn=ndb_f32(kn))
     assert dr.device_status() == 0
 
@@ -198,7 +201,7 @@ def check_step(dr, tag, G, vr, vc, F, V0, lam, X, U, root, prec, fidx, gidx, pow
     assert dr.device_status() == 0
 
 
-def test_config3_one_llama_layer_ndb_fp32():
+def test_llama_layer_d2048_ndb_3xtf32():
     """One d=2048 layer: 52 bf16 gradient blocks, 104 factors; NDB in fp32 (3xTF32)."""
     require_gpu()
     dr = library()
@@ -215,14 +218,14 @@ def test_config3_one_llama_layer_ndb_fp32():
     assert torch.equal(Fp[512:, 512:], torch.eye(512))
     fidx = np.array([0, 17, ng + 5, ng + padded[0], 2 * ng - 1])
     gidx = np.array([0, padded[0], ng - 1])
-    check_step(dr, "cfg3", G, vr, vc, F, V0, lam, X, U, "ndb", "3xtf32", fidx, gidx)
+    check_step(dr, "llama layer", G, vr, vc, F, V0, lam, X, U, "ndb", "3xtf32", fidx, gidx)
     # The root of a padded factor is close to the identity on the padded part.
     Xp = to64(X[ng + padded[0]])[512:, 512:]
-    print("cfg3 padded root deviation from I: %.3e" % np.abs(Xp - np.eye(512)).max())
+    print("llama layer padded root deviation from I: %.3e" % np.abs(Xp - np.eye(512)).max())
 
 
 @pytest.mark.parametrize("root,prec", [("cn", "fp16"), ("ndb", "3xtf32")])
-def test_config4_24_layer_step(root, prec):
+def test_llama24_step(root, prec):
     """24 layers: (2496, 1024, 1024) factor stack, the full f=1 step; 16 sampled factors.
     Scaling by the half-precision power iteration, as bench.py runs this step."""
     require_gpu()
@@ -234,10 +237,10 @@ def test_config4_24_layer_step(root, prec):
     rng = np.random.default_rng(4)
     fidx = np.sort(rng.choice(2 * ng, 16, replace=False))
     gidx = np.sort(rng.choice(ng, 4, replace=False))
-    check_step(dr, "cfg4", *out, root, prec, fidx, gidx, power="fp16")
+    check_step(dr, "llama24", *out, root, prec, fidx, gidx, power="fp16")
 
 
-def test_config4_tiered_roots():
+def test_llama24_tiered_roots():
     """24 layers, roots with the solver chosen per block ([pt] Significancia e
     Alegacoes, Direcoes Futuras): lambda_min estimates, tier choice and each sampled
     block's root against oracle.lambda_min_estimate / select_tiers / auto_inv_root."""
@@ -262,7 +265,7 @@ def test_config4_tiered_roots():
     want = oracle.select_tiers(oracle.condition_estimate(lam64, lmin64), TIERS)
     assert choice == want.tolist()
     counts = np.bincount(np.array(choice), minlength=len(TIERS))
-    print("cfg4 tiers: %s blocks per tier" % counts.tolist())
+    print("llama24 tiers: %s blocks per tier" % counts.tolist())
     # Sample both tiers: 10 random factors plus the first 3 of each tier.
     rng = np.random.default_rng(44)
     fidx = set(rng.choice(2 * ng, 10, replace=False).tolist())
@@ -274,7 +277,7 @@ def test_config4_tiered_roots():
     want_min = oracle.lambda_min_estimate(to64(F[fidx]), lam64[fidx], to64(V0[fidx]), 10,
                                           ridge=RIDGE)
     dmin = np.abs(lmin64[fidx] - want_min) / lam64[fidx]
-    print("cfg4 lambda_min: max |diff| / lambda_max %.3e" % dmin.max())
+    print("llama24 lambda_min: max |diff| / lambda_max %.3e" % dmin.max())
     assert dmin.max() < 1e-5
     A64 = to64(F[fidx])
     ref = oracle.auto_inv_root(A64, lam64[fidx], np.array(choice)[fidx], TIERS, ridge=RIDGE)
@@ -289,7 +292,7 @@ def test_config4_tiered_roots():
             e32 = rel_fro_blocks(x32, ref[t:t + 1])[0]
             gate = max(gate, F32_FACTOR * e32)
             note = " (float32 run %.3e)" % e32
-        print("cfg4 tiered block %d (tier %d, kappa_hat %.1e): rel err %.3e, gate %.3e%s" % (
+        print("llama24 tiered block %d (tier %d, kappa_hat %.1e): rel err %.3e, gate %.3e%s" % (
             i, choice[i], lam64[i] / max(lmin64[i], 1e-30), err[t], gate, note))
         assert err[t] < gate, (i, err[t], gate)
 
@@ -298,7 +301,7 @@ SWEEP = [(256, 61035, 4), (512, 15259, 3), (1024, 3815, 2), (2048, 954, 1)]
 
 
 @pytest.mark.parametrize("b,n,nsample", SWEEP)
-def test_config5_sweep(b, n, nsample):
+def test_wishart_sweep_b256_2048(b, n, nsample):
     """Wishart stacks of ~16 GB per B: CN fp16/bf16/tf32/3xtf32, NDB tf32/3xtf32, Cheb 8/16/32."""
     require_gpu()
     dr = library()
@@ -330,5 +333,5 @@ def test_config5_sweep(b, n, nsample):
             ref_fn = lambda a, sc, d=d: oracle.cheb_inv_root(a, sc, d, 1e-2, 1.05)[0]
         torch.cuda.synchronize()
         del ws
-        check_root("cfg5 B=%d %s %s" % (b, solver, prec), X, A, s, idx, ref_fn, GATE[prec])
+        check_root("sweep B=%d %s %s" % (b, solver, prec), X, A, s, idx, ref_fn, GATE[prec])
     assert dr.device_status() == 0
