@@ -1294,13 +1294,17 @@ static dash_status apply_impl(const void* G, int gdt, const float* Froot, int64_
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return DASH_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int fmt = prec_fmt(prec);
-  const long long chunk = fit_chunk(prec, B, Ng, APPLY_BUFS, ws_bytes);
+  // TF32-rounded roots need no operand buffers of their own: G and T only.
+  const long long chunk = fit_chunk(prec, B, Ng, roots_ready ? 2 : APPLY_BUFS, ws_bytes);
   if (chunk < 1) return DASH_ERR_WORKSPACE_TOO_SMALL;
   Carver cv(ws, ws_bytes);
   Buf bG = cv.take_buf(prec, B, chunk);
-  Buf bL = cv.take_buf(prec, B, chunk);
-  Buf bR = cv.take_buf(prec, B, chunk);
   Buf bT = cv.take_buf(prec, B, chunk);
+  Buf bL, bR;
+  if (!roots_ready) {
+    bL = cv.take_buf(prec, B, chunk);
+    bR = cv.take_buf(prec, B, chunk);
+  }
   if (!cv.ok) return DASH_ERR_WORKSPACE_TOO_SMALL;
   const int gfmt = (gdt == DASH_DT_F32) ? FMT_F32 : (gdt == DASH_DT_BF16 ? FMT_BF16 : FMT_F16);
   const size_t gsz = (gdt == DASH_DT_F32) ? 4 : 2;
