@@ -296,8 +296,10 @@ dash_status dash_device_status(void) {
   const int a = gemm_read_clear_error();
   const int b = elementwise_read_clear_error();
   const int c = power_tc_read_clear_error();
-  if (a < 0 || b < 0 || c < 0) return DASH_ERR_CUDA;
-  if (a == DASH_ERR_TIMEOUT || b == DASH_ERR_TIMEOUT || c == DASH_ERR_TIMEOUT)
+  const int d = power_cluster_read_clear_error();
+  if (a < 0 || b < 0 || c < 0 || d < 0) return DASH_ERR_CUDA;
+  if (a == DASH_ERR_TIMEOUT || b == DASH_ERR_TIMEOUT || c == DASH_ERR_TIMEOUT ||
+      d == DASH_ERR_TIMEOUT)
     return DASH_ERR_TIMEOUT;
   return DASH_OK;
 }
@@ -489,8 +491,36 @@ dash_status spectral_scale(const float* A, float ridge, int64_t N, int B, int mo
     DASH_TRY(launch_frob_acc(A, ridge, B, N, acc, st));
     return launch_sqrt_scale(acc, lambda_out, N, 1.0f, st);
   }
+  if (half && power_cluster_supported(B)) {
+    // Half precision, B <= 1024: the whole iteration in one launch, each block read
+    // once (clusters of B / 128 CTAs, two blocks per cluster at a time, their 16-bit
+    // copies kept in L2 for all products).  Needs three 16-bit block slots per
+    // cluster; a workspace too small for three takes the one-launch-per-product path
+    // below.
+    const int bf = (mode == DASH_SCALE_POWER_BF16) ? 1 : 0;
+    Carver cv(ws, ws_bytes);
+    float* sigma = static_cast<float*>(cv.take(static_cast<size_t>(N) * 4));
+    uint16_t* Vt = static_cast<uint16_t*>(cv.take(static_cast<size_t>(N) * 32 * B * 2));
+    const size_t slot = power_cluster_slot_bytes(B);
+    const long long nslots = cv.ok ? static_cast<long long>(cv.left / slot) : 0;
+    if (nslots >= 3) {
+      long long ncl = power_cluster_max_clusters(B, bf);
+      if (ncl < 1) return DASH_ERR_CUDA;
+      if (ncl > (N + 1) / 2) ncl = (N + 1) / 2;
+      if (ncl > nslots / 3) ncl = nslots / 3;
+      uint16_t* scratch = static_cast<uint16_t*>(cv.take(static_cast<size_t>(ncl) * 3 * slot));
+      if (!cv.ok) return DASH_ERR_WORKSPACE_TOO_SMALL;
+      // sigma: each block's 16-bit copy holds sigma A with sigma an exact power of
+      // two, so that it keeps fp16's range whatever the factor's magnitude.
+      DASH_TRY(launch_diag_pow2_scale(A, ridge, B, N, sigma, st));
+      DASH_TRY(launch_pad_vectors_t(V0, n_vec, B, N, bf, Vt, st));
+      return launch_power_cluster(A, bf, ridge, sigma, B, N, Vt, n_vec, power_iters, scratch,
+                                  static_cast<int>(ncl), lambda_out, st);
+    }
+  }
   if (half) {
-    // Half precision: a 16-bit copy of each block, vectors transposed (32, B).
+    // Half precision: a 16-bit copy of each block, vectors transposed (32, B), one
+    // launch per product.
     const int bf = (mode == DASH_SCALE_POWER_BF16) ? 1 : 0;
     const size_t per_blk = static_cast<size_t>(B) * B * 2 + 2 * static_cast<size_t>(B) * 32 * 2 +
                            3 * 32 * 4 + 4;

@@ -129,6 +129,24 @@ dash_status launch_power_step_half(const void* Ah, int bf16, float ridge, const 
                                    const float* in_nrm2, uint16_t* Vt_out, float* acc0,
                                    float* acc1, int last, cudaStream_t st);
 
+// The whole half-precision power iteration (iters products and lambda) with each
+// block read from A once: clusters of dim / 128 CTAs, each running two blocks at a
+// time ("lanes"), their 16-bit copies sigma A kept in `scratch` (3 ncl slots of dim^2
+// 16-bit elements) for all products.  Vt (nblocks, 32, dim) 16-bit: the start
+// vectors transposed (launch_pad_vectors_t); lambda[k] = max_c (v.w / v.v) /
+// sigma[k] after the last product.
+bool power_cluster_supported(int dim);  // dim a multiple of 128, at most 1024
+size_t power_cluster_slot_bytes(int dim);
+int power_cluster_max_clusters(int dim, int bf16);  // 0 on error
+dash_status launch_power_cluster(const float* A, int bf16, float ridge, const float* sigma,
+                                 int dim, long long nblocks, const uint16_t* Vt, int nv,
+                                 int iters, uint16_t* scratch, int ncl, float* lambda,
+                                 cudaStream_t st);
+
+// 3-D tensor map over 16-bit elements (inner, outer, nblk), 128B swizzle.
+bool map_3d_u16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t nblk,
+                uint32_t box_inner, uint32_t box_outer);
+
 // V0 (nblocks, dim, nv) fp32 -> Vt (nblocks, 32, dim) 16-bit, rows c >= nv zero.
 dash_status launch_pad_vectors_t(const float* V0, int nv, int dim, long long nblocks, int bf16,
                                  uint16_t* Vt, cudaStream_t st);
@@ -161,6 +179,7 @@ dash_status launch_wait_selftest(int limit_us, cudaStream_t st);
 
 int gemm_read_clear_error();
 int power_tc_read_clear_error();
+int power_cluster_read_clear_error();
 int elementwise_read_clear_error();
 
 int device_sm_count();

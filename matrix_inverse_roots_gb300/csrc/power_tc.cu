@@ -665,6 +665,11 @@ bool map_3d_h16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer
 
 }  // namespace
 
+bool map_3d_u16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t nblk,
+                uint32_t box_inner, uint32_t box_outer) {
+  return map_3d_h16(m, base, inner, outer, nblk, box_inner, box_outer);
+}
+
 dash_status launch_power_step_half(const void* Ah, int bf16, float ridge, const float* blk_scale,
                                    int dim, long long nblocks, const uint16_t* Vt_in, int nv,
                                    const float* in_nrm2, uint16_t* Vt_out, float* acc0,
