@@ -166,7 +166,13 @@ dash_status shampoo_accumulate(const void* G, int gdt, int64_t Ng, int B, float 
  *     max(max_i |A_k[i][i]|, |ridge|) into [1/2, 1); it is exact, so a block whose
  *     16-bit copy would neither overflow nor underflow gets the same lambda as
  *     with sigma_k = 1, and a positive semidefinite block (|A_ij| <= max_i A_ii)
- *     stays within fp16's range whatever its magnitude.
+ *     stays within fp16's range whatever its magnitude.  For B <= 1024, B a
+ *     multiple of 128, the whole iteration is one launch that reads each fp32
+ *     block once and keeps its 16-bit copy in L2 (thread-block clusters; it needs
+ *     three 16-bit block slots of workspace besides the vectors, which
+ *     dash_workspace_size covers); otherwise, or with less workspace, each product
+ *     is one launch over a 16-bit copy of the whole stack.  Both round the same
+ *     values to the same formats; their fp32 sums run in different orders.
  *   mode DASH_SCALE_FROBENIUS: lambda_out[k] = ||A_k + ridge I||_F
  *     (n_vec, power_iters, V0 ignored; may be 0 / NULL).
  *   A (N, B, B) fp32 symmetric blocks; lambda_out (N,) fp32.
