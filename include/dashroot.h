@@ -43,6 +43,13 @@
  *   DASH_ERR_TIMEOUT in a device flag and returns; dash_device_status reads
  *   and clears that flag.  Non-finite numbers are not errors: they propagate
  *   into the outputs and residuals.
+ * Concurrency.  Calls on one stream run in order.  Calls on different streams may
+ *   overlap, with their own workspaces, as long as fewer than 4096 of the
+ *   library's matrix-product launches (at most a few dozen per call) are in
+ *   flight at once: their CTA-pair products hand out tiles from one of 4096
+ *   counters per device, tagged with the launch.  A launch that finds its
+ *   counter taken by a later launch stops and records DASH_ERR_CONFLICT for
+ *   dash_device_status; its outputs are then incomplete.
  */
 #ifndef DASHROOT_H
 #define DASHROOT_H
@@ -60,7 +67,8 @@ typedef enum {
   DASH_ERR_UNSUPPORTED = 2,
   DASH_ERR_CUDA = 3,
   DASH_ERR_WORKSPACE_TOO_SMALL = 4,
-  DASH_ERR_TIMEOUT = 5
+  DASH_ERR_TIMEOUT = 5,
+  DASH_ERR_CONFLICT = 6
 } dash_status;
 
 typedef enum {
@@ -483,8 +491,9 @@ int dash_trace_count(void);
 dash_status dash_trace_read(int i, int* kind, double* flops, double* bytes, float* ms);
 dash_status dash_trace_stop(void);
 
-/* Reads and clears the device-side error flag of the current device
- * (DASH_OK or DASH_ERR_TIMEOUT).  Synchronises the device. */
+/* Reads and clears the device-side error flags of the current device
+ * (DASH_OK, DASH_ERR_TIMEOUT, or DASH_ERR_CONFLICT: see "Concurrency" above).
+ * Synchronises the device. */
 dash_status dash_device_status(void);
 
 /* Failure-detection self-test (no counterpart on the pages): enqueues one

@@ -285,6 +285,8 @@ const char* dash_status_string(int s) {
     case DASH_ERR_CUDA: return "DASH_ERR_CUDA: CUDA runtime or launch error";
     case DASH_ERR_WORKSPACE_TOO_SMALL: return "DASH_ERR_WORKSPACE_TOO_SMALL: workspace too small";
     case DASH_ERR_TIMEOUT: return "DASH_ERR_TIMEOUT: a device-side wait timed out";
+    case DASH_ERR_CONFLICT:
+      return "DASH_ERR_CONFLICT: too many product launches in flight across streams";
     default: return "unknown dash_status";
   }
 }
@@ -301,6 +303,7 @@ dash_status dash_device_status(void) {
   if (a == DASH_ERR_TIMEOUT || b == DASH_ERR_TIMEOUT || c == DASH_ERR_TIMEOUT ||
       d == DASH_ERR_TIMEOUT)
     return DASH_ERR_TIMEOUT;
+  if (a == DASH_ERR_CONFLICT) return DASH_ERR_CONFLICT;
   return DASH_OK;
 }
 

@@ -39,6 +39,7 @@ enum Kind : int {
 
 // Device error codes recorded in g_dash_error (mirrors dash_status values).
 constexpr int DEV_ERR_TIMEOUT = 5;
+constexpr int DEV_ERR_CONFLICT = 6;
 
 // Time limit of any single device-side wait, in nanoseconds of %globaltimer.
 constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;
@@ -98,6 +99,33 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   uint32_t n = 0;
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
+    if ((++n & 255u) == 0) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+        *abort = 1;
+        atomicExch(&g_dash_error, DEV_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// mbar_wait with acquire at cluster scope, for a barrier that other CTAs of the
+// cluster arrive on (their release orders their earlier accesses before ours).
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
+                                                  volatile int* abort) {
+  const unsigned long long t0 = globaltimer_ns();
+  uint32_t n = 0;
+  while (true) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
     if ((++n & 255u) == 0) {
       if (*abort) return false;
       if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {

@@ -19,11 +19,17 @@
 //               in the requested format (fp32, TF32-rounded, hi/lo split, fp16,
 //               bf16).  Chunks away from the diagonal take a branch-free path.
 // Tiles are ordered block-major so that concurrently running CTAs share the
-// operands of a few blocks in L2.
+// operands of a few blocks in L2.  The CTA-pair kernels hand the tiles out in that
+// order at run time (a global counter per launch, drawn by the even CTA's producer
+// and passed to every role of the pair through a small ring in shared memory): with
+// a fixed round-robin split, pairs that run slightly faster drift ahead over a long
+// stack, the tiles in flight spread over more blocks than L2 holds, and operands
+// are read from DRAM more than once.
 // Precisions: kind::f16 (fp16 / bf16 operands), kind::tf32, and 3xTF32, which
 // issues hi*lo, lo*hi and hi*hi products into the same accumulator.
 // Every wait is bounded (see mbar_wait); a time-out sets the device error flag
 // and the CTA drains its in-flight copies and MMAs, frees TMEM and returns.
+#include <atomic>
 #include <cstdio>
 #include <mutex>
 
@@ -35,6 +41,9 @@
 #endif
 #ifndef DASH_KPS
 #define DASH_KPS 2  // k-blocks per pipeline stage of the 16-bit and TF32 pair kernels
+#endif
+#ifndef DASH_DYN_SCHED
+#define DASH_DYN_SCHED 1  // build-time: 0 gives the pair kernels the fixed round-robin order
 #endif
 
 namespace dash {
@@ -99,7 +108,7 @@ struct Cfg {
   // groups K in slabs of 4 rows (512 B), the 16-byte-atom layout in slabs of 8.
   static constexpr uint32_t MN_LAYOUT = H16 ? LAYOUT_SW128 : LAYOUT_SW128_BASE32;
   static constexpr uint32_t MN_SBO = H16 ? 1024 : 512;
-  static constexpr int BAR_BYTES = 256;
+  static constexpr int BAR_BYTES = 512;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + BAR_BYTES + EPI_BYTES;
   static_assert(STAGES >= 2, "need at least two pipeline stages");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -126,8 +135,66 @@ struct KParams {
   int sym_in, sym_in_b, sym_out, sym_any;
   int t256;         // dim / 256
   uint32_t idesc0;  // instruction descriptor without the operand-major bits
+  // Run-time tile order (CTA-pair kernels): this launch's counter, whose high word
+  // is the launch's tag sched_id and low word the units drawn so far; nullptr for
+  // the fixed order cid, cid + ncl, ...
+  unsigned long long* sched;
+  uint32_t sched_id;
   EpiParams epi;
 };
+
+// The next unit of a launch from its tile counter *w: (sched_id << 32) + units
+// handed out; t is the value an atomicAdd(w, 1) returned (issued earlier, so that
+// its latency overlaps other work).  A counter tagged by an earlier launch, or
+// untagged (0), is re-tagged, the caller taking unit 0.  A counter tagged by a later
+// launch means two launches overlap on it: `conflict` is set and -1 returned.
+// Returns -1 too once every unit is handed out.  Each of the launch's `parts`
+// drawers (CTA pairs) stops at its first index past the end, so the one that draws
+// total + parts - 1 is the last to touch the counter: it clears the tag, and a
+// replay of the same launch (a captured graph, same tag) starts afresh.
+__device__ __forceinline__ long long resolve_unit(unsigned long long* w, uint32_t id,
+                                                  long long total, long long parts,
+                                                  unsigned long long t, bool& conflict) {
+  for (int n = 0; n < 1024; ++n) {
+    if (n > 0) t = atomicAdd(w, 1ull);
+    uint32_t hi = static_cast<uint32_t>(t >> 32);
+    if (hi == id) {
+      const long long u = static_cast<long long>(t & 0xffffffffull);
+      if (u < total) return u;
+      if (u == total + parts - 1) {
+        const unsigned long long fin =
+            (static_cast<unsigned long long>(id) << 32) | static_cast<unsigned long long>(total + parts);
+        atomicCAS(w, fin, 0ull);
+      }
+      return -1;
+    }
+    unsigned long long cur = t + 1ull;
+    for (int m = 0; m < 1024; ++m) {
+      hi = static_cast<uint32_t>(cur >> 32);
+      if (hi == id) break;  // re-tagged by another pair: draw again
+      if (hi != 0u && static_cast<int32_t>(hi - id) > 0) {
+        conflict = true;
+        return -1;
+      }
+      const unsigned long long prev =
+          atomicCAS(w, cur, (static_cast<unsigned long long>(id) << 32) | 1ull);
+      if (prev == cur) return total > 0 ? 0 : -1;
+      cur = prev;
+    }
+    if (static_cast<uint32_t>(cur >> 32) != id) break;
+  }
+  conflict = true;
+  return -1;
+}
+
+// 64-bit store into shared memory of a CTA of the cluster (shared::cluster address)
+// that completes 8 bytes of transaction count on that CTA's mbarrier `bar`.
+__device__ __forceinline__ void st_async_b64(uint32_t addr, long long v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b64 [%0], %1, [%2];" ::"r"(
+                   addr),
+               "l"(v), "r"(bar)
+               : "memory");
+}
 
 // A unit is the group of CL tiles one cluster computes together: the CTAs of a
 // cluster take adjacent 128-row M tiles that share one BN-wide N tile.
@@ -383,6 +450,19 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t fin_bar = bar0 + 8u * (2 * C::STAGES + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * (2 * C::STAGES + 5));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * (2 * C::STAGES + 5) + 8);
+  // Ring of the run-time tile order (CTA pairs): RING unit indices, each with a
+  // "full" barrier in both CTAs.  The leader's producer writes slot it % RING one
+  // unit before it loads unit it.  A slot is rewritten RING units later, and by then
+  // every reader has moved on: when the leader's producer starts unit it, the MMA
+  // has started unit it - 1 (the stages hold less than a unit), which needed both
+  // CTAs' loads of it - 1 and the epilogues' release of the accumulator of it - 3.
+  constexpr int RING = 8;
+  constexpr uint32_t ring_off = 8u * (2 * C::STAGES + 5) + 16u;
+  static_assert(ring_off + 16u * RING <= static_cast<uint32_t>(C::BAR_BYTES), "barrier area");
+  volatile long long* ring_u = reinterpret_cast<volatile long long*>(bar_area + ring_off);
+  const uint32_t ring_u0 = bar0 + ring_off;
+  auto rfull_bar = [&](int r) { return bar0 + ring_off + 8u * (RING + r); };
+  const bool dyn = (MODE == 2) && (DASH_DYN_SCHED != 0) && (p.sched != nullptr);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -393,12 +473,39 @@ __global__ void __launch_bounds__(320, 1)
   const long long ncl = gridDim.x / CL;
   constexpr uint16_t kMask = (1u << CL) - 1u;
 
+  // Unit `it` (it = 0, 1, ...) of this pair in the run-time order: the leader's
+  // producer draws it (publish) into both CTAs' rings, one unit before it loads it;
+  // the other roles read it (take).  The peer's copy arrives by st.async, which
+  // completes on the peer's barrier; the peer's producer arms that barrier for the
+  // 8 bytes (arm).  A drawn index of -1 ends the loops.
+  auto publish = [&](long long it, unsigned long long t, long long& u) {
+    const int r = static_cast<int>(it % RING);
+    bool conflict = false;
+    u = resolve_unit(p.sched, p.sched_id, p.total_units, ncl, t, conflict);
+    if (conflict) atomicExch(&g_dash_error, DEV_ERR_CONFLICT);
+    ring_u[r] = u;
+    mbar_arrive(rfull_bar(r));
+    st_async_b64(mapa_shared(ring_u0 + 8u * static_cast<uint32_t>(r), crank | 1u), u,
+                 mapa_shared(rfull_bar(r), crank | 1u));
+  };
+  auto take = [&](long long it, bool arm, long long& u) -> bool {
+    const int r = static_cast<int>(it % RING);
+    if (arm) mbar_arrive_expect_tx(rfull_bar(r), 8u);
+    if (!mbar_wait(rfull_bar(r), static_cast<uint32_t>((it / RING) & 1), abort_flag))
+      return false;
+    u = ring_u[r];
+    return true;
+  };
+
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(full_bar(s), 1);
       // Released by the MMA warp (in a pair, the leader's).
       mbar_init(empty_bar(s), 1);
     }
+    // One arrival per use: the leader's producer (leader), the peer's producer
+    // arming it for the st.async (peer).
+    for (int r = 0; r < RING; ++r) mbar_init(rfull_bar(r), 1);
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
       // Eight epilogue warps per CTA; in MODE 2 the leader's accumulator is freed
@@ -465,7 +572,32 @@ __global__ void __launch_bounds__(320, 1)
             op(mb, 1, i * C::MN_BOX_BYTES, nb + i * C::MN_ATOM, k0, vz);
         }
       };
-      for (long long u = cid; u < p.total_units && ok; u += ncl) {
+      // Leader, run-time order: the unit published for this iteration, and a
+      // counter draw made one unit ahead (resolved and published as the next unit
+      // while this one loads, so that neither producer waits for the counter).
+      long long u_next = -1;
+      unsigned long long pend = 0;
+      if (dyn && leader) {
+        publish(0, atomicAdd(p.sched, 1ull), u_next);
+        if (u_next >= 0) pend = atomicAdd(p.sched, 1ull);
+      }
+      for (long long it = 0; ok; ++it) {
+        long long u = cid + it * ncl;
+        if (dyn) {
+          if (leader) {
+            u = u_next;
+            if (u >= 0) {
+              publish(it + 1, pend, u_next);
+              if (u_next >= 0) pend = atomicAdd(p.sched, 1ull);
+            }
+          } else if (!take(it, true, u)) {
+            ok = false;
+            break;
+          }
+          if (u < 0) break;
+        } else if (u >= p.total_units) {
+          break;
+        }
         long long blk;
         int m0, n0;
         decode_unit<CL>(u, p, crank, blk, m0, n0, BN);
@@ -538,7 +670,17 @@ __global__ void __launch_bounds__(320, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (long long u = cid; u < p.total_units && ok; u += ncl) {
+      for (long long it = 0; ok; ++it) {
+        long long u = cid + it * ncl;
+        if (dyn) {
+          if (!take(it, false, u)) {
+            ok = false;
+            break;
+          }
+          if (u < 0) break;
+        } else if (u >= p.total_units) {
+          break;
+        }
         if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag)) {
           ok = false;
           break;
@@ -651,7 +793,20 @@ __global__ void __launch_bounds__(320, 1)
     const long long dd = static_cast<long long>(p.dim) * p.dim;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (long long u = cid; u < p.total_units; u += ncl) {
+    for (long long it = 0;; ++it) {
+      long long u = cid + it * ncl;
+      if (dyn) {
+        // Lane 0 reads the unit and hands it to the warp.
+        long long uu = 0;
+        int got = 1;
+        if (lane == 0) got = take(it, false, uu) ? 1 : 0;
+        got = __shfl_sync(0xffffffffu, got, 0);
+        uu = __shfl_sync(0xffffffffu, uu, 0);
+        if (!got || uu < 0) break;
+        u = uu;
+      } else if (u >= p.total_units) {
+        break;
+      }
       if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag)) break;
       tc_fence_after();
       long long blk;
@@ -1149,6 +1304,32 @@ int device_sm_count() {
   return cache[dev];
 }
 
+// Tile counters of the run-time order, 4096 per device.  Launch v (v = 1, 2, ...
+// in issue order, over all streams) uses counter v mod 4096 and tags it with v; its
+// last draw clears the tag (resolve_unit), so the counter needs no reset between
+// launches and a captured launch can be replayed.
+constexpr int SCHED_SLOTS = 4096;
+__device__ unsigned long long g_gemm_sched[SCHED_SLOTS];
+
+static bool sched_slot(unsigned long long** w, uint32_t* id) {
+  static std::atomic<unsigned long long*> base[64];
+  static std::atomic<uint32_t> seq{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  unsigned long long* b = base[dev].load();
+  if (b == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_gemm_sched) != cudaSuccess) return false;
+    b = static_cast<unsigned long long*>(ptr);
+    base[dev].store(b);
+  }
+  uint32_t v = seq.fetch_add(1u) + 1u;
+  if (v == 0u) v = seq.fetch_add(1u) + 1u;
+  *w = b + (v % SCHED_SLOTS);
+  *id = v;
+  return true;
+}
+
 // Kernel entry of a configuration (ACC: the accurate 3xTF32 pair variant).
 template <int BN, int KT, int MODE, bool ACC, bool MIR>
 struct KernelOf {
@@ -1258,6 +1439,11 @@ static dash_status run_gemm(const GemmLaunch& g, cudaStream_t st) {
                                       !b_mn ? mn_swz : CU_TENSOR_MAP_SWIZZLE_128B))
       return DASH_ERR_CUDA;
   }
+  p.sched = nullptr;
+  p.sched_id = 0u;
+  if (MODE == 2 && !ACC && DASH_DYN_SCHED && p.total_units < (1LL << 31) &&
+      !sched_slot(&p.sched, &p.sched_id))
+    return DASH_ERR_CUDA;
   p.staged = (DASH_STAGED_EPILOGUE && C::EPI_BYTES > 0 && g.epi.nout >= 1 && g.epi.nout <= 2) ? 1 : 0;
   for (int o = 0; o < g.epi.nout && p.staged; ++o) {
     const EpiOut& O = g.epi.out[o];

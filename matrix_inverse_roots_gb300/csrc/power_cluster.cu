@@ -153,33 +153,6 @@ __device__ __forceinline__ uint16_t ld_shared_u16(uint32_t addr) {
   return v;
 }
 
-// mbar_wait with acquire at cluster scope, for a barrier that other CTAs of the
-// cluster arrive on (their release orders their earlier accesses before ours).
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
-                                                  volatile int* abort) {
-  const unsigned long long t0 = globaltimer_ns();
-  uint32_t n = 0;
-  while (true) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    if (ok) return true;
-    if ((++n & 255u) == 0) {
-      if (*abort) return false;
-      if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
-        *abort = 1;
-        atomicExch(&g_dash_error, DEV_ERR_TIMEOUT);
-        return false;
-      }
-    }
-  }
-}
-
 // Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from this
 // CTA's shared memory to shared memory of a CTA of the cluster (shared::cluster
 // address from mapa_shared), completing on that CTA's mbarrier `bar`.

@@ -34,7 +34,7 @@ def test_library_exports_every_declared_symbol():
 
 def test_status_strings():
     dr = library()
-    for s in range(6):
+    for s in range(7):
         assert dr.status_string(s).startswith("DASH_")
 
 

@@ -68,6 +68,36 @@ def test_gemm_large_k_and_many_blocks():
         assert rel_fro_blocks(to64(C[idx]), ref).max() < 1e-5
 
 
+def test_gemm_graph_replay_and_back_to_back_launches():
+    """The CTA-pair kernels hand out their tiles from a tagged counter at run time.
+    A launch captured in a CUDA graph keeps its tag, so each replay must find the
+    counter cleared by the previous run; launches in between take other counters.
+    Every replay and every eager launch must produce the same bits."""
+    require_gpu()
+    dr = library()
+    n, b = 24, 512
+    g = torch.Generator(device="cuda")
+    g.manual_seed(77)
+    A = torch.randn((n, b, b), generator=g, device="cuda").half()
+    B = torch.randn((n, b, b), generator=g, device="cuda").half()
+    ref = dr.gemm(A, B, prec="fp16")  # eager; also fills the library's caches
+    torch.cuda.synchronize()
+    C = torch.zeros_like(ref)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        dr.gemm(A, B, prec="fp16", C=C)
+    for rep in range(3):
+        C.zero_()
+        graph.replay()
+        for _ in range(rep):
+            dr.gemm(B, A, prec="fp16")  # other launches between the replays
+        torch.cuda.synchronize()
+        assert torch.equal(C, ref), rep
+    for _ in range(3):
+        assert torch.equal(dr.gemm(A, B, prec="fp16"), ref)
+    assert dr.device_status() == 0
+
+
 def sym_operand(b, n, seed):
     """(n, b, b) fp32 symmetric matrices whose 256-tiles below the diagonal are NaN:
     a symmetric-half product must never read them."""

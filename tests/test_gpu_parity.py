@@ -79,6 +79,37 @@ def test_power_lambda_half(name, dt, u, b, n):
     assert dr.device_status() == 0
 
 
+@pytest.mark.parametrize("name,dt,u", HALF_MODES)
+@pytest.mark.parametrize("b,n,iters,nv", [
+    (1024, 1, 1, 1),      # one block: one cluster, lane 1 empty, a single product
+    (128, 1, 2, 32),      # clusters of one CTA
+    (640, 7, 1, 3),       # clusters of 5 CTAs, lanes without a stagger (one product)
+    (896, 3, 4, 16),      # clusters of 7 CTAs, an odd block count
+    (128, 1000, 10, 32),  # many blocks per cluster: every scratch slot reused
+    (256, 700, 3, 32),
+    (1024, 64, 10, 32),   # blocks of 1024, four or five per cluster
+])
+def test_power_lambda_half_shapes(name, dt, u, b, n, iters, nv):
+    """The half-precision iteration over block orders, counts and iteration counts
+    that exercise its launch shapes (cluster size B / 128, blocks per cluster, the
+    lanes' start offset, the slots' reuse).  Gate: 4u against the oracle on the
+    16-bit A, as in test_power_lambda_half."""
+    require_gpu()
+    dr = library()
+    mode = dr.SCALE_POWER_F16 if name == "fp16" else dr.SCALE_POWER_BF16
+    A, V0 = wishart_case(n, b, 2300 + b + n)
+    V = V0[:, :, :nv].contiguous()
+    lam = to64(dr.spectral_scale(A, mode, V, iters, ridge=0.2))
+    sig = half_power_sigma(A, 0.2)
+    Ah = to64((A * sig[:, None, None]).to(dt)) / to64(sig)[:, None, None]
+    ref_h = oracle.power_lambda(Ah, to64(V), iters, ridge=0.2)
+    err_h = np.abs(lam - ref_h) / ref_h
+    print("%s B=%d N=%d iters=%d nv=%d: vs oracle on the 16-bit A %.2e" % (
+        name, b, n, iters, nv, err_h.max()))
+    assert err_h.max() < 4 * u, err_h
+    assert dr.device_status() == 0
+
+
 def half_power_sigma(A, ridge):
     """The exact power of two the half modes scale each block by, as the header
     states it: 2^-e with max(max_i |A_ii|, |ridge|) = f 2^e, f in [1/2, 1)."""
