@@ -19,12 +19,13 @@
 //               in the requested format (fp32, TF32-rounded, hi/lo split, fp16,
 //               bf16).  Chunks away from the diagonal take a branch-free path.
 // Tiles are ordered block-major so that concurrently running CTAs share the
-// operands of a few blocks in L2.  The CTA-pair kernels hand the tiles out in that
-// order at run time (a global counter per launch, drawn by the even CTA's producer
-// and passed to every role of the pair through a small ring in shared memory): with
-// a fixed round-robin split, pairs that run slightly faster drift ahead over a long
-// stack, the tiles in flight spread over more blocks than L2 holds, and operands
-// are read from DRAM more than once.
+// operands of a few blocks in L2.  The mirrored-store pair instances (fp32 results
+// of symmetric products) hand the tiles out in that order at run time (a global
+// counter per launch, drawn by the even CTA's producer and passed to every role of
+// the pair through a small ring in shared memory): with a fixed round-robin split,
+// pairs that run slightly faster drift ahead over a long stack, the tiles in flight
+// spread over more blocks than L2 holds, and operands are read from DRAM more than
+// once.
 // Precisions: kind::f16 (fp16 / bf16 operands), kind::tf32, and 3xTF32, which
 // issues hi*lo, lo*hi and hi*hi products into the same accumulator.
 // Every wait is bounded (see mbar_wait); a time-out sets the device error flag
@@ -176,9 +177,13 @@ __device__ __forceinline__ long long resolve_unit(unsigned long long* w, uint32_
         conflict = true;
         return -1;
       }
-      const unsigned long long prev =
-          atomicCAS(w, cur, (static_cast<unsigned long long>(id) << 32) | 1ull);
-      if (prev == cur) return total > 0 ? 0 : -1;
+      const unsigned long long tagged = (static_cast<unsigned long long>(id) << 32) | 1ull;
+      const unsigned long long prev = atomicCAS(w, cur, tagged);
+      if (prev == cur) {
+        if (total > 0) return 0;
+        if (parts == 1) atomicCAS(w, tagged, 0ull);  // that was the launch's only draw
+        return -1;
+      }
       cur = prev;
     }
     if (static_cast<uint32_t>(cur >> 32) != id) break;
@@ -450,19 +455,27 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t fin_bar = bar0 + 8u * (2 * C::STAGES + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * (2 * C::STAGES + 5));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 8 * (2 * C::STAGES + 5) + 8);
-  // Ring of the run-time tile order (CTA pairs): RING unit indices, each with a
-  // "full" barrier in both CTAs.  The leader's producer writes slot it % RING one
-  // unit before it loads unit it.  A slot is rewritten RING units later, and by then
-  // every reader has moved on: when the leader's producer starts unit it, the MMA
-  // has started unit it - 1 (the stages hold less than a unit), which needed both
-  // CTAs' loads of it - 1 and the epilogues' release of the accumulator of it - 3.
+  // Ring of the run-time tile order (CTA pairs).  Pair c's first unit is c; its
+  // unit of iteration it >= 1 is drawn from the counter (indices past the first
+  // ncl units) and sits in ring slot (it - 1) % RING, with a "full" barrier in
+  // both CTAs.  The leader's producer writes it once it has issued the first stage
+  // of unit it - 1.  A slot is rewritten RING units later, and by then every reader
+  // has moved on: when the leader's producer issues a stage of unit it, the MMA has
+  // consumed unit it - 4 or later (at most 8 stages in flight, at least 2 per unit),
+  // which needed both CTAs' loads of it - 4 and the epilogues' release of the
+  // accumulator of it - 6; each of those roles reads a unit's slot before working on
+  // it, and RING exceeds 6.
   constexpr int RING = 8;
+  static_assert(C::STAGES <= 8, "the ring's slack assumes at most 8 stages");
   constexpr uint32_t ring_off = 8u * (2 * C::STAGES + 5) + 16u;
   static_assert(ring_off + 16u * RING <= static_cast<uint32_t>(C::BAR_BYTES), "barrier area");
   volatile long long* ring_u = reinterpret_cast<volatile long long*>(bar_area + ring_off);
   const uint32_t ring_u0 = bar0 + ring_off;
   auto rfull_bar = [&](int r) { return bar0 + ring_off + 8u * (RING + r); };
-  const bool dyn = (MODE == 2) && (DASH_DYN_SCHED != 0) && (p.sched != nullptr);
+  // Compiled into the mirrored-store instances only (the fp32 products with
+  // direct stores); the other instances keep the fixed order and the code of it.
+  constexpr bool DYN = MIR && (MODE == 2) && (DASH_DYN_SCHED != 0);
+  const bool dyn = DYN && (p.sched != nullptr);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -473,25 +486,26 @@ __global__ void __launch_bounds__(320, 1)
   const long long ncl = gridDim.x / CL;
   constexpr uint16_t kMask = (1u << CL) - 1u;
 
-  // Unit `it` (it = 0, 1, ...) of this pair in the run-time order: the leader's
-  // producer draws it (publish) into both CTAs' rings, one unit before it loads it;
-  // the other roles read it (take).  The peer's copy arrives by st.async, which
-  // completes on the peer's barrier; the peer's producer arms that barrier for the
-  // 8 bytes (arm).  A drawn index of -1 ends the loops.
+  // Unit of iteration it >= 1 of this pair in the run-time order: the leader's
+  // producer draws it (publish, from a counter value drawn one unit earlier) into
+  // both CTAs' rings; the other roles read it (take).  The peer's copy arrives by
+  // st.async, which completes on the peer's barrier; the peer's producer arms that
+  // barrier for the 8 bytes (arm).  A unit of -1 ends the loops.
   auto publish = [&](long long it, unsigned long long t, long long& u) {
-    const int r = static_cast<int>(it % RING);
+    const int r = static_cast<int>((it - 1) % RING);
     bool conflict = false;
-    u = resolve_unit(p.sched, p.sched_id, p.total_units, ncl, t, conflict);
+    const long long d = resolve_unit(p.sched, p.sched_id, p.total_units - ncl, ncl, t, conflict);
     if (conflict) atomicExch(&g_dash_error, DEV_ERR_CONFLICT);
+    u = d < 0 ? -1 : ncl + d;
     ring_u[r] = u;
     mbar_arrive(rfull_bar(r));
     st_async_b64(mapa_shared(ring_u0 + 8u * static_cast<uint32_t>(r), crank | 1u), u,
                  mapa_shared(rfull_bar(r), crank | 1u));
   };
   auto take = [&](long long it, bool arm, long long& u) -> bool {
-    const int r = static_cast<int>(it % RING);
+    const int r = static_cast<int>((it - 1) % RING);
     if (arm) mbar_arrive_expect_tx(rfull_bar(r), 8u);
-    if (!mbar_wait(rfull_bar(r), static_cast<uint32_t>((it / RING) & 1), abort_flag))
+    if (!mbar_wait(rfull_bar(r), static_cast<uint32_t>(((it - 1) / RING) & 1), abort_flag))
       return false;
     u = ring_u[r];
     return true;
@@ -572,30 +586,23 @@ __global__ void __launch_bounds__(320, 1)
             op(mb, 1, i * C::MN_BOX_BYTES, nb + i * C::MN_ATOM, k0, vz);
         }
       };
-      // Leader, run-time order: the unit published for this iteration, and a
-      // counter draw made one unit ahead (resolved and published as the next unit
-      // while this one loads, so that neither producer waits for the counter).
+      // Leader, run-time order: the unit of the next iteration, published once this
+      // iteration's first stage is issued, from a counter draw made one unit earlier,
+      // so that neither producer waits for the counter.
       long long u_next = -1;
       unsigned long long pend = 0;
-      if (dyn && leader) {
-        publish(0, atomicAdd(p.sched, 1ull), u_next);
-        if (u_next >= 0) pend = atomicAdd(p.sched, 1ull);
-      }
+      if (dyn && leader) pend = atomicAdd(p.sched, 1ull);
       for (long long it = 0; ok; ++it) {
         long long u = cid + it * ncl;
-        if (dyn) {
+        if (dyn && it > 0) {
           if (leader) {
             u = u_next;
-            if (u >= 0) {
-              publish(it + 1, pend, u_next);
-              if (u_next >= 0) pend = atomicAdd(p.sched, 1ull);
-            }
           } else if (!take(it, true, u)) {
             ok = false;
             break;
           }
           if (u < 0) break;
-        } else if (u >= p.total_units) {
+        } else if (!dyn && u >= p.total_units) {
           break;
         }
         long long blk;
@@ -654,6 +661,12 @@ __global__ void __launch_bounds__(320, 1)
             stage = 0;
             phase ^= 1u;
           }
+          if (dyn && leader && kb0 == 0) {
+            // The next iteration's unit, once this unit's first stage is on its way:
+            // the peer's producer and the other roles find it well before they need it.
+            publish(it + 1, pend, u_next);
+            if (u_next >= 0) pend = atomicAdd(p.sched, 1ull);
+          }
         }
       }
       if (!ok) {
@@ -672,13 +685,13 @@ __global__ void __launch_bounds__(320, 1)
       bool ok = true;
       for (long long it = 0; ok; ++it) {
         long long u = cid + it * ncl;
-        if (dyn) {
+        if (dyn && it > 0) {
           if (!take(it, false, u)) {
             ok = false;
             break;
           }
           if (u < 0) break;
-        } else if (u >= p.total_units) {
+        } else if (!dyn && u >= p.total_units) {
           break;
         }
         if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag)) {
@@ -795,7 +808,7 @@ __global__ void __launch_bounds__(320, 1)
     uint32_t acc_phase = 0;
     for (long long it = 0;; ++it) {
       long long u = cid + it * ncl;
-      if (dyn) {
+      if (dyn && it > 0) {
         // Lane 0 reads the unit and hands it to the warp.
         long long uu = 0;
         int got = 1;
@@ -804,7 +817,7 @@ __global__ void __launch_bounds__(320, 1)
         uu = __shfl_sync(0xffffffffu, uu, 0);
         if (!got || uu < 0) break;
         u = uu;
-      } else if (u >= p.total_units) {
+      } else if (!dyn && u >= p.total_units) {
         break;
       }
       if (!mbar_wait(tfull_bar(acc), acc_phase, abort_flag)) break;
@@ -1439,11 +1452,6 @@ static dash_status run_gemm(const GemmLaunch& g, cudaStream_t st) {
                                       !b_mn ? mn_swz : CU_TENSOR_MAP_SWIZZLE_128B))
       return DASH_ERR_CUDA;
   }
-  p.sched = nullptr;
-  p.sched_id = 0u;
-  if (MODE == 2 && !ACC && DASH_DYN_SCHED && p.total_units < (1LL << 31) &&
-      !sched_slot(&p.sched, &p.sched_id))
-    return DASH_ERR_CUDA;
   p.staged = (DASH_STAGED_EPILOGUE && C::EPI_BYTES > 0 && g.epi.nout >= 1 && g.epi.nout <= 2) ? 1 : 0;
   for (int o = 0; o < g.epi.nout && p.staged; ++o) {
     const EpiOut& O = g.epi.out[o];
@@ -1460,6 +1468,16 @@ static dash_status run_gemm(const GemmLaunch& g, cudaStream_t st) {
                      one ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
         return DASH_ERR_CUDA;
   }
+  // Run-time tile order for the mirrored-store pair instances (the accumulate and
+  // the roots' fp32 results).  Timed launch by launch in the benchmark step (CUDA
+  // events, interleaved rounds on several boxes), those launches were 8-16% faster
+  // with it every time; the other products gained nothing consistent, and carrying
+  // the ring's code slowed them, so they keep the fixed order.
+  p.sched = nullptr;
+  p.sched_id = 0u;
+  if (MODE == 2 && MIR && !ACC && DASH_DYN_SCHED && !p.staged && p.total_units < (1LL << 31) &&
+      !sched_slot(&p.sched, &p.sched_id))
+    return DASH_ERR_CUDA;
   if (cudaFuncSetAttribute(KernelOf<BN, KT, MODE, ACC, MIR>::get(),
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::SMEM_BYTES) != cudaSuccess)

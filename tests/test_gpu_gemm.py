@@ -68,33 +68,36 @@ def test_gemm_large_k_and_many_blocks():
         assert rel_fro_blocks(to64(C[idx]), ref).max() < 1e-5
 
 
-def test_gemm_graph_replay_and_back_to_back_launches():
-    """The CTA-pair kernels hand out their tiles from a tagged counter at run time.
-    A launch captured in a CUDA graph keeps its tag, so each replay must find the
-    counter cleared by the previous run; launches in between take other counters.
-    Every replay and every eager launch must produce the same bits."""
+def test_graph_replay_and_back_to_back_launches():
+    """The mirrored-store pair products (the accumulate, the roots' fp32 results)
+    hand out their tiles from a tagged counter at run time.  A launch captured in a
+    CUDA graph keeps its tag, so each replay must find the counter cleared by the
+    previous run; launches in between take other counters.  Replays of a captured
+    accumulate must give the bits of the same accumulates run eagerly."""
     require_gpu()
     dr = library()
-    n, b = 24, 512
+    ng, b = 64, 512  # 192 upper pair tiles per launch: more than the pairs, so most come from the counter
     g = torch.Generator(device="cuda")
     g.manual_seed(77)
-    A = torch.randn((n, b, b), generator=g, device="cuda").half()
-    B = torch.randn((n, b, b), generator=g, device="cuda").half()
-    ref = dr.gemm(A, B, prec="fp16")  # eager; also fills the library's caches
+    G = (0.1 * torch.randn((ng, b, b), generator=g, device="cuda")).to(torch.bfloat16)
+    F0 = torch.zeros((2 * ng, b, b), device="cuda")
+    ref = F0.clone()
+    refs = []
+    for _ in range(3):
+        dr.shampoo_accumulate(G, ref, 0.9)  # eager; also fills the library's caches
+        refs.append(ref.clone())
     torch.cuda.synchronize()
-    C = torch.zeros_like(ref)
+    F = F0.clone()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
-        dr.gemm(A, B, prec="fp16", C=C)
+        dr.shampoo_accumulate(G, F, 0.9)
+    F.copy_(F0)
     for rep in range(3):
-        C.zero_()
         graph.replay()
         for _ in range(rep):
-            dr.gemm(B, A, prec="fp16")  # other launches between the replays
+            dr.shampoo_accumulate(G, F0.clone(), 0.9)  # other launches between replays
         torch.cuda.synchronize()
-        assert torch.equal(C, ref), rep
-    for _ in range(3):
-        assert torch.equal(dr.gemm(A, B, prec="fp16"), ref)
+        assert torch.equal(F, refs[rep]), rep
     assert dr.device_status() == 0
 
 
