@@ -46,10 +46,12 @@
  * Concurrency.  Calls on one stream run in order.  Calls on different streams may
  *   overlap, with their own workspaces, as long as fewer than 4096 of the
  *   library's matrix-product launches (at most a few dozen per call) are in
- *   flight at once: their CTA-pair products hand out tiles from one of 4096
- *   counters per device, tagged with the launch.  A launch that finds its
- *   counter taken by a later launch stops and records DASH_ERR_CONFLICT for
- *   dash_device_status; its outputs are then incomplete.
+ *   flight at once: the products that write symmetric fp32 results (the
+ *   accumulate, the roots) hand out their tiles from one of 4096 counters per
+ *   device, tagged with the launch.  A launch that finds its counter taken by a
+ *   later launch stops and records DASH_ERR_CONFLICT for dash_device_status; its
+ *   outputs are then incomplete.  Launches captured in a CUDA graph may be
+ *   replayed.
  */
 #ifndef DASHROOT_H
 #define DASHROOT_H
