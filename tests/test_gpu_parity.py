@@ -225,11 +225,12 @@ def test_ndb_parity(prec, iters):
     assert dr.device_status() == 0
     Xr, rr, _ = oracle.ndb_inv_root(to64(A), to64(lam), iters)
     err = rel_fro_blocks(to64(X), Xr)
-    print("NDB %s iters=%d max rel err %.3e" % (prec, iters, err.max()))
+    rerr = np.max(np.abs(to64(r) - rr)) / max(1.0, rr.max())
+    print("NDB %s iters=%d max rel err %.3e, residual err %.3e" % (prec, iters, err.max(), rerr))
     if prec in ("3xtf32", "tf32"):
+        # Roots and residuals are held to the precision's stated root tolerance.
         assert err.max() < GATE[prec], err
-        tol = 1e-4 if prec == "3xtf32" else 5e-2
-        assert np.max(np.abs(to64(r) - rr)) < tol * max(1.0, rr.max())
+        assert rerr < GATE[prec], rerr
     else:
         pass  # half-precision NDB: reported above, not gated
 
