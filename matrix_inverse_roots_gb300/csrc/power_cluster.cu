@@ -37,6 +37,8 @@
 // Every wait is bounded; every branch after a wait is taken by all threads of a
 // role (a barrier with an AND vote); a time-out sets the device flag, the CTA
 // drains its copies and MMAs, frees TMEM and returns.
+#include <atomic>
+
 #include "dash_common.cuh"
 #include "dash_internal.h"
 
@@ -144,14 +146,6 @@ __device__ __forceinline__ uint32_t vt_off(int c, int g) {
          (bc ^ (static_cast<uint32_t>(c & 7) << 4));
 }
 
-__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
-  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
-}
-__device__ __forceinline__ uint16_t ld_shared_u16(uint32_t addr) {
-  uint16_t v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
-  return v;
-}
 
 // Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from this
 // CTA's shared memory to shared memory of a CTA of the cluster (shared::cluster
@@ -629,23 +623,22 @@ __global__ void __launch_bounds__(PC_THREADS, 1)
   }
 }
 
-struct Occupancy {
-  int clusters = 0;
-};
-
 }  // namespace
 
 bool power_cluster_supported(int dim) { return dim % PC_BM == 0 && dim / PC_BM <= PC_MAX_CL; }
 
 size_t power_cluster_slot_bytes(int dim) { return static_cast<size_t>(dim) * dim * 2; }
 
-// Clusters of dim / 128 CTAs of this kernel that fit on the device at once (0 on
-// error).
+// Clusters of dim / 128 CTAs of this kernel that fit on the current device at once
+// (0 on error), cached per device, cluster size and format.
 int power_cluster_max_clusters(int dim, int bf16) {
-  static Occupancy cache[2 * (PC_MAX_CL + 1)];
+  static std::atomic<int> cache[64][2 * (PC_MAX_CL + 1)];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   const int C = dim / PC_BM;
-  Occupancy& oc = cache[2 * C + (bf16 ? 1 : 0)];
-  if (oc.clusters > 0) return oc.clusters;
+  std::atomic<int>& oc = cache[dev][2 * C + (bf16 ? 1 : 0)];
+  const int known = oc.load();
+  if (known > 0) return known;
   auto kern = bf16 ? power_cluster_kernel<true> : power_cluster_kernel<false>;
   const size_t smem = pc_smem_bytes(dim);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -664,7 +657,7 @@ int power_cluster_max_clusters(int dim, int bf16) {
   cfg.numAttrs = 1;
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) return 0;
-  oc.clusters = n;
+  oc.store(n);
   return n;
 }
 
