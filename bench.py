@@ -685,9 +685,10 @@ def run_sweep(args):
 def run_case(args):
     """A small untimed case for ncu captures: Wishart blocks, a scale, one root call;
     --case accumulate: one accumulate of n bf16 Llama-like gradient blocks into 2n
-    factors (two GEMM launches, then two mirror launches when B is a multiple of
-    256); --case apply: one preconditioned update of n blocks (three conversions,
-    two GEMMs); --case pack: n stacked 2048 x 5632 bf16 gradients into blocks;
+    factors (two GEMM launches, with mirrored stores when B is a multiple of 256);
+    --case apply: one preconditioned update of n blocks (the gradient conversion, two
+    GEMMs); --case pack: n stacked 2048 x 5632 bf16 gradients into blocks and back;
+    --case auto: per-block solver choice on n blocks alternating between two tiers;
     --case step: two steps of the benchmark workload (profile the second)."""
     import torch
 
@@ -715,9 +716,22 @@ def run_case(args):
             dr.precondition_apply(G, R, args.case_prec)
         else:
             # n Llama MLP weights' gradients stacked (2048 n x 5632, row-major) into
-            # their blocks (184 MB at n = 8: more than L2).
+            # their blocks (184 MB at n = 8: more than L2), and back.
             M = (0.1 * torch.randn((2048 * n, 5632), generator=g, device="cuda")).to(torch.bfloat16)
-            dr.pack_blocks(M, b)
+            P, _, _ = dr.pack_blocks(M, b)
+            dr.unpack_blocks(P, M.shape[0], M.shape[1], out=torch.empty_like(M))
+        torch.cuda.synchronize()
+        print("case ok, device status", dr.device_status())
+        return
+    if args.case == "auto":
+        # Per-block solver choice on blocks alternating between the two default tiers
+        # (kappa 2 and 1e4): lambda_max and lambda_min in the fp32-accurate mode, then
+        # each tier gathered, solved and scattered back.
+        A = synth.two_cluster_blocks(n, b, 5).cuda()
+        V0 = synth.start_vectors(n, b, 32, seed=6, device="cuda")
+        lam = dr.spectral_scale(A, dr.SCALE_POWER, V0, POWER_ITERS)
+        lmin = dr.spectral_lambda_min(A, lam, dr.SCALE_POWER, V0, POWER_ITERS)
+        dr.inv_root_auto(A, lam, lmin, dr.DEFAULT_TIERS)
         torch.cuda.synchronize()
         print("case ok, device status", dr.device_status())
         return
@@ -806,7 +820,8 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="inverse-root throughput sweep over block sizes and precisions")
     ap.add_argument("--sweep-b", type=int, nargs="*", default=None)
-    ap.add_argument("--case", choices=["cn", "ndb", "cheb", "accumulate", "apply", "pack", "step"],
+    ap.add_argument("--case", choices=["cn", "ndb", "cheb", "accumulate", "apply", "pack", "step",
+                                       "auto"],
                     default=None,
                     help="run one small untimed case (for profiler captures)")
     ap.add_argument("--case-n", type=int, default=64)

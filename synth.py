@@ -21,6 +21,11 @@ oracle the exact fp32 bits the GPU consumed):
   column block of each MLP weight zero-padded; entries i.i.d. N(0, var).
   Blocks are ordered layer, weight, row block, column block.
 * ``start_vectors``: power-iteration start vectors, i.i.d. N(0, 1).
+* ``two_cluster_blocks``: A_k = Q_k diag(lam_k) Q_k^T (Q_k as in
+  ``prescribed_spectrum``); even k: lam uniform on [0.5, 1] (kappa 2); odd k: half
+  of lam at 1, half at 1e-4 (kappa 1e4, with a gap that the shifted power
+  iteration resolves quickly).  Consecutive blocks thus fall into different
+  solver tiers.
 """
 
 import torch
@@ -74,6 +79,28 @@ def prescribed_spectrum(n, b, seed, lo=1e-6, hi=1.0, device="cpu"):
     A = (Q * lam[None, None, :]) @ Q.transpose(1, 2)
     A = 0.5 * (A + A.transpose(1, 2))
     return A.to(torch.float32).to(device), Q, lam
+
+
+def two_cluster_blocks(n, b, seed, device="cpu"):
+    """(n, b, b) fp32 blocks alternating between kappa 2 and kappa 1e4 (see above);
+    drawn and formed in float64 on `device`."""
+    g = _gen(seed, device)
+    out = torch.empty((n, b, b), dtype=torch.float32, device=device)
+    for k in range(n):
+        Z = torch.randn((b, b), generator=g, dtype=torch.float64, device=device)
+        Q, R = torch.linalg.qr(Z)
+        sgn = torch.sign(torch.diagonal(R))
+        sgn[sgn == 0] = 1.0
+        Q = Q * sgn[None, :]
+        if k % 2 == 0:
+            lam = 0.5 + 0.5 * torch.rand(b, generator=g, dtype=torch.float64, device=device)
+        else:
+            lam = torch.cat([torch.ones(b // 2, dtype=torch.float64, device=device),
+                             torch.full((b - b // 2,), 1e-4, dtype=torch.float64,
+                                        device=device)])
+        A = (Q * lam[None, :]) @ Q.T
+        out[k] = (0.5 * (A + A.T)).to(torch.float32)
+    return out
 
 
 def llama_weight_shapes(layers=1):

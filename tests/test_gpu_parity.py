@@ -540,3 +540,39 @@ def test_symmetric_half_iterates(prec, b):
         err = rel_fro_blocks(to64(X), ref)
         assert err.max() < GATE[prec], ("cheb", d, err)
         assert np.all(np.isfinite(to64(X)))
+
+
+def test_auto_roots_with_interleaved_tiers():
+    """Per-block solver choice ([pt] Significancia e Alegacoes, Direcoes Futuras) on a
+    stack whose blocks alternate between the two default tiers, so that each tier is
+    gathered into a sub-stack, solved and scattered back.  The choice must be the
+    oracle's rule on the GPU's estimates, and every root must meet its tier's gate
+    against the oracle (the 3xTF32 tier at most twice a plain float32 run's error
+    where that exceeds 1e-4)."""
+    require_gpu()
+    dr = library()
+    n, b = 8, 256
+    A = synth.two_cluster_blocks(n, b, 4242, device="cuda")
+    V0 = synth.start_vectors(n, b, 32, seed=4243, device="cuda")
+    lam = dr.spectral_scale(A, dr.SCALE_POWER, V0, 10)
+    lmin = dr.spectral_lambda_min(A, lam, dr.SCALE_POWER, V0, 10)
+    tiers = dr.DEFAULT_TIERS
+    X, choice = dr.inv_root_auto(A, lam, lmin, tiers)
+    torch.cuda.synchronize()
+    assert dr.device_status() == 0
+    lam64, lmin64 = to64(lam), to64(lmin)
+    want = oracle.select_tiers(oracle.condition_estimate(lam64, lmin64), tiers)
+    assert choice == want.tolist()
+    assert choice == [k % 2 for k in range(n)], choice
+    A64 = to64(A)
+    ref = oracle.auto_inv_root(A64, lam64, np.array(choice), tiers)
+    err = rel_fro_blocks(to64(X), ref)
+    for k in range(n):
+        tier = tiers[choice[k]]
+        gate = tier["gate"]
+        if tier["prec"] == "3xtf32":
+            x32 = oracle.cn_inv_root(A64[k:k + 1], lam64[k:k + 1], tier["iters"],
+                                     dtype=np.float32)[0]
+            gate = max(gate, 2.0 * rel_fro_blocks(x32, ref[k:k + 1])[0])
+        print("auto block %d tier %d: rel err %.3e, gate %.3e" % (k, choice[k], err[k], gate))
+        assert err[k] < gate, (k, err[k], gate)
