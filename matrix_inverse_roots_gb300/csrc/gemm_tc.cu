@@ -43,6 +43,9 @@
 #ifndef DASH_KPS
 #define DASH_KPS 2  // k-blocks per pipeline stage of the 16-bit and TF32 pair kernels
 #endif
+#ifndef DASH_ACC_KPS
+#define DASH_ACC_KPS 1  // k-blocks per pipeline stage of the accurate 3xTF32 pair kernel
+#endif
 #ifndef DASH_DYN_SCHED
 #define DASH_DYN_SCHED 1  // build-time: 0 gives the pair kernels the fixed round-robin order
 #endif
@@ -88,7 +91,8 @@ struct Cfg {
   // trip (three 64 KB stages instead of six of 32 KB): the MMA warp then waits,
   // issues and commits once per eight MMAs instead of four.  Measured on CN FP16
   // (1024^2 blocks): 13% fewer cycles per tile, 3% less wall time under the power cap.
-  static constexpr int KPS = (MODE == 2 && (KT == 0 || KT == 1)) ? DASH_KPS : 1;
+  static constexpr int KPS =
+      (MODE == 2 && (KT == 0 || KT == 1)) ? DASH_KPS : ((MODE == 2 && KT == 2) ? DASH_ACC_KPS : 1);
   static constexpr int SUB_BYTES = A_BYTES * NPART_A + B_BYTES * NPART_B;  // one k-block
   static constexpr int STAGE_BYTES = KPS * SUB_BYTES;
   // Bytes the barrier owner waits for per stage (both CTAs' loads for a pair).
@@ -1025,7 +1029,7 @@ __global__ void __launch_bounds__(ACC_THREADS, 1)
         int m0, n0;
         decode_unit<CL>(u, p, crank, blk, m0, n0, BN);
         const int z = static_cast<int>(blk);
-        for (int kb = 0; kb < p.nkb; ++kb) {
+        for (int kb0 = 0; kb0 < p.nkb; kb0 += C::KPS) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
             ok = false;
             break;
@@ -1037,11 +1041,14 @@ __global__ void __launch_bounds__(ACC_THREADS, 1)
             armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
           }
           fb = leader ? fb : mapa_shared(fb, 0);
+          for (int j = 0; j < C::KPS; ++j) {
+          const int kb = kb0 + j;
           const int k0 = kb * C::BK;
           const bool amir = p.sym_in && (k0 >> 8) < (m0 >> 8);
           const bool bmir = p.sym_in_b && (k0 >> 8) > (n0 >> 8);
           for (int part = 0; part < C::NPART; ++part) {
-            const uint32_t sA = sbase + stage * C::STAGE_BYTES + part * (C::A_BYTES + C::B_BYTES);
+            const uint32_t sA = sbase + stage * C::STAGE_BYTES + j * C::SUB_BYTES +
+                                part * (C::A_BYTES + C::B_BYTES);
             const uint32_t sB = sA + C::A_BYTES;
             const CUtensorMap* ma = amir ? (part ? &p.tAlm : &p.tAm) : (part ? &tAl : &tA);
             const CUtensorMap* mb = bmir ? (part ? &p.tBlm : &p.tBm) : (part ? &tBl : &tB);
@@ -1061,6 +1068,7 @@ __global__ void __launch_bounds__(ACC_THREADS, 1)
                 tma_load_3d_pair(sB + i * C::MN_BOX_BYTES, mb, fb, nb + i * C::MN_ATOM, k0, z);
             }
           }
+          }  // k-blocks of the stage
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -1085,13 +1093,15 @@ __global__ void __launch_bounds__(ACC_THREADS, 1)
         long long ublk;
         int um0 = 0, un0 = 0;
         if (p.sym_any) decode_unit<CL>(u, p, 0u, ublk, um0, un0, BN);
-        for (int kb = 0; kb < p.nkb && ok; ++kb) {
+        for (int kb0 = 0; kb0 < p.nkb && ok; kb0 += C::KPS) {
           if (!mbar_wait(full_bar(stage), phase, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sA = sbase + stage * C::STAGE_BYTES;
+          for (int j = 0; j < C::KPS && ok; ++j) {
+          const int kb = kb0 + j;
+          const uint32_t sA = sbase + stage * C::STAGE_BYTES + j * C::SUB_BYTES;
           const uint32_t sB = sA + C::A_BYTES;
           const uint32_t lo_off = C::A_BYTES + C::B_BYTES;
           const int k0 = kb * C::BK;
@@ -1136,6 +1146,7 @@ __global__ void __launch_bounds__(ACC_THREADS, 1)
               ++gidx;
             }
           }
+          }  // k-blocks of the stage
           if (!ok) break;
           mma_commit_pair_mc(empty_bar(stage), kMask);
           if (++stage == C::STAGES) {

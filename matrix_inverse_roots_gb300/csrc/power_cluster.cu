@@ -625,7 +625,9 @@ __global__ void __launch_bounds__(PC_THREADS, 1)
 
 }  // namespace
 
-bool power_cluster_supported(int dim) { return dim % PC_BM == 0 && dim / PC_BM <= PC_MAX_CL; }
+bool power_cluster_supported(int dim) {
+  return dim >= PC_BM && dim % PC_BM == 0 && dim / PC_BM <= PC_MAX_CL;
+}
 
 size_t power_cluster_slot_bytes(int dim) { return static_cast<size_t>(dim) * dim * 2; }
 
