@@ -52,8 +52,8 @@ TF32_RATIO = 1.1 / 2.25
 # `bench.py --case step` with gpu__time_duration.sum, dram__bytes_read.sum and
 # dram__bytes_write.sum (one pass).  Valid only for the sources it was taken on,
 # identified by GEMM_TRAFFIC_SRC (None: not measured for these sources).
-GEMM_TRAFFIC_PER_LAUNCH = 16.784e9  # 36 launches: 604.2 GB in 139.8 ms (serialised)
-GEMM_TRAFFIC_SRC = "ae72f0eea8626709"
+GEMM_TRAFFIC_PER_LAUNCH = 16.419e9  # 36 launches: 591.1 GB in 138.7 ms (serialised)
+GEMM_TRAFFIC_SRC = "eb77bf6bd03f1d3d"
 GEMM_SOURCES = ("matrix_inverse_roots_gb300/csrc/gemm_tc.cu",
                 "matrix_inverse_roots_gb300/csrc/dash_common.cuh",
                 "matrix_inverse_roots_gb300/csrc/dash_api.cu")
