@@ -56,8 +56,11 @@ __global__ void __launch_bounds__(EW_THREADS) affine_kernel(const __grid_constan
     for (long long v = static_cast<long long>(blockIdx.x) * EW_THREADS + threadIdx.x; v < n4;
          v += static_cast<long long>(gridDim.x) * EW_THREADS) {
       const long long e = blk * dd + 4 * v;
-      const int row = static_cast<int>((4 * v) / p.dim);
-      const int col0 = static_cast<int>((4 * v) % p.dim);
+      // The element index within the block is below dim^2 <= 2^22: 32-bit arithmetic
+      // (a 64-bit division per vector made this loop issue-bound).
+      const unsigned q = static_cast<unsigned>(4 * v);
+      const int row = static_cast<int>(q / static_cast<unsigned>(p.dim));
+      const int col0 = static_cast<int>(q - static_cast<unsigned>(row) * static_cast<unsigned>(p.dim));
       float x[4];
       load4(p.src_fmt, p.src_hi, p.src_lo, e, x);
 #pragma unroll
@@ -155,8 +158,9 @@ __global__ void __launch_bounds__(EW_THREADS)
     for (long long v = static_cast<long long>(blockIdx.x) * EW_THREADS + threadIdx.x; v < n4;
          v += static_cast<long long>(gridDim.x) * EW_THREADS) {
       const float4 a = *reinterpret_cast<const float4*>(A + blk * dd + 4 * v);
-      const int row = static_cast<int>((4 * v) / dim);
-      const int col0 = static_cast<int>((4 * v) % dim);
+      const unsigned q = static_cast<unsigned>(4 * v);  // below dim^2 <= 2^22
+      const int row = static_cast<int>(q / static_cast<unsigned>(dim));
+      const int col0 = static_cast<int>(q - static_cast<unsigned>(row) * static_cast<unsigned>(dim));
       float x[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -206,25 +210,43 @@ dash_status launch_pad_vectors(const float* V0, int nv, int dim, long long nbloc
   return err == cudaSuccess ? DASH_OK : DASH_ERR_CUDA;
 }
 
-__global__ void pad_vectors_t_kernel(const float* V0, int nv, int dim, long long nblocks, int bf16,
-                                     uint16_t* Vt) {
-  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= nblocks * PW_NV * dim) return;
-  const int r = static_cast<int>(i % dim);
-  const long long bc = i / dim;
-  const int c = static_cast<int>(bc % PW_NV);
-  const long long b = bc / PW_NV;
-  const float x = (c < nv) ? V0[(b * dim + r) * nv + c] : 0.0f;
-  Vt[i] = bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(x)) : __half_as_ushort(__float2half_rn(x));
+// One CTA per chunk of PT_ROWS rows of a block: it reads the chunk's start vectors
+// (rows of nv floats, consecutive threads on consecutive floats), transposes them in
+// shared memory and writes 32 rows of PT_ROWS 16-bit values (128 contiguous bytes
+// each) of Vt.
+constexpr int PT_ROWS = 64;
+
+__global__ void __launch_bounds__(256)
+    pad_vectors_t_kernel(const float* V0, int nv, int dim, long long nblocks, int bf16,
+                         uint16_t* Vt) {
+  __shared__ float t[PW_NV][PT_ROWS + 1];
+  const int r0 = static_cast<int>(blockIdx.x) * PT_ROWS;
+  for (long long b = blockIdx.y; b < nblocks; b += gridDim.y) {
+    const float* src = V0 + (b * dim + r0) * nv;
+    for (int i = threadIdx.x; i < PT_ROWS * PW_NV; i += blockDim.x) {
+      const int rr = i / PW_NV, c = i % PW_NV;
+      t[c][rr] = (c < nv) ? src[rr * nv + c] : 0.0f;
+    }
+    __syncthreads();
+    uint16_t* dst = Vt + b * PW_NV * dim + r0;
+    for (int i = threadIdx.x; i < PW_NV * PT_ROWS; i += blockDim.x) {
+      const int c = i / PT_ROWS, rr = i % PT_ROWS;
+      const float x = t[c][rr];
+      dst[static_cast<long long>(c) * dim + rr] =
+          bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(x)) : __half_as_ushort(__float2half_rn(x));
+    }
+    __syncthreads();
+  }
 }
 
 dash_status launch_pad_vectors_t(const float* V0, int nv, int dim, long long nblocks, int bf16,
                                  uint16_t* Vt, cudaStream_t st) {
   if (nblocks <= 0) return DASH_OK;
-  const long long n = nblocks * PW_NV * dim;
+  if (dim % PT_ROWS != 0 || nv < 1 || nv > PW_NV) return DASH_ERR_INVALID_ARG;
   const int rec = trace_begin(st);
-  pad_vectors_t_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(V0, nv, dim,
-                                                                               nblocks, bf16, Vt);
+  const dim3 grid(static_cast<unsigned>(dim / PT_ROWS),
+                  static_cast<unsigned>(nblocks < 65535 ? nblocks : 65535), 1);
+  pad_vectors_t_kernel<<<grid, 256, 0, st>>>(V0, nv, dim, nblocks, bf16, Vt);
   const cudaError_t err = cudaGetLastError();
   trace_end(rec, st, DASH_TRACE_ELEMENTWISE, 0.0,
             static_cast<double>(dim) * nblocks * (4.0 * nv + 2.0 * PW_NV));
