@@ -77,14 +77,20 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// Upper bound, in ns, on how long one try_wait may keep its thread suspended before
+// returning false; the thread resumes as soon as the phase completes.  Waiting warps
+// then issue less while they wait: in the benchmark step, timed launch by launch on
+// two boxes, the step ran 0.7% and 1.4% faster than with the default limit.
+constexpr uint32_t SUSPEND_HINT_NS = 20000u;
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(SUSPEND_HINT_NS)
       : "memory");
   return ok != 0;
 }
