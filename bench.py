@@ -52,8 +52,8 @@ TF32_RATIO = 1.1 / 2.25
 # `bench.py --case step` with gpu__time_duration.sum, dram__bytes_read.sum and
 # dram__bytes_write.sum (one pass).  Valid only for the sources it was taken on,
 # identified by GEMM_TRAFFIC_SRC (None: not measured for these sources).
-GEMM_TRAFFIC_PER_LAUNCH = 14.935e9  # 36 launches: 537.7 GB in 133.6 ms (serialised)
-GEMM_TRAFFIC_SRC = "f9d3c3c688dcec07"
+GEMM_TRAFFIC_PER_LAUNCH = 14.967e9  # 36 launches: 538.8 GB in 127.3 ms (serialised)
+GEMM_TRAFFIC_SRC = "d1ec292ae7b61eb2"
 GEMM_SOURCES = ("matrix_inverse_roots_gb300/csrc/gemm_tc.cu",
                 "matrix_inverse_roots_gb300/csrc/dash_common.cuh",
                 "matrix_inverse_roots_gb300/csrc/dash_api.cu")

@@ -9,6 +9,11 @@
 // accumulator rows):
 //   warp 0      TMA producer: streams 128-byte-wide, 128B-swizzled operand tiles
 //               into a ring of shared-memory stages (mbarrier full/empty pairs).
+//   warp 10     in the fixed-order pair instances, a second producer thread that
+//               loads the B operand while warp 0 loads A: one thread's loop of
+//               barrier waits and tiled TMA issues caps the copies it can start
+//               (about one 16 KB box per 600 cycles), and two threads double it.
+//               Each arms the stage's barrier for its own bytes (two arrivals).
 //   warp 1      allocates TMEM and issues tcgen05.mma from one thread into one of
 //               two TMEM accumulators (128 x BN fp32 each), so the epilogue of
 //               tile i overlaps the MMAs of tile i+1.
@@ -435,8 +440,19 @@ __device__ __forceinline__ bool chunk_on_diag(int r0, int c0) {
   return c0 < r0 + 32 && r0 < c0 + 16;
 }
 
+// Instances with the second (B) producer thread, warp 10: the pair kernels whose
+// tile order is fixed (the run-time order's ring is read by one producer only).
+template <int MODE, bool MIR>
+constexpr bool gemm_split() {
+  return MODE == 2 && !(MIR && DASH_DYN_SCHED != 0);
+}
+template <int MODE, bool MIR>
+constexpr int gemm_threads() {
+  return gemm_split<MODE, MIR>() ? 352 : 320;
+}
+
 template <int BN, int KT, int MODE, bool MIR>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(gemm_threads<MODE, MIR>(), 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tA, const __grid_constant__ CUtensorMap tB,
                    const __grid_constant__ CUtensorMap tAl,
                    const __grid_constant__ CUtensorMap tBl, const __grid_constant__ KParams p) {
@@ -480,6 +496,10 @@ __global__ void __launch_bounds__(320, 1)
   // direct stores); the other instances keep the fixed order and the code of it.
   constexpr bool DYN = MIR && (MODE == 2) && (DASH_DYN_SCHED != 0);
   const bool dyn = DYN && (p.sched != nullptr);
+  constexpr bool SPLIT = gemm_split<MODE, MIR>();
+  constexpr int EXP_A = (MODE == 2 ? 2 : 1) * C::KPS * C::A_BYTES * C::NPART_A;
+  constexpr int EXP_B = (MODE == 2 ? 2 : 1) * C::KPS * C::B_BYTES * C::NPART_B;
+  static_assert(!SPLIT || EXP_A + EXP_B == C::EXPECT_BYTES, "split of the stage bytes");
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -517,7 +537,7 @@ __global__ void __launch_bounds__(320, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
+      mbar_init(full_bar(s), SPLIT ? 2 : 1);
       // Released by the MMA warp (in a pair, the leader's).
       mbar_init(empty_bar(s), 1);
     }
@@ -620,7 +640,7 @@ __global__ void __launch_bounds__(320, 1)
           }
           uint32_t fb = full_bar(stage);
           if (MODE != 2 || leader) {
-            mbar_arrive_expect_tx(fb, C::EXPECT_BYTES);
+            mbar_arrive_expect_tx(fb, SPLIT ? EXP_A : C::EXPECT_BYTES);
             armed |= 1u << stage;
             armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
           }
@@ -641,6 +661,7 @@ __global__ void __launch_bounds__(320, 1)
               // read as the transpose of the stored tile, i.e. in the other major.
               for_boxes(z, m0, n0, kb, part, [&](const CUtensorMap* m, int isB, int off, int x,
                                                  int y, int zz) {
+                if (SPLIT && isB) return;
                 tma_load_3d_pair((isB ? sB : sA) + off, m, fb, x, y, zz);
               });
               continue;
@@ -797,6 +818,58 @@ __global__ void __launch_bounds__(320, 1)
       else
         mma_commit(fin_bar);
       mbar_wait_drain(fin_bar, 0);
+    }
+  } else if (SPLIT && warp == 10) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- B producer
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_par = 0;
+      bool ok = true;
+      for (long long u = cid; ok && u < p.total_units; u += ncl) {
+        long long blk;
+        int m0, n0;
+        decode_unit<CL>(u, p, crank, blk, m0, n0, BN);
+        const int z = static_cast<int>(blk);
+        for (int kb0 = 0; kb0 < p.nkb; kb0 += C::KPS) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint32_t fb = full_bar(stage);
+          if (leader) {
+            mbar_arrive_expect_tx(fb, EXP_B);
+            armed |= 1u << stage;
+            armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          }
+          fb = leader ? fb : mapa_shared(fb, crank & ~1u);
+          for (int j = 0; j < C::KPS; ++j)
+          for (int part = 0; part < C::NPART_B; ++part) {
+            const int kb = kb0 + j;
+            const int k0 = kb * C::BK;
+            const uint32_t s0 = sbase + stage * C::STAGE_BYTES + j * C::SUB_BYTES;
+            const uint32_t sB = s0 + C::A_BYTES + part * C::LO_B;
+            const bool bmir = p.sym_in_b && (k0 >> 8) > (n0 >> 8);
+            const CUtensorMap* mb = bmir ? (part ? &p.tBlm : &p.tBm) : (part ? &tBl : &tB);
+            const int nb = n0 + static_cast<int>(crank) * C::B_ROWS;
+            if (!(p.b_mn ^ bmir)) {
+              tma_load_3d_pair(sB, mb, fb, k0, nb, z);
+            } else {
+#pragma unroll
+              for (int i = 0; i < C::B_BOXES_MN; ++i)
+                tma_load_3d_pair(sB + i * C::MN_BOX_BYTES, mb, fb, nb + i * C::MN_ATOM, k0, z);
+            }
+          }
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < C::STAGES; ++s)
+          if (armed & (1u << s)) mbar_wait_drain(full_bar(s), (armed_par >> s) & 1u);
+      }
     }
   } else {
     // -------------------------------------------------------------- epilogue
@@ -1357,7 +1430,7 @@ static bool sched_slot(unsigned long long** w, uint32_t* id) {
 // Kernel entry of a configuration (ACC: the accurate 3xTF32 pair variant).
 template <int BN, int KT, int MODE, bool ACC, bool MIR>
 struct KernelOf {
-  static constexpr int THREADS = ACC ? ACC_THREADS : 320;
+  static constexpr int THREADS = ACC ? ACC_THREADS : gemm_threads<MODE, MIR>();
   static auto get() {
     if constexpr (ACC)
       return gemm_tc_acc_kernel<KT>;
